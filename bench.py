@@ -1,0 +1,425 @@
+"""Benchmark of the MiniMax-H3 BF16 pre-attention stage on GB300.
+
+One step = one whole stage call (kernel 1 norm/AdaLN + kernel 2 QKV GEMM
+with the fused epilogue) over the production video sequence workload
+(M = 32760 tokens of a 21x30x52 grid, rows = 9 strided AdaLN chunks, P = 8,
+explicit positions into an S = 40000 cache with 0.1% clamped, x ~ N(0, 2)
+with 0.01% outliers, caller-provided workspace).  Inputs are seeded and
+synthetic and are larger than L2 (x 352 MB, weight 231 MB), so no flush is
+needed between steps.
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+
+N > 1 runs N independent replicas (one per rank, launched by torchrun; the
+stage has no cross-GPU step), timed with a barrier and the max over ranks.
+``--impl reference`` times the CPU oracle on the host cores instead.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+import torch
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = ("pre-attn µs/call & GEMM TFLOP/s at M=4096/32760; "
+          "% of BF16 tensor/HBM roofline")
+UNIT = "us/call"
+WORKLOAD = "c3"
+ALSO = "c2"
+FLOP_PER_TOKEN = 2 * 5376 * 21504
+K2_SOURCES = ("norm_adaln_qkv_gb300/csrc/k2_qkv_gemm.cu", "norm_adaln_qkv_gb300/csrc/ptx.cuh",
+              "norm_adaln_qkv_gb300/csrc/common.cuh")
+TRAFFIC_FILE = os.path.join(ROOT, "profiles", "k2_traffic.json")
+
+
+def _peaks():
+    try:
+        with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
+            p = json.load(f)
+        return dict(hbm=float(p["hbm_gbs"]), bf16=float(p["bf16_tflops"]),
+                    bf16_sus=float(p["bf16_tflops_sustained"]), src="measured")
+    except Exception:
+        return dict(hbm=6800.0, bf16=1900.0, bf16_sus=1700.0, src="fallback")
+
+
+def _k2_source_hash() -> str:
+    h = hashlib.sha256()
+    for rel in K2_SOURCES:
+        with open(os.path.join(ROOT, rel), "rb") as f:
+            h.update(f.read())
+    return h.hexdigest()[:16]
+
+
+def _k2_traffic(M: int):
+    """DRAM bytes per launch of kernel 2 from the committed ncu summary, or
+    None when the kernel source changed since the counters were taken."""
+    try:
+        with open(TRAFFIC_FILE) as f:
+            t = json.load(f)
+    except Exception:
+        return None
+    if t.get("source_hash") != _k2_source_hash():
+        return None
+    per_token = t.get("dram_bytes_per_token")
+    fixed = t.get("dram_bytes_fixed", 0)
+    if per_token is None:
+        return None
+    return float(fixed + per_token * M)
+
+
+class ClockSampler:
+    """nvidia-smi clocks and throttle reasons sampled while the GPU works."""
+
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.gpu = gpu_index
+        self.proc = None
+        self.path = None
+
+    def start(self):
+        import tempfile
+        fd, self.path = tempfile.mkstemp(prefix="clocks_", suffix=".csv")
+        os.close(fd)
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.gpu), f"--query-gpu={self.FIELDS}",
+                 "--format=csv,noheader,nounits", "-lms", "100"],
+                stdout=open(self.path, "w"), stderr=subprocess.DEVNULL)
+        except Exception:
+            self.proc = None
+
+    def stop(self):
+        if self.proc is None:
+            return None
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except Exception:
+            self.proc.kill()
+        rows = []
+        with open(self.path) as f:
+            for line in f:
+                parts = [p.strip() for p in line.split(",")]
+                if len(parts) >= 9:
+                    rows.append(parts)
+        os.unlink(self.path)
+        if not rows:
+            return None
+
+        def num(s):
+            try:
+                return float(s)
+            except ValueError:
+                return None
+        sm = [num(r[1]) for r in rows if num(r[1]) is not None]
+        smax = [num(r[2]) for r in rows if num(r[2]) is not None]
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted({names[i] for r in rows for i in range(4) if r[5 + i].lower() == "active"})
+        busy = [s for s in sm if smax and s > 0.5 * max(smax)] or sm
+        return {"sm_mhz": statistics.median(busy) if busy else None,
+                "sm_max_mhz": max(smax) if smax else None,
+                "reasons": reasons, "samples": len(rows)}
+
+
+def _dist():
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return world, rank, local
+
+
+# ------------------------------------------------------------ reference arm
+def run_reference(args, world, rank):
+    if rank != 0:
+        return
+    import oracle
+    from norm_adaln_qkv_gb300.inputs import make_workload
+    wl = make_workload(WORKLOAD)
+    sc, sh = wl.table_views()
+    rows_per_step = args.ref_rows
+    M = wl.M
+
+    def step(i):
+        t0 = (i * 997) % (M - rows_per_step)
+        toks = list(range(t0, t0 + rows_per_step))
+        oracle.pre_attention_tokens(
+            wl.x, wl.x_norm_weight, sc, sh, wl.adaln_index, wl.qkv_weight, wl.q_norm_weight,
+            wl.k_norm_weight, wl.rope_cos_sin, eps=wl.spec.eps, qk_eps=wl.spec.qk_eps,
+            rope_positions=wl.rope_positions, tokens=toks)
+
+    for i in range(args.warmup):
+        step(i)
+    t = time.perf_counter()
+    for i in range(args.steps):
+        step(args.warmup + i)
+    el = time.perf_counter() - t
+    us_per_call = el / args.steps * (M / rows_per_step) * 1e6
+    cores = torch.get_num_threads()
+    sample = (f"{rows_per_step} consecutive tokens of M={M} per step, time scaled "
+              f"by M/{rows_per_step} (tokens are independent)")
+    line = {
+        "impl": "reference", "metric": METRIC, "value": us_per_call, "unit": UNIT,
+        "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": el / args.steps * 1e3, "higher_is_better": False, "scaling": "weak",
+        "vs_baseline": None, "dtype": "f64-accumulate/f32/bf16", "data": "synthetic",
+        "config": {"workload": wl.spec.name, "M": M, "P": wl.spec.P, "S": wl.spec.S,
+                   "rows": wl.spec.rows},
+        "cpu_baseline": {"value": us_per_call, "unit": UNIT, "cores": cores, "kind": "oracle",
+                         "sample": sample},
+        "e2e": {"value": us_per_call, "unit": UNIT, "h2d_bytes_per_step": 0,
+                "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+
+
+# ------------------------------------------------------------------ our arm
+def cpu_baseline(wl, rows: int):
+    """The oracle as it stands, on a bounded sample of the bench workload."""
+    import oracle
+    sc, sh = wl.table_views()
+    toks = list(range(0, rows))
+    t = time.perf_counter()
+    oracle.pre_attention_tokens(
+        wl.x, wl.x_norm_weight, sc, sh, wl.adaln_index, wl.qkv_weight, wl.q_norm_weight,
+        wl.k_norm_weight, wl.rope_cos_sin, eps=wl.spec.eps, qk_eps=wl.spec.qk_eps,
+        rope_positions=wl.rope_positions, tokens=toks)
+    el = time.perf_counter() - t
+    return {"value": el * (wl.M / rows) * 1e6, "unit": UNIT, "cores": torch.get_num_threads(),
+            "kind": "oracle",
+            "sample": f"first {rows} tokens of M={wl.M} in {el:.1f} s, scaled by M/{rows}"}
+
+
+def run_ours(args, world, rank, local):
+    from norm_adaln_qkv_gb300 import binding, build
+    from norm_adaln_qkv_gb300.inputs import make_workload
+
+    # Oracle CPU baseline first (rank 0 only, N = 1 only), before any CUDA work.
+    wl = make_workload(WORKLOAD)
+    cpu = cpu_baseline(wl, args.cpu_rows) if (rank == 0 and world == 1 and args.cpu_rows > 0) \
+        else None
+
+    torch.cuda.set_device(local)
+    if world > 1:
+        torch.distributed.init_process_group("nccl", device_id=torch.device("cuda", local))
+    build.build()
+    h = binding.Handle(local)
+    dev = torch.device("cuda", local)
+    stream = torch.cuda.current_stream(dev)
+    peaks = _peaks()
+
+    def prepare(w):
+        mod = w.adaln_mod.to(dev)
+        sc, sh = w.table_views(mod)
+        d = dict(x=w.x.to(dev), xw=w.x_norm_weight.to(dev), mod=mod, sc=sc, sh=sh,
+                 idx=w.adaln_index.to(dev), W=w.qkv_weight.to(dev), qw=w.q_norm_weight.to(dev),
+                 kw=w.k_norm_weight.to(dev), cs=w.rope_cos_sin.to(dev),
+                 pos=None if w.rope_positions is None else w.rope_positions.to(dev))
+        d["ws"] = torch.empty((w.M, 5376), dtype=torch.bfloat16, device=dev)
+        d["out"] = torch.empty((w.spec.P, w.M, 56 // w.spec.P, 3, 128), dtype=torch.bfloat16,
+                               device=dev)
+        return d
+
+    def stage(w, d):
+        binding.mh3_preattn_run(h, stream, w.M, d["x"], d["xw"], d["sc"], d["sc"].stride(0),
+                                d["sh"], d["sh"].stride(0), w.spec.rows, d["idx"], d["W"],
+                                d["qw"], d["kw"], d["cs"], w.spec.S, d["pos"], w.spec.P,
+                                w.spec.eps, w.spec.qk_eps, d["ws"], d["out"])
+
+    def k1(w, d):
+        binding.mh3_preattn_norm_adaln(h, stream, w.M, d["x"], d["xw"], d["sc"],
+                                       d["sc"].stride(0), d["sh"], d["sh"].stride(0), w.spec.rows,
+                                       d["idx"], w.spec.eps, d["ws"])
+
+    def k2(w, d):
+        qk = w.spec.qk_eps if w.spec.qk_eps is not None else w.spec.eps
+        binding.mh3_preattn_qkv(h, stream, w.M, d["ws"], d["W"], d["qw"], d["kw"], d["cs"],
+                                w.spec.S, d["pos"], w.spec.P, qk, d["out"])
+
+    def barrier():
+        if world > 1:
+            torch.distributed.barrier()
+
+    def max_over_ranks(v: float) -> float:
+        if world == 1:
+            return v
+        t = torch.tensor([v], dtype=torch.float64, device=dev)
+        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+        return float(t.item())
+
+    d = prepare(wl)
+    clocks = ClockSampler(local)
+    clocks.start()
+    for _ in range(max(args.warmup, 3)):
+        stage(wl, d)
+    torch.cuda.synchronize()
+
+    # ---- timed region: exactly K whole-stage steps
+    barrier()
+    torch.cuda.synchronize()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for _ in range(args.steps):
+        stage(wl, d)
+    e1.record(stream)
+    torch.cuda.synchronize()
+    barrier()
+    ms_total = max_over_ranks(e0.elapsed_time(e1))
+    gpu_launches = 2 * args.steps
+    assert h.device_status(stream) == 0, "a kernel recorded a timeout"
+
+    # ---- per-kernel breakdown (same workload, events on the launching stream)
+    def breakdown(w, dd, n):
+        ev = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(n)]
+        for i in range(n):
+            ev[i][0].record(stream)
+            k1(w, dd)
+            ev[i][1].record(stream)
+            k2(w, dd)
+            ev[i][2].record(stream)
+        torch.cuda.synchronize()
+        t1 = [e[0].elapsed_time(e[1]) for e in ev]
+        t2 = [e[1].elapsed_time(e[2]) for e in ev]
+        return sum(t1) / n, sum(t2) / n
+
+    k1_ms, k2_ms = breakdown(wl, d, args.steps)
+
+    # ---- end to end through the public API: pinned host inputs in, out back
+    hx = wl.x.pin_memory()
+    hidx = wl.adaln_index.pin_memory()
+    hpos = wl.rope_positions.pin_memory() if wl.rope_positions is not None else None
+    hmod = wl.adaln_mod.pin_memory()
+    hout = torch.empty(d["out"].shape, dtype=torch.bfloat16).pin_memory()
+    h2d = hx.numel() * 2 + hidx.numel() * 8 + hmod.numel() * 2 + \
+        (hpos.numel() * 8 if hpos is not None else 0)
+    d2h = hout.numel() * 2
+    x_in = torch.empty_like(d["x"])
+    idx_in = torch.empty_like(d["idx"])
+    mod_in = torch.empty_like(d["mod"])
+    pos_in = torch.empty_like(d["pos"]) if d["pos"] is not None else None
+    sc_in, sh_in = wl.table_views(mod_in)
+    e2e_d = dict(d, x=x_in, idx=idx_in, mod=mod_in, sc=sc_in, sh=sh_in, pos=pos_in)
+    n_e2e = max(3, min(args.steps, 10))
+
+    def e2e_step():
+        x_in.copy_(hx, non_blocking=True)
+        idx_in.copy_(hidx, non_blocking=True)
+        mod_in.copy_(hmod, non_blocking=True)
+        if pos_in is not None:
+            pos_in.copy_(hpos, non_blocking=True)
+        stage(wl, e2e_d)
+        hout.copy_(e2e_d["out"], non_blocking=True)
+
+    e2e_step()
+    torch.cuda.synchronize()
+    barrier()
+    s0, s1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    s0.record(stream)
+    for _ in range(n_e2e):
+        e2e_step()
+    s1.record(stream)
+    torch.cuda.synchronize()
+    barrier()
+    e2e_ms = max_over_ranks(s0.elapsed_time(s1)) / n_e2e
+
+    # ---- the 4096-token block named by the metric (same stage, P = 2)
+    also = None
+    if not args.skip_also:
+        wl2 = make_workload(ALSO)
+        d2 = prepare(wl2)
+        for _ in range(3):
+            stage(wl2, d2)
+        torch.cuda.synchronize()
+        a0, a1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a0.record(stream)
+        for _ in range(args.steps):
+            stage(wl2, d2)
+        a1.record(stream)
+        torch.cuda.synchronize()
+        st_ms = a0.elapsed_time(a1) / args.steps
+        b1, b2 = breakdown(wl2, d2, args.steps)
+        also = {"workload": wl2.spec.name, "stage_us": st_ms * 1e3, "k1_us": b1 * 1e3,
+                "k2_us": b2 * 1e3,
+                "k2_tflops": FLOP_PER_TOKEN * wl2.M / (b2 * 1e-3) / 1e12,
+                "k2_frac_of_measured_bf16": FLOP_PER_TOKEN * wl2.M / (b2 * 1e-3) / 1e12 / peaks["bf16"]}
+        del d2
+    clk = clocks.stop()
+    assert h.device_status(stream) == 0, "a kernel recorded a timeout"
+
+    if rank != 0:
+        return
+    M = wl.M
+    ms_step = ms_total / args.steps
+    value_us = ms_step * 1e3 / world  # whole-job time per call: N replicas per step
+    k2_tflops = FLOP_PER_TOKEN * M / (k2_ms * 1e-3) / 1e12
+    k1_bytes = M * 5376 * 2 * 2 + M * 8
+    k1_gbs = k1_bytes / (k1_ms * 1e-3) / 1e9
+    flop_time = FLOP_PER_TOKEN * M / (peaks["bf16"] * 1e12)
+    comp_bytes = (M * 10752 + 21504 * 5376 * 2 + M * 43008 + 8 * M +
+                  (8 * M if wl.rope_positions is not None else 0) + min(wl.spec.S, M) * 192 +
+                  wl.spec.rows * 2 * 5376 * 2)
+    bytes_time = comp_bytes / (peaks["hbm"] * 1e9)
+    stage_roof_us = max(flop_time, bytes_time) * 1e6
+    line = {
+        "metric": METRIC, "value": value_us, "unit": UNIT, "n_gpus": world,
+        "steps": args.steps, "warmup": max(args.warmup, 3), "ms_per_step": ms_step,
+        "higher_is_better": False, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
+        "data": "synthetic",
+        "config": {"workload": wl.spec.name, "M": M, "P": wl.spec.P, "S": wl.spec.S,
+                   "rows": wl.spec.rows, "l2": "inputs larger than L2 (x 352 MB, W 231 MB); no flush",
+                   "parallelism": f"replicas x{world}" if world > 1 else "single GPU"},
+        "gemm_tflops": k2_tflops,
+        "stage_roofline_us": stage_roof_us,
+        "stage_roofline_frac": stage_roof_us / (ms_step * 1e3),
+        "kernels_us": {"k1_norm_adaln": k1_ms * 1e3, "k2_qkv_gemm": k2_ms * 1e3},
+        "roofline": {"bound": "tensor", "achieved": k2_tflops, "peak": peaks["bf16"],
+                     "unit": "TFLOP/s", "frac": k2_tflops / peaks["bf16"],
+                     "traffic": _k2_traffic(M),
+                     "peak_source": f"{peaks['src']} bf16 burst (kernel timed alone)",
+                     "frac_of_sustained": k2_tflops / peaks["bf16_sus"]},
+        "k1_roofline": {"bound": "hbm", "achieved": k1_gbs, "peak": peaks["hbm"], "unit": "GB/s",
+                        "frac": k1_gbs / peaks["hbm"], "bytes_per_launch": k1_bytes},
+        "cpu_baseline": cpu,
+        "e2e": {"value": e2e_ms * 1e3 / world, "unit": UNIT, "h2d_bytes_per_step": h2d,
+                "d2h_bytes_per_step": d2h},
+        "gpu_launches": gpu_launches,
+        "clocks": clk,
+        "also": also,
+    }
+    print(json.dumps(line), flush=True)
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=30)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--cpu-rows", type=int, default=256,
+                    help="tokens of the oracle CPU-baseline sample (0 disables)")
+    ap.add_argument("--ref-rows", type=int, default=32,
+                    help="tokens per step of the reference (oracle) arm")
+    ap.add_argument("--skip-also", action="store_true", help="skip the M=4096 side measurement")
+    args = ap.parse_args()
+    world, rank, local = _dist()
+    if args.impl == "reference":
+        run_reference(args, world, rank)
+    else:
+        run_ours(args, world, rank, local)
+    if world > 1 and torch.distributed.is_initialized():
+        torch.distributed.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,176 @@
+/*
+ * mh3_preattn.h -- C ABI of the MiniMax-H3 BF16 pre-attention stage on GB300
+ * (sm_103a).
+ *
+ * The operation is the one the page
+ * "flashinfer.diffusion_ops.minimax_h3_bf16_pre_attention" defines (summary
+ * paragraph, Parameters and Notes), with the norm/AdaLN formulas of the
+ * formula block of "flashinfer.diffusion_ops.minimax_h3_mlp_fp8_sm120":
+ *
+ *   n  = bf16(rmsnorm(x, eps) * x_norm_weight)       FP32 sum of squares
+ *   a  = bf16(shift[i] + n * bf16(1 + scale[i]))     i = adaln_index[m]
+ *   a  = 0 for the whole row when i is outside [0, rows)
+ *   y  = bf16(a @ qkv_weight^T)                      FP32 accumulation
+ *   q,k: per-head (128) RMSNorm with qk_eps and q/k_norm_weight, then the
+ *        split-half rotation of dims [0, 96) by cache row
+ *        p = clamp(positions[m], 0, S-1) (or p = m), dims [96, 128) unchanged
+ *   out[dst, m, hl, kind, d], dst = head / (56/P), hl = head % (56/P),
+ *        kind 0 = q, 1 = k, 2 = v
+ *
+ * Conventions shared by every entry point:
+ *   - All tensor arguments are DEVICE pointers into the current device's
+ *     memory.  bf16 values are stored as 16-bit patterns (mh3_bf16).  The
+ *     library never takes ownership of caller memory and never frees it.
+ *   - Every call validates all arguments on the host before it launches
+ *     anything; on a validation error nothing is launched and the status is
+ *     returned.  mh3_preattn_last_error() gives a message for the calling
+ *     thread's last failure.
+ *   - Launches go on `stream` (a cudaStream_t passed as void*; NULL is the
+ *     legacy default stream), in stream order, with no host synchronisation
+ *     and no host<->device copies.
+ *   - Index and position VALUES are never errors: an adaln_index outside
+ *     [0, rows) zeroes its row and a position outside [0, S) is clamped, on
+ *     the device (page Notes and Parameters: adaln_index, rope_positions).
+ *   - The kernels bound every wait they make; a wait that runs out records a
+ *     code in the handle's device status word instead of hanging.  Read it
+ *     with mh3_preattn_device_status().
+ *   - Sizes: hidden H = 5376, heads NH = 56, head_dim D = 128, qkv rows
+ *     N = 3*NH*D = 21504, rotary dims 96.  These are fixed by the page.
+ */
+#ifndef MH3_PREATTN_H
+#define MH3_PREATTN_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+#define MH3_HIDDEN 5376
+#define MH3_NUM_HEADS 56
+#define MH3_HEAD_DIM 128
+#define MH3_QKV_ROWS 21504
+#define MH3_ROPE_DIMS 96
+
+typedef uint16_t mh3_bf16; /* storage of one bfloat16 value */
+
+typedef enum mh3_status {
+  MH3_OK = 0,
+  MH3_ERR_INVALID_ARG = 1, /* null pointer, bad size, bad P, bad eps, S < M with identity positions */
+  MH3_ERR_ALIGNMENT = 2,   /* a base pointer or row stride breaks the 16-byte rule */
+  MH3_ERR_UNSUPPORTED = 3, /* device is not sm_103 / lacks the shared memory the GEMM needs */
+  MH3_ERR_CUDA = 4,        /* a CUDA runtime/driver call failed (message has the CUDA error) */
+  MH3_ERR_OOM = 5,         /* the handle could not grow its own workspace */
+  MH3_ERR_DEVICE = 6       /* a kernel recorded a bounded-wait timeout (mh3_preattn_device_status) */
+} mh3_status;
+
+typedef struct mh3_preattn_ctx* mh3_preattn_t;
+
+/* Create a handle bound to CUDA device `device` (made current for the call).
+ * Caches the SM count, raises the GEMM's shared-memory limit and allocates a
+ * 4-byte device status word.  No per-M state.  *handle is set only on MH3_OK. */
+int mh3_preattn_create(mh3_preattn_t* handle, int device);
+
+/* Destroy a handle: frees its status word and its own workspace (if any).
+ * The caller must ensure no launch that uses the handle is still running. */
+int mh3_preattn_destroy(mh3_preattn_t handle);
+
+/* Bytes of the BF16 [M, 5376] workspace: M * 5376 * 2.  0 when M <= 0. */
+size_t mh3_preattn_workspace_bytes(int64_t M);
+
+/* Bytes of out, [P, M, 56/P, 3, 128] BF16: M * 21504 * 2 (independent of P). */
+size_t mh3_preattn_out_bytes(int64_t M);
+
+/* Host-only validation of a full argument set (no device access, no launch).
+ * Same rules and status codes as mh3_preattn_run; pointers are checked for
+ * NULL and alignment only, never dereferenced.  Arguments as in
+ * mh3_preattn_run. */
+int mh3_preattn_validate(int64_t M, const mh3_bf16* x, const mh3_bf16* x_norm_weight,
+                         const mh3_bf16* adaln_scale, int64_t scale_row_stride,
+                         const mh3_bf16* adaln_shift, int64_t shift_row_stride, int64_t rows,
+                         const int64_t* adaln_index, const mh3_bf16* qkv_weight,
+                         const mh3_bf16* q_norm_weight, const mh3_bf16* k_norm_weight,
+                         const mh3_bf16* rope_cos_sin, int64_t S, const int64_t* rope_positions,
+                         int P, float eps, float qk_eps, const mh3_bf16* workspace,
+                         const mh3_bf16* out);
+
+/* The whole stage: kernel 1 (RMSNorm + indexed AdaLN into the workspace) then
+ * kernel 2 (persistent QKV GEMM with the Q/K norm, RoPE and pack epilogue),
+ * two launches on `stream` (page summary: "two kernel launches on the current
+ * stream").
+ *
+ *   M                 tokens, >= 0 (M == 0 launches nothing and returns MH3_OK)
+ *   x                 [M, 5376] row-major, 16-byte aligned
+ *   x_norm_weight     [5376], 16-byte aligned
+ *   adaln_scale/shift [rows, 5376] views: unit column stride, row strides
+ *                     scale_row_stride / shift_row_stride in ELEMENTS,
+ *                     each >= 5376 and a multiple of 8 (16 bytes), base
+ *                     16-byte aligned.  Column chunks of a wider
+ *                     [rows, k*5376] projection qualify as they are
+ *                     (Parameters: adaln_scale).
+ *   rows              >= 1
+ *   adaln_index       [M] int64, 8-byte aligned; any value (guarded)
+ *   qkv_weight        [21504, 5376] row-major, rows in the order
+ *                     [qkv_kind, head, head_dim] (Parameters: qkv_weight)
+ *   q/k_norm_weight   [128] each
+ *   rope_cos_sin      [S, 96] row-major, S >= 1; columns [0,48) cos, [48,96) sin
+ *   rope_positions    [M] int64 or NULL.  NULL means row m uses cache row m
+ *                     and requires S >= M (Parameters: rope_positions); it
+ *                     needs no allocation, so it is graph-safe from the
+ *                     first call.
+ *   P                 destinations (ulysses_degree), one of 1, 2, 4, 8
+ *   eps               input RMSNorm epsilon, finite and > 0
+ *   qk_eps            Q/K RMSNorm epsilon; a negative value or NaN means
+ *                     "use eps" (Parameters: qk_eps, None uses eps);
+ *                     otherwise finite and > 0
+ *   workspace         [M, 5376] BF16 scratch (overwritten), 16-byte aligned,
+ *                     or NULL: the handle then uses its own buffer, grown
+ *                     with stream-ordered cudaMallocAsync on `stream` when M
+ *                     exceeds its size (Parameters: workspace).  With NULL,
+ *                     runs of one handle on different streams race on that
+ *                     buffer.
+ *   out               [P, M, 56/P, 3, 128] contiguous BF16, 16-byte aligned,
+ *                     caller-owned (Parameters: out)
+ */
+int mh3_preattn_run(mh3_preattn_t handle, void* stream, int64_t M, const mh3_bf16* x,
+                    const mh3_bf16* x_norm_weight, const mh3_bf16* adaln_scale,
+                    int64_t scale_row_stride, const mh3_bf16* adaln_shift,
+                    int64_t shift_row_stride, int64_t rows, const int64_t* adaln_index,
+                    const mh3_bf16* qkv_weight, const mh3_bf16* q_norm_weight,
+                    const mh3_bf16* k_norm_weight, const mh3_bf16* rope_cos_sin, int64_t S,
+                    const int64_t* rope_positions, int P, float eps, float qk_eps,
+                    mh3_bf16* workspace, mh3_bf16* out);
+
+/* Kernel 1 alone: workspace[m] = a (the formula block's n and a lines, with
+ * the index guard).  Arguments as in mh3_preattn_run; workspace must not be
+ * NULL. */
+int mh3_preattn_norm_adaln(mh3_preattn_t handle, void* stream, int64_t M, const mh3_bf16* x,
+                           const mh3_bf16* x_norm_weight, const mh3_bf16* adaln_scale,
+                           int64_t scale_row_stride, const mh3_bf16* adaln_shift,
+                           int64_t shift_row_stride, int64_t rows, const int64_t* adaln_index,
+                           float eps, mh3_bf16* workspace);
+
+/* Kernel 2 alone: out = pack(rope(norm(bf16(workspace @ qkv_weight^T)))),
+ * reading an already-filled workspace [M, 5376].  Arguments as in
+ * mh3_preattn_run (qk_eps here must be finite and > 0: there is no eps to
+ * fall back to). */
+int mh3_preattn_qkv(mh3_preattn_t handle, void* stream, int64_t M, const mh3_bf16* workspace,
+                    const mh3_bf16* qkv_weight, const mh3_bf16* q_norm_weight,
+                    const mh3_bf16* k_norm_weight, const mh3_bf16* rope_cos_sin, int64_t S,
+                    const int64_t* rope_positions, int P, float qk_eps, mh3_bf16* out);
+
+/* Synchronise `stream`, then read and clear the handle's device status word.
+ * *device_code receives 0 when no kernel recorded a timeout since the last
+ * read, else a nonzero code (which wait gave up).  Returns MH3_OK, or
+ * MH3_ERR_CUDA if the synchronisation or the copy failed. */
+int mh3_preattn_device_status(mh3_preattn_t handle, void* stream, int* device_code);
+
+/* Message of the calling thread's last failed call ("" if none). */
+const char* mh3_preattn_last_error(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* MH3_PREATTN_H */

@@ -1,0 +1,257 @@
+"""ctypes binding of the C ABI in include/mh3_preattn.h.
+
+Argument marshalling only: every step of the stage runs in the CUDA library.
+The functions keep the C names and take torch CUDA tensors (or raw integer
+device pointers) plus sizes.  There is no fallback: if the library is missing
+or a call fails, a RuntimeError is raised.
+"""
+from __future__ import annotations
+
+import ctypes
+import math
+import os
+from typing import Optional
+
+import torch
+
+from . import inputs as _inputs
+
+_PKG = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_PKG, "libmh3_preattn.so")
+
+HIDDEN = _inputs.HIDDEN
+NUM_HEADS = _inputs.NUM_HEADS
+HEAD_DIM = _inputs.HEAD_DIM
+QKV_ROWS = _inputs.QKV_ROWS
+ROPE_DIMS = _inputs.ROPE_DIMS
+
+STATUS = {0: "MH3_OK", 1: "MH3_ERR_INVALID_ARG", 2: "MH3_ERR_ALIGNMENT", 3: "MH3_ERR_UNSUPPORTED",
+          4: "MH3_ERR_CUDA", 5: "MH3_ERR_OOM", 6: "MH3_ERR_DEVICE"}
+
+# Every symbol include/mh3_preattn.h declares.
+EXPORTS = ("mh3_preattn_create", "mh3_preattn_destroy", "mh3_preattn_workspace_bytes",
+           "mh3_preattn_out_bytes", "mh3_preattn_validate", "mh3_preattn_run",
+           "mh3_preattn_norm_adaln", "mh3_preattn_qkv", "mh3_preattn_device_status",
+           "mh3_preattn_last_error")
+
+_vp = ctypes.c_void_p
+_i64 = ctypes.c_int64
+_i32 = ctypes.c_int
+_f32 = ctypes.c_float
+
+_SIGS = {
+    "mh3_preattn_create": (_i32, [ctypes.POINTER(_vp), _i32]),
+    "mh3_preattn_destroy": (_i32, [_vp]),
+    "mh3_preattn_workspace_bytes": (ctypes.c_size_t, [_i64]),
+    "mh3_preattn_out_bytes": (ctypes.c_size_t, [_i64]),
+    "mh3_preattn_validate": (_i32, [_i64, _vp, _vp, _vp, _i64, _vp, _i64, _i64, _vp, _vp, _vp, _vp,
+                                    _vp, _i64, _vp, _i32, _f32, _f32, _vp, _vp]),
+    "mh3_preattn_run": (_i32, [_vp, _vp, _i64, _vp, _vp, _vp, _i64, _vp, _i64, _i64, _vp, _vp, _vp,
+                               _vp, _vp, _i64, _vp, _i32, _f32, _f32, _vp, _vp]),
+    "mh3_preattn_norm_adaln": (_i32, [_vp, _vp, _i64, _vp, _vp, _vp, _i64, _vp, _i64, _i64, _vp,
+                                      _f32, _vp]),
+    "mh3_preattn_qkv": (_i32, [_vp, _vp, _i64, _vp, _vp, _vp, _vp, _vp, _i64, _vp, _i32, _f32, _vp]),
+    "mh3_preattn_device_status": (_i32, [_vp, _vp, ctypes.POINTER(_i32)]),
+    "mh3_preattn_last_error": (ctypes.c_char_p, []),
+}
+
+_lib = None
+
+
+def load(path: str = LIB_PATH) -> ctypes.CDLL:
+    """Load the CUDA library (built by norm_adaln_qkv_gb300.build.build())."""
+    global _lib
+    if _lib is not None:
+        return _lib
+    if not os.path.exists(path):
+        raise RuntimeError(f"CUDA library not built: {path} is missing "
+                           "(run norm_adaln_qkv_gb300.build.build())")
+    lib = ctypes.CDLL(path)
+    for name, (res, args) in _SIGS.items():
+        fn = getattr(lib, name)
+        fn.restype = res
+        fn.argtypes = args
+    _lib = lib
+    return lib
+
+
+def last_error() -> str:
+    return load().mh3_preattn_last_error().decode()
+
+
+def _check(rc: int, what: str) -> None:
+    if rc != 0:
+        raise RuntimeError(f"{what} failed: {STATUS.get(rc, rc)}: {last_error()}")
+
+
+def _ptr(t) -> Optional[int]:
+    if t is None:
+        return None
+    if isinstance(t, int):
+        return t
+    return t.data_ptr()
+
+
+def _stream_ptr(stream) -> Optional[int]:
+    if stream is None:
+        stream = torch.cuda.current_stream()
+    if isinstance(stream, int):
+        return stream
+    return stream.cuda_stream
+
+
+def _qk_eps_arg(qk_eps: Optional[float]) -> float:
+    return -1.0 if qk_eps is None else float(qk_eps)
+
+
+class Handle:
+    """Owns an mh3_preattn_t for one device."""
+
+    def __init__(self, device: Optional[int] = None):
+        lib = load()
+        if device is None:
+            device = torch.cuda.current_device()
+        self.device = device
+        h = _vp()
+        _check(lib.mh3_preattn_create(ctypes.byref(h), device), "mh3_preattn_create")
+        self._h = h
+
+    @property
+    def ptr(self):
+        return self._h
+
+    def close(self) -> None:
+        if getattr(self, "_h", None) is not None and self._h.value is not None:
+            _check(load().mh3_preattn_destroy(self._h), "mh3_preattn_destroy")
+            self._h = _vp()
+
+    def __del__(self):
+        try:
+            self.close()
+        except Exception:
+            pass
+
+    def device_status(self, stream=None) -> int:
+        code = _i32(0)
+        _check(load().mh3_preattn_device_status(self._h, _stream_ptr(stream), ctypes.byref(code)),
+               "mh3_preattn_device_status")
+        return code.value
+
+
+_handles = {}
+
+
+def default_handle(device: Optional[int] = None) -> Handle:
+    if device is None:
+        device = torch.cuda.current_device()
+    if device not in _handles:
+        _handles[device] = Handle(device)
+    return _handles[device]
+
+
+def workspace_bytes(M: int) -> int:
+    return load().mh3_preattn_workspace_bytes(M)
+
+
+def out_bytes(M: int) -> int:
+    return load().mh3_preattn_out_bytes(M)
+
+
+def mh3_preattn_validate(M, x, x_norm_weight, adaln_scale, scale_row_stride, adaln_shift,
+                         shift_row_stride, rows, adaln_index, qkv_weight, q_norm_weight,
+                         k_norm_weight, rope_cos_sin, S, rope_positions, P, eps, qk_eps,
+                         workspace, out) -> int:
+    """Host-only validation; returns the status code (pointers may be ints)."""
+    return load().mh3_preattn_validate(
+        M, _ptr(x), _ptr(x_norm_weight), _ptr(adaln_scale), scale_row_stride, _ptr(adaln_shift),
+        shift_row_stride, rows, _ptr(adaln_index), _ptr(qkv_weight), _ptr(q_norm_weight),
+        _ptr(k_norm_weight), _ptr(rope_cos_sin), S, _ptr(rope_positions), P, float(eps),
+        _qk_eps_arg(qk_eps), _ptr(workspace), _ptr(out))
+
+
+def mh3_preattn_run(handle: Handle, stream, M, x, x_norm_weight, adaln_scale, scale_row_stride,
+                    adaln_shift, shift_row_stride, rows, adaln_index, qkv_weight, q_norm_weight,
+                    k_norm_weight, rope_cos_sin, S, rope_positions, P, eps, qk_eps, workspace,
+                    out) -> None:
+    _check(load().mh3_preattn_run(
+        handle.ptr, _stream_ptr(stream), M, _ptr(x), _ptr(x_norm_weight), _ptr(adaln_scale),
+        scale_row_stride, _ptr(adaln_shift), shift_row_stride, rows, _ptr(adaln_index),
+        _ptr(qkv_weight), _ptr(q_norm_weight), _ptr(k_norm_weight), _ptr(rope_cos_sin), S,
+        _ptr(rope_positions), P, float(eps), _qk_eps_arg(qk_eps), _ptr(workspace), _ptr(out)),
+        "mh3_preattn_run")
+
+
+def mh3_preattn_norm_adaln(handle: Handle, stream, M, x, x_norm_weight, adaln_scale,
+                           scale_row_stride, adaln_shift, shift_row_stride, rows, adaln_index,
+                           eps, workspace) -> None:
+    _check(load().mh3_preattn_norm_adaln(
+        handle.ptr, _stream_ptr(stream), M, _ptr(x), _ptr(x_norm_weight), _ptr(adaln_scale),
+        scale_row_stride, _ptr(adaln_shift), shift_row_stride, rows, _ptr(adaln_index),
+        float(eps), _ptr(workspace)), "mh3_preattn_norm_adaln")
+
+
+def mh3_preattn_qkv(handle: Handle, stream, M, workspace, qkv_weight, q_norm_weight,
+                    k_norm_weight, rope_cos_sin, S, rope_positions, P, qk_eps, out) -> None:
+    _check(load().mh3_preattn_qkv(
+        handle.ptr, _stream_ptr(stream), M, _ptr(workspace), _ptr(qkv_weight),
+        _ptr(q_norm_weight), _ptr(k_norm_weight), _ptr(rope_cos_sin), S, _ptr(rope_positions), P,
+        float(qk_eps), _ptr(out)), "mh3_preattn_qkv")
+
+
+def _check_tensor(t: torch.Tensor, name: str, dtype, shape=None, contiguous=True):
+    if not isinstance(t, torch.Tensor):
+        raise TypeError(f"{name} must be a torch.Tensor")
+    if t.dtype != dtype:
+        raise TypeError(f"{name} must be {dtype} (got {t.dtype})")
+    if not t.is_cuda:
+        raise ValueError(f"{name} must be a CUDA tensor")
+    if shape is not None and tuple(t.shape) != tuple(shape):
+        raise ValueError(f"{name} must have shape {tuple(shape)} (got {tuple(t.shape)})")
+    if contiguous and not t.is_contiguous():
+        raise ValueError(f"{name} must be contiguous")
+
+
+def minimax_h3_bf16_pre_attention(x, x_norm_weight, adaln_scale, adaln_shift, adaln_index,
+                                  qkv_weight, q_norm_weight, k_norm_weight, rope_cos_sin, *,
+                                  ulysses_degree: int, out: torch.Tensor, eps: float = 1e-5,
+                                  qk_eps: Optional[float] = None, rope_positions=None,
+                                  workspace: Optional[torch.Tensor] = None, stream=None,
+                                  handle: Optional[Handle] = None) -> torch.Tensor:
+    """Torch-tensor entry point with the argument list of the page
+    flashinfer.diffusion_ops.minimax_h3_bf16_pre_attention; returns ``out``.
+
+    Shapes/dtypes are checked here (tensor metadata only); every other rule
+    is checked by the C library before it launches.
+    """
+    M = x.shape[0]
+    P = int(ulysses_degree)
+    bf = torch.bfloat16
+    _check_tensor(x, "x", bf, (M, HIDDEN))
+    _check_tensor(x_norm_weight, "x_norm_weight", bf, (HIDDEN,))
+    for name, t in (("adaln_scale", adaln_scale), ("adaln_shift", adaln_shift)):
+        _check_tensor(t, name, bf, contiguous=False)
+        if t.dim() != 2 or t.shape[1] != HIDDEN or t.stride(1) != 1:
+            raise ValueError(f"{name} must be [rows, {HIDDEN}] with stride(1) == 1")
+    if adaln_scale.shape[0] != adaln_shift.shape[0]:
+        raise ValueError("adaln_scale and adaln_shift must have the same row count")
+    _check_tensor(adaln_index, "adaln_index", torch.int64, (M,))
+    _check_tensor(qkv_weight, "qkv_weight", bf, (QKV_ROWS, HIDDEN))
+    _check_tensor(q_norm_weight, "q_norm_weight", bf, (HEAD_DIM,))
+    _check_tensor(k_norm_weight, "k_norm_weight", bf, (HEAD_DIM,))
+    _check_tensor(rope_cos_sin, "rope_cos_sin", bf)
+    if rope_cos_sin.dim() != 2 or rope_cos_sin.shape[1] != ROPE_DIMS:
+        raise ValueError(f"rope_cos_sin must be [S, {ROPE_DIMS}]")
+    if P not in (1, 2, 4, 8):
+        raise ValueError("ulysses_degree must be 1, 2, 4 or 8")
+    _check_tensor(out, "out", bf, (P, M, NUM_HEADS // P, 3, HEAD_DIM))
+    if rope_positions is not None:
+        _check_tensor(rope_positions, "rope_positions", torch.int64, (M,))
+    if workspace is not None:
+        _check_tensor(workspace, "workspace", bf, (M, HIDDEN))
+    h = handle if handle is not None else default_handle(x.device.index)
+    mh3_preattn_run(h, stream, M, x, x_norm_weight, adaln_scale, adaln_scale.stride(0),
+                    adaln_shift, adaln_shift.stride(0), adaln_scale.shape[0], adaln_index,
+                    qkv_weight, q_norm_weight, k_norm_weight, rope_cos_sin, rope_cos_sin.shape[0],
+                    rope_positions, P, eps, qk_eps, workspace, out)
+    return out
+

@@ -1,0 +1,89 @@
+// common.cuh -- sizes, parameter blocks and small bf16 helpers shared by the
+// two kernels and the C-ABI host code of the pre-attention stage.
+#pragma once
+
+#include <cstdint>
+#include <cuda.h>
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+
+namespace mh3 {
+
+// Fixed by flashinfer.diffusion_ops.minimax_h3_bf16_pre_attention (Parameters:
+// x [M, 5376], qkv_weight [21504, 5376], q/k_norm_weight [128],
+// rope_cos_sin [S, 96], out [P, M, 56 // P, 3, 128]).
+constexpr int kHidden = 5376;
+constexpr int kHeads = 56;
+constexpr int kHeadDim = 128;
+constexpr int kQkvRows = 3 * kHeads * kHeadDim;  // 21504
+constexpr int kKindCols = kHeads * kHeadDim;     // 7168 columns per q/k/v kind
+constexpr int kRopeDims = 96;
+constexpr int kRopeHalf = kRopeDims / 2;  // 48
+
+// Device status codes (first writer wins): which bounded wait gave up.
+enum : int {
+  kStatusOk = 0,
+  kStatusProducerEmpty = 0x101,
+  kStatusMmaFull = 0x102,
+  kStatusMmaTmemEmpty = 0x103,
+  kStatusEpiTmemFull = 0x104,
+  kStatusDrain = 0x105,
+};
+
+struct NormAdalnParams {
+  const __nv_bfloat16* x;
+  const __nv_bfloat16* x_norm_weight;
+  const __nv_bfloat16* scale;
+  const __nv_bfloat16* shift;
+  int64_t scale_stride;  // elements
+  int64_t shift_stride;  // elements
+  int64_t rows;
+  const int64_t* index;
+  __nv_bfloat16* workspace;
+  int64_t M;
+  float eps;
+};
+
+struct QkvParams {
+  const int64_t* positions;  // [M] or nullptr (identity)
+  const __nv_bfloat16* cos_sin;  // [S, 96]
+  const __nv_bfloat16* q_norm_weight;  // [128]
+  const __nv_bfloat16* k_norm_weight;  // [128]
+  int64_t M;
+  int64_t S;
+  int heads_per_dst;  // 56 / P
+  float qk_eps;
+  int num_m_tiles;
+  int num_tiles;
+  int* status;  // device status word
+};
+
+cudaError_t launch_norm_adaln(const NormAdalnParams& p, cudaStream_t stream);
+
+// Tensor maps are encoded by the host for each call.
+struct QkvMaps {
+  CUtensorMap a;    // workspace [M, 5376], box 64 x 128, 128-B swizzle
+  CUtensorMap b;    // qkv_weight [21504, 5376], box 64 x 256, 128-B swizzle
+  CUtensorMap out;  // out as 4-D (d 128, slot 168/P, m M, dst P), box 64x1x32x1
+};
+
+int qkv_smem_bytes();
+cudaError_t qkv_prepare_device();  // raise the dynamic shared-memory limit
+cudaError_t launch_qkv(const QkvMaps& maps, const QkvParams& p, int grid, cudaStream_t stream);
+
+// --------------------------------------------------------------- bf16 bits
+__device__ __forceinline__ float bf16_lo(uint32_t u) { return __uint_as_float(u << 16); }
+__device__ __forceinline__ float bf16_hi(uint32_t u) { return __uint_as_float(u & 0xFFFF0000u); }
+
+// Round an FP32 value to bf16 (nearest-even) and return it as FP32.
+__device__ __forceinline__ float round_bf16(float v) {
+  return __bfloat162float(__float2bfloat16_rn(v));
+}
+
+// Two FP32 values -> packed bf16x2 (lo in bits 0-15), nearest-even.
+__device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
+  __nv_bfloat162 v = __floats2bfloat162_rn(lo, hi);
+  return *reinterpret_cast<uint32_t*>(&v);
+}
+
+}  // namespace mh3

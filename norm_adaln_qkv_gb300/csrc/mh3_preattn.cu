@@ -1,0 +1,400 @@
+// mh3_preattn.cu -- the C ABI of the pre-attention stage (declared in
+// include/mh3_preattn.h): argument validation, the handle, TMA tensor-map
+// encoding and the two launches.
+//
+// Validation follows flashinfer.diffusion_ops.minimax_h3_bf16_pre_attention,
+// Parameters: contiguous x/out/weights, AdaLN tables with unit column stride
+// and a row stride that is a multiple of 8 elements with a 16-byte aligned
+// base, rows >= 1, S >= 1, S >= M for identity positions, P in {1,2,4,8},
+// qk_eps None -> eps.  Index and position VALUES are never validated on the
+// host (no synchronising reduction): kernel 1 guards indices and kernel 2
+// clamps positions (Notes; Parameters: adaln_index, rope_positions).
+#include <cmath>
+#include <cstdarg>
+#include <cstdio>
+#include <cstring>
+#include <string>
+
+#include <cudaTypedefs.h>
+
+#include "mh3_preattn.h"
+#include "common.cuh"
+
+using namespace mh3;
+
+struct mh3_preattn_ctx {
+  int device = 0;
+  int num_sms = 0;
+  int* d_status = nullptr;
+  void* ws = nullptr;  // handle-owned workspace (grown on demand)
+  size_t ws_bytes = 0;
+};
+
+namespace {
+
+thread_local std::string g_last_error;
+
+int fail(int code, const char* fmt, ...) {
+  char buf[512];
+  va_list ap;
+  va_start(ap, fmt);
+  vsnprintf(buf, sizeof(buf), fmt, ap);
+  va_end(ap);
+  g_last_error = buf;
+  return code;
+}
+
+int cuda_fail(cudaError_t e, const char* what) {
+  return fail(MH3_ERR_CUDA, "%s: %s (%s)", what, cudaGetErrorName(e), cudaGetErrorString(e));
+}
+
+constexpr int64_t kMaxM = int64_t(1) << 30;  // TMA coordinates are 32-bit
+
+bool aligned(const void* p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
+
+int check_ptr(const void* p, const char* name, uintptr_t align) {
+  if (p == nullptr) return fail(MH3_ERR_INVALID_ARG, "%s is NULL", name);
+  if (!aligned(p, align))
+    return fail(MH3_ERR_ALIGNMENT, "%s must be %d-byte aligned", name, static_cast<int>(align));
+  return MH3_OK;
+}
+
+bool valid_eps(float e) { return std::isfinite(e) && e > 0.0f; }
+bool qk_eps_means_default(float e) { return std::isnan(e) || e < 0.0f; }
+
+int check_M(int64_t M) {
+  if (M < 0) return fail(MH3_ERR_INVALID_ARG, "M must be >= 0 (got %lld)", (long long)M);
+  if (M > kMaxM) return fail(MH3_ERR_INVALID_ARG, "M must be <= 2^30 (got %lld)", (long long)M);
+  return MH3_OK;
+}
+
+int check_norm_adaln_args(int64_t M, const mh3_bf16* x, const mh3_bf16* xw, const mh3_bf16* sc,
+                          int64_t sc_stride, const mh3_bf16* sh, int64_t sh_stride, int64_t rows,
+                          const int64_t* idx, float eps, const mh3_bf16* ws, bool ws_required) {
+  int rc;
+  if ((rc = check_M(M))) return rc;
+  if (rows < 1) return fail(MH3_ERR_INVALID_ARG, "rows must be >= 1 (got %lld)", (long long)rows);
+  if (!valid_eps(eps)) return fail(MH3_ERR_INVALID_ARG, "eps must be finite and > 0");
+  const char* names[2] = {"scale_row_stride", "shift_row_stride"};
+  const int64_t strides[2] = {sc_stride, sh_stride};
+  for (int i = 0; i < 2; ++i) {
+    if (strides[i] < kHidden)
+      return fail(MH3_ERR_INVALID_ARG, "%s must be >= 5376 (got %lld)", names[i],
+                  (long long)strides[i]);
+    if (strides[i] % 8 != 0)
+      return fail(MH3_ERR_ALIGNMENT, "%s must be a multiple of 8 elements (got %lld)", names[i],
+                  (long long)strides[i]);
+  }
+  if ((rc = check_ptr(xw, "x_norm_weight", 16))) return rc;
+  if ((rc = check_ptr(sc, "adaln_scale", 16))) return rc;
+  if ((rc = check_ptr(sh, "adaln_shift", 16))) return rc;
+  if (M == 0) return MH3_OK;
+  if ((rc = check_ptr(x, "x", 16))) return rc;
+  if ((rc = check_ptr(idx, "adaln_index", 8))) return rc;
+  if (ws_required || ws != nullptr)
+    if ((rc = check_ptr(ws, "workspace", 16))) return rc;
+  return MH3_OK;
+}
+
+int check_qkv_args(int64_t M, const mh3_bf16* W, const mh3_bf16* qw, const mh3_bf16* kw,
+                   const mh3_bf16* cs, int64_t S, const int64_t* pos, int P, const mh3_bf16* out) {
+  int rc;
+  if ((rc = check_M(M))) return rc;
+  if (!(P == 1 || P == 2 || P == 4 || P == 8))
+    return fail(MH3_ERR_INVALID_ARG, "P (ulysses_degree) must be 1, 2, 4 or 8 (got %d)", P);
+  if (S < 1) return fail(MH3_ERR_INVALID_ARG, "S must be >= 1 (got %lld)", (long long)S);
+  if (pos == nullptr && S < M)
+    return fail(MH3_ERR_INVALID_ARG,
+                "identity positions (NULL) need S >= M (S=%lld, M=%lld)", (long long)S,
+                (long long)M);
+  if ((rc = check_ptr(W, "qkv_weight", 16))) return rc;
+  if ((rc = check_ptr(qw, "q_norm_weight", 2))) return rc;
+  if ((rc = check_ptr(kw, "k_norm_weight", 2))) return rc;
+  if ((rc = check_ptr(cs, "rope_cos_sin", 16))) return rc;
+  if (M == 0) return MH3_OK;
+  if (pos != nullptr && !aligned(pos, 8))
+    return fail(MH3_ERR_ALIGNMENT, "rope_positions must be 8-byte aligned");
+  if ((rc = check_ptr(out, "out", 16))) return rc;
+  return MH3_OK;
+}
+
+int check_handle(mh3_preattn_t h) {
+  if (h == nullptr) return fail(MH3_ERR_INVALID_ARG, "handle is NULL");
+  int dev = -1;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return cuda_fail(e, "cudaGetDevice");
+  if (dev != h->device)
+    return fail(MH3_ERR_INVALID_ARG, "current device %d differs from the handle's device %d", dev,
+                h->device);
+  return MH3_OK;
+}
+
+PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
+  static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+  if (fn == nullptr) {
+    void* p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault,
+                                         &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
+  }
+  return fn;
+}
+
+int encode_maps(QkvMaps& maps, int64_t M, const mh3_bf16* ws, const mh3_bf16* W, int P,
+                mh3_bf16* out) {
+  PFN_cuTensorMapEncodeTiled_v12000 enc = encode_fn();
+  if (enc == nullptr) return fail(MH3_ERR_CUDA, "cuTensorMapEncodeTiled entry point not found");
+  const cuuint32_t unit[4] = {1, 1, 1, 1};
+  {
+    const cuuint64_t dims[2] = {static_cast<cuuint64_t>(kHidden), static_cast<cuuint64_t>(M)};
+    const cuuint64_t strides[1] = {static_cast<cuuint64_t>(kHidden) * 2};
+    const cuuint32_t box[2] = {64, 128};
+    CUresult r = enc(&maps.a, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<mh3_bf16*>(ws), dims,
+                     strides, box, unit, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                     CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    if (r != CUDA_SUCCESS) return fail(MH3_ERR_CUDA, "tensor map (workspace) failed: %d", (int)r);
+  }
+  {
+    const cuuint64_t dims[2] = {static_cast<cuuint64_t>(kHidden),
+                                static_cast<cuuint64_t>(kQkvRows)};
+    const cuuint64_t strides[1] = {static_cast<cuuint64_t>(kHidden) * 2};
+    const cuuint32_t box[2] = {64, 256};
+    CUresult r = enc(&maps.b, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<mh3_bf16*>(W), dims,
+                     strides, box, unit, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                     CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    if (r != CUDA_SUCCESS) return fail(MH3_ERR_CUDA, "tensor map (qkv_weight) failed: %d", (int)r);
+  }
+  {
+    // out[P, M, 56/P, 3, 128] as (d, slot = hl*3 + kind, m, dst)
+    const int64_t slots = 3 * (kHeads / P);
+    const cuuint64_t dims[4] = {static_cast<cuuint64_t>(kHeadDim), static_cast<cuuint64_t>(slots),
+                                static_cast<cuuint64_t>(M), static_cast<cuuint64_t>(P)};
+    const cuuint64_t strides[3] = {static_cast<cuuint64_t>(kHeadDim) * 2,
+                                   static_cast<cuuint64_t>(slots) * kHeadDim * 2,
+                                   static_cast<cuuint64_t>(M) * slots * kHeadDim * 2};
+    const cuuint32_t box[4] = {64, 1, 32, 1};
+    CUresult r = enc(&maps.out, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, out, dims, strides, box, unit,
+                     CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                     CU_TENSOR_MAP_L2_PROMOTION_NONE, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    if (r != CUDA_SUCCESS) return fail(MH3_ERR_CUDA, "tensor map (out) failed: %d", (int)r);
+  }
+  return MH3_OK;
+}
+
+int launch_stage1(cudaStream_t s, int64_t M, const mh3_bf16* x, const mh3_bf16* xw,
+                  const mh3_bf16* sc, int64_t sc_stride, const mh3_bf16* sh, int64_t sh_stride,
+                  int64_t rows, const int64_t* idx, float eps, mh3_bf16* ws) {
+  NormAdalnParams p;
+  p.x = reinterpret_cast<const __nv_bfloat16*>(x);
+  p.x_norm_weight = reinterpret_cast<const __nv_bfloat16*>(xw);
+  p.scale = reinterpret_cast<const __nv_bfloat16*>(sc);
+  p.shift = reinterpret_cast<const __nv_bfloat16*>(sh);
+  p.scale_stride = sc_stride;
+  p.shift_stride = sh_stride;
+  p.rows = rows;
+  p.index = idx;
+  p.workspace = reinterpret_cast<__nv_bfloat16*>(ws);
+  p.M = M;
+  p.eps = eps;
+  cudaError_t e = launch_norm_adaln(p, s);
+  if (e != cudaSuccess) return cuda_fail(e, "norm/AdaLN launch");
+  return MH3_OK;
+}
+
+int launch_stage2(mh3_preattn_t h, cudaStream_t s, int64_t M, const mh3_bf16* ws,
+                  const mh3_bf16* W, const mh3_bf16* qw, const mh3_bf16* kw, const mh3_bf16* cs,
+                  int64_t S, const int64_t* pos, int P, float qk_eps, mh3_bf16* out) {
+  QkvMaps maps;
+  int rc = encode_maps(maps, M, ws, W, P, out);
+  if (rc) return rc;
+  QkvParams p;
+  p.positions = pos;
+  p.cos_sin = reinterpret_cast<const __nv_bfloat16*>(cs);
+  p.q_norm_weight = reinterpret_cast<const __nv_bfloat16*>(qw);
+  p.k_norm_weight = reinterpret_cast<const __nv_bfloat16*>(kw);
+  p.M = M;
+  p.S = S;
+  p.heads_per_dst = kHeads / P;
+  p.qk_eps = qk_eps;
+  p.num_m_tiles = static_cast<int>((M + 127) / 128);
+  p.num_tiles = p.num_m_tiles * (kQkvRows / 256);
+  p.status = h->d_status;
+  const int grid = p.num_tiles < h->num_sms ? p.num_tiles : h->num_sms;
+  cudaError_t e = launch_qkv(maps, p, grid, s);
+  if (e != cudaSuccess) return cuda_fail(e, "QKV GEMM launch");
+  return MH3_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+const char* mh3_preattn_last_error(void) { return g_last_error.c_str(); }
+
+size_t mh3_preattn_workspace_bytes(int64_t M) {
+  return M <= 0 ? 0 : static_cast<size_t>(M) * kHidden * 2;
+}
+
+size_t mh3_preattn_out_bytes(int64_t M) {
+  return M <= 0 ? 0 : static_cast<size_t>(M) * kQkvRows * 2;
+}
+
+int mh3_preattn_create(mh3_preattn_t* handle, int device) {
+  if (handle == nullptr) return fail(MH3_ERR_INVALID_ARG, "handle pointer is NULL");
+  *handle = nullptr;
+  cudaError_t e = cudaSetDevice(device);
+  if (e != cudaSuccess) return cuda_fail(e, "cudaSetDevice");
+  cudaDeviceProp prop;
+  e = cudaGetDeviceProperties(&prop, device);
+  if (e != cudaSuccess) return cuda_fail(e, "cudaGetDeviceProperties");
+  if (!(prop.major == 10 && prop.minor == 3))
+    return fail(MH3_ERR_UNSUPPORTED, "device %d is sm_%d%d; this library is built for sm_103a",
+                device, prop.major, prop.minor);
+  if (static_cast<int>(prop.sharedMemPerBlockOptin) < qkv_smem_bytes())
+    return fail(MH3_ERR_UNSUPPORTED, "device allows %zu B of shared memory per block, need %d",
+                prop.sharedMemPerBlockOptin, qkv_smem_bytes());
+  e = qkv_prepare_device();
+  if (e != cudaSuccess) return cuda_fail(e, "cudaFuncSetAttribute");
+  mh3_preattn_ctx* h = new mh3_preattn_ctx();
+  h->device = device;
+  h->num_sms = prop.multiProcessorCount;
+  e = cudaMalloc(&h->d_status, sizeof(int));
+  if (e == cudaSuccess) e = cudaMemset(h->d_status, 0, sizeof(int));
+  if (e != cudaSuccess) {
+    if (h->d_status) cudaFree(h->d_status);
+    delete h;
+    return cuda_fail(e, "allocating the status word");
+  }
+  *handle = h;
+  return MH3_OK;
+}
+
+int mh3_preattn_destroy(mh3_preattn_t h) {
+  if (h == nullptr) return MH3_OK;
+  int rc = MH3_OK;
+  if (h->ws) {
+    cudaError_t e = cudaFree(h->ws);
+    if (e != cudaSuccess) rc = cuda_fail(e, "freeing the handle workspace");
+  }
+  if (h->d_status) {
+    cudaError_t e = cudaFree(h->d_status);
+    if (e != cudaSuccess && rc == MH3_OK) rc = cuda_fail(e, "freeing the status word");
+  }
+  delete h;
+  return rc;
+}
+
+int mh3_preattn_validate(int64_t M, const mh3_bf16* x, const mh3_bf16* x_norm_weight,
+                         const mh3_bf16* adaln_scale, int64_t scale_row_stride,
+                         const mh3_bf16* adaln_shift, int64_t shift_row_stride, int64_t rows,
+                         const int64_t* adaln_index, const mh3_bf16* qkv_weight,
+                         const mh3_bf16* q_norm_weight, const mh3_bf16* k_norm_weight,
+                         const mh3_bf16* rope_cos_sin, int64_t S, const int64_t* rope_positions,
+                         int P, float eps, float qk_eps, const mh3_bf16* workspace,
+                         const mh3_bf16* out) {
+  int rc = check_norm_adaln_args(M, x, x_norm_weight, adaln_scale, scale_row_stride, adaln_shift,
+                                 shift_row_stride, rows, adaln_index, eps, workspace, false);
+  if (rc) return rc;
+  if (!qk_eps_means_default(qk_eps) && !valid_eps(qk_eps))
+    return fail(MH3_ERR_INVALID_ARG, "qk_eps must be finite and > 0 (or negative/NaN for eps)");
+  return check_qkv_args(M, qkv_weight, q_norm_weight, k_norm_weight, rope_cos_sin, S,
+                        rope_positions, P, out);
+}
+
+int mh3_preattn_run(mh3_preattn_t h, void* stream, int64_t M, const mh3_bf16* x,
+                    const mh3_bf16* x_norm_weight, const mh3_bf16* adaln_scale,
+                    int64_t scale_row_stride, const mh3_bf16* adaln_shift,
+                    int64_t shift_row_stride, int64_t rows, const int64_t* adaln_index,
+                    const mh3_bf16* qkv_weight, const mh3_bf16* q_norm_weight,
+                    const mh3_bf16* k_norm_weight, const mh3_bf16* rope_cos_sin, int64_t S,
+                    const int64_t* rope_positions, int P, float eps, float qk_eps,
+                    mh3_bf16* workspace, mh3_bf16* out) {
+  int rc = check_handle(h);
+  if (rc) return rc;
+  rc = mh3_preattn_validate(M, x, x_norm_weight, adaln_scale, scale_row_stride, adaln_shift,
+                            shift_row_stride, rows, adaln_index, qkv_weight, q_norm_weight,
+                            k_norm_weight, rope_cos_sin, S, rope_positions, P, eps, qk_eps,
+                            workspace, out);
+  if (rc) return rc;
+  if (M == 0) return MH3_OK;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  const float qk = qk_eps_means_default(qk_eps) ? eps : qk_eps;
+  if (workspace == nullptr) {
+    const size_t need = mh3_preattn_workspace_bytes(M);
+    if (h->ws_bytes < need) {
+      if (h->ws) {
+        cudaError_t e = cudaFreeAsync(h->ws, s);
+        h->ws = nullptr;
+        h->ws_bytes = 0;
+        if (e != cudaSuccess) return cuda_fail(e, "cudaFreeAsync (workspace)");
+      }
+      cudaError_t e = cudaMallocAsync(&h->ws, need, s);
+      if (e != cudaSuccess) {
+        h->ws = nullptr;
+        return fail(MH3_ERR_OOM, "cudaMallocAsync of %zu B workspace failed: %s", need,
+                    cudaGetErrorString(e));
+      }
+      h->ws_bytes = need;
+    }
+    workspace = static_cast<mh3_bf16*>(h->ws);
+  }
+  rc = launch_stage1(s, M, x, x_norm_weight, adaln_scale, scale_row_stride, adaln_shift,
+                     shift_row_stride, rows, adaln_index, eps, workspace);
+  if (rc) return rc;
+  return launch_stage2(h, s, M, workspace, qkv_weight, q_norm_weight, k_norm_weight,
+                       rope_cos_sin, S, rope_positions, P, qk, out);
+}
+
+int mh3_preattn_norm_adaln(mh3_preattn_t h, void* stream, int64_t M, const mh3_bf16* x,
+                           const mh3_bf16* x_norm_weight, const mh3_bf16* adaln_scale,
+                           int64_t scale_row_stride, const mh3_bf16* adaln_shift,
+                           int64_t shift_row_stride, int64_t rows, const int64_t* adaln_index,
+                           float eps, mh3_bf16* workspace) {
+  int rc = check_handle(h);
+  if (rc) return rc;
+  rc = check_norm_adaln_args(M, x, x_norm_weight, adaln_scale, scale_row_stride, adaln_shift,
+                             shift_row_stride, rows, adaln_index, eps, workspace, true);
+  if (rc) return rc;
+  if (M == 0) return MH3_OK;
+  return launch_stage1(static_cast<cudaStream_t>(stream), M, x, x_norm_weight, adaln_scale,
+                       scale_row_stride, adaln_shift, shift_row_stride, rows, adaln_index, eps,
+                       workspace);
+}
+
+int mh3_preattn_qkv(mh3_preattn_t h, void* stream, int64_t M, const mh3_bf16* workspace,
+                    const mh3_bf16* qkv_weight, const mh3_bf16* q_norm_weight,
+                    const mh3_bf16* k_norm_weight, const mh3_bf16* rope_cos_sin, int64_t S,
+                    const int64_t* rope_positions, int P, float qk_eps, mh3_bf16* out) {
+  int rc = check_handle(h);
+  if (rc) return rc;
+  if (!valid_eps(qk_eps)) return fail(MH3_ERR_INVALID_ARG, "qk_eps must be finite and > 0");
+  rc = check_qkv_args(M, qkv_weight, q_norm_weight, k_norm_weight, rope_cos_sin, S,
+                      rope_positions, P, out);
+  if (rc) return rc;
+  if (M == 0) return MH3_OK;
+  if ((rc = check_ptr(workspace, "workspace", 16))) return rc;
+  return launch_stage2(h, static_cast<cudaStream_t>(stream), M, workspace, qkv_weight,
+                       q_norm_weight, k_norm_weight, rope_cos_sin, S, rope_positions, P, qk_eps,
+                       out);
+}
+
+int mh3_preattn_device_status(mh3_preattn_t h, void* stream, int* device_code) {
+  if (h == nullptr || device_code == nullptr)
+    return fail(MH3_ERR_INVALID_ARG, "handle or device_code is NULL");
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  cudaError_t e = cudaStreamSynchronize(s);
+  if (e != cudaSuccess) return cuda_fail(e, "cudaStreamSynchronize");
+  int v = 0;
+  e = cudaMemcpy(&v, h->d_status, sizeof(int), cudaMemcpyDeviceToHost);
+  if (e != cudaSuccess) return cuda_fail(e, "reading the status word");
+  if (v != 0) {
+    e = cudaMemset(h->d_status, 0, sizeof(int));
+    if (e != cudaSuccess) return cuda_fail(e, "clearing the status word");
+  }
+  *device_code = v;
+  return MH3_OK;
+}
+
+}  // extern "C"
