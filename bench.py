@@ -146,7 +146,7 @@ def run_reference(args, world, rank):
         return
     import oracle
     from norm_adaln_qkv_gb300.inputs import make_workload
-    wl = make_workload(WORKLOAD)
+    wl = make_workload(args.workload)
     sc, sh = wl.table_views()
     rows_per_step = args.ref_rows
     M = wl.M
@@ -185,20 +185,23 @@ def run_reference(args, world, rank):
 
 
 # ------------------------------------------------------------------ our arm
-def cpu_baseline(wl, rows: int):
-    """The oracle as it stands, on a bounded sample of the bench workload."""
+def cpu_baseline(wl, rows: int, chunk: int = 4096):
+    """The oracle as it stands, on the first ``rows`` tokens of the bench
+    workload (in chunks of ``chunk`` tokens to bound host memory)."""
     import oracle
     sc, sh = wl.table_views()
-    toks = list(range(0, rows))
+    rows = min(rows, wl.M)
     t = time.perf_counter()
-    oracle.pre_attention_tokens(
-        wl.x, wl.x_norm_weight, sc, sh, wl.adaln_index, wl.qkv_weight, wl.q_norm_weight,
-        wl.k_norm_weight, wl.rope_cos_sin, eps=wl.spec.eps, qk_eps=wl.spec.qk_eps,
-        rope_positions=wl.rope_positions, tokens=toks)
+    for t0 in range(0, rows, chunk):
+        oracle.pre_attention_tokens(
+            wl.x, wl.x_norm_weight, sc, sh, wl.adaln_index, wl.qkv_weight, wl.q_norm_weight,
+            wl.k_norm_weight, wl.rope_cos_sin, eps=wl.spec.eps, qk_eps=wl.spec.qk_eps,
+            rope_positions=wl.rope_positions, tokens=range(t0, min(rows, t0 + chunk)))
     el = time.perf_counter() - t
+    what = (f"all {rows} tokens" if rows == wl.M else
+            f"first {rows} tokens of M={wl.M}, scaled by M/{rows}")
     return {"value": el * (wl.M / rows) * 1e6, "unit": UNIT, "cores": torch.get_num_threads(),
-            "kind": "oracle",
-            "sample": f"first {rows} tokens of M={wl.M} in {el:.1f} s, scaled by M/{rows}"}
+            "kind": "oracle", "sample": f"{what}, {el:.1f} s of CPU time"}
 
 
 def run_ours(args, world, rank, local):
@@ -206,7 +209,7 @@ def run_ours(args, world, rank, local):
     from norm_adaln_qkv_gb300.inputs import make_workload
 
     # Oracle CPU baseline first (rank 0 only, N = 1 only), before any CUDA work.
-    wl = make_workload(WORKLOAD)
+    wl = make_workload(args.workload)
     cpu = cpu_baseline(wl, args.cpu_rows) if (rank == 0 and world == 1 and args.cpu_rows > 0) \
         else None
 
@@ -335,7 +338,7 @@ def run_ours(args, world, rank, local):
 
     # ---- the 4096-token block named by the metric (same stage, P = 2)
     also = None
-    if not args.skip_also:
+    if not args.skip_also and args.workload != ALSO:
         wl2 = make_workload(ALSO)
         d2 = prepare(wl2)
         for _ in range(3):
@@ -406,11 +409,13 @@ def main():
     ap.add_argument("--steps", type=int, default=30)
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
-    ap.add_argument("--cpu-rows", type=int, default=256,
+    ap.add_argument("--cpu-rows", type=int, default=32760,
                     help="tokens of the oracle CPU-baseline sample (0 disables)")
-    ap.add_argument("--ref-rows", type=int, default=32,
+    ap.add_argument("--ref-rows", type=int, default=1024,
                     help="tokens per step of the reference (oracle) arm")
     ap.add_argument("--skip-also", action="store_true", help="skip the M=4096 side measurement")
+    ap.add_argument("--workload", default=WORKLOAD, choices=["c0", "c1", "c2", "c3", "c4"],
+                    help="seeded workload (default: the M=32760 production sequence)")
     args = ap.parse_args()
     world, rank, local = _dist()
     if args.impl == "reference":
