@@ -166,6 +166,37 @@ int mh3_preattn_qkv(mh3_preattn_t handle, void* stream, int64_t M, const mh3_bf1
  * MH3_ERR_CUDA if the synchronisation or the copy failed. */
 int mh3_preattn_device_status(mh3_preattn_t handle, void* stream, int* device_code);
 
+/* The whole stage without any allocation, for callers that cannot call
+ * cudaMalloc (a custom allocator owns all device memory, or allocation is
+ * forbidden after start-up).  There is no counterpart of this call on the
+ * pages; it is mh3_preattn_run with the workspace taken from a static device
+ * array instead of the caller or a handle.
+ *
+ * The array holds at most 1024 tokens (1024 x 5376 bf16 = 10.5 MiB); it is
+ * reserved on every GPU that loads the library and kept until the process
+ * exits.  M > 1024 is rejected with MH3_ERR_INVALID_ARG before anything is
+ * launched.  No cudaMalloc, cudaFree or other allocating call is made.
+ *
+ * The first call on a device does a one-time set-up on that device (it looks
+ * up the array's device address, raises the GEMM's shared-memory limit and
+ * reads the SM count); make that first call before any stream capture.
+ * Every call uses the same array, which keeps the last call's contents;
+ * calls that overlap on the GPU (other streams, other threads) race on it.
+ *
+ *   device_status  caller-owned device int, 4-byte aligned: set to 0 on
+ *                  `stream` before the kernels run, then to a nonzero code if
+ *                  a kernel's bounded wait gives up (read it after a sync).
+ *   other arguments as in mh3_preattn_run (no handle, no workspace).
+ */
+int mh3_preattn_run_noalloc(void* stream, int64_t M, const mh3_bf16* x,
+                            const mh3_bf16* x_norm_weight, const mh3_bf16* adaln_scale,
+                            int64_t scale_row_stride, const mh3_bf16* adaln_shift,
+                            int64_t shift_row_stride, int64_t rows, const int64_t* adaln_index,
+                            const mh3_bf16* qkv_weight, const mh3_bf16* q_norm_weight,
+                            const mh3_bf16* k_norm_weight, const mh3_bf16* rope_cos_sin,
+                            int64_t S, const int64_t* rope_positions, int P, float eps,
+                            float qk_eps, mh3_bf16* out, int* device_status);
+
 /* Message of the calling thread's last failed call ("" if none). */
 const char* mh3_preattn_last_error(void);
 

@@ -32,7 +32,7 @@ STATUS = {0: "MH3_OK", 1: "MH3_ERR_INVALID_ARG", 2: "MH3_ERR_ALIGNMENT", 3: "MH3
 EXPORTS = ("mh3_preattn_create", "mh3_preattn_destroy", "mh3_preattn_workspace_bytes",
            "mh3_preattn_out_bytes", "mh3_preattn_validate", "mh3_preattn_run",
            "mh3_preattn_norm_adaln", "mh3_preattn_qkv", "mh3_preattn_device_status",
-           "mh3_preattn_last_error")
+           "mh3_preattn_last_error", "mh3_preattn_run_noalloc")
 
 _vp = ctypes.c_void_p
 _i64 = ctypes.c_int64
@@ -53,6 +53,8 @@ _SIGS = {
     "mh3_preattn_qkv": (_i32, [_vp, _vp, _i64, _vp, _vp, _vp, _vp, _vp, _i64, _vp, _i32, _f32, _vp]),
     "mh3_preattn_device_status": (_i32, [_vp, _vp, ctypes.POINTER(_i32)]),
     "mh3_preattn_last_error": (ctypes.c_char_p, []),
+    "mh3_preattn_run_noalloc": (_i32, [_vp, _i64, _vp, _vp, _vp, _i64, _vp, _i64, _i64, _vp, _vp,
+                                       _vp, _vp, _vp, _i64, _vp, _i32, _f32, _f32, _vp, _vp]),
 }
 
 _lib = None
@@ -179,6 +181,20 @@ def mh3_preattn_run(handle: Handle, stream, M, x, x_norm_weight, adaln_scale, sc
         _ptr(qkv_weight), _ptr(q_norm_weight), _ptr(k_norm_weight), _ptr(rope_cos_sin), S,
         _ptr(rope_positions), P, float(eps), _qk_eps_arg(qk_eps), _ptr(workspace), _ptr(out)),
         "mh3_preattn_run")
+
+
+def mh3_preattn_run_noalloc(stream, M, x, x_norm_weight, adaln_scale, scale_row_stride,
+                            adaln_shift, shift_row_stride, rows, adaln_index, qkv_weight,
+                            q_norm_weight, k_norm_weight, rope_cos_sin, S, rope_positions, P, eps,
+                            qk_eps, out, device_status) -> None:
+    """The stage with the library's static workspace (M <= 1024); allocates
+    nothing.  ``device_status`` is a caller-owned device int32 tensor."""
+    _check(load().mh3_preattn_run_noalloc(
+        _stream_ptr(stream), M, _ptr(x), _ptr(x_norm_weight), _ptr(adaln_scale),
+        scale_row_stride, _ptr(adaln_shift), shift_row_stride, rows, _ptr(adaln_index),
+        _ptr(qkv_weight), _ptr(q_norm_weight), _ptr(k_norm_weight), _ptr(rope_cos_sin), S,
+        _ptr(rope_positions), P, float(eps), _qk_eps_arg(qk_eps), _ptr(out),
+        _ptr(device_status)), "mh3_preattn_run_noalloc")
 
 
 def mh3_preattn_norm_adaln(handle: Handle, stream, M, x, x_norm_weight, adaln_scale,

@@ -13,6 +13,7 @@
 #include <cstdarg>
 #include <cstdio>
 #include <cstring>
+#include <mutex>
 #include <string>
 
 #include <cudaTypedefs.h>
@@ -398,3 +399,105 @@ int mh3_preattn_device_status(mh3_preattn_t h, void* stream, int* device_code) {
 }
 
 }  // extern "C"
+
+// ------------------------------------------------------ no-allocation variant
+// The whole stage for callers that cannot call cudaMalloc (for example code
+// running where a custom allocator owns all device memory, or inside a
+// process whose allocation calls are forbidden after start-up): the BF16
+// workspace lives in the file-scope array below, which the CUDA module
+// reserves when it loads, so the call itself allocates nothing.
+namespace {
+
+constexpr int64_t kNoAllocMaxM = 1024;  // 1024 x 5376 bf16 = 10.5 MiB per device
+static __device__ __align__(256) mh3_bf16 g_noalloc_workspace[kNoAllocMaxM * kHidden];
+
+constexpr int kNoAllocMaxDevices = 64;
+struct NoAllocDevice {
+  std::once_flag once;
+  int rc = MH3_OK;
+  std::string err;
+  mh3_bf16* workspace = nullptr;  // device address of g_noalloc_workspace
+  int num_sms = 0;
+};
+NoAllocDevice g_noalloc_dev[kNoAllocMaxDevices];
+
+// Once per device, with that device current: the device address of the
+// array (the host-side name is only a stand-in), the GEMM's shared-memory
+// limit, and the SM count.
+void noalloc_setup(int dev, NoAllocDevice& d) {
+  cudaDeviceProp prop;
+  cudaError_t e = cudaGetDeviceProperties(&prop, dev);
+  if (e != cudaSuccess) {
+    d.rc = cuda_fail(e, "cudaGetDeviceProperties");
+  } else if (!(prop.major == 10 && prop.minor == 3)) {
+    d.rc = fail(MH3_ERR_UNSUPPORTED, "device %d is sm_%d%d; this library is built for sm_103a",
+                dev, prop.major, prop.minor);
+  } else if ((e = cudaGetSymbolAddress(reinterpret_cast<void**>(&d.workspace),
+                                       g_noalloc_workspace)) != cudaSuccess) {
+    d.rc = cuda_fail(e, "cudaGetSymbolAddress (static workspace)");
+  } else if ((e = qkv_prepare_device()) != cudaSuccess) {
+    d.rc = cuda_fail(e, "cudaFuncSetAttribute");
+  } else {
+    d.num_sms = prop.multiProcessorCount;
+    d.rc = MH3_OK;
+  }
+  if (d.rc != MH3_OK) d.err = g_last_error;
+}
+
+}  // namespace
+
+extern "C" int mh3_preattn_run_noalloc(
+    void* stream, int64_t M, const mh3_bf16* x, const mh3_bf16* x_norm_weight,
+    const mh3_bf16* adaln_scale, int64_t scale_row_stride, const mh3_bf16* adaln_shift,
+    int64_t shift_row_stride, int64_t rows, const int64_t* adaln_index,
+    const mh3_bf16* qkv_weight, const mh3_bf16* q_norm_weight, const mh3_bf16* k_norm_weight,
+    const mh3_bf16* rope_cos_sin, int64_t S, const int64_t* rope_positions, int P, float eps,
+    float qk_eps, mh3_bf16* out, int* device_status) {
+  if (M > kNoAllocMaxM)
+    return fail(MH3_ERR_INVALID_ARG,
+                "M=%lld exceeds the %lld tokens the static workspace of "
+                "mh3_preattn_run_noalloc holds; use mh3_preattn_run",
+                (long long)M, (long long)kNoAllocMaxM);
+  int rc = mh3_preattn_validate(M, x, x_norm_weight, adaln_scale, scale_row_stride, adaln_shift,
+                                shift_row_stride, rows, adaln_index, qkv_weight, q_norm_weight,
+                                k_norm_weight, rope_cos_sin, S, rope_positions, P, eps, qk_eps,
+                                nullptr, out);
+  if (rc) return rc;
+  if (M == 0) return MH3_OK;
+  if ((rc = check_ptr(device_status, "device_status", 4))) return rc;
+  int dev = -1;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return cuda_fail(e, "cudaGetDevice");
+  if (dev < 0 || dev >= kNoAllocMaxDevices)
+    return fail(MH3_ERR_UNSUPPORTED, "device index %d out of range", dev);
+  NoAllocDevice& d = g_noalloc_dev[dev];
+  std::call_once(d.once, noalloc_setup, dev, std::ref(d));
+  if (d.rc != MH3_OK) return fail(d.rc, "%s", d.err.c_str());
+
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  // the timeout code must start at zero for this call
+  e = cudaMemsetAsync(device_status, 0, sizeof(int), s);
+  if (e != cudaSuccess) return cuda_fail(e, "cudaMemsetAsync (device_status)");
+  rc = launch_stage1(s, M, x, x_norm_weight, adaln_scale, scale_row_stride, adaln_shift,
+                     shift_row_stride, rows, adaln_index, eps, d.workspace);
+  if (rc) return rc;
+  QkvMaps maps;
+  rc = encode_maps(maps, M, d.workspace, qkv_weight, P, out);
+  if (rc) return rc;
+  QkvParams p;
+  p.positions = rope_positions;
+  p.cos_sin = reinterpret_cast<const __nv_bfloat16*>(rope_cos_sin);
+  p.q_norm_weight = reinterpret_cast<const __nv_bfloat16*>(q_norm_weight);
+  p.k_norm_weight = reinterpret_cast<const __nv_bfloat16*>(k_norm_weight);
+  p.M = M;
+  p.S = S;
+  p.heads_per_dst = kHeads / P;
+  p.qk_eps = qk_eps_means_default(qk_eps) ? eps : qk_eps;
+  p.num_m_tiles = static_cast<int>((M + 127) / 128);
+  p.num_tiles = p.num_m_tiles * (kQkvRows / 256);
+  p.status = device_status;
+  const int grid = p.num_tiles < d.num_sms ? p.num_tiles : d.num_sms;
+  e = launch_qkv(maps, p, grid, s);
+  if (e != cudaSuccess) return cuda_fail(e, "QKV GEMM launch");
+  return MH3_OK;
+}
