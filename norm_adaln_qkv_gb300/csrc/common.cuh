@@ -28,6 +28,7 @@ enum : int {
   kStatusMmaTmemEmpty = 0x103,
   kStatusEpiTmemFull = 0x104,
   kStatusDrain = 0x105,
+  kStatusRowFull = 0x106,
 };
 
 struct NormAdalnParams {
@@ -42,6 +43,7 @@ struct NormAdalnParams {
   __nv_bfloat16* workspace;
   int64_t M;
   float eps;
+  int* status;  // device status word (bounded-wait timeouts)
 };
 
 struct QkvParams {
@@ -58,7 +60,8 @@ struct QkvParams {
   int* status;  // device status word
 };
 
-cudaError_t launch_norm_adaln(const NormAdalnParams& p, cudaStream_t stream);
+// num_sms: SM count of the device (the kernel is persistent over rows).
+cudaError_t launch_norm_adaln(const NormAdalnParams& p, int num_sms, cudaStream_t stream);
 
 // Tensor maps are encoded by the host for each call.
 struct QkvMaps {

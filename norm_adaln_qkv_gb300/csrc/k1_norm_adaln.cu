@@ -8,116 +8,190 @@
 // which flashinfer.diffusion_ops.minimax_h3_bf16_pre_attention runs as its
 // first launch (summary; Parameters: adaln_scale, adaln_index; Notes).
 //
-// Design (HBM-bound row streaming): one CTA of 224 threads per token row.
-// A row is 5376 bf16 = 672 16-byte vectors = 3 per thread, loaded up front
-// with evict-first hints (x is read exactly once); many small CTAs per SM keep
-// ~100 KB of loads in flight per SM.  The sum of squares is FP32: per-thread
-// partial sums, a butterfly shuffle per warp, then the seven warp sums added
-// in one fixed order by every thread, so all threads hold the same total.
-// r = 1 / sqrt(ss/H + eps) and every elementwise step use IEEE
-// round-to-nearest FP32 operations in the formula's order with no contraction
-// into FMA.  The guard is an int64 compare: a bad index writes +0.0 and never
-// forms a table address.  Workspace stores keep the default write-back policy
-// so the GEMM that follows finds the rows in L2 when they fit.
+// Design (HBM-bound row streaming).  Persistent CTAs of 224 threads, several
+// per SM; CTA b handles rows b, b + G, b + 2G, ...  One thread streams whole
+// x rows (10752 B) into a ring of shared-memory row buffers with bulk async
+// copies (evict-first: x is read exactly once), so the bytes in flight per SM
+// are set by the ring depth, not by registers.  Each thread then owns 3
+// 16-byte vectors of the row.  The sum of squares is FP32: per-thread
+// partials, a butterfly shuffle per warp, then the seven warp sums added in
+// one fixed order by every thread.  r = 1 / sqrt(ss/H + eps) uses IEEE
+// division and square root; the elementwise steps are packed two-lane FP32
+// operations (each lane one IEEE round-to-nearest operation, in the
+// formula's order, never contracted into an FMA) and one bf16x2 add for
+// bf16(1 + scale).  The guard is an int64 compare: a bad index writes +0.0
+// and never forms a table address.  Workspace stores keep the default
+// write-back policy so the GEMM that follows finds the rows in L2 when they
+// fit.  The ring wait is bounded (2 s) and records a status code instead of
+// hanging.
 #include "common.cuh"
+#include "ptx.cuh"
 
 namespace mh3 {
 
 namespace {
 
-constexpr int kVecPerRow = kHidden / 8;  // 672
-constexpr int kThreads = 224;             // 7 warps
+#ifndef MH3_K1_STAGES
+#define MH3_K1_STAGES 4
+#endif
+#ifndef MH3_K1_CTAS_PER_SM
+#define MH3_K1_CTAS_PER_SM 4
+#endif
+
+constexpr int kRowBytes = kHidden * 2;               // 10752
+constexpr int kVecPerRow = kHidden / 8;              // 672 16-byte vectors
+constexpr int kThreads = 224;                        // 7 warps
 constexpr int kWarps = kThreads / 32;
 constexpr int kVecPerThread = kVecPerRow / kThreads;  // 3
+constexpr int kStages = MH3_K1_STAGES;
+constexpr int kCtasPerSm = MH3_K1_CTAS_PER_SM;
+constexpr uint64_t kWaitLimitNs = 2000000000ull;
 static_assert(kVecPerRow % kThreads == 0, "row must split evenly over the CTA");
+static_assert(kRowBytes % 16 == 0, "bulk copies move multiples of 16 bytes");
 
-__device__ __forceinline__ uint4 ld_stream_v4(const uint4* p) { return __ldcs(p); }
-
-__device__ __forceinline__ void sq_acc(uint32_t u, float& a0, float& a1) {
-  const float lo = bf16_lo(u), hi = bf16_hi(u);
-  // bf16 squares are exact in FP32, so the fused form equals mul-then-add.
-  a0 = __fmaf_rn(lo, lo, a0);
-  a1 = __fmaf_rn(hi, hi, a1);
-}
-
-// One bf16 pair of the AdaLN output, in the formula's rounding order.
-__device__ __forceinline__ uint32_t adaln_pair(uint32_t xu, uint32_t wu, uint32_t scu, uint32_t shu,
-                                               float r) {
-  float out[2];
-#pragma unroll
-  for (int h = 0; h < 2; ++h) {
-    const float xv = h ? bf16_hi(xu) : bf16_lo(xu);
-    const float wv = h ? bf16_hi(wu) : bf16_lo(wu);
-    const float sc = h ? bf16_hi(scu) : bf16_lo(scu);
-    const float sh = h ? bf16_hi(shu) : bf16_lo(shu);
-    const float n = round_bf16(__fmul_rn(__fmul_rn(xv, r), wv));
-    const float g = round_bf16(__fadd_rn(1.0f, sc));
-    out[h] = __fadd_rn(sh, __fmul_rn(n, g));
+// Bounded wait on one phase of a row-buffer barrier.
+__device__ __noinline__ bool wait_row(uint32_t bar, uint32_t parity, int* status) {
+  if (mbar_try_wait(bar, parity)) return true;
+  const uint64_t t0 = globaltimer_ns();
+  while (!mbar_try_wait(bar, parity)) {
+    if (globaltimer_ns() - t0 > kWaitLimitNs) {
+      atomicCAS(status, 0, kStatusRowFull);
+      return false;
+    }
   }
-  return pack_bf16x2(out[0], out[1]);
+  return true;
 }
 
-__global__ void __launch_bounds__(kThreads) norm_adaln_kernel(const NormAdalnParams p) {
+// One bf16x2 word of x (as packed FP32), weight, scale and shift -> one
+// bf16x2 word of a.
+__device__ __forceinline__ uint32_t adaln_pair(uint64_t x2, uint32_t w, uint32_t sc, uint32_t sh,
+                                               uint64_t r2) {
+  // n = bf16((x * r) * w)
+  const uint32_t n = f2_to_bf16x2(f2_mul(f2_mul(x2, r2), f2_from_bf16x2(w)));
+  // g = bf16(1 + scale): one correctly rounded bf16 addition per lane
+  const uint32_t g = bf16x2_add(0x3F803F80u, sc);
+  // a = bf16(shift + n * g), multiply and add rounded separately
+  const uint64_t ng = f2_mul(f2_from_bf16x2(n), f2_from_bf16x2(g));
+  return f2_to_bf16x2(f2_add(f2_from_bf16x2(sh), ng));
+}
+
+__global__ void __launch_bounds__(kThreads, kCtasPerSm) norm_adaln_kernel(const NormAdalnParams p) {
+  __shared__ __align__(128) uint8_t rows_buf[kStages][kRowBytes];
+  __shared__ __align__(8) uint64_t full[kStages];
   __shared__ float warp_ss[kWarps];
+  __shared__ int go;
+
   const int tid = threadIdx.x;
   const int lane = tid & 31;
-  const int64_t m = blockIdx.x;
+  const int64_t G = gridDim.x;
+  const int64_t first = blockIdx.x;
+  const int64_t n_rows = (p.M - first + G - 1) / G;  // >= 1: the grid is at most M
+  const uint32_t buf0 = smem_u32(&rows_buf[0][0]);
+  const uint32_t bar0 = smem_u32(&full[0]);
 
-  const uint4* xr = reinterpret_cast<const uint4*>(p.x + m * kHidden);
-  uint4 v[kVecPerThread];
-#pragma unroll
-  for (int i = 0; i < kVecPerThread; ++i) v[i] = ld_stream_v4(xr + tid + kThreads * i);
-  const int64_t idx = __ldg(p.index + m);
-
-  float acc[4] = {0.f, 0.f, 0.f, 0.f};
-#pragma unroll
-  for (int i = 0; i < kVecPerThread; ++i) {
-    sq_acc(v[i].x, acc[0], acc[1]);
-    sq_acc(v[i].y, acc[2], acc[3]);
-    sq_acc(v[i].z, acc[0], acc[1]);
-    sq_acc(v[i].w, acc[2], acc[3]);
+  uint64_t policy = 0;
+  if (tid == 0) {
+    for (int s = 0; s < kStages; ++s) mbar_init(bar0 + 8 * s, 1);
+    fence_mbar_init();
+    policy = policy_evict_first();
+    for (int64_t i = 0; i < kStages && i < n_rows; ++i) {
+      mbar_arrive_expect_tx(bar0 + 8 * i, kRowBytes);
+      bulk_load_1d(buf0 + i * kRowBytes, p.x + (first + i * G) * kHidden, kRowBytes, bar0 + 8 * i,
+                   policy);
+    }
   }
-  float ss = __fadd_rn(__fadd_rn(acc[0], acc[1]), __fadd_rn(acc[2], acc[3]));
-#pragma unroll
-  for (int o = 16; o > 0; o >>= 1) ss = __fadd_rn(ss, __shfl_xor_sync(0xFFFFFFFFu, ss, o));
-  if (lane == 0) warp_ss[tid >> 5] = ss;
   __syncthreads();
-  ss = __fadd_rn(__fadd_rn(__fadd_rn(warp_ss[0], warp_ss[1]), __fadd_rn(warp_ss[2], warp_ss[3])),
-                 __fadd_rn(__fadd_rn(warp_ss[4], warp_ss[5]), warp_ss[6]));
 
-  uint4* wr = reinterpret_cast<uint4*>(p.workspace + m * kHidden);
-  if (idx < 0 || idx >= p.rows) {
-    const uint4 z = make_uint4(0u, 0u, 0u, 0u);
+  int64_t i = 0;
+  for (; i < n_rows; ++i) {
+    const int s = static_cast<int>(i % kStages);
+    const uint32_t parity = static_cast<uint32_t>((i / kStages) & 1);
+    const int64_t m = first + i * G;
+    const int64_t idx = __ldg(p.index + m);
+    if (tid == 0) go = wait_row(bar0 + 8 * s, parity, p.status) ? 1 : 0;
+    __syncthreads();
+    if (!go) break;
+    // already complete: gives every thread its own acquire of the copied row
+    (void)mbar_try_wait(bar0 + 8 * s, parity);
+
+    const uint32_t row = buf0 + s * kRowBytes;
+    uint4 v[kVecPerThread];
+    uint64_t acc = 0;  // two FP32 partial sums (+0.0, +0.0)
 #pragma unroll
-    for (int i = 0; i < kVecPerThread; ++i) wr[tid + kThreads * i] = z;
-    return;
+    for (int j = 0; j < kVecPerThread; ++j) {
+      v[j] = ld_shared_v4(row + 16 * (tid + kThreads * j));
+      // bf16 squares are exact in FP32, so the fused form equals mul-then-add
+      uint64_t q = f2_from_bf16x2(v[j].x);
+      acc = f2_fma(q, q, acc);
+      q = f2_from_bf16x2(v[j].y);
+      acc = f2_fma(q, q, acc);
+      q = f2_from_bf16x2(v[j].z);
+      acc = f2_fma(q, q, acc);
+      q = f2_from_bf16x2(v[j].w);
+      acc = f2_fma(q, q, acc);
+    }
+    float lo, hi;
+    f2_unpack(acc, lo, hi);
+    float ss = __fadd_rn(lo, hi);
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) ss = __fadd_rn(ss, __shfl_xor_sync(0xFFFFFFFFu, ss, o));
+    if (lane == 0) warp_ss[tid >> 5] = ss;
+    __syncthreads();  // every thread holds its vectors; the warp sums are complete
+
+    if (tid == 0 && i + kStages < n_rows) {
+      // refill this buffer with row i + kStages (all reads of it are done)
+      fence_proxy_async_smem();
+      mbar_arrive_expect_tx(bar0 + 8 * s, kRowBytes);
+      bulk_load_1d(row, p.x + (first + (i + kStages) * G) * kHidden, kRowBytes, bar0 + 8 * s,
+                   policy);
+    }
+    ss = __fadd_rn(__fadd_rn(__fadd_rn(warp_ss[0], warp_ss[1]), __fadd_rn(warp_ss[2], warp_ss[3])),
+                   __fadd_rn(__fadd_rn(warp_ss[4], warp_ss[5]), warp_ss[6]));
+
+    uint4* wr = reinterpret_cast<uint4*>(p.workspace + m * kHidden);
+    if (idx < 0 || idx >= p.rows) {
+      const uint4 z = make_uint4(0u, 0u, 0u, 0u);
+#pragma unroll
+      for (int j = 0; j < kVecPerThread; ++j) wr[tid + kThreads * j] = z;
+      continue;
+    }
+    const float r =
+        __fdiv_rn(1.0f, __fsqrt_rn(__fadd_rn(__fdiv_rn(ss, static_cast<float>(kHidden)), p.eps)));
+    const uint64_t r2 = f2_pack(r, r);
+    const uint4* wv = reinterpret_cast<const uint4*>(p.x_norm_weight);
+    const uint4* scr = reinterpret_cast<const uint4*>(p.scale + idx * p.scale_stride);
+    const uint4* shr = reinterpret_cast<const uint4*>(p.shift + idx * p.shift_stride);
+#pragma unroll
+    for (int j = 0; j < kVecPerThread; ++j) {
+      const int c = tid + kThreads * j;
+      const uint4 w = __ldg(wv + c);
+      const uint4 sc = __ldg(scr + c);
+      const uint4 sh = __ldg(shr + c);
+      uint4 o;
+      o.x = adaln_pair(f2_from_bf16x2(v[j].x), w.x, sc.x, sh.x, r2);
+      o.y = adaln_pair(f2_from_bf16x2(v[j].y), w.y, sc.y, sh.y, r2);
+      o.z = adaln_pair(f2_from_bf16x2(v[j].z), w.z, sc.z, sh.z, r2);
+      o.w = adaln_pair(f2_from_bf16x2(v[j].w), w.w, sc.w, sh.w, r2);
+      wr[c] = o;
+    }
   }
-  const float r =
-      __fdiv_rn(1.0f, __fsqrt_rn(__fadd_rn(__fdiv_rn(ss, static_cast<float>(kHidden)), p.eps)));
 
-  const uint4* wv = reinterpret_cast<const uint4*>(p.x_norm_weight);
-  const uint4* scr = reinterpret_cast<const uint4*>(p.scale + idx * p.scale_stride);
-  const uint4* shr = reinterpret_cast<const uint4*>(p.shift + idx * p.shift_stride);
-#pragma unroll
-  for (int i = 0; i < kVecPerThread; ++i) {
-    const int c = tid + kThreads * i;
-    const uint4 w = __ldg(wv + c);
-    const uint4 sc = __ldg(scr + c);
-    const uint4 sh = __ldg(shr + c);
-    uint4 o;
-    o.x = adaln_pair(v[i].x, w.x, sc.x, sh.x, r);
-    o.y = adaln_pair(v[i].y, w.y, sc.y, sh.y, r);
-    o.z = adaln_pair(v[i].z, w.z, sc.z, sh.z, r);
-    o.w = adaln_pair(v[i].w, w.w, sc.w, sh.w, r);
-    wr[c] = o;
+  if (tid == 0 && i < n_rows) {
+    // Stopped early: let the copies still in flight land before exiting.
+    for (int64_t k = i; k < n_rows && k < i + kStages; ++k) {
+      const int s = static_cast<int>(k % kStages);
+      wait_row(bar0 + 8 * s, static_cast<uint32_t>((k / kStages) & 1), p.status);
+    }
   }
 }
 
 }  // namespace
 
-cudaError_t launch_norm_adaln(const NormAdalnParams& p, cudaStream_t stream) {
+cudaError_t launch_norm_adaln(const NormAdalnParams& p, int num_sms, cudaStream_t stream) {
   if (p.M <= 0) return cudaSuccess;
-  norm_adaln_kernel<<<static_cast<unsigned>(p.M), kThreads, 0, stream>>>(p);
+  const int64_t want = static_cast<int64_t>(num_sms) * kCtasPerSm;
+  const int64_t grid = p.M < want ? p.M : want;
+  norm_adaln_kernel<<<static_cast<unsigned>(grid), kThreads, 0, stream>>>(p);
   return cudaGetLastError();
 }
 

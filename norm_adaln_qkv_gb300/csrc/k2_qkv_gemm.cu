@@ -52,7 +52,13 @@ constexpr int kStages = 4;
 constexpr int kKBlocks = kHidden / BK;    // 84
 constexpr int kNTiles = kQkvRows / BN;    // 84
 constexpr int kNTilesPerKind = kKindCols / BN;  // 28
-constexpr int kGroupM = 16;
+#ifndef MH3_GROUP_M
+#define MH3_GROUP_M 16
+#endif
+#ifndef MH3_PREFETCH_NEXT_B
+#define MH3_PREFETCH_NEXT_B 0
+#endif
+constexpr int kGroupM = MH3_GROUP_M;
 constexpr int kABytes = BM * BK * 2;      // 16 KB
 constexpr int kBBytes = BN * BK * 2;      // 32 KB
 constexpr int kStageBytes = kABytes + kBBytes;
@@ -305,7 +311,17 @@ __global__ void __launch_bounds__(kThreads, 1)
       for (int t = blockIdx.x; t < p.num_tiles && ok; t += gridDim.x) {
         int m_blk, n_blk;
         tile_coords(t, p.num_m_tiles, m_blk, n_blk);
+        // Weight columns of this CTA's next tile, pulled into L2 one tile
+        // ahead: in a wave every weight tile is touched for the first time,
+        // and HBM latency would otherwise outrun the shared-memory ring.
+        int n_next = -1;
+        if (MH3_PREFETCH_NEXT_B && t + static_cast<int>(gridDim.x) < p.num_tiles) {
+          int m_next;
+          tile_coords(t + gridDim.x, p.num_m_tiles, m_next, n_next);
+          if (n_next == n_blk) n_next = -1;
+        }
         for (int kb = 0; kb < kKBlocks; ++kb) {
+          if (n_next >= 0) tma_prefetch_l2_2d(&tm_b, kb * BK, n_next * BN);
           if (!wait_phase(sm.empty(stage), phase ^ 1u, abort_flag, p.status, kStatusProducerEmpty)) {
             ok = false;
             break;

@@ -184,9 +184,9 @@ int encode_maps(QkvMaps& maps, int64_t M, const mh3_bf16* ws, const mh3_bf16* W,
   return MH3_OK;
 }
 
-int launch_stage1(cudaStream_t s, int64_t M, const mh3_bf16* x, const mh3_bf16* xw,
-                  const mh3_bf16* sc, int64_t sc_stride, const mh3_bf16* sh, int64_t sh_stride,
-                  int64_t rows, const int64_t* idx, float eps, mh3_bf16* ws) {
+int launch_stage1(cudaStream_t s, int num_sms, int* status, int64_t M, const mh3_bf16* x,
+                  const mh3_bf16* xw, const mh3_bf16* sc, int64_t sc_stride, const mh3_bf16* sh,
+                  int64_t sh_stride, int64_t rows, const int64_t* idx, float eps, mh3_bf16* ws) {
   NormAdalnParams p;
   p.x = reinterpret_cast<const __nv_bfloat16*>(x);
   p.x_norm_weight = reinterpret_cast<const __nv_bfloat16*>(xw);
@@ -199,7 +199,8 @@ int launch_stage1(cudaStream_t s, int64_t M, const mh3_bf16* x, const mh3_bf16* 
   p.workspace = reinterpret_cast<__nv_bfloat16*>(ws);
   p.M = M;
   p.eps = eps;
-  cudaError_t e = launch_norm_adaln(p, s);
+  p.status = status;
+  cudaError_t e = launch_norm_adaln(p, num_sms, s);
   if (e != cudaSuccess) return cuda_fail(e, "norm/AdaLN launch");
   return MH3_OK;
 }
@@ -341,8 +342,9 @@ int mh3_preattn_run(mh3_preattn_t h, void* stream, int64_t M, const mh3_bf16* x,
     }
     workspace = static_cast<mh3_bf16*>(h->ws);
   }
-  rc = launch_stage1(s, M, x, x_norm_weight, adaln_scale, scale_row_stride, adaln_shift,
-                     shift_row_stride, rows, adaln_index, eps, workspace);
+  rc = launch_stage1(s, h->num_sms, h->d_status, M, x, x_norm_weight, adaln_scale,
+                     scale_row_stride, adaln_shift, shift_row_stride, rows, adaln_index, eps,
+                     workspace);
   if (rc) return rc;
   return launch_stage2(h, s, M, workspace, qkv_weight, q_norm_weight, k_norm_weight,
                        rope_cos_sin, S, rope_positions, P, qk, out);
@@ -359,9 +361,9 @@ int mh3_preattn_norm_adaln(mh3_preattn_t h, void* stream, int64_t M, const mh3_b
                              shift_row_stride, rows, adaln_index, eps, workspace, true);
   if (rc) return rc;
   if (M == 0) return MH3_OK;
-  return launch_stage1(static_cast<cudaStream_t>(stream), M, x, x_norm_weight, adaln_scale,
-                       scale_row_stride, adaln_shift, shift_row_stride, rows, adaln_index, eps,
-                       workspace);
+  return launch_stage1(static_cast<cudaStream_t>(stream), h->num_sms, h->d_status, M, x,
+                       x_norm_weight, adaln_scale, scale_row_stride, adaln_shift,
+                       shift_row_stride, rows, adaln_index, eps, workspace);
 }
 
 int mh3_preattn_qkv(mh3_preattn_t h, void* stream, int64_t M, const mh3_bf16* workspace,
@@ -478,8 +480,9 @@ extern "C" int mh3_preattn_run_noalloc(
   // the timeout code must start at zero for this call
   e = cudaMemsetAsync(device_status, 0, sizeof(int), s);
   if (e != cudaSuccess) return cuda_fail(e, "cudaMemsetAsync (device_status)");
-  rc = launch_stage1(s, M, x, x_norm_weight, adaln_scale, scale_row_stride, adaln_shift,
-                     shift_row_stride, rows, adaln_index, eps, d.workspace);
+  rc = launch_stage1(s, d.num_sms, device_status, M, x, x_norm_weight, adaln_scale,
+                     scale_row_stride, adaln_shift, shift_row_stride, rows, adaln_index, eps,
+                     d.workspace);
   if (rc) return rc;
   QkvMaps maps;
   rc = encode_maps(maps, M, d.workspace, qkv_weight, P, out);
