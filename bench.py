@@ -36,7 +36,10 @@ UNIT = "us/call"
 WORKLOAD = "c3"
 ALSO = "c2"
 FLOP_PER_TOKEN = 2 * 5376 * 21504
-K2_SOURCES = ("norm_adaln_qkv_gb300/csrc/k2_qkv_gemm.cu", "norm_adaln_qkv_gb300/csrc/ptx.cuh",
+# kernel 2 at the bench size is the CTA-pair form; its traffic figure is tied
+# to these sources
+K2_SOURCES = ("norm_adaln_qkv_gb300/csrc/k2_qkv_gemm_pair.cu",
+              "norm_adaln_qkv_gb300/csrc/k2_common.cuh", "norm_adaln_qkv_gb300/csrc/ptx.cuh",
               "norm_adaln_qkv_gb300/csrc/common.cuh")
 TRAFFIC_FILE = os.path.join(ROOT, "profiles", "k2_traffic.json")
 

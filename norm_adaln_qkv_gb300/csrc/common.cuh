@@ -55,8 +55,8 @@ struct QkvParams {
   int64_t S;
   int heads_per_dst;  // 56 / P
   float qk_eps;
-  int num_m_tiles;
-  int num_tiles;
+  int num_m_tiles;  // row blocks: of 128 rows (single-CTA form) or 256 (pair form)
+  int num_tiles;    // num_m_tiles * 84
   int* status;  // device status word
 };
 
@@ -66,13 +66,22 @@ cudaError_t launch_norm_adaln(const NormAdalnParams& p, int num_sms, cudaStream_
 // Tensor maps are encoded by the host for each call.
 struct QkvMaps {
   CUtensorMap a;    // workspace [M, 5376], box 64 x 128, 128-B swizzle
-  CUtensorMap b;    // qkv_weight [21504, 5376], box 64 x 256, 128-B swizzle
+  CUtensorMap b;    // qkv_weight [21504, 5376], box 64 x 256 (single) / 64 x 128 (pair)
   CUtensorMap out;  // out as 4-D (d 128, slot 168/P, m M, dst P), box 64x1x32x1
 };
 
+// Single-CTA form (128 x 256 tiles), used for M <= 128.
 int qkv_smem_bytes();
 cudaError_t qkv_prepare_device();  // raise the dynamic shared-memory limit
 cudaError_t launch_qkv(const QkvMaps& maps, const QkvParams& p, int grid, cudaStream_t stream);
+
+// CTA-pair form (256 x 256 tiles on two SMs), used for M > 128.
+int qkv_pair_smem_bytes();
+// Raises the shared-memory limit and reports how many 2-CTA clusters can be
+// resident at once (0: the pair form cannot run on this device).
+cudaError_t qkv_pair_prepare_device(int* max_clusters);
+cudaError_t launch_qkv_pair(const QkvMaps& maps, const QkvParams& p, int clusters,
+                            cudaStream_t stream);
 
 // --------------------------------------------------------------- bf16 bits
 __device__ __forceinline__ float bf16_lo(uint32_t u) { return __uint_as_float(u << 16); }

@@ -1,0 +1,252 @@
+// k2_common.cuh -- pieces shared by the two forms of kernel 2 (one CTA per
+// 128x256 tile, and a CTA pair per 256x256 tile): tile order, bounded
+// mbarrier waits, and the fused epilogue of one 128-row x 256-column
+// accumulator block held in TMEM.
+//
+// The epilogue computes, per token row m and per head of the tile
+// (flashinfer.diffusion_ops.minimax_h3_bf16_pre_attention, summary and
+// Parameters: q/k_norm_weight, qk_eps, rope_cos_sin, rope_positions, out):
+//   y = bf16(acc)
+//   kind q/k: t = bf16((y * rr) * w_kind[d]), rr = 1/sqrt(sum_d y^2/128 + qk_eps)
+//             p = clamp(positions[m], 0, S-1) (or m); for j < 48:
+//             o_j = bf16(t_j c_j - t_{j+48} s_j), o_{j+48} = bf16(t_{j+48} c_j + t_j s_j)
+//             with c_j = cos_sin[p, j], s_j = cos_sin[p, 48 + j]; o_d = t_d, d >= 96
+//   kind v:   o = y
+//   out[head / (56/P), m, head % (56/P), kind, d] = o_d
+// Each thread owns one accumulator row (one TMEM lane), so the per-head sum of
+// squares and the (j, j+48) pairs are thread-local.  Results go through a
+// 128-B-swizzled staging buffer (one head, 32 rows, per warp) and leave by
+// 4-D TMA stores straight into out[P, M, 56/P, 3, 128]; rows past M are
+// clipped by TMA and fully out-of-range boxes are skipped.
+#pragma once
+
+#include "common.cuh"
+#include "ptx.cuh"
+
+namespace mh3 {
+namespace k2 {
+
+constexpr int BK = 64;                          // k-block: 64 bf16 = one 128-B swizzle row
+constexpr int kKBlocks = kHidden / BK;          // 84
+constexpr int kTileN = 256;                     // two heads of one kind
+constexpr int kNTiles = kQkvRows / kTileN;      // 84
+constexpr int kNTilesPerKind = kKindCols / kTileN;  // 28
+constexpr int kEpiWarps = 4;
+constexpr int kStgHalfBytes = 32 * 64 * 2;         // 32 rows x 64 cols bf16 = 4 KB
+constexpr int kStgWarpBytes = 2 * kStgHalfBytes;  // one head (128 cols) per warp
+constexpr uint32_t kTmemCols = 512;               // 2 accumulators x 256 columns
+constexpr uint64_t kWaitLimitNs = 2000000000ull;
+static_assert(kHidden % BK == 0, "K must tile");
+static_assert(kKindCols % kTileN == 0, "a tile must not straddle q/k/v");
+static_assert(kTileN == 2 * kHeadDim, "two heads per tile");
+
+// Bounded wait on one mbarrier phase; false when this CTA is aborting.
+template <bool kClusterScope>
+__device__ __noinline__ bool wait_phase(uint32_t bar, uint32_t parity, volatile int* abort_flag,
+                                        int* status, int code) {
+  auto poll = [&]() {
+    return kClusterScope ? mbar_try_wait_cluster(bar, parity) : mbar_try_wait(bar, parity);
+  };
+  if (poll()) return true;
+  const uint64_t t0 = globaltimer_ns();
+  for (uint32_t n = 1;; ++n) {
+    if (poll()) return true;
+    if ((n & 63u) == 0) {
+      if (*abort_flag) return false;
+      if (globaltimer_ns() - t0 > kWaitLimitNs) {
+        *abort_flag = 1;
+        atomicCAS(status, 0, code);
+        return false;
+      }
+    }
+  }
+}
+
+// Short bounded wait used only while draining after an abort.
+__device__ __noinline__ inline void drain_wait(uint32_t bar, uint32_t parity, int* status) {
+  const uint64_t t0 = globaltimer_ns();
+  while (!mbar_try_wait(bar, parity)) {
+    if (globaltimer_ns() - t0 > kWaitLimitNs) {
+      atomicCAS(status, 0, kStatusDrain);
+      return;
+    }
+  }
+}
+
+// Tile t -> (row block, column block): groups of kGroup row blocks, row
+// block fastest inside a group, so that the weight columns and activation
+// rows of the tiles in flight stay in L2.
+template <int kGroup>
+__device__ __forceinline__ void tile_coords(int t, int num_row_blocks, int& r_blk, int& n_blk) {
+  const int group_tiles = kGroup * kNTiles;
+  const int g = t / group_tiles;
+  const int first = g * kGroup;
+  const int gm = min(kGroup, num_row_blocks - first);
+  const int local = t - g * group_tiles;
+  r_blk = first + local % gm;
+  n_blk = local / gm;
+}
+
+// Staging address of 16-byte chunk `chunk` (0..15 over the head's 128
+// columns) of row `row` (0..31): two 4 KB halves of 64 columns, each laid out
+// as TMA's 128-byte swizzle expects (chunk index XOR row % 8).
+__device__ __forceinline__ uint32_t stg_addr(uint32_t stg, int row, int chunk) {
+  const int half = chunk >> 3;
+  const int c = chunk & 7;
+  return stg + half * kStgHalfBytes + row * 128 + ((c ^ (row & 7)) << 4);
+}
+
+__device__ __forceinline__ float acc_to_y(uint32_t bits) { return round_bf16(__uint_as_float(bits)); }
+
+// V head: o = bf16(acc).
+__device__ __forceinline__ void epi_v_head(uint32_t tcol, uint32_t stg, int lane) {
+#pragma unroll
+  for (int c = 0; c < 4; ++c) {
+    uint32_t v[32];
+    tmem_ld_x32(tcol + 32 * c, v);
+    tmem_wait_ld();
+#pragma unroll
+    for (int g = 0; g < 4; ++g) {
+      uint4 w;
+      w.x = pack_bf16x2(__uint_as_float(v[8 * g + 0]), __uint_as_float(v[8 * g + 1]));
+      w.y = pack_bf16x2(__uint_as_float(v[8 * g + 2]), __uint_as_float(v[8 * g + 3]));
+      w.z = pack_bf16x2(__uint_as_float(v[8 * g + 4]), __uint_as_float(v[8 * g + 5]));
+      w.w = pack_bf16x2(__uint_as_float(v[8 * g + 6]), __uint_as_float(v[8 * g + 7]));
+      st_shared_v4(stg_addr(stg, lane, 4 * c + g), w);
+    }
+  }
+}
+
+// Q or K head: RMSNorm over the 128 columns, rotation of [0, 96), pass-through
+// of [96, 128).
+__device__ __forceinline__ void epi_qk_head(uint32_t tcol, uint32_t stg, int lane, const float* nw,
+                                            const uint4* cs_row, float qk_eps) {
+  // Pass 1: FP32 sum of squares of the bf16-rounded projection.
+  float s0 = 0.f, s1 = 0.f, s2 = 0.f, s3 = 0.f;
+#pragma unroll
+  for (int c = 0; c < 4; ++c) {
+    uint32_t v[32];
+    tmem_ld_x32(tcol + 32 * c, v);
+    tmem_wait_ld();
+#pragma unroll
+    for (int i = 0; i < 32; i += 4) {
+      const float y0 = acc_to_y(v[i]), y1 = acc_to_y(v[i + 1]);
+      const float y2 = acc_to_y(v[i + 2]), y3 = acc_to_y(v[i + 3]);
+      s0 = __fmaf_rn(y0, y0, s0);
+      s1 = __fmaf_rn(y1, y1, s1);
+      s2 = __fmaf_rn(y2, y2, s2);
+      s3 = __fmaf_rn(y3, y3, s3);
+    }
+  }
+  const float ss = __fadd_rn(__fadd_rn(s0, s1), __fadd_rn(s2, s3));
+  const float rr = __fdiv_rn(1.0f, __fsqrt_rn(__fadd_rn(__fdiv_rn(ss, 128.0f), qk_eps)));
+
+  // Pass 2a: the rotated dims, 16 pairs (j, j + 48) at a time.
+#pragma unroll
+  for (int g = 0; g < 3; ++g) {
+    uint32_t lo[16], hi[16];
+    tmem_ld_x16(tcol + 16 * g, lo);
+    tmem_ld_x16(tcol + kRopeHalf + 16 * g, hi);
+    tmem_wait_ld();
+    // cos for j in [16g, 16g+16): row elements [16g, 16g+16) = uint4 2g, 2g+1;
+    // sin: elements [48+16g, ...) = uint4 6+2g, 7+2g.
+    const uint4 cv[2] = {__ldg(cs_row + 2 * g), __ldg(cs_row + 2 * g + 1)};
+    const uint4 sv[2] = {__ldg(cs_row + 6 + 2 * g), __ldg(cs_row + 7 + 2 * g)};
+    uint32_t o1[8], o2[8];
+#pragma unroll
+    for (int i = 0; i < 16; i += 2) {
+      const uint32_t cw = (&cv[i >> 3].x)[(i & 7) >> 1];
+      const uint32_t sw = (&sv[i >> 3].x)[(i & 7) >> 1];
+      float r1[2], r2[2];
+#pragma unroll
+      for (int e = 0; e < 2; ++e) {
+        const int j = 16 * g + i + e;
+        const float c = e ? bf16_hi(cw) : bf16_lo(cw);
+        const float s = e ? bf16_hi(sw) : bf16_lo(sw);
+        const float t1 = round_bf16(__fmul_rn(__fmul_rn(acc_to_y(lo[i + e]), rr), nw[j]));
+        const float t2 =
+            round_bf16(__fmul_rn(__fmul_rn(acc_to_y(hi[i + e]), rr), nw[j + kRopeHalf]));
+        r1[e] = __fsub_rn(__fmul_rn(t1, c), __fmul_rn(t2, s));
+        r2[e] = __fadd_rn(__fmul_rn(t2, c), __fmul_rn(t1, s));
+      }
+      o1[i >> 1] = pack_bf16x2(r1[0], r1[1]);
+      o2[i >> 1] = pack_bf16x2(r2[0], r2[1]);
+    }
+    // columns [16g, 16g+16) are chunks 2g, 2g+1; [48+16g, ...) are 6+2g, 7+2g
+    st_shared_v4(stg_addr(stg, lane, 2 * g), make_uint4(o1[0], o1[1], o1[2], o1[3]));
+    st_shared_v4(stg_addr(stg, lane, 2 * g + 1), make_uint4(o1[4], o1[5], o1[6], o1[7]));
+    st_shared_v4(stg_addr(stg, lane, 6 + 2 * g), make_uint4(o2[0], o2[1], o2[2], o2[3]));
+    st_shared_v4(stg_addr(stg, lane, 7 + 2 * g), make_uint4(o2[4], o2[5], o2[6], o2[7]));
+  }
+
+  // Pass 2b: dims [96, 128) pass through the rotation.
+  {
+    uint32_t v[32];
+    tmem_ld_x32(tcol + kRopeDims, v);
+    tmem_wait_ld();
+#pragma unroll
+    for (int g = 0; g < 4; ++g) {
+      uint32_t o[4];
+#pragma unroll
+      for (int e = 0; e < 4; ++e) {
+        const int i = 8 * g + 2 * e;
+        const int d = kRopeDims + i;
+        const float t0 = __fmul_rn(__fmul_rn(acc_to_y(v[i]), rr), nw[d]);
+        const float t1 = __fmul_rn(__fmul_rn(acc_to_y(v[i + 1]), rr), nw[d + 1]);
+        o[e] = pack_bf16x2(t0, t1);
+      }
+      st_shared_v4(stg_addr(stg, lane, 12 + g), make_uint4(o[0], o[1], o[2], o[3]));
+    }
+  }
+}
+
+// The epilogue of one 128-row x 256-column accumulator block.
+//   tmem_acc  TMEM address of the block (lane 0, first column)
+//   quad      TMEM lane quadrant this warp may read (warp index % 4)
+//   row0      token row of TMEM lane 0 of the block
+//   n_blk     256-column block of the 21504 projection columns
+// Returns after every TMEM read of the block has completed; the stores may
+// still be in flight (bulk groups of this warp's lane 0).
+__device__ __forceinline__ void epilogue_block(uint32_t tmem_acc, int quad, int lane, uint32_t stg,
+                                               const float* nw_all, const QkvParams& p,
+                                               int64_t row0, int n_blk, const CUtensorMap* tm_out) {
+  const int kind = n_blk / kNTilesPerKind;
+  const int head0 = (n_blk % kNTilesPerKind) * 2;
+  const int64_t m = row0 + quad * 32 + lane;
+  int64_t prow = 0;
+  if (kind < 2 && m < p.M) {
+    if (p.positions) {
+      const int64_t pv = __ldg(p.positions + m);
+      prow = pv < 0 ? 0 : (pv >= p.S ? p.S - 1 : pv);
+    } else {
+      prow = m;
+    }
+  }
+  const uint4* cs_row = reinterpret_cast<const uint4*>(p.cos_sin + prow * kRopeDims);
+  const int64_t m0 = row0 + quad * 32;
+#pragma unroll 1
+  for (int j = 0; j < 2; ++j) {
+    const uint32_t tcol = tmem_acc + (static_cast<uint32_t>(quad * 32) << 16) +
+                          static_cast<uint32_t>(j * kHeadDim);
+    // the previous store from this staging buffer must have read it
+    if (lane == 0) bulk_wait_group_read0();
+    __syncwarp();
+    if (kind == 2)
+      epi_v_head(tcol, stg, lane);
+    else
+      epi_qk_head(tcol, stg, lane, nw_all + kind * kHeadDim, cs_row, p.qk_eps);
+    fence_proxy_async_smem();
+    __syncwarp();
+    if (lane == 0 && m0 < p.M) {
+      const int head = head0 + j;
+      const int dst = head / p.heads_per_dst;
+      const int slot = (head % p.heads_per_dst) * 3 + kind;
+      tma_store_4d(tm_out, stg, 0, slot, static_cast<int32_t>(m0), dst);
+      tma_store_4d(tm_out, stg + kStgHalfBytes, 64, slot, static_cast<int32_t>(m0), dst);
+      bulk_commit_group();
+    }
+  }
+}
+
+}  // namespace k2
+}  // namespace mh3

@@ -26,6 +26,7 @@ using namespace mh3;
 struct mh3_preattn_ctx {
   int device = 0;
   int num_sms = 0;
+  int max_clusters = 0;  // resident 2-CTA clusters of the pair GEMM
   int* d_status = nullptr;
   void* ws = nullptr;  // handle-owned workspace (grown on demand)
   size_t ws_bytes = 0;
@@ -144,7 +145,7 @@ PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
 }
 
 int encode_maps(QkvMaps& maps, int64_t M, const mh3_bf16* ws, const mh3_bf16* W, int P,
-                mh3_bf16* out) {
+                mh3_bf16* out, unsigned b_box_rows) {
   PFN_cuTensorMapEncodeTiled_v12000 enc = encode_fn();
   if (enc == nullptr) return fail(MH3_ERR_CUDA, "cuTensorMapEncodeTiled entry point not found");
   const cuuint32_t unit[4] = {1, 1, 1, 1};
@@ -161,7 +162,7 @@ int encode_maps(QkvMaps& maps, int64_t M, const mh3_bf16* ws, const mh3_bf16* W,
     const cuuint64_t dims[2] = {static_cast<cuuint64_t>(kHidden),
                                 static_cast<cuuint64_t>(kQkvRows)};
     const cuuint64_t strides[1] = {static_cast<cuuint64_t>(kHidden) * 2};
-    const cuuint32_t box[2] = {64, 256};
+    const cuuint32_t box[2] = {64, b_box_rows};
     CUresult r = enc(&maps.b, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<mh3_bf16*>(W), dims,
                      strides, box, unit, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
                      CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
@@ -205,11 +206,15 @@ int launch_stage1(cudaStream_t s, int num_sms, int* status, int64_t M, const mh3
   return MH3_OK;
 }
 
-int launch_stage2(mh3_preattn_t h, cudaStream_t s, int64_t M, const mh3_bf16* ws,
-                  const mh3_bf16* W, const mh3_bf16* qw, const mh3_bf16* kw, const mh3_bf16* cs,
-                  int64_t S, const int64_t* pos, int P, float qk_eps, mh3_bf16* out) {
+// Kernel 2: the CTA-pair form for M > 128 (when pairs can be resident), the
+// single-CTA form otherwise.
+int launch_stage2(cudaStream_t s, int num_sms, int max_clusters, int* status, int64_t M,
+                  const mh3_bf16* ws, const mh3_bf16* W, const mh3_bf16* qw, const mh3_bf16* kw,
+                  const mh3_bf16* cs, int64_t S, const int64_t* pos, int P, float qk_eps,
+                  mh3_bf16* out) {
+  const bool pair = M > 128 && max_clusters > 0;
   QkvMaps maps;
-  int rc = encode_maps(maps, M, ws, W, P, out);
+  int rc = encode_maps(maps, M, ws, W, P, out, pair ? 128u : 256u);
   if (rc) return rc;
   QkvParams p;
   p.positions = pos;
@@ -220,11 +225,19 @@ int launch_stage2(mh3_preattn_t h, cudaStream_t s, int64_t M, const mh3_bf16* ws
   p.S = S;
   p.heads_per_dst = kHeads / P;
   p.qk_eps = qk_eps;
-  p.num_m_tiles = static_cast<int>((M + 127) / 128);
-  p.num_tiles = p.num_m_tiles * (kQkvRows / 256);
-  p.status = h->d_status;
-  const int grid = p.num_tiles < h->num_sms ? p.num_tiles : h->num_sms;
-  cudaError_t e = launch_qkv(maps, p, grid, s);
+  p.status = status;
+  cudaError_t e;
+  if (pair) {
+    p.num_m_tiles = static_cast<int>((M + 255) / 256);
+    p.num_tiles = p.num_m_tiles * (kQkvRows / 256);
+    const int clusters = p.num_tiles < max_clusters ? p.num_tiles : max_clusters;
+    e = launch_qkv_pair(maps, p, clusters, s);
+  } else {
+    p.num_m_tiles = static_cast<int>((M + 127) / 128);
+    p.num_tiles = p.num_m_tiles * (kQkvRows / 256);
+    const int grid = p.num_tiles < num_sms ? p.num_tiles : num_sms;
+    e = launch_qkv(maps, p, grid, s);
+  }
   if (e != cudaSuccess) return cuda_fail(e, "QKV GEMM launch");
   return MH3_OK;
 }
@@ -259,9 +272,13 @@ int mh3_preattn_create(mh3_preattn_t* handle, int device) {
                 prop.sharedMemPerBlockOptin, qkv_smem_bytes());
   e = qkv_prepare_device();
   if (e != cudaSuccess) return cuda_fail(e, "cudaFuncSetAttribute");
+  int max_clusters = 0;
+  e = qkv_pair_prepare_device(&max_clusters);
+  if (e != cudaSuccess) return cuda_fail(e, "preparing the pair GEMM");
   mh3_preattn_ctx* h = new mh3_preattn_ctx();
   h->device = device;
   h->num_sms = prop.multiProcessorCount;
+  h->max_clusters = max_clusters;
   e = cudaMalloc(&h->d_status, sizeof(int));
   if (e == cudaSuccess) e = cudaMemset(h->d_status, 0, sizeof(int));
   if (e != cudaSuccess) {
@@ -346,8 +363,8 @@ int mh3_preattn_run(mh3_preattn_t h, void* stream, int64_t M, const mh3_bf16* x,
                      scale_row_stride, adaln_shift, shift_row_stride, rows, adaln_index, eps,
                      workspace);
   if (rc) return rc;
-  return launch_stage2(h, s, M, workspace, qkv_weight, q_norm_weight, k_norm_weight,
-                       rope_cos_sin, S, rope_positions, P, qk, out);
+  return launch_stage2(s, h->num_sms, h->max_clusters, h->d_status, M, workspace, qkv_weight,
+                       q_norm_weight, k_norm_weight, rope_cos_sin, S, rope_positions, P, qk, out);
 }
 
 int mh3_preattn_norm_adaln(mh3_preattn_t h, void* stream, int64_t M, const mh3_bf16* x,
@@ -378,9 +395,9 @@ int mh3_preattn_qkv(mh3_preattn_t h, void* stream, int64_t M, const mh3_bf16* wo
   if (rc) return rc;
   if (M == 0) return MH3_OK;
   if ((rc = check_ptr(workspace, "workspace", 16))) return rc;
-  return launch_stage2(h, static_cast<cudaStream_t>(stream), M, workspace, qkv_weight,
-                       q_norm_weight, k_norm_weight, rope_cos_sin, S, rope_positions, P, qk_eps,
-                       out);
+  return launch_stage2(static_cast<cudaStream_t>(stream), h->num_sms, h->max_clusters,
+                       h->d_status, M, workspace, qkv_weight, q_norm_weight, k_norm_weight,
+                       rope_cos_sin, S, rope_positions, P, qk_eps, out);
 }
 
 int mh3_preattn_device_status(mh3_preattn_t h, void* stream, int* device_code) {
@@ -420,6 +437,7 @@ struct NoAllocDevice {
   std::string err;
   mh3_bf16* workspace = nullptr;  // device address of g_noalloc_workspace
   int num_sms = 0;
+  int max_clusters = 0;
 };
 NoAllocDevice g_noalloc_dev[kNoAllocMaxDevices];
 
@@ -439,6 +457,8 @@ void noalloc_setup(int dev, NoAllocDevice& d) {
     d.rc = cuda_fail(e, "cudaGetSymbolAddress (static workspace)");
   } else if ((e = qkv_prepare_device()) != cudaSuccess) {
     d.rc = cuda_fail(e, "cudaFuncSetAttribute");
+  } else if ((e = qkv_pair_prepare_device(&d.max_clusters)) != cudaSuccess) {
+    d.rc = cuda_fail(e, "preparing the pair GEMM");
   } else {
     d.num_sms = prop.multiProcessorCount;
     d.rc = MH3_OK;
@@ -484,23 +504,7 @@ extern "C" int mh3_preattn_run_noalloc(
                      scale_row_stride, adaln_shift, shift_row_stride, rows, adaln_index, eps,
                      d.workspace);
   if (rc) return rc;
-  QkvMaps maps;
-  rc = encode_maps(maps, M, d.workspace, qkv_weight, P, out);
-  if (rc) return rc;
-  QkvParams p;
-  p.positions = rope_positions;
-  p.cos_sin = reinterpret_cast<const __nv_bfloat16*>(rope_cos_sin);
-  p.q_norm_weight = reinterpret_cast<const __nv_bfloat16*>(q_norm_weight);
-  p.k_norm_weight = reinterpret_cast<const __nv_bfloat16*>(k_norm_weight);
-  p.M = M;
-  p.S = S;
-  p.heads_per_dst = kHeads / P;
-  p.qk_eps = qk_eps_means_default(qk_eps) ? eps : qk_eps;
-  p.num_m_tiles = static_cast<int>((M + 127) / 128);
-  p.num_tiles = p.num_m_tiles * (kQkvRows / 256);
-  p.status = device_status;
-  const int grid = p.num_tiles < d.num_sms ? p.num_tiles : d.num_sms;
-  e = launch_qkv(maps, p, grid, s);
-  if (e != cudaSuccess) return cuda_fail(e, "QKV GEMM launch");
-  return MH3_OK;
+  return launch_stage2(s, d.num_sms, d.max_clusters, device_status, M, d.workspace, qkv_weight,
+                       q_norm_weight, k_norm_weight, rope_cos_sin, S, rope_positions, P,
+                       qk_eps_means_default(qk_eps) ? eps : qk_eps, out);
 }
