@@ -89,6 +89,10 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm) norm_adaln_kernel(const 
   const uint32_t buf0 = smem_u32(&rows_buf[0][0]);
   const uint32_t bar0 = smem_u32(&full[0]);
 
+  // kernel 2 may start its prologue (barriers, TMEM, tensor maps) now; it
+  // waits for this grid's completion before it reads the workspace
+  griddep_launch_dependents();
+
   uint64_t policy = 0;
   if (tid == 0) {
     for (int s = 0; s < kStages; ++s) mbar_init(bar0 + 8 * s, 1);

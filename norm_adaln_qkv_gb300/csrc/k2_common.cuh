@@ -36,9 +36,34 @@ constexpr int kStgHalfBytes = 32 * 64 * 2;         // 32 rows x 64 cols bf16 = 4
 constexpr int kStgWarpBytes = 2 * kStgHalfBytes;  // one head (128 cols) per warp
 constexpr uint32_t kTmemCols = 512;               // 2 accumulators x 256 columns
 constexpr uint64_t kWaitLimitNs = 2000000000ull;
+#ifndef MH3_PDL
+#define MH3_PDL 1
+#endif
+#ifndef MH3_OUT_EVICT_FIRST
+#define MH3_OUT_EVICT_FIRST 1
+#endif
 static_assert(kHidden % BK == 0, "K must tile");
 static_assert(kKindCols % kTileN == 0, "a tile must not straddle q/k/v");
 static_assert(kTileN == 2 * kHeadDim, "two heads per tile");
+
+// Launch kernel 2 so that its prologue may overlap the end of the kernel
+// before it on the stream (programmatic dependent launch); the producer's
+// griddepcontrol.wait keeps the workspace reads behind that kernel.
+template <typename Kernel>
+inline cudaError_t launch_k2(Kernel kernel, int grid, int threads, int smem, cudaStream_t stream,
+                             const QkvMaps& maps, const QkvParams& p) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(static_cast<unsigned>(grid), 1, 1);
+  cfg.blockDim = dim3(static_cast<unsigned>(threads), 1, 1);
+  cfg.dynamicSmemBytes = static_cast<size_t>(smem);
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = MH3_PDL ? 1 : 0;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, kernel, maps.a, maps.b, maps.out, p);
+}
 
 // Bounded wait on one mbarrier phase; false when this CTA is aborting.
 template <bool kClusterScope>
@@ -241,8 +266,17 @@ __device__ __forceinline__ void epilogue_block(uint32_t tmem_acc, int quad, int 
       const int head = head0 + j;
       const int dst = head / p.heads_per_dst;
       const int slot = (head % p.heads_per_dst) * 3 + kind;
-      tma_store_4d(tm_out, stg, 0, slot, static_cast<int32_t>(m0), dst);
-      tma_store_4d(tm_out, stg + kStgHalfBytes, 64, slot, static_cast<int32_t>(m0), dst);
+      if (MH3_OUT_EVICT_FIRST) {
+        // out is written once and read by the next operation, not by this
+        // one: evict-first keeps it from lingering dirty in L2
+        const uint64_t pol = policy_evict_first();
+        tma_store_4d_hint(tm_out, stg, 0, slot, static_cast<int32_t>(m0), dst, pol);
+        tma_store_4d_hint(tm_out, stg + kStgHalfBytes, 64, slot, static_cast<int32_t>(m0), dst,
+                          pol);
+      } else {
+        tma_store_4d(tm_out, stg, 0, slot, static_cast<int32_t>(m0), dst);
+        tma_store_4d(tm_out, stg + kStgHalfBytes, 64, slot, static_cast<int32_t>(m0), dst);
+      }
       bulk_commit_group();
     }
   }

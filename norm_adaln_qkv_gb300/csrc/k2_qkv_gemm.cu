@@ -120,6 +120,8 @@ __global__ void __launch_bounds__(kThreads, 1)
   if (warp == 0) {
     // ------------------------------------------------------------ producer
     if (lane == 0) {
+      // the workspace is written by kernel 1, which may still be finishing
+      griddep_wait();
       int stage = 0;
       uint32_t phase = 0;
       bool ok = true;
@@ -240,8 +242,7 @@ cudaError_t qkv_prepare_device() {
 
 cudaError_t launch_qkv(const QkvMaps& maps, const QkvParams& p, int grid, cudaStream_t stream) {
   if (p.M <= 0) return cudaSuccess;
-  qkv_gemm_kernel<<<grid, kThreads, kSmemAlloc, stream>>>(maps.a, maps.b, maps.out, p);
-  return cudaGetLastError();
+  return launch_k2(qkv_gemm_kernel, grid, kThreads, kSmemAlloc, stream, maps, p);
 }
 
 }  // namespace mh3

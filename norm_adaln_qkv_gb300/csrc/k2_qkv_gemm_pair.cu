@@ -157,6 +157,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
   if (warp == 0) {
     // ------------------------------------------------- producer (both CTAs)
     if (lane == 0) {
+      // the workspace is written by kernel 1, which may still be finishing
+      griddep_wait();
       int stage = 0;
       uint32_t phase = 0;
       bool ok = true;
@@ -286,9 +288,7 @@ cudaError_t qkv_pair_prepare_device(int* max_clusters) {
 cudaError_t launch_qkv_pair(const QkvMaps& maps, const QkvParams& p, int clusters,
                             cudaStream_t stream) {
   if (p.M <= 0) return cudaSuccess;
-  qkv_gemm_pair_kernel<<<2 * clusters, kThreads, kSmemAlloc, stream>>>(maps.a, maps.b, maps.out,
-                                                                       p);
-  return cudaGetLastError();
+  return launch_k2(qkv_gemm_pair_kernel, 2 * clusters, kThreads, kSmemAlloc, stream, maps, p);
 }
 
 }  // namespace mh3

@@ -236,6 +236,27 @@ __device__ __forceinline__ void tma_store_4d(const CUtensorMap* m, uint32_t src,
       : "memory");
 }
 
+// Same, with an L2 eviction-priority policy for the written lines.
+__device__ __forceinline__ void tma_store_4d_hint(const CUtensorMap* m, uint32_t src, int32_t c0,
+                                                  int32_t c1, int32_t c2, int32_t c3,
+                                                  uint64_t policy) {
+  asm volatile(
+      "cp.async.bulk.tensor.4d.global.shared::cta.bulk_group.L2::cache_hint"
+      " [%0, {%2, %3, %4, %5}], [%1], %6;" ::"l"(reinterpret_cast<uint64_t>(m)),
+      "r"(src), "r"(c0), "r"(c1), "r"(c2), "r"(c3), "l"(policy)
+      : "memory");
+}
+
+// Programmatic dependent launch: let the next kernel on the stream start its
+// prologue now; and wait until the previous kernel has completed and its
+// memory is visible (a no-op when the launch was not programmatic).
+__device__ __forceinline__ void griddep_launch_dependents() {
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+__device__ __forceinline__ void griddep_wait() {
+  asm volatile("griddepcontrol.wait;" ::: "memory");
+}
+
 __device__ __forceinline__ void bulk_commit_group() {
   asm volatile("cp.async.bulk.commit_group;" ::: "memory");
 }
