@@ -136,6 +136,21 @@ class ClockSampler:
                 "reasons": reasons, "samples": len(rows)}
 
 
+def max_over_ranks(v: float, device=None) -> float:
+    """Largest value over all ranks (the identity without a process group)."""
+    if not (torch.distributed.is_available() and torch.distributed.is_initialized()):
+        return v
+    t = torch.tensor([v], dtype=torch.float64, device=device)
+    torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+    return float(t.item())
+
+
+def job_value_us(ms_total_max: float, steps: int, world: int) -> float:
+    """Whole-job time per call: every rank runs one call per step, so the
+    job completes steps * world calls in the slowest rank's time."""
+    return ms_total_max * 1e3 / (steps * world)
+
+
 def _dist():
     world = int(os.environ.get("WORLD_SIZE", "1"))
     rank = int(os.environ.get("RANK", "0"))
@@ -257,13 +272,6 @@ def run_ours(args, world, rank, local):
         if world > 1:
             torch.distributed.barrier()
 
-    def max_over_ranks(v: float) -> float:
-        if world == 1:
-            return v
-        t = torch.tensor([v], dtype=torch.float64, device=dev)
-        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
-        return float(t.item())
-
     d = prepare(wl)
     clocks = ClockSampler(local)
     clocks.start()
@@ -281,7 +289,7 @@ def run_ours(args, world, rank, local):
     e1.record(stream)
     torch.cuda.synchronize()
     barrier()
-    ms_total = max_over_ranks(e0.elapsed_time(e1))
+    ms_total = max_over_ranks(e0.elapsed_time(e1), dev)
     gpu_launches = 2 * args.steps
     assert h.device_status(stream) == 0, "a kernel recorded a timeout"
 
@@ -346,7 +354,7 @@ def run_ours(args, world, rank, local):
     s1.record(stream)
     torch.cuda.synchronize()
     barrier()
-    e2e_ms = max_over_ranks(s0.elapsed_time(s1)) / n_e2e
+    e2e_ms = max_over_ranks(s0.elapsed_time(s1), dev) / n_e2e
 
     # ---- the 4096-token block named by the metric (same stage, P = 2)
     also = None
@@ -376,7 +384,7 @@ def run_ours(args, world, rank, local):
         return
     M = wl.M
     ms_step = ms_total / args.steps
-    value_us = ms_step * 1e3 / world  # whole-job time per call: N replicas per step
+    value_us = job_value_us(ms_total, args.steps, world)
     k2_tflops = FLOP_PER_TOKEN * M / (k2_ms * 1e-3) / 1e12
     k1_bytes = M * 5376 * 2 * 2 + M * 8
     k1_gbs = k1_bytes / (k1_alone_ms * 1e-3) / 1e9
