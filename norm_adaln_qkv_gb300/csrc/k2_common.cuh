@@ -101,9 +101,9 @@ __device__ __noinline__ inline void drain_wait(uint32_t bar, uint32_t parity, in
 // Tile t -> (row block, column block): groups of kGroup row blocks, row
 // block fastest inside a group, so that the weight columns and activation
 // rows of the tiles in flight stay in L2.
-template <int kGroup>
+template <int kGroup, int kN = kNTiles>
 __device__ __forceinline__ void tile_coords(int t, int num_row_blocks, int& r_blk, int& n_blk) {
-  const int group_tiles = kGroup * kNTiles;
+  const int group_tiles = kGroup * kN;
   const int g = t / group_tiles;
   const int first = g * kGroup;
   const int gm = min(kGroup, num_row_blocks - first);

@@ -277,3 +277,54 @@ def sample_rows(wl: Workload, every: int = 64, limit: Optional[int] = None) -> l
         stride = max(1, len(out) // limit)
         out = sorted(set(out[::stride]) | keep)
     return out
+
+
+# --------------------------------------------------- attention output projection
+ATTN_WIDTH = NUM_HEADS * HEAD_DIM  # 7168
+GATE_CHUNK = 2  # gate_msa: chunk 2 of the [rows, 6*hidden] modulation projection
+BAD_GATE_CYCLE = (-1, 9, 2 ** 30)
+
+
+@dataclass
+class OutProjWorkload:
+    """Host tensors of one out-projection case (shapes of
+    flashinfer.diffusion_ops.minimax_h3_nvfp4_out_proj, Parameters: attn_out
+    [M, 7168], o weight [5376, 7168], gate [9, 5376], gate_index int32 [M],
+    residual [M, 5376])."""
+
+    M: int
+    attn_out: torch.Tensor
+    o_weight: torch.Tensor
+    adaln_mod: torch.Tensor  # [rows, 6*HIDDEN]; the gate is chunk GATE_CHUNK
+    gate_index: torch.Tensor
+    residual: torch.Tensor
+
+    def gate_view(self, mod: Optional[torch.Tensor] = None) -> torch.Tensor:
+        mod = self.adaln_mod if mod is None else mod
+        return mod[:, GATE_CHUNK * HIDDEN:(GATE_CHUNK + 1) * HIDDEN]
+
+
+def make_out_proj_workload(M: int, seed: int = SEED_BASE + 100, rows: int = 9,
+                           bad_rate: float = 0.01) -> OutProjWorkload:
+    """attn_out ~ N(0,1); o weight ~ N(0, 1/7168); modulation 0.1*N(0,1) with
+    the gate as chunk 2 (row stride 6*5376); gate_index uniform in [0, rows)
+    with bad_rate of the tokens set cyclically to -1, 9, 2^30; residual ~ N(0,1)."""
+    gen = torch.Generator().manual_seed(seed)
+    attn = torch.empty((M, ATTN_WIDTH), dtype=torch.bfloat16)
+    for r0 in range(0, M, 8192):
+        r1 = min(M, r0 + 8192)
+        attn[r0:r1] = _normal(gen, (r1 - r0, ATTN_WIDTH)).to(torch.bfloat16)
+    w = (_normal(gen, (HIDDEN, ATTN_WIDTH)) / math.sqrt(ATTN_WIDTH)).to(torch.bfloat16)
+    mod = (0.1 * _normal(gen, (rows, 6 * HIDDEN))).to(torch.bfloat16)
+    gi = torch.randint(0, rows, (M,), generator=gen, dtype=torch.int64).to(torch.int32)
+    n_bad = int(round(bad_rate * M))
+    if n_bad:
+        toks = torch.randperm(M, generator=gen)[:n_bad]
+        for j, t in enumerate(toks.tolist()):
+            gi[t] = BAD_GATE_CYCLE[j % len(BAD_GATE_CYCLE)]
+    res = torch.empty((M, HIDDEN), dtype=torch.bfloat16)
+    for r0 in range(0, M, 8192):
+        r1 = min(M, r0 + 8192)
+        res[r0:r1] = _normal(gen, (r1 - r0, HIDDEN)).to(torch.bfloat16)
+    return OutProjWorkload(M=M, attn_out=attn, o_weight=w, adaln_mod=mod, gate_index=gi,
+                           residual=res)

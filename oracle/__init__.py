@@ -27,3 +27,4 @@ from .preattn import (  # noqa: F401
     pre_attention,
     PreAttnTokens,
 )
+from . import out_proj  # noqa: F401  (attention output projection + gated residual)
