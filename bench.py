@@ -39,8 +39,10 @@ FLOP_PER_TOKEN = 2 * 5376 * 21504
 # kernel 2 at the bench size is the CTA-pair form; its traffic figure is tied
 # to these sources
 K2_SOURCES = ("norm_adaln_qkv_gb300/csrc/k2_qkv_gemm_pair.cu",
+              "norm_adaln_qkv_gb300/csrc/gemm_pair.cuh",
               "norm_adaln_qkv_gb300/csrc/k2_common.cuh", "norm_adaln_qkv_gb300/csrc/ptx.cuh",
               "norm_adaln_qkv_gb300/csrc/common.cuh")
+OUT_PROJ_FLOP_PER_TOKEN = 2 * 7168 * 5376
 TRAFFIC_FILE = os.path.join(ROOT, "profiles", "k2_traffic.json")
 
 
@@ -377,6 +379,35 @@ def run_ours(args, world, rank, local):
                 "k2_tflops": FLOP_PER_TOKEN * wl2.M / (b2 * 1e-3) / 1e12,
                 "k2_frac_of_measured_bf16": FLOP_PER_TOKEN * wl2.M / (b2 * 1e-3) / 1e12 / peaks["bf16"]}
         del d2
+    # ---- the attention output projection with the gated residual (the
+    # step after attention, same GEMM machinery), at the bench's M
+    out_proj = None
+    if not args.skip_also:
+        from norm_adaln_qkv_gb300.inputs import make_out_proj_workload
+        wo = make_out_proj_workload(wl.M)
+        mod_o = wo.adaln_mod.to(dev)
+        gate_o = wo.gate_view(mod_o)
+        ao, Wo, gio, reso = (wo.attn_out.to(dev), wo.o_weight.to(dev), wo.gate_index.to(dev),
+                             wo.residual.to(dev))
+        outo = torch.empty_like(reso)
+
+        def op_call():
+            binding.mh3_out_proj_run(h, stream, wo.M, ao, Wo, gate_o, gate_o.stride(0),
+                                     gate_o.shape[0], gio, reso, outo)
+        for _ in range(3):
+            op_call()
+        torch.cuda.synchronize()
+        o0, o1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        o0.record(stream)
+        for _ in range(args.steps):
+            op_call()
+        o1.record(stream)
+        torch.cuda.synchronize()
+        op_ms = o0.elapsed_time(o1) / args.steps
+        op_tf = OUT_PROJ_FLOP_PER_TOKEN * wo.M / (op_ms * 1e-3) / 1e12
+        out_proj = {"workload": f"out-projection + gated residual, M={wo.M}, K=7168, N=5376",
+                    "us": op_ms * 1e3, "tflops": op_tf, "frac_of_measured_bf16": op_tf / peaks["bf16"]}
+        del ao, Wo, gio, reso, outo, mod_o
     clk = clocks.stop()
     assert h.device_status(stream) == 0, "a kernel recorded a timeout"
 
@@ -425,6 +456,7 @@ def run_ours(args, world, rank, local):
         "gpu_launches": gpu_launches,
         "clocks": clk,
         "also": also,
+        "out_proj": out_proj,
     }
     print(json.dumps(line), flush=True)
 

@@ -197,6 +197,43 @@ int mh3_preattn_run_noalloc(void* stream, int64_t M, const mh3_bf16* x,
                             int64_t S, const int64_t* rope_positions, int P, float eps,
                             float qk_eps, mh3_bf16* out, int* device_status);
 
+/* ---------------------------------------------------------------------------
+ * Attention output projection with the fused gated residual (the step after
+ * attention), from the page "flashinfer.diffusion_ops.minimax_h3_nvfp4_out_proj"
+ * (summary formula; Parameters: attn_out, gate, gate_index, residual, out),
+ * computed here with BF16 operands on the same CTA-pair tcgen05 GEMM:
+ *
+ *   o   = bf16(attn_out @ o_weight^T)                 FP32 accumulation
+ *   out = bf16(residual + bf16(g * o)),  g = gate[gate_index[m]]
+ *   g   = 0 when gate_index[m] lies outside [0, gate_rows)   (out = residual)
+ *
+ *   M                 tokens, >= 0 (M == 0 launches nothing)
+ *   attn_out          [M, 7168] row-major (7168 = 56 heads x 128), 16-B aligned
+ *   o_weight          [5376, 7168] row-major, 16-B aligned
+ *   gate              [gate_rows, 5376] view: unit column stride, row stride
+ *                     gate_row_stride (elements, >= 5376, multiple of 8),
+ *                     base 16-B aligned; a column chunk of the [rows, 6*5376]
+ *                     modulation projection qualifies as it is
+ *   gate_rows         >= 1
+ *   gate_index        [M] int32, 4-B aligned; any value (guarded on the device)
+ *   residual          [M, 5376] row-major, 16-B aligned
+ *   out               [M, 5376] row-major, 16-B aligned; may be the same
+ *                     buffer as residual (each block is read before it is
+ *                     written), must not partially overlap it
+ * One launch on `stream`; no host synchronisation.  Bounded waits report to
+ * the handle's status word (mh3_preattn_device_status). */
+int mh3_out_proj_run(mh3_preattn_t handle, void* stream, int64_t M, const mh3_bf16* attn_out,
+                     const mh3_bf16* o_weight, const mh3_bf16* gate, int64_t gate_row_stride,
+                     int64_t gate_rows, const int32_t* gate_index, const mh3_bf16* residual,
+                     mh3_bf16* out);
+
+/* Host-only validation of an mh3_out_proj_run argument set (no device
+ * access, no launch); same rules and status codes. */
+int mh3_out_proj_validate(int64_t M, const mh3_bf16* attn_out, const mh3_bf16* o_weight,
+                          const mh3_bf16* gate, int64_t gate_row_stride, int64_t gate_rows,
+                          const int32_t* gate_index, const mh3_bf16* residual,
+                          const mh3_bf16* out);
+
 /* Message of the calling thread's last failed call ("" if none). */
 const char* mh3_preattn_last_error(void);
 

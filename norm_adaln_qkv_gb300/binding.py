@@ -32,7 +32,8 @@ STATUS = {0: "MH3_OK", 1: "MH3_ERR_INVALID_ARG", 2: "MH3_ERR_ALIGNMENT", 3: "MH3
 EXPORTS = ("mh3_preattn_create", "mh3_preattn_destroy", "mh3_preattn_workspace_bytes",
            "mh3_preattn_out_bytes", "mh3_preattn_validate", "mh3_preattn_run",
            "mh3_preattn_norm_adaln", "mh3_preattn_qkv", "mh3_preattn_device_status",
-           "mh3_preattn_last_error", "mh3_preattn_run_noalloc")
+           "mh3_preattn_last_error", "mh3_preattn_run_noalloc", "mh3_out_proj_run",
+           "mh3_out_proj_validate")
 
 _vp = ctypes.c_void_p
 _i64 = ctypes.c_int64
@@ -53,6 +54,8 @@ _SIGS = {
     "mh3_preattn_qkv": (_i32, [_vp, _vp, _i64, _vp, _vp, _vp, _vp, _vp, _i64, _vp, _i32, _f32, _vp]),
     "mh3_preattn_device_status": (_i32, [_vp, _vp, ctypes.POINTER(_i32)]),
     "mh3_preattn_last_error": (ctypes.c_char_p, []),
+    "mh3_out_proj_run": (_i32, [_vp, _vp, _i64, _vp, _vp, _vp, _i64, _i64, _vp, _vp, _vp]),
+    "mh3_out_proj_validate": (_i32, [_i64, _vp, _vp, _vp, _i64, _i64, _vp, _vp, _vp]),
     "mh3_preattn_run_noalloc": (_i32, [_vp, _i64, _vp, _vp, _vp, _i64, _vp, _i64, _i64, _vp, _vp,
                                        _vp, _vp, _vp, _i64, _vp, _i32, _f32, _f32, _vp, _vp]),
 }
@@ -195,6 +198,46 @@ def mh3_preattn_run_noalloc(stream, M, x, x_norm_weight, adaln_scale, scale_row_
         _ptr(qkv_weight), _ptr(q_norm_weight), _ptr(k_norm_weight), _ptr(rope_cos_sin), S,
         _ptr(rope_positions), P, float(eps), _qk_eps_arg(qk_eps), _ptr(out),
         _ptr(device_status)), "mh3_preattn_run_noalloc")
+
+
+def mh3_out_proj_validate(M, attn_out, o_weight, gate, gate_row_stride, gate_rows, gate_index,
+                          residual, out) -> int:
+    """Host-only validation of an output-projection call; returns the status."""
+    return load().mh3_out_proj_validate(M, _ptr(attn_out), _ptr(o_weight), _ptr(gate),
+                                        gate_row_stride, gate_rows, _ptr(gate_index),
+                                        _ptr(residual), _ptr(out))
+
+
+def mh3_out_proj_run(handle: Handle, stream, M, attn_out, o_weight, gate, gate_row_stride,
+                     gate_rows, gate_index, residual, out) -> None:
+    _check(load().mh3_out_proj_run(handle.ptr, _stream_ptr(stream), M, _ptr(attn_out),
+                                   _ptr(o_weight), _ptr(gate), gate_row_stride, gate_rows,
+                                   _ptr(gate_index), _ptr(residual), _ptr(out)),
+           "mh3_out_proj_run")
+
+
+def minimax_h3_bf16_out_proj(attn_out, o_weight, gate, gate_index, residual, *,
+                             out: Optional[torch.Tensor] = None, stream=None,
+                             handle: Optional[Handle] = None) -> torch.Tensor:
+    """Torch-tensor entry point of the output projection with the fused gated
+    residual (argument names of flashinfer.diffusion_ops.minimax_h3_nvfp4_out_proj,
+    BF16 weight); returns ``out`` (allocated when None; may be ``residual``)."""
+    M = attn_out.shape[0]
+    bf = torch.bfloat16
+    _check_tensor(attn_out, "attn_out", bf, (M, NUM_HEADS * HEAD_DIM))
+    _check_tensor(o_weight, "o_weight", bf, (HIDDEN, NUM_HEADS * HEAD_DIM))
+    _check_tensor(gate, "gate", bf, contiguous=False)
+    if gate.dim() != 2 or gate.shape[1] != HIDDEN or gate.stride(1) != 1:
+        raise ValueError(f"gate must be [rows, {HIDDEN}] with stride(1) == 1")
+    _check_tensor(gate_index, "gate_index", torch.int32, (M,))
+    _check_tensor(residual, "residual", bf, (M, HIDDEN))
+    if out is None:
+        out = torch.empty_like(residual)
+    _check_tensor(out, "out", bf, (M, HIDDEN))
+    h = handle if handle is not None else default_handle(attn_out.device.index)
+    mh3_out_proj_run(h, stream, M, attn_out, o_weight, gate, gate.stride(0), gate.shape[0],
+                     gate_index, residual, out)
+    return out
 
 
 def mh3_preattn_norm_adaln(handle: Handle, stream, M, x, x_norm_weight, adaln_scale,

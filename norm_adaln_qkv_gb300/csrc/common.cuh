@@ -29,6 +29,7 @@ enum : int {
   kStatusEpiTmemFull = 0x104,
   kStatusDrain = 0x105,
   kStatusRowFull = 0x106,
+  kStatusEpiResidual = 0x107,
 };
 
 struct NormAdalnParams {
@@ -69,6 +70,32 @@ struct QkvMaps {
   CUtensorMap b;    // qkv_weight [21504, 5376], box 64 x 256 (single) / 64 x 128 (pair)
   CUtensorMap out;  // out as 4-D (d 128, slot 168/P, m M, dst P), box 64x1x32x1
 };
+
+// ----------------------------------------- attention output projection
+// out = bf16(residual + bf16(gate[gate_index[m]] * bf16(attn_out @ o_weight^T)))
+constexpr int kAttnWidth = kHeads * kHeadDim;  // 7168
+
+struct OutProjParams {
+  const __nv_bfloat16* gate;  // [gate_rows, 5376] view
+  int64_t gate_stride;        // elements
+  int64_t gate_rows;
+  const int32_t* gate_index;  // [M]
+  int64_t M;
+  int num_m_tiles;  // 256-row blocks
+  int num_tiles;    // num_m_tiles * 21
+  int* status;
+};
+
+struct OutProjMaps {
+  CUtensorMap a;         // attn_out [M, 7168], box 64 x 128, 128-B swizzle
+  CUtensorMap b;         // o_weight [5376, 7168], box 64 x 128, 128-B swizzle
+  CUtensorMap out;       // out [M, 5376], box 64 x 32, 128-B swizzle (store)
+  CUtensorMap residual;  // residual [M, 5376], box 64 x 32, 128-B swizzle (load)
+};
+
+cudaError_t out_proj_prepare_device(int* max_clusters);
+cudaError_t launch_out_proj(const OutProjMaps& maps, const OutProjParams& p, int clusters,
+                            cudaStream_t stream);
 
 // Single-CTA form (128 x 256 tiles), used for M <= 128.
 int qkv_smem_bytes();

@@ -27,6 +27,7 @@ struct mh3_preattn_ctx {
   int device = 0;
   int num_sms = 0;
   int max_clusters = 0;  // resident 2-CTA clusters of the pair GEMM
+  int out_proj_clusters = 0;  // the same for the output projection
   int* d_status = nullptr;
   void* ws = nullptr;  // handle-owned workspace (grown on demand)
   size_t ws_bytes = 0;
@@ -185,6 +186,22 @@ int encode_maps(QkvMaps& maps, int64_t M, const mh3_bf16* ws, const mh3_bf16* W,
   return MH3_OK;
 }
 
+// 2-D row-major bf16 tensor [rows, cols] (cols contiguous), 128-B swizzle.
+int encode_2d(CUtensorMap* map, const void* base, uint64_t cols, uint64_t rows, uint32_t box_cols,
+              uint32_t box_rows, const char* what) {
+  PFN_cuTensorMapEncodeTiled_v12000 enc = encode_fn();
+  if (enc == nullptr) return fail(MH3_ERR_CUDA, "cuTensorMapEncodeTiled entry point not found");
+  const cuuint64_t dims[2] = {cols, rows};
+  const cuuint64_t strides[1] = {cols * 2};
+  const cuuint32_t box[2] = {box_cols, box_rows};
+  const cuuint32_t unit[2] = {1, 1};
+  CUresult r = enc(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base), dims, strides,
+                   box, unit, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                   CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  if (r != CUDA_SUCCESS) return fail(MH3_ERR_CUDA, "tensor map (%s) failed: %d", what, (int)r);
+  return MH3_OK;
+}
+
 int launch_stage1(cudaStream_t s, int num_sms, int* status, int64_t M, const mh3_bf16* x,
                   const mh3_bf16* xw, const mh3_bf16* sc, int64_t sc_stride, const mh3_bf16* sh,
                   int64_t sh_stride, int64_t rows, const int64_t* idx, float eps, mh3_bf16* ws) {
@@ -275,10 +292,14 @@ int mh3_preattn_create(mh3_preattn_t* handle, int device) {
   int max_clusters = 0;
   e = qkv_pair_prepare_device(&max_clusters);
   if (e != cudaSuccess) return cuda_fail(e, "preparing the pair GEMM");
+  int out_proj_clusters = 0;
+  e = out_proj_prepare_device(&out_proj_clusters);
+  if (e != cudaSuccess) return cuda_fail(e, "preparing the output-projection GEMM");
   mh3_preattn_ctx* h = new mh3_preattn_ctx();
   h->device = device;
   h->num_sms = prop.multiProcessorCount;
   h->max_clusters = max_clusters;
+  h->out_proj_clusters = out_proj_clusters;
   e = cudaMalloc(&h->d_status, sizeof(int));
   if (e == cudaSuccess) e = cudaMemset(h->d_status, 0, sizeof(int));
   if (e != cudaSuccess) {
@@ -418,6 +439,68 @@ int mh3_preattn_device_status(mh3_preattn_t h, void* stream, int* device_code) {
 }
 
 }  // extern "C"
+
+// --------------------------------------------- attention output projection
+extern "C" int mh3_out_proj_validate(int64_t M, const mh3_bf16* attn_out, const mh3_bf16* o_weight,
+                                     const mh3_bf16* gate, int64_t gate_row_stride,
+                                     int64_t gate_rows, const int32_t* gate_index,
+                                     const mh3_bf16* residual, const mh3_bf16* out) {
+  int rc;
+  if ((rc = check_M(M))) return rc;
+  if (gate_rows < 1)
+    return fail(MH3_ERR_INVALID_ARG, "gate_rows must be >= 1 (got %lld)", (long long)gate_rows);
+  if (gate_row_stride < kHidden)
+    return fail(MH3_ERR_INVALID_ARG, "gate_row_stride must be >= 5376 (got %lld)",
+                (long long)gate_row_stride);
+  if (gate_row_stride % 8 != 0)
+    return fail(MH3_ERR_ALIGNMENT, "gate_row_stride must be a multiple of 8 elements (got %lld)",
+                (long long)gate_row_stride);
+  if ((rc = check_ptr(o_weight, "o_weight", 16))) return rc;
+  if ((rc = check_ptr(gate, "gate", 16))) return rc;
+  if (M == 0) return MH3_OK;
+  if ((rc = check_ptr(attn_out, "attn_out", 16))) return rc;
+  if ((rc = check_ptr(gate_index, "gate_index", 4))) return rc;
+  if ((rc = check_ptr(residual, "residual", 16))) return rc;
+  if ((rc = check_ptr(out, "out", 16))) return rc;
+  const uintptr_t ro = reinterpret_cast<uintptr_t>(residual), oo = reinterpret_cast<uintptr_t>(out);
+  const uintptr_t bytes = static_cast<uintptr_t>(M) * kHidden * 2;
+  if (ro != oo && ro < oo + bytes && oo < ro + bytes)
+    return fail(MH3_ERR_INVALID_ARG, "out may equal residual but must not partially overlap it");
+  return MH3_OK;
+}
+
+extern "C" int mh3_out_proj_run(mh3_preattn_t h, void* stream, int64_t M, const mh3_bf16* attn_out,
+                                const mh3_bf16* o_weight, const mh3_bf16* gate,
+                                int64_t gate_row_stride, int64_t gate_rows,
+                                const int32_t* gate_index, const mh3_bf16* residual,
+                                mh3_bf16* out) {
+  int rc = check_handle(h);
+  if (rc) return rc;
+  rc = mh3_out_proj_validate(M, attn_out, o_weight, gate, gate_row_stride, gate_rows, gate_index,
+                             residual, out);
+  if (rc) return rc;
+  if (M == 0) return MH3_OK;
+  if (h->out_proj_clusters <= 0)
+    return fail(MH3_ERR_UNSUPPORTED, "no 2-CTA cluster of the output projection fits this device");
+  OutProjMaps maps;
+  if ((rc = encode_2d(&maps.a, attn_out, kAttnWidth, M, 64, 128, "attn_out"))) return rc;
+  if ((rc = encode_2d(&maps.b, o_weight, kAttnWidth, kHidden, 64, 128, "o_weight"))) return rc;
+  if ((rc = encode_2d(&maps.out, out, kHidden, M, 64, 32, "out"))) return rc;
+  if ((rc = encode_2d(&maps.residual, residual, kHidden, M, 64, 32, "residual"))) return rc;
+  OutProjParams p;
+  p.gate = reinterpret_cast<const __nv_bfloat16*>(gate);
+  p.gate_stride = gate_row_stride;
+  p.gate_rows = gate_rows;
+  p.gate_index = gate_index;
+  p.M = M;
+  p.status = h->d_status;
+  p.num_m_tiles = static_cast<int>((M + 255) / 256);
+  p.num_tiles = p.num_m_tiles * (kHidden / 256);
+  const int clusters = p.num_tiles < h->out_proj_clusters ? p.num_tiles : h->out_proj_clusters;
+  cudaError_t e = launch_out_proj(maps, p, clusters, static_cast<cudaStream_t>(stream));
+  if (e != cudaSuccess) return cuda_fail(e, "output projection launch");
+  return MH3_OK;
+}
 
 // ------------------------------------------------------ no-allocation variant
 // The whole stage for callers that cannot call cudaMalloc (for example code

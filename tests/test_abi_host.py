@@ -24,7 +24,7 @@ def lib():
 
 def declared_functions():
     text = open(HEADER).read()
-    return sorted(set(re.findall(r"^\s*(?:const\s+)?[\w\s\*]+?\b(mh3_preattn_\w+)\s*\(", text, re.M)))
+    return sorted(set(re.findall(r"^\s*(?:const\s+)?[\w\s\*]+?\b(mh3_\w+)\s*\(", text, re.M)))
 
 
 def test_header_declares_the_binding_exports():
@@ -110,3 +110,36 @@ def test_run_without_handle_is_rejected(lib):
         -1.0, None, a["out"])
     assert rc == 1
     assert "handle" in binding.last_error()
+
+
+def op_args(**over):
+    a = dict(M=64, attn_out=BASE, o_weight=BASE + 0x1000, gate=BASE + 0x2000,
+             gate_row_stride=6 * H, gate_rows=9, gate_index=BASE + 0x3000,
+             residual=BASE + 0x10000000, out=BASE + 0x20000000)
+    a.update(over)
+    return a
+
+
+def op_validate(**over):
+    return binding.mh3_out_proj_validate(**op_args(**over))
+
+
+def test_out_proj_validate_accepts_good_arguments(lib):
+    assert op_validate() == 0
+    assert op_validate(out=BASE + 0x10000000) == 0  # out may be the residual itself
+    assert op_validate(M=0, attn_out=None, gate_index=None, residual=None, out=None) == 0
+    assert op_validate(gate_row_stride=H, gate_rows=1) == 0
+
+
+@pytest.mark.parametrize("over,code", [
+    (dict(M=-1), 1), (dict(gate_rows=0), 1), (dict(gate_row_stride=H - 8), 1),
+    (dict(gate_row_stride=H + 4), 2), (dict(attn_out=None), 1), (dict(o_weight=None), 1),
+    (dict(gate=None), 1), (dict(gate_index=None), 1), (dict(residual=None), 1),
+    (dict(out=None), 1), (dict(attn_out=BASE + 8), 2), (dict(gate=BASE + 0x2002), 2),
+    (dict(gate_index=BASE + 0x3002), 2), (dict(out=BASE + 0x20000008), 2),
+    # partial overlap of out and residual (64 rows x 10752 B)
+    (dict(out=BASE + 0x10000000 + 10752 * 3), 1),
+])
+def test_out_proj_validate_rejects(lib, over, code):
+    assert op_validate(**over) == code
+    assert binding.last_error() != ""
