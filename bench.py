@@ -461,6 +461,44 @@ def run_ours(args, world, rank, local):
     print(json.dumps(line), flush=True)
 
 
+def run_out_proj_only(args, world, rank, local):
+    """The attention output projection alone (small cases and profiling)."""
+    from norm_adaln_qkv_gb300 import binding, build
+    from norm_adaln_qkv_gb300.inputs import make_out_proj_workload
+    torch.cuda.set_device(local)
+    build.build()
+    h = binding.Handle(local)
+    dev = torch.device("cuda", local)
+    stream = torch.cuda.current_stream(dev)
+    peaks = _peaks()
+    wo = make_out_proj_workload(args.op_tokens)
+    mod = wo.adaln_mod.to(dev)
+    gate = wo.gate_view(mod)
+    a, W, gi, res = (wo.attn_out.to(dev), wo.o_weight.to(dev), wo.gate_index.to(dev),
+                     wo.residual.to(dev))
+    out = torch.empty_like(res)
+
+    def call():
+        binding.mh3_out_proj_run(h, stream, wo.M, a, W, gate, gate.stride(0), gate.shape[0], gi,
+                                 res, out)
+    for _ in range(max(args.warmup, 3)):
+        call()
+    torch.cuda.synchronize()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for _ in range(args.steps):
+        call()
+    e1.record(stream)
+    torch.cuda.synchronize()
+    assert h.device_status(stream) == 0, "a kernel recorded a timeout"
+    ms = e0.elapsed_time(e1) / args.steps
+    tf = OUT_PROJ_FLOP_PER_TOKEN * wo.M / (ms * 1e-3) / 1e12
+    if rank == 0:
+        print(json.dumps({"only": "out_proj", "M": wo.M, "us": ms * 1e3, "tflops": tf,
+                          "frac_of_measured_bf16": tf / peaks["bf16"], "steps": args.steps}),
+              flush=True)
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -474,10 +512,16 @@ def main():
     ap.add_argument("--skip-also", action="store_true", help="skip the M=4096 side measurement")
     ap.add_argument("--workload", default=WORKLOAD, choices=["c0", "c1", "c2", "c3", "c4"],
                     help="seeded workload (default: the M=32760 production sequence)")
+    ap.add_argument("--only", choices=["stage", "out_proj"], default="stage",
+                    help="out_proj: time the output projection alone (no JSON bench line)")
+    ap.add_argument("--op-tokens", type=int, default=4096,
+                    help="tokens of the --only out_proj case")
     args = ap.parse_args()
     world, rank, local = _dist()
     if args.impl == "reference":
         run_reference(args, world, rank)
+    elif args.only == "out_proj":
+        run_out_proj_only(args, world, rank, local)
     else:
         run_ours(args, world, rank, local)
     if world > 1 and torch.distributed.is_initialized():

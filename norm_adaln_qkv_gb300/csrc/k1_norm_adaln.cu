@@ -18,8 +18,8 @@
 // one fixed order by every thread.  r = 1 / sqrt(ss/H + eps) uses IEEE
 // division and square root; the elementwise steps are packed two-lane FP32
 // operations (each lane one IEEE round-to-nearest operation, in the
-// formula's order, never contracted into an FMA) and one bf16x2 add for
-// bf16(1 + scale).  The guard is an int64 compare: a bad index writes +0.0
+// formula's order; the one fused multiply-add computes shift + n * g, whose
+// product is exact) and one bf16x2 add for bf16(1 + scale).  The guard is an int64 compare: a bad index writes +0.0
 // and never forms a table address.  Workspace stores keep the default
 // write-back policy so the GEMM that follows finds the rows in L2 when they
 // fit.  The ring wait is bounded (2 s) and records a status code instead of
@@ -70,9 +70,10 @@ __device__ __forceinline__ uint32_t adaln_pair(uint64_t x2, uint32_t w, uint32_t
   const uint32_t n = f2_to_bf16x2(f2_mul(f2_mul(x2, r2), f2_from_bf16x2(w)));
   // g = bf16(1 + scale): one correctly rounded bf16 addition per lane
   const uint32_t g = bf16x2_add(0x3F803F80u, sc);
-  // a = bf16(shift + n * g), multiply and add rounded separately
-  const uint64_t ng = f2_mul(f2_from_bf16x2(n), f2_from_bf16x2(g));
-  return f2_to_bf16x2(f2_add(f2_from_bf16x2(sh), ng));
+  // a = bf16(shift + n * g).  n and g are bf16, so n * g (at most 16
+  // significant bits) is exact in FP32 and one fused multiply-add rounds
+  // exactly as the multiply followed by the rounded add.
+  return f2_to_bf16x2(f2_fma(f2_from_bf16x2(n), f2_from_bf16x2(g), f2_from_bf16x2(sh)));
 }
 
 __global__ void __launch_bounds__(kThreads, kCtasPerSm) norm_adaln_kernel(const NormAdalnParams p) {
