@@ -75,16 +75,20 @@ struct QkvMaps {
 // out = bf16(residual + bf16(gate[gate_index[m]] * bf16(attn_out @ o_weight^T)))
 constexpr int kAttnWidth = kHeads * kHeadDim;  // 7168
 
-struct OutProjParams {
+// Parameters of a GEMM whose epilogue applies the gated residual
+// out = bf16(residual + bf16(gate[index[m]] * o)); IndexT is the index type.
+template <typename IndexT>
+struct GatedResidualParams {
   const __nv_bfloat16* gate;  // [gate_rows, 5376] view
   int64_t gate_stride;        // elements
   int64_t gate_rows;
-  const int32_t* gate_index;  // [M]
+  const IndexT* gate_index;   // [M]
   int64_t M;
   int num_m_tiles;  // 256-row blocks
   int num_tiles;    // num_m_tiles * 21
   int* status;
 };
+using OutProjParams = GatedResidualParams<int32_t>;
 
 struct OutProjMaps {
   CUtensorMap a;         // attn_out [M, 7168], box 64 x 128, 128-B swizzle

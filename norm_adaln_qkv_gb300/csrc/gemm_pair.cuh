@@ -5,7 +5,8 @@
 //   struct Epi {
 //     using Params = ...;                    // has M, num_m_tiles, num_tiles, status
 //     static constexpr int kKBlocks;         // K / 64
-//     static constexpr int kNTiles;          // N / 256
+//     static constexpr int kNTiles;          // number of 256-column accumulator tiles
+//     __device__ static int b_row(int n_blk, int rank);  // first B row CTA `rank` loads
 //     __device__ static void prologue(float* scratch, int tid, int nthreads, const Params&);
 //     __device__ static void tile(const EpiCtx&, const Params&, int64_t row0, int n_blk);
 //   };
@@ -115,6 +116,11 @@ __device__ __noinline__ inline void grace_period() {
   }
 }
 
+// The usual B split: the tile's 256 B rows, 128 per CTA of the pair.
+__device__ __forceinline__ int contiguous_b_row(int n_blk, int rank) {
+  return n_blk * kTileN + rank * BNC;
+}
+
 // What an epilogue warp gets for one 128-row x 256-column accumulator block.
 struct EpiCtx {
   uint32_t tmem_acc;  // TMEM address of the block (lane 0, first column)
@@ -195,7 +201,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
         int pr, n_blk;
         tile_coords<kGroupPairs, kN>(t, p.num_m_tiles, pr, n_blk);
         const int a_row = pr * kPairRows + static_cast<int>(rank) * BM;
-        const int b_row = n_blk * kTileN + static_cast<int>(rank) * BNC;
+        const int b_row = Epi::b_row(n_blk, static_cast<int>(rank));
         for (int kb = 0; kb < kKB; ++kb) {
           if (!pair_wait(ctx, sm.empty(stage), phase ^ 1u, kStatusProducerEmpty)) {
             ok = false;

@@ -19,6 +19,7 @@ struct QkvPairEpi {
   using Params = QkvParams;
   static constexpr int kKBlocks = k2::kKBlocks;  // 84
   static constexpr int kNTiles = k2::kNTiles;    // 84
+  __device__ static int b_row(int n_blk, int rank) { return gp::contiguous_b_row(n_blk, rank); }
 
   // q then k norm weights, as FP32, into the epilogue scratch.
   __device__ static void prologue(float* scratch, int tid, int nthreads, const Params& p) {

@@ -328,3 +328,54 @@ def make_out_proj_workload(M: int, seed: int = SEED_BASE + 100, rows: int = 9,
         res[r0:r1] = _normal(gen, (r1 - r0, HIDDEN)).to(torch.bfloat16)
     return OutProjWorkload(M=M, attn_out=attn, o_weight=w, adaln_mod=mod, gate_index=gi,
                            residual=res)
+
+
+# ------------------------------------------------------------- the MLP block
+MLP_INTER = 14336  # SwiGLU width; fc1 has 2 * 14336 = 28672 rows [gate | up]
+MLP_CHUNKS = (3, 4, 5)  # shift, scale, gate of the MLP in the [rows, 6*hidden] plan
+
+
+@dataclass
+class MlpWorkload:
+    """Host tensors of one MLP-block case (shapes of
+    flashinfer.diffusion_ops.minimax_h3_mlp_fp8_sm120, Parameters: x [M, 5376],
+    tables [rows, 5376] sharing one row count, int64 adaln_index, residual
+    [M, 5376], fc1 [28672, 5376], fc2 [5376, 14336]), with bf16 weights."""
+
+    M: int
+    x: torch.Tensor
+    x_norm_weight: torch.Tensor
+    adaln_mod: torch.Tensor  # [rows, 6*HIDDEN]
+    adaln_index: torch.Tensor
+    residual: torch.Tensor
+    fc1_weight: torch.Tensor
+    fc2_weight: torch.Tensor
+    eps: float = 1e-5
+
+    def tables(self, mod: Optional[torch.Tensor] = None):
+        """(scale, shift, gate) views of the modulation tensor."""
+        mod = self.adaln_mod if mod is None else mod
+        sh, sc, gt = (mod[:, c * HIDDEN:(c + 1) * HIDDEN] for c in MLP_CHUNKS)
+        return sc, sh, gt
+
+
+def make_mlp_workload(M: int, seed: int = SEED_BASE + 200, rows: int = 9,
+                      bad_rate: float = 0.01) -> MlpWorkload:
+    """x, residual ~ N(0,1); x_norm_weight 1 + 0.1*N(0,1); modulation
+    0.1*N(0,1); fc1 ~ N(0, 1/5376); fc2 ~ N(0, 1/14336); index uniform in
+    [0, rows) with bad_rate of the tokens set cyclically to -1, 9, 2^40."""
+    gen = torch.Generator().manual_seed(seed)
+    x = _x_bf16(gen, M, 1.0)
+    xw = (1.0 + 0.1 * _normal(gen, (HIDDEN,))).to(torch.bfloat16)
+    mod = (0.1 * _normal(gen, (rows, 6 * HIDDEN))).to(torch.bfloat16)
+    idx = torch.randint(0, rows, (M,), generator=gen, dtype=torch.int64)
+    n_bad = int(round(bad_rate * M))
+    if n_bad:
+        toks = torch.randperm(M, generator=gen)[:n_bad]
+        for j, t in enumerate(toks.tolist()):
+            idx[t] = BAD_INDEX_CYCLE[j % len(BAD_INDEX_CYCLE)]
+    res = _x_bf16(gen, M, 1.0)
+    fc1 = (_normal(gen, (2 * MLP_INTER, HIDDEN)) / math.sqrt(HIDDEN)).to(torch.bfloat16)
+    fc2 = (_normal(gen, (HIDDEN, MLP_INTER)) / math.sqrt(MLP_INTER)).to(torch.bfloat16)
+    return MlpWorkload(M=M, x=x, x_norm_weight=xw, adaln_mod=mod, adaln_index=idx, residual=res,
+                       fc1_weight=fc1, fc2_weight=fc2)

@@ -28,3 +28,4 @@ from .preattn import (  # noqa: F401
     PreAttnTokens,
 )
 from . import out_proj  # noqa: F401  (attention output projection + gated residual)
+from . import mlp  # noqa: F401  (MLP block)
