@@ -43,6 +43,7 @@ K2_SOURCES = ("norm_adaln_qkv_gb300/csrc/k2_qkv_gemm_pair.cu",
               "norm_adaln_qkv_gb300/csrc/k2_common.cuh", "norm_adaln_qkv_gb300/csrc/ptx.cuh",
               "norm_adaln_qkv_gb300/csrc/common.cuh")
 OUT_PROJ_FLOP_PER_TOKEN = 2 * 7168 * 5376
+MLP_FLOP_PER_TOKEN = 2 * 5376 * 28672 + 2 * 14336 * 5376
 TRAFFIC_FILE = os.path.join(ROOT, "profiles", "k2_traffic.json")
 
 
@@ -408,6 +409,39 @@ def run_ours(args, world, rank, local):
         out_proj = {"workload": f"out-projection + gated residual, M={wo.M}, K=7168, N=5376",
                     "us": op_ms * 1e3, "tflops": op_tf, "frac_of_measured_bf16": op_tf / peaks["bf16"]}
         del ao, Wo, gio, reso, outo, mod_o
+    # ---- the MLP block (norm/AdaLN, fc1 + SwiGLU, fc2 + gated residual)
+    mlp_line = None
+    if not args.skip_also:
+        from norm_adaln_qkv_gb300.inputs import make_mlp_workload
+        wm = make_mlp_workload(wl.M)
+        mod_m = wm.adaln_mod.to(dev)
+        sc_m, sh_m, gt_m = wm.tables(mod_m)
+        xm, xwm, im, rm = (wm.x.to(dev), wm.x_norm_weight.to(dev), wm.adaln_index.to(dev),
+                           wm.residual.to(dev))
+        f1, f2 = wm.fc1_weight.to(dev), wm.fc2_weight.to(dev)
+        wam = torch.empty((wm.M, 5376), dtype=torch.bfloat16, device=dev)
+        wym = torch.empty((wm.M, 14336), dtype=torch.bfloat16, device=dev)
+        outm = torch.empty_like(rm)
+
+        def mlp_call():
+            binding.mh3_mlp_run(h, stream, wm.M, xm, xwm, sc_m, sc_m.stride(0), sh_m,
+                                sh_m.stride(0), gt_m, gt_m.stride(0), sc_m.shape[0], im, rm, f1,
+                                f2, wm.eps, wam, wym, outm)
+        for _ in range(3):
+            mlp_call()
+        torch.cuda.synchronize()
+        m0, m1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        m0.record(stream)
+        for _ in range(args.steps):
+            mlp_call()
+        m1.record(stream)
+        torch.cuda.synchronize()
+        mlp_ms = m0.elapsed_time(m1) / args.steps
+        mlp_tf = MLP_FLOP_PER_TOKEN * wm.M / (mlp_ms * 1e-3) / 1e12
+        mlp_line = {"workload": f"MLP block (bf16), M={wm.M}, 5376 -> 2x14336 -> 5376",
+                    "us": mlp_ms * 1e3, "tflops": mlp_tf,
+                    "frac_of_measured_bf16": mlp_tf / peaks["bf16"], "launches_per_call": 3}
+        del xm, f1, f2, wam, wym, outm, rm
     clk = clocks.stop()
     assert h.device_status(stream) == 0, "a kernel recorded a timeout"
 
@@ -457,6 +491,7 @@ def run_ours(args, world, rank, local):
         "clocks": clk,
         "also": also,
         "out_proj": out_proj,
+        "mlp": mlp_line,
     }
     print(json.dumps(line), flush=True)
 

@@ -234,6 +234,56 @@ int mh3_out_proj_validate(int64_t M, const mh3_bf16* attn_out, const mh3_bf16* o
                           const int32_t* gate_index, const mh3_bf16* residual,
                           const mh3_bf16* out);
 
+/* ---------------------------------------------------------------------------
+ * The MLP block with BF16 operands, after the formula block of the page
+ * "flashinfer.diffusion_ops.minimax_h3_mlp_fp8_sm120" without its FP8 lines:
+ *
+ *   n   = bf16(rmsnorm(x, eps) * x_norm_weight)
+ *   a   = bf16(shift[i] + n * bf16(1 + scale[i]))     i = adaln_index[m]
+ *   a   = 0 for the whole row when i is outside [0, rows)
+ *   h   = bf16(a @ fc1_weight^T)                      [M, 28672], FP32 accumulation
+ *   y   = bf16(bf16(silu(h_gate)) * h_up)             h_gate = h[:, :14336], h_up = h[:, 14336:]
+ *   o   = bf16(y @ fc2_weight^T)                      [M, 5376], FP32 accumulation
+ *   out = bf16(residual + bf16(gate[i] * o))          gate 0 (out = residual) for a bad i
+ *
+ * Three launches on `stream`: kernel 1 of the pre-attention stage into
+ * workspace_a, fc1 with the SwiGLU epilogue into workspace_y, fc2 with the
+ * gated-residual epilogue into out.  No host synchronisation.
+ *
+ *   x, x_norm_weight, adaln_scale/shift (+ row strides), rows, adaln_index, eps
+ *                     as in mh3_preattn_run
+ *   gate              [rows, 5376] view, row stride gate_row_stride (elements,
+ *                     >= 5376, multiple of 8), base 16-B aligned
+ *   residual          [M, 5376] row-major, 16-B aligned
+ *   fc1_weight        [28672, 5376] row-major: rows [0, 14336) the gate
+ *                     projection, rows [14336, 28672) the up projection
+ *   fc2_weight        [5376, 14336] row-major
+ *   workspace_a       [M, 5376] bf16 scratch or NULL (handle-owned)
+ *   workspace_y       [M, 14336] bf16 scratch or NULL (handle-owned); with NULL
+ *                     workspaces, runs of one handle on different streams race
+ *   out               [M, 5376], 16-B aligned; may be residual or x itself
+ *                     (both are read before out is written), must not
+ *                     partially overlap either */
+int mh3_mlp_run(mh3_preattn_t handle, void* stream, int64_t M, const mh3_bf16* x,
+                const mh3_bf16* x_norm_weight, const mh3_bf16* adaln_scale,
+                int64_t scale_row_stride, const mh3_bf16* adaln_shift, int64_t shift_row_stride,
+                const mh3_bf16* gate, int64_t gate_row_stride, int64_t rows,
+                const int64_t* adaln_index, const mh3_bf16* residual, const mh3_bf16* fc1_weight,
+                const mh3_bf16* fc2_weight, float eps, mh3_bf16* workspace_a,
+                mh3_bf16* workspace_y, mh3_bf16* out);
+
+/* Host-only validation of an mh3_mlp_run argument set; same rules and codes. */
+int mh3_mlp_validate(int64_t M, const mh3_bf16* x, const mh3_bf16* x_norm_weight,
+                     const mh3_bf16* adaln_scale, int64_t scale_row_stride,
+                     const mh3_bf16* adaln_shift, int64_t shift_row_stride, const mh3_bf16* gate,
+                     int64_t gate_row_stride, int64_t rows, const int64_t* adaln_index,
+                     const mh3_bf16* residual, const mh3_bf16* fc1_weight,
+                     const mh3_bf16* fc2_weight, float eps, const mh3_bf16* workspace_a,
+                     const mh3_bf16* workspace_y, const mh3_bf16* out);
+
+/* Bytes of the MLP intermediate y, [M, 14336] bf16: M * 14336 * 2 (0 for M <= 0). */
+size_t mh3_mlp_workspace_y_bytes(int64_t M);
+
 /* Message of the calling thread's last failed call ("" if none). */
 const char* mh3_preattn_last_error(void);
 

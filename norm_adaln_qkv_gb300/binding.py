@@ -33,7 +33,8 @@ EXPORTS = ("mh3_preattn_create", "mh3_preattn_destroy", "mh3_preattn_workspace_b
            "mh3_preattn_out_bytes", "mh3_preattn_validate", "mh3_preattn_run",
            "mh3_preattn_norm_adaln", "mh3_preattn_qkv", "mh3_preattn_device_status",
            "mh3_preattn_last_error", "mh3_preattn_run_noalloc", "mh3_out_proj_run",
-           "mh3_out_proj_validate")
+           "mh3_out_proj_validate", "mh3_mlp_run", "mh3_mlp_validate",
+           "mh3_mlp_workspace_y_bytes")
 
 _vp = ctypes.c_void_p
 _i64 = ctypes.c_int64
@@ -56,6 +57,11 @@ _SIGS = {
     "mh3_preattn_last_error": (ctypes.c_char_p, []),
     "mh3_out_proj_run": (_i32, [_vp, _vp, _i64, _vp, _vp, _vp, _i64, _i64, _vp, _vp, _vp]),
     "mh3_out_proj_validate": (_i32, [_i64, _vp, _vp, _vp, _i64, _i64, _vp, _vp, _vp]),
+    "mh3_mlp_run": (_i32, [_vp, _vp, _i64, _vp, _vp, _vp, _i64, _vp, _i64, _vp, _i64, _i64, _vp, _vp,
+                           _vp, _vp, _f32, _vp, _vp, _vp]),
+    "mh3_mlp_validate": (_i32, [_i64, _vp, _vp, _vp, _i64, _vp, _i64, _vp, _i64, _i64, _vp, _vp,
+                                _vp, _vp, _f32, _vp, _vp, _vp]),
+    "mh3_mlp_workspace_y_bytes": (ctypes.c_size_t, [_i64]),
     "mh3_preattn_run_noalloc": (_i32, [_vp, _i64, _vp, _vp, _vp, _i64, _vp, _i64, _i64, _vp, _vp,
                                        _vp, _vp, _vp, _i64, _vp, _i32, _f32, _f32, _vp, _vp]),
 }
@@ -237,6 +243,59 @@ def minimax_h3_bf16_out_proj(attn_out, o_weight, gate, gate_index, residual, *,
     h = handle if handle is not None else default_handle(attn_out.device.index)
     mh3_out_proj_run(h, stream, M, attn_out, o_weight, gate, gate.stride(0), gate.shape[0],
                      gate_index, residual, out)
+    return out
+
+
+def mh3_mlp_validate(M, x, x_norm_weight, adaln_scale, scale_row_stride, adaln_shift,
+                     shift_row_stride, gate, gate_row_stride, rows, adaln_index, residual,
+                     fc1_weight, fc2_weight, eps, workspace_a, workspace_y, out) -> int:
+    """Host-only validation of an MLP call; returns the status code."""
+    return load().mh3_mlp_validate(
+        M, _ptr(x), _ptr(x_norm_weight), _ptr(adaln_scale), scale_row_stride, _ptr(adaln_shift),
+        shift_row_stride, _ptr(gate), gate_row_stride, rows, _ptr(adaln_index), _ptr(residual),
+        _ptr(fc1_weight), _ptr(fc2_weight), float(eps), _ptr(workspace_a), _ptr(workspace_y),
+        _ptr(out))
+
+
+def mh3_mlp_run(handle: Handle, stream, M, x, x_norm_weight, adaln_scale, scale_row_stride,
+                adaln_shift, shift_row_stride, gate, gate_row_stride, rows, adaln_index, residual,
+                fc1_weight, fc2_weight, eps, workspace_a, workspace_y, out) -> None:
+    _check(load().mh3_mlp_run(
+        handle.ptr, _stream_ptr(stream), M, _ptr(x), _ptr(x_norm_weight), _ptr(adaln_scale),
+        scale_row_stride, _ptr(adaln_shift), shift_row_stride, _ptr(gate), gate_row_stride, rows,
+        _ptr(adaln_index), _ptr(residual), _ptr(fc1_weight), _ptr(fc2_weight), float(eps),
+        _ptr(workspace_a), _ptr(workspace_y), _ptr(out)), "mh3_mlp_run")
+
+
+def minimax_h3_bf16_mlp(x, x_norm_weight, adaln_scale, adaln_shift, adaln_index, gate, residual,
+                        fc1_weight, fc2_weight, *, out: Optional[torch.Tensor] = None,
+                        workspace_a=None, workspace_y=None, eps: float = 1e-5, stream=None,
+                        handle: Optional[Handle] = None) -> torch.Tensor:
+    """Torch-tensor entry point of the MLP block (argument names of
+    flashinfer.diffusion_ops.minimax_h3_mlp_fp8_sm120, BF16 weights); returns
+    ``out`` (allocated when None; may be ``residual`` or ``x``)."""
+    M = x.shape[0]
+    bf = torch.bfloat16
+    _check_tensor(x, "x", bf, (M, HIDDEN))
+    _check_tensor(x_norm_weight, "x_norm_weight", bf, (HIDDEN,))
+    for name, t in (("adaln_scale", adaln_scale), ("adaln_shift", adaln_shift), ("gate", gate)):
+        _check_tensor(t, name, bf, contiguous=False)
+        if t.dim() != 2 or t.shape[1] != HIDDEN or t.stride(1) != 1:
+            raise ValueError(f"{name} must be [rows, {HIDDEN}] with stride(1) == 1")
+    rows = adaln_scale.shape[0]
+    if adaln_shift.shape[0] != rows or gate.shape[0] != rows:
+        raise ValueError("adaln_scale, adaln_shift and gate must share one row count")
+    _check_tensor(adaln_index, "adaln_index", torch.int64, (M,))
+    _check_tensor(residual, "residual", bf, (M, HIDDEN))
+    _check_tensor(fc1_weight, "fc1_weight", bf, (2 * 14336, HIDDEN))
+    _check_tensor(fc2_weight, "fc2_weight", bf, (HIDDEN, 14336))
+    if out is None:
+        out = torch.empty_like(residual)
+    _check_tensor(out, "out", bf, (M, HIDDEN))
+    h = handle if handle is not None else default_handle(x.device.index)
+    mh3_mlp_run(h, stream, M, x, x_norm_weight, adaln_scale, adaln_scale.stride(0), adaln_shift,
+                adaln_shift.stride(0), gate, gate.stride(0), rows, adaln_index, residual,
+                fc1_weight, fc2_weight, eps, workspace_a, workspace_y, out)
     return out
 
 

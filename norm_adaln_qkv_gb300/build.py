@@ -1,7 +1,7 @@
 """Build the C-ABI library ``libmh3_preattn.so`` in-tree with nvcc for sm_103a.
 
-Five translation units (the C ABI host code, kernel 1, the two forms of
-kernel 2, the output projection) are
+Six translation units (the C ABI host code, kernel 1, the two forms of
+kernel 2, the output projection, the MLP GEMMs) are
 compiled in parallel and linked with the CUDA runtime linked statically, so
 the library loads on a machine without a GPU driver (the driver is resolved
 on the first CUDA call).  Output: ``norm_adaln_qkv_gb300/libmh3_preattn.so``.
@@ -19,7 +19,7 @@ CSRC = os.path.join(PKG, "csrc")
 BUILD = os.path.join(PKG, "_build")
 LIB = os.path.join(PKG, "libmh3_preattn.so")
 SOURCES = ["mh3_preattn.cu", "k1_norm_adaln.cu", "k2_qkv_gemm.cu", "k2_qkv_gemm_pair.cu",
-           "out_proj.cu"]
+           "out_proj.cu", "mlp.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 
 

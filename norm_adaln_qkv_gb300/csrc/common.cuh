@@ -101,6 +101,28 @@ cudaError_t out_proj_prepare_device(int* max_clusters);
 cudaError_t launch_out_proj(const OutProjMaps& maps, const OutProjParams& p, int clusters,
                             cudaStream_t stream);
 
+// ------------------------------------------------------------- the MLP block
+constexpr int kMlpInter = 14336;  // SwiGLU width; fc1 rows [gate | up] = 28672
+
+struct SwigluParams {
+  int64_t M;
+  int num_m_tiles;  // 256-row blocks
+  int num_tiles;    // num_m_tiles * 112
+  int* status;
+};
+
+// fc1 + SwiGLU: y = bf16(bf16(silu(h_gate)) * h_up), h = bf16(a @ fc1^T).
+//   a: workspace [M, 5376]; b: fc1 [28672, 5376]; out: y [M, 14336] (store).
+cudaError_t mlp_fc1_prepare_device(int* max_clusters);
+cudaError_t launch_mlp_fc1(const CUtensorMap& a, const CUtensorMap& b, const CUtensorMap& y,
+                           const SwigluParams& p, int clusters, cudaStream_t stream);
+// fc2 + gated residual: out = bf16(residual + bf16(gate[i] * bf16(y @ fc2^T))).
+//   a: y [M, 14336]; b: fc2 [5376, 14336]; out, residual: [M, 5376].
+cudaError_t mlp_fc2_prepare_device(int* max_clusters);
+cudaError_t launch_mlp_fc2(const CUtensorMap& a, const CUtensorMap& b, const CUtensorMap& out,
+                           const CUtensorMap& residual, const GatedResidualParams<int64_t>& p,
+                           int clusters, cudaStream_t stream);
+
 // Single-CTA form (128 x 256 tiles), used for M <= 128.
 int qkv_smem_bytes();
 cudaError_t qkv_prepare_device();  // raise the dynamic shared-memory limit

@@ -28,6 +28,10 @@ struct mh3_preattn_ctx {
   int num_sms = 0;
   int max_clusters = 0;  // resident 2-CTA clusters of the pair GEMM
   int out_proj_clusters = 0;  // the same for the output projection
+  int fc1_clusters = 0;       // ... and the two MLP GEMMs
+  int fc2_clusters = 0;
+  void* ws_y = nullptr;  // handle-owned MLP intermediate y [M, 14336]
+  size_t ws_y_bytes = 0;
   int* d_status = nullptr;
   void* ws = nullptr;  // handle-owned workspace (grown on demand)
   size_t ws_bytes = 0;
@@ -186,6 +190,25 @@ int encode_maps(QkvMaps& maps, int64_t M, const mh3_bf16* ws, const mh3_bf16* W,
   return MH3_OK;
 }
 
+// Grow a handle-owned buffer to `need` bytes with stream-ordered allocation.
+int grow_buffer(void** buf, size_t* cap, size_t need, cudaStream_t s) {
+  if (*cap >= need) return MH3_OK;
+  if (*buf) {
+    cudaError_t e = cudaFreeAsync(*buf, s);
+    *buf = nullptr;
+    *cap = 0;
+    if (e != cudaSuccess) return cuda_fail(e, "cudaFreeAsync (workspace)");
+  }
+  cudaError_t e = cudaMallocAsync(buf, need, s);
+  if (e != cudaSuccess) {
+    *buf = nullptr;
+    return fail(MH3_ERR_OOM, "cudaMallocAsync of %zu B workspace failed: %s", need,
+                cudaGetErrorString(e));
+  }
+  *cap = need;
+  return MH3_OK;
+}
+
 // 2-D row-major bf16 tensor [rows, cols] (cols contiguous), 128-B swizzle.
 int encode_2d(CUtensorMap* map, const void* base, uint64_t cols, uint64_t rows, uint32_t box_cols,
               uint32_t box_rows, const char* what) {
@@ -295,8 +318,14 @@ int mh3_preattn_create(mh3_preattn_t* handle, int device) {
   int out_proj_clusters = 0;
   e = out_proj_prepare_device(&out_proj_clusters);
   if (e != cudaSuccess) return cuda_fail(e, "preparing the output-projection GEMM");
+  int fc1_clusters = 0, fc2_clusters = 0;
+  e = mlp_fc1_prepare_device(&fc1_clusters);
+  if (e == cudaSuccess) e = mlp_fc2_prepare_device(&fc2_clusters);
+  if (e != cudaSuccess) return cuda_fail(e, "preparing the MLP GEMMs");
   mh3_preattn_ctx* h = new mh3_preattn_ctx();
   h->device = device;
+  h->fc1_clusters = fc1_clusters;
+  h->fc2_clusters = fc2_clusters;
   h->num_sms = prop.multiProcessorCount;
   h->max_clusters = max_clusters;
   h->out_proj_clusters = out_proj_clusters;
@@ -317,6 +346,10 @@ int mh3_preattn_destroy(mh3_preattn_t h) {
   if (h->ws) {
     cudaError_t e = cudaFree(h->ws);
     if (e != cudaSuccess) rc = cuda_fail(e, "freeing the handle workspace");
+  }
+  if (h->ws_y) {
+    cudaError_t e = cudaFree(h->ws_y);
+    if (e != cudaSuccess && rc == MH3_OK) rc = cuda_fail(e, "freeing the handle workspace");
   }
   if (h->d_status) {
     cudaError_t e = cudaFree(h->d_status);
@@ -499,6 +532,107 @@ extern "C" int mh3_out_proj_run(mh3_preattn_t h, void* stream, int64_t M, const 
   const int clusters = p.num_tiles < h->out_proj_clusters ? p.num_tiles : h->out_proj_clusters;
   cudaError_t e = launch_out_proj(maps, p, clusters, static_cast<cudaStream_t>(stream));
   if (e != cudaSuccess) return cuda_fail(e, "output projection launch");
+  return MH3_OK;
+}
+
+// ------------------------------------------------------------- MLP block
+extern "C" size_t mh3_mlp_workspace_y_bytes(int64_t M) {
+  return M <= 0 ? 0 : static_cast<size_t>(M) * kMlpInter * 2;
+}
+
+extern "C" int mh3_mlp_validate(int64_t M, const mh3_bf16* x, const mh3_bf16* x_norm_weight,
+                                const mh3_bf16* adaln_scale, int64_t scale_row_stride,
+                                const mh3_bf16* adaln_shift, int64_t shift_row_stride,
+                                const mh3_bf16* gate, int64_t gate_row_stride, int64_t rows,
+                                const int64_t* adaln_index, const mh3_bf16* residual,
+                                const mh3_bf16* fc1_weight, const mh3_bf16* fc2_weight,
+                                float eps, const mh3_bf16* workspace_a,
+                                const mh3_bf16* workspace_y, const mh3_bf16* out) {
+  int rc = check_norm_adaln_args(M, x, x_norm_weight, adaln_scale, scale_row_stride, adaln_shift,
+                                 shift_row_stride, rows, adaln_index, eps, workspace_a, false);
+  if (rc) return rc;
+  if (gate_row_stride < kHidden)
+    return fail(MH3_ERR_INVALID_ARG, "gate_row_stride must be >= 5376 (got %lld)",
+                (long long)gate_row_stride);
+  if (gate_row_stride % 8 != 0)
+    return fail(MH3_ERR_ALIGNMENT, "gate_row_stride must be a multiple of 8 elements (got %lld)",
+                (long long)gate_row_stride);
+  if ((rc = check_ptr(gate, "gate", 16))) return rc;
+  if ((rc = check_ptr(fc1_weight, "fc1_weight", 16))) return rc;
+  if ((rc = check_ptr(fc2_weight, "fc2_weight", 16))) return rc;
+  if (M == 0) return MH3_OK;
+  if ((rc = check_ptr(residual, "residual", 16))) return rc;
+  if ((rc = check_ptr(out, "out", 16))) return rc;
+  if (workspace_y != nullptr && (rc = check_ptr(workspace_y, "workspace_y", 16))) return rc;
+  const uintptr_t bytes = static_cast<uintptr_t>(M) * kHidden * 2;
+  const uintptr_t oo = reinterpret_cast<uintptr_t>(out);
+  const uintptr_t cands[2] = {reinterpret_cast<uintptr_t>(residual), reinterpret_cast<uintptr_t>(x)};
+  for (uintptr_t c : cands)
+    if (c != oo && c < oo + bytes && oo < c + bytes)
+      return fail(MH3_ERR_INVALID_ARG, "out may equal residual or x but must not partially overlap them");
+  return MH3_OK;
+}
+
+extern "C" int mh3_mlp_run(mh3_preattn_t h, void* stream, int64_t M, const mh3_bf16* x,
+                           const mh3_bf16* x_norm_weight, const mh3_bf16* adaln_scale,
+                           int64_t scale_row_stride, const mh3_bf16* adaln_shift,
+                           int64_t shift_row_stride, const mh3_bf16* gate,
+                           int64_t gate_row_stride, int64_t rows, const int64_t* adaln_index,
+                           const mh3_bf16* residual, const mh3_bf16* fc1_weight,
+                           const mh3_bf16* fc2_weight, float eps, mh3_bf16* workspace_a,
+                           mh3_bf16* workspace_y, mh3_bf16* out) {
+  int rc = check_handle(h);
+  if (rc) return rc;
+  rc = mh3_mlp_validate(M, x, x_norm_weight, adaln_scale, scale_row_stride, adaln_shift,
+                        shift_row_stride, gate, gate_row_stride, rows, adaln_index, residual,
+                        fc1_weight, fc2_weight, eps, workspace_a, workspace_y, out);
+  if (rc) return rc;
+  if (M == 0) return MH3_OK;
+  if (h->fc1_clusters <= 0 || h->fc2_clusters <= 0)
+    return fail(MH3_ERR_UNSUPPORTED, "no 2-CTA cluster of the MLP GEMMs fits this device");
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  if (workspace_a == nullptr) {
+    if ((rc = grow_buffer(&h->ws, &h->ws_bytes, mh3_preattn_workspace_bytes(M), s))) return rc;
+    workspace_a = static_cast<mh3_bf16*>(h->ws);
+  }
+  if (workspace_y == nullptr) {
+    if ((rc = grow_buffer(&h->ws_y, &h->ws_y_bytes, mh3_mlp_workspace_y_bytes(M), s))) return rc;
+    workspace_y = static_cast<mh3_bf16*>(h->ws_y);
+  }
+  rc = launch_stage1(s, h->num_sms, h->d_status, M, x, x_norm_weight, adaln_scale,
+                     scale_row_stride, adaln_shift, shift_row_stride, rows, adaln_index, eps,
+                     workspace_a);
+  if (rc) return rc;
+  const int pairs = static_cast<int>((M + 255) / 256);
+  CUtensorMap ma, mb, my;
+  if ((rc = encode_2d(&ma, workspace_a, kHidden, M, 64, 128, "workspace_a"))) return rc;
+  if ((rc = encode_2d(&mb, fc1_weight, kHidden, 2 * kMlpInter, 64, 128, "fc1_weight"))) return rc;
+  if ((rc = encode_2d(&my, workspace_y, kMlpInter, M, 64, 32, "workspace_y (store)"))) return rc;
+  SwigluParams p1;
+  p1.M = M;
+  p1.num_m_tiles = pairs;
+  p1.num_tiles = pairs * (kMlpInter / 128);
+  p1.status = h->d_status;
+  cudaError_t e = launch_mlp_fc1(ma, mb, my, p1, p1.num_tiles < h->fc1_clusters ? p1.num_tiles
+                                                                                 : h->fc1_clusters, s);
+  if (e != cudaSuccess) return cuda_fail(e, "MLP fc1 launch");
+  CUtensorMap ya, wb, mo, mr;
+  if ((rc = encode_2d(&ya, workspace_y, kMlpInter, M, 64, 128, "workspace_y (load)"))) return rc;
+  if ((rc = encode_2d(&wb, fc2_weight, kMlpInter, kHidden, 64, 128, "fc2_weight"))) return rc;
+  if ((rc = encode_2d(&mo, out, kHidden, M, 64, 32, "out"))) return rc;
+  if ((rc = encode_2d(&mr, residual, kHidden, M, 64, 32, "residual"))) return rc;
+  GatedResidualParams<int64_t> p2;
+  p2.gate = reinterpret_cast<const __nv_bfloat16*>(gate);
+  p2.gate_stride = gate_row_stride;
+  p2.gate_rows = rows;
+  p2.gate_index = adaln_index;
+  p2.M = M;
+  p2.num_m_tiles = pairs;
+  p2.num_tiles = pairs * (kHidden / 256);
+  p2.status = h->d_status;
+  e = launch_mlp_fc2(ya, wb, mo, mr, p2, p2.num_tiles < h->fc2_clusters ? p2.num_tiles
+                                                                         : h->fc2_clusters, s);
+  if (e != cudaSuccess) return cuda_fail(e, "MLP fc2 launch");
   return MH3_OK;
 }
 

@@ -247,6 +247,15 @@ __device__ __forceinline__ void tma_store_4d_hint(const CUtensorMap* m, uint32_t
       : "memory");
 }
 
+// 2-D tiled store shared -> global (bulk-group completion).
+__device__ __forceinline__ void tma_store_2d(const CUtensorMap* m, uint32_t src, int32_t c0,
+                                             int32_t c1) {
+  asm volatile("cp.async.bulk.tensor.2d.global.shared::cta.bulk_group [%0, {%2, %3}], [%1];" ::"l"(
+                   reinterpret_cast<uint64_t>(m)),
+               "r"(src), "r"(c0), "r"(c1)
+               : "memory");
+}
+
 // 2-D tiled store shared -> global with an L2 policy (bulk-group completion).
 __device__ __forceinline__ void tma_store_2d_hint(const CUtensorMap* m, uint32_t src, int32_t c0,
                                                   int32_t c1, uint64_t policy) {

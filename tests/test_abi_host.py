@@ -143,3 +143,29 @@ def test_out_proj_validate_accepts_good_arguments(lib):
 def test_out_proj_validate_rejects(lib, over, code):
     assert op_validate(**over) == code
     assert binding.last_error() != ""
+
+
+def mlp_args(**over):
+    a = dict(M=64, x=BASE, x_norm_weight=BASE + 0x1000, adaln_scale=BASE + 0x2000,
+             scale_row_stride=6 * H, adaln_shift=BASE + 0x3000, shift_row_stride=6 * H,
+             gate=BASE + 0x4000, gate_row_stride=6 * H, rows=9, adaln_index=BASE + 0x5000,
+             residual=BASE + 0x10000000, fc1_weight=BASE + 0x6000, fc2_weight=BASE + 0x7000,
+             eps=1e-5, workspace_a=None, workspace_y=None, out=BASE + 0x20000000)
+    a.update(over)
+    return a
+
+
+def test_mlp_validate(lib):
+    v = lambda **o: binding.mh3_mlp_validate(**mlp_args(**o))  # noqa: E731
+    assert v() == 0
+    assert v(out=BASE + 0x10000000) == 0  # out is the residual
+    assert v(out=BASE) == 0  # out is x
+    assert v(M=0, x=None, adaln_index=None, residual=None, out=None) == 0
+    assert v(workspace_a=BASE + 0x30000000, workspace_y=BASE + 0x40000000) == 0
+    assert binding.load().mh3_mlp_workspace_y_bytes(3) == 3 * 14336 * 2
+    for over, code in [(dict(rows=0), 1), (dict(gate_row_stride=H - 8), 1),
+                       (dict(gate_row_stride=H + 4), 2), (dict(gate=None), 1),
+                       (dict(fc1_weight=None), 1), (dict(fc2_weight=BASE + 0x7008), 2),
+                       (dict(workspace_y=BASE + 0x40000004), 2), (dict(eps=0.0), 1),
+                       (dict(out=BASE + 10752 * 2), 1), (dict(residual=None), 1)]:
+        assert v(**over) == code, over
