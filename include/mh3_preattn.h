@@ -142,6 +142,30 @@ int mh3_preattn_run(mh3_preattn_t handle, void* stream, int64_t M, const mh3_bf1
                     const int64_t* rope_positions, int P, float eps, float qk_eps,
                     mh3_bf16* workspace, mh3_bf16* out);
 
+/* The whole stage with e4m3 outputs (out_mode "e4m3" of the page
+ * "flashinfer.diffusion_ops.minimax_h3_nvfp4_pre_attention", Parameters:
+ * out_mode, q_descale / k_descale / v_descale).  Every output value is the
+ * bf16 value of mh3_preattn_run divided by its kind's dequantisation scale
+ * in FP32 and rounded to nearest-even e4m3, saturated to +-448:
+ *   code = e4m3(o / descale[kind]),  o ~ code * descale[kind].
+ *   qkv_descale   DEVICE pointer to 3 floats (q, k, v), read on the device
+ *                 (no host synchronisation), 4-byte aligned
+ *   out           [P, M, 56/P, 3, 128] bytes (e4m3 codes), the bf16 mode's
+ *                 pack, 16-byte aligned; M * 21504 bytes
+ * Other arguments and rules as in mh3_preattn_run.  Kernel 2 always runs in
+ * its CTA-pair form here. */
+int mh3_preattn_run_e4m3(mh3_preattn_t handle, void* stream, int64_t M, const mh3_bf16* x,
+                         const mh3_bf16* x_norm_weight, const mh3_bf16* adaln_scale,
+                         int64_t scale_row_stride, const mh3_bf16* adaln_shift,
+                         int64_t shift_row_stride, int64_t rows, const int64_t* adaln_index,
+                         const mh3_bf16* qkv_weight, const mh3_bf16* q_norm_weight,
+                         const mh3_bf16* k_norm_weight, const mh3_bf16* rope_cos_sin, int64_t S,
+                         const int64_t* rope_positions, int P, float eps, float qk_eps,
+                         const float* qkv_descale, mh3_bf16* workspace, uint8_t* out);
+
+/* Bytes of the e4m3 out: M * 21504 (0 for M <= 0). */
+size_t mh3_preattn_out_e4m3_bytes(int64_t M);
+
 /* Kernel 1 alone: workspace[m] = a (the formula block's n and a lines, with
  * the index guard).  Arguments as in mh3_preattn_run; workspace must not be
  * NULL. */

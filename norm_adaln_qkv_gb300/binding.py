@@ -34,7 +34,7 @@ EXPORTS = ("mh3_preattn_create", "mh3_preattn_destroy", "mh3_preattn_workspace_b
            "mh3_preattn_norm_adaln", "mh3_preattn_qkv", "mh3_preattn_device_status",
            "mh3_preattn_last_error", "mh3_preattn_run_noalloc", "mh3_out_proj_run",
            "mh3_out_proj_validate", "mh3_mlp_run", "mh3_mlp_validate",
-           "mh3_mlp_workspace_y_bytes")
+           "mh3_mlp_workspace_y_bytes", "mh3_preattn_run_e4m3", "mh3_preattn_out_e4m3_bytes")
 
 _vp = ctypes.c_void_p
 _i64 = ctypes.c_int64
@@ -62,6 +62,9 @@ _SIGS = {
     "mh3_mlp_validate": (_i32, [_i64, _vp, _vp, _vp, _i64, _vp, _i64, _vp, _i64, _i64, _vp, _vp,
                                 _vp, _vp, _f32, _vp, _vp, _vp]),
     "mh3_mlp_workspace_y_bytes": (ctypes.c_size_t, [_i64]),
+    "mh3_preattn_run_e4m3": (_i32, [_vp, _vp, _i64, _vp, _vp, _vp, _i64, _vp, _i64, _i64, _vp, _vp,
+                                    _vp, _vp, _vp, _i64, _vp, _i32, _f32, _f32, _vp, _vp, _vp]),
+    "mh3_preattn_out_e4m3_bytes": (ctypes.c_size_t, [_i64]),
     "mh3_preattn_run_noalloc": (_i32, [_vp, _i64, _vp, _vp, _vp, _i64, _vp, _i64, _i64, _vp, _vp,
                                        _vp, _vp, _vp, _i64, _vp, _i32, _f32, _f32, _vp, _vp]),
 }
@@ -297,6 +300,20 @@ def minimax_h3_bf16_mlp(x, x_norm_weight, adaln_scale, adaln_shift, adaln_index,
                 adaln_shift.stride(0), gate, gate.stride(0), rows, adaln_index, residual,
                 fc1_weight, fc2_weight, eps, workspace_a, workspace_y, out)
     return out
+
+
+def mh3_preattn_run_e4m3(handle: Handle, stream, M, x, x_norm_weight, adaln_scale,
+                         scale_row_stride, adaln_shift, shift_row_stride, rows, adaln_index,
+                         qkv_weight, q_norm_weight, k_norm_weight, rope_cos_sin, S,
+                         rope_positions, P, eps, qk_eps, qkv_descale, workspace, out) -> None:
+    """The stage with e4m3 outputs; qkv_descale is a device float32 tensor [3]
+    (q, k, v) and out a uint8 tensor of the bf16 mode's packed shape."""
+    _check(load().mh3_preattn_run_e4m3(
+        handle.ptr, _stream_ptr(stream), M, _ptr(x), _ptr(x_norm_weight), _ptr(adaln_scale),
+        scale_row_stride, _ptr(adaln_shift), shift_row_stride, rows, _ptr(adaln_index),
+        _ptr(qkv_weight), _ptr(q_norm_weight), _ptr(k_norm_weight), _ptr(rope_cos_sin), S,
+        _ptr(rope_positions), P, float(eps), _qk_eps_arg(qk_eps), _ptr(qkv_descale),
+        _ptr(workspace), _ptr(out)), "mh3_preattn_run_e4m3")
 
 
 def mh3_preattn_norm_adaln(handle: Handle, stream, M, x, x_norm_weight, adaln_scale,

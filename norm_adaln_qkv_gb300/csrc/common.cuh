@@ -58,6 +58,7 @@ struct QkvParams {
   float qk_eps;
   int num_m_tiles;  // row blocks: of 128 rows (single-CTA form) or 256 (pair form)
   int num_tiles;    // num_m_tiles * 84
+  const float* descales;  // e4m3 output mode: q, k, v dequantisation scales (device)
   int* status;  // device status word
 };
 
@@ -122,6 +123,12 @@ cudaError_t mlp_fc2_prepare_device(int* max_clusters);
 cudaError_t launch_mlp_fc2(const CUtensorMap& a, const CUtensorMap& b, const CUtensorMap& out,
                            const CUtensorMap& residual, const GatedResidualParams<int64_t>& p,
                            int clusters, cudaStream_t stream);
+
+// The pair form with e4m3 outputs: out as 4-D uint8 (d 128, slot, m, dst),
+// box 128 x 1 x 32 x 1.
+cudaError_t qkv_e4m3_prepare_device(int* max_clusters);
+cudaError_t launch_qkv_e4m3(const QkvMaps& maps, const QkvParams& p, int clusters,
+                            cudaStream_t stream);
 
 // Single-CTA form (128 x 256 tiles), used for M <= 128.
 int qkv_smem_bytes();

@@ -225,6 +225,34 @@ __device__ __forceinline__ void epi_qk_head(uint32_t tcol, uint32_t stg, int lan
   }
 }
 
+// e4m3 output mode: turn this thread's staged bf16 row (16 chunks over both
+// halves) into 128 e4m3 codes, value / descale, written in place over the
+// first half as one 128-byte swizzled row (the layout of a 128 x 32 byte box).
+// Only this thread's row is read or written.
+__device__ __forceinline__ void stage_to_e4m3(uint32_t stg, int lane, float descale) {
+  uint4 w[16];
+#pragma unroll
+  for (int c = 0; c < 16; ++c) w[c] = ld_shared_v4(stg_addr(stg, lane, c));
+#pragma unroll
+  for (int c = 0; c < 8; ++c) {  // e4m3 chunk c = bf16 chunks 2c, 2c+1
+    uint32_t o[4];
+#pragma unroll
+    for (int h = 0; h < 2; ++h) {
+      const uint4 b = w[2 * c + h];
+      const uint32_t words[4] = {b.x, b.y, b.z, b.w};
+#pragma unroll
+      for (int e = 0; e < 2; ++e) {
+        const uint32_t lo = e4m3x2_satfinite(__fdiv_rn(bf16_lo(words[2 * e]), descale),
+                                             __fdiv_rn(bf16_hi(words[2 * e]), descale));
+        const uint32_t hi = e4m3x2_satfinite(__fdiv_rn(bf16_lo(words[2 * e + 1]), descale),
+                                             __fdiv_rn(bf16_hi(words[2 * e + 1]), descale));
+        o[2 * h + e] = lo | (hi << 16);
+      }
+    }
+    st_shared_v4(stg_addr(stg, lane, c), make_uint4(o[0], o[1], o[2], o[3]));
+  }
+}
+
 // The epilogue of one 128-row x 256-column accumulator block.
 //   tmem_acc  TMEM address of the block (lane 0, first column)
 //   quad      TMEM lane quadrant this warp may read (warp index % 4)
@@ -232,6 +260,7 @@ __device__ __forceinline__ void epi_qk_head(uint32_t tcol, uint32_t stg, int lan
 //   n_blk     256-column block of the 21504 projection columns
 // Returns after every TMEM read of the block has completed; the stores may
 // still be in flight (bulk groups of this warp's lane 0).
+template <bool kE4m3 = false>
 __device__ __forceinline__ void epilogue_block(uint32_t tmem_acc, int quad, int lane, uint32_t stg,
                                                const float* nw_all, const QkvParams& p,
                                                int64_t row0, int n_blk, const CUtensorMap* tm_out) {
@@ -260,9 +289,16 @@ __device__ __forceinline__ void epilogue_block(uint32_t tmem_acc, int quad, int 
       epi_v_head(tcol, stg, lane);
     else
       epi_qk_head(tcol, stg, lane, nw_all + kind * kHeadDim, cs_row, p.qk_eps);
+    if (kE4m3) stage_to_e4m3(stg, lane, __ldg(p.descales + kind));
     fence_proxy_async_smem();
     __syncwarp();
-    if (lane == 0 && m0 < p.M) {
+    if (kE4m3 && lane == 0 && m0 < p.M) {
+      const int head = head0 + j;
+      const int slot = (head % p.heads_per_dst) * 3 + kind;
+      tma_store_4d_hint(tm_out, stg, 0, slot, static_cast<int32_t>(m0), head / p.heads_per_dst,
+                        policy_evict_first());
+      bulk_commit_group();
+    } else if (!kE4m3 && lane == 0 && m0 < p.M) {
       const int head = head0 + j;
       const int dst = head / p.heads_per_dst;
       const int slot = (head % p.heads_per_dst) * 3 + kind;

@@ -15,7 +15,8 @@ namespace mh3 {
 
 namespace {
 
-struct QkvPairEpi {
+template <bool kE4m3>
+struct QkvPairEpiT {
   using Params = QkvParams;
   static constexpr int kKBlocks = k2::kKBlocks;  // 84
   static constexpr int kNTiles = k2::kNTiles;    // 84
@@ -30,9 +31,12 @@ struct QkvPairEpi {
   }
 
   __device__ static void tile(const gp::EpiCtx& c, const Params& p, int64_t row0, int n_blk) {
-    k2::epilogue_block(c.tmem_acc, c.quad, c.lane, c.stg, c.scratch, p, row0, n_blk, c.tm_out);
+    k2::epilogue_block<kE4m3>(c.tmem_acc, c.quad, c.lane, c.stg, c.scratch, p, row0, n_blk,
+                              c.tm_out);
   }
 };
+using QkvPairEpi = QkvPairEpiT<false>;
+using QkvE4m3PairEpi = QkvPairEpiT<true>;
 
 }  // namespace
 
@@ -47,6 +51,17 @@ cudaError_t launch_qkv_pair(const QkvMaps& maps, const QkvParams& p, int cluster
   if (p.M <= 0) return cudaSuccess;
   // no auxiliary input: the output map stands in for the unused operand
   return gp::gemm_pair_launch<QkvPairEpi>(maps.a, maps.b, maps.out, maps.out, p, clusters, stream);
+}
+
+cudaError_t qkv_e4m3_prepare_device(int* max_clusters) {
+  return gp::gemm_pair_prepare<QkvE4m3PairEpi>(max_clusters);
+}
+
+cudaError_t launch_qkv_e4m3(const QkvMaps& maps, const QkvParams& p, int clusters,
+                            cudaStream_t stream) {
+  if (p.M <= 0) return cudaSuccess;
+  return gp::gemm_pair_launch<QkvE4m3PairEpi>(maps.a, maps.b, maps.out, maps.out, p, clusters,
+                                              stream);
 }
 
 }  // namespace mh3

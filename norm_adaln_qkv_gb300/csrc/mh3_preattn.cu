@@ -28,6 +28,7 @@ struct mh3_preattn_ctx {
   int num_sms = 0;
   int max_clusters = 0;  // resident 2-CTA clusters of the pair GEMM
   int out_proj_clusters = 0;  // the same for the output projection
+  int e4m3_clusters = 0;      // ... the e4m3-output QKV GEMM
   int fc1_clusters = 0;       // ... and the two MLP GEMMs
   int fc2_clusters = 0;
   void* ws_y = nullptr;  // handle-owned MLP intermediate y [M, 14336]
@@ -266,6 +267,7 @@ int launch_stage2(cudaStream_t s, int num_sms, int max_clusters, int* status, in
   p.heads_per_dst = kHeads / P;
   p.qk_eps = qk_eps;
   p.status = status;
+  p.descales = nullptr;
   cudaError_t e;
   if (pair) {
     p.num_m_tiles = static_cast<int>((M + 255) / 256);
@@ -318,6 +320,9 @@ int mh3_preattn_create(mh3_preattn_t* handle, int device) {
   int out_proj_clusters = 0;
   e = out_proj_prepare_device(&out_proj_clusters);
   if (e != cudaSuccess) return cuda_fail(e, "preparing the output-projection GEMM");
+  int e4m3_clusters = 0;
+  e = qkv_e4m3_prepare_device(&e4m3_clusters);
+  if (e != cudaSuccess) return cuda_fail(e, "preparing the e4m3-output GEMM");
   int fc1_clusters = 0, fc2_clusters = 0;
   e = mlp_fc1_prepare_device(&fc1_clusters);
   if (e == cudaSuccess) e = mlp_fc2_prepare_device(&fc2_clusters);
@@ -325,6 +330,7 @@ int mh3_preattn_create(mh3_preattn_t* handle, int device) {
   mh3_preattn_ctx* h = new mh3_preattn_ctx();
   h->device = device;
   h->fc1_clusters = fc1_clusters;
+  h->e4m3_clusters = e4m3_clusters;
   h->fc2_clusters = fc2_clusters;
   h->num_sms = prop.multiProcessorCount;
   h->max_clusters = max_clusters;
@@ -532,6 +538,77 @@ extern "C" int mh3_out_proj_run(mh3_preattn_t h, void* stream, int64_t M, const 
   const int clusters = p.num_tiles < h->out_proj_clusters ? p.num_tiles : h->out_proj_clusters;
   cudaError_t e = launch_out_proj(maps, p, clusters, static_cast<cudaStream_t>(stream));
   if (e != cudaSuccess) return cuda_fail(e, "output projection launch");
+  return MH3_OK;
+}
+
+// ------------------------------------------------------- e4m3 output mode
+extern "C" size_t mh3_preattn_out_e4m3_bytes(int64_t M) {
+  return M <= 0 ? 0 : static_cast<size_t>(M) * kQkvRows;
+}
+
+extern "C" int mh3_preattn_run_e4m3(
+    mh3_preattn_t h, void* stream, int64_t M, const mh3_bf16* x, const mh3_bf16* x_norm_weight,
+    const mh3_bf16* adaln_scale, int64_t scale_row_stride, const mh3_bf16* adaln_shift,
+    int64_t shift_row_stride, int64_t rows, const int64_t* adaln_index,
+    const mh3_bf16* qkv_weight, const mh3_bf16* q_norm_weight, const mh3_bf16* k_norm_weight,
+    const mh3_bf16* rope_cos_sin, int64_t S, const int64_t* rope_positions, int P, float eps,
+    float qk_eps, const float* qkv_descale, mh3_bf16* workspace, uint8_t* out) {
+  int rc = check_handle(h);
+  if (rc) return rc;
+  // the bf16 rules, with `out` checked as a 16-byte aligned buffer
+  rc = mh3_preattn_validate(M, x, x_norm_weight, adaln_scale, scale_row_stride, adaln_shift,
+                            shift_row_stride, rows, adaln_index, qkv_weight, q_norm_weight,
+                            k_norm_weight, rope_cos_sin, S, rope_positions, P, eps, qk_eps,
+                            workspace, reinterpret_cast<const mh3_bf16*>(out));
+  if (rc) return rc;
+  if (M == 0) return MH3_OK;
+  if ((rc = check_ptr(qkv_descale, "qkv_descale", 4))) return rc;
+  if (h->e4m3_clusters <= 0)
+    return fail(MH3_ERR_UNSUPPORTED, "no 2-CTA cluster of the e4m3 GEMM fits this device");
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  if (workspace == nullptr) {
+    if ((rc = grow_buffer(&h->ws, &h->ws_bytes, mh3_preattn_workspace_bytes(M), s))) return rc;
+    workspace = static_cast<mh3_bf16*>(h->ws);
+  }
+  rc = launch_stage1(s, h->num_sms, h->d_status, M, x, x_norm_weight, adaln_scale,
+                     scale_row_stride, adaln_shift, shift_row_stride, rows, adaln_index, eps,
+                     workspace);
+  if (rc) return rc;
+  QkvMaps maps;
+  if ((rc = encode_2d(&maps.a, workspace, kHidden, M, 64, 128, "workspace"))) return rc;
+  if ((rc = encode_2d(&maps.b, qkv_weight, kHidden, kQkvRows, 64, 128, "qkv_weight"))) return rc;
+  {
+    PFN_cuTensorMapEncodeTiled_v12000 enc = encode_fn();
+    if (enc == nullptr) return fail(MH3_ERR_CUDA, "cuTensorMapEncodeTiled entry point not found");
+    const int64_t slots = 3 * (kHeads / P);
+    const cuuint64_t dims[4] = {static_cast<cuuint64_t>(kHeadDim), static_cast<cuuint64_t>(slots),
+                                static_cast<cuuint64_t>(M), static_cast<cuuint64_t>(P)};
+    const cuuint64_t strides[3] = {static_cast<cuuint64_t>(kHeadDim),
+                                   static_cast<cuuint64_t>(slots) * kHeadDim,
+                                   static_cast<cuuint64_t>(M) * slots * kHeadDim};
+    const cuuint32_t box[4] = {128, 1, 32, 1};
+    const cuuint32_t unit[4] = {1, 1, 1, 1};
+    CUresult r = enc(&maps.out, CU_TENSOR_MAP_DATA_TYPE_UINT8, 4, out, dims, strides, box, unit,
+                     CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                     CU_TENSOR_MAP_L2_PROMOTION_NONE, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    if (r != CUDA_SUCCESS) return fail(MH3_ERR_CUDA, "tensor map (e4m3 out) failed: %d", (int)r);
+  }
+  QkvParams p;
+  p.positions = rope_positions;
+  p.cos_sin = reinterpret_cast<const __nv_bfloat16*>(rope_cos_sin);
+  p.q_norm_weight = reinterpret_cast<const __nv_bfloat16*>(q_norm_weight);
+  p.k_norm_weight = reinterpret_cast<const __nv_bfloat16*>(k_norm_weight);
+  p.M = M;
+  p.S = S;
+  p.heads_per_dst = kHeads / P;
+  p.qk_eps = qk_eps_means_default(qk_eps) ? eps : qk_eps;
+  p.status = h->d_status;
+  p.descales = qkv_descale;
+  p.num_m_tiles = static_cast<int>((M + 255) / 256);
+  p.num_tiles = p.num_m_tiles * (kQkvRows / 256);
+  const int clusters = p.num_tiles < h->e4m3_clusters ? p.num_tiles : h->e4m3_clusters;
+  cudaError_t e = launch_qkv_e4m3(maps, p, clusters, s);
+  if (e != cudaSuccess) return cuda_fail(e, "e4m3 QKV GEMM launch");
   return MH3_OK;
 }
 

@@ -168,6 +168,14 @@ __device__ __forceinline__ uint4 ld_shared_v4(uint32_t addr) {
   return v;
 }
 
+// Two FP32 values -> two e4m3 codes (nearest-even, saturated to +-448),
+// `lo` in bits 0-7.
+__device__ __forceinline__ uint32_t e4m3x2_satfinite(float lo, float hi) {
+  uint16_t d;
+  asm("cvt.rn.satfinite.e4m3x2.f32 %0, %1, %2;" : "=h"(d) : "f"(hi), "f"(lo));
+  return d;
+}
+
 // ------------------------------------------------- packed FP32 (two lanes)
 // Blackwell's f32x2 arithmetic: each lane is one IEEE round-to-nearest FP32
 // operation, exactly as the scalar __fmul_rn / __fadd_rn / __fmaf_rn.
