@@ -166,6 +166,23 @@ int mh3_preattn_run_e4m3(mh3_preattn_t handle, void* stream, int64_t M, const mh
 /* Bytes of the e4m3 out: M * 21504 (0 for M <= 0). */
 size_t mh3_preattn_out_e4m3_bytes(int64_t M);
 
+/* The e4m3 conversion of mh3_preattn_run_e4m3 on its own, for any bf16
+ * tensor with one per-tensor dequantisation scale:
+ *   codes[i] = e4m3(values[i] / *descale)   (FP32 quotient, nearest-even,
+ *                                            saturated to +-448)
+ *   stream   cudaStream_t or NULL (legacy default stream)
+ *   n        number of elements, >= 0 (0 launches nothing)
+ *   values   DEVICE, n bf16, 2-byte aligned
+ *   descale  DEVICE pointer to one float, read on the device
+ *   codes    DEVICE, n bytes, caller-owned; must not overlap `values`
+ * Any alignment works; 16-byte aligned `values` with 8-byte aligned `codes`
+ * take the vector path.  Returns MH3_ERR_INVALID_ARG for n < 0, a NULL
+ * pointer with n > 0 or overlapping buffers, MH3_ERR_ALIGNMENT for an odd
+ * `values` or a misaligned `descale`, MH3_ERR_CUDA for a failed launch.
+ * Needs no handle. */
+int mh3_e4m3_quantize(void* stream, int64_t n, const mh3_bf16* values, const float* descale,
+                      uint8_t* codes);
+
 /* Kernel 1 alone: workspace[m] = a (the formula block's n and a lines, with
  * the index guard).  Arguments as in mh3_preattn_run; workspace must not be
  * NULL. */

@@ -34,7 +34,8 @@ EXPORTS = ("mh3_preattn_create", "mh3_preattn_destroy", "mh3_preattn_workspace_b
            "mh3_preattn_norm_adaln", "mh3_preattn_qkv", "mh3_preattn_device_status",
            "mh3_preattn_last_error", "mh3_preattn_run_noalloc", "mh3_out_proj_run",
            "mh3_out_proj_validate", "mh3_mlp_run", "mh3_mlp_validate",
-           "mh3_mlp_workspace_y_bytes", "mh3_preattn_run_e4m3", "mh3_preattn_out_e4m3_bytes")
+           "mh3_mlp_workspace_y_bytes", "mh3_preattn_run_e4m3", "mh3_preattn_out_e4m3_bytes",
+           "mh3_e4m3_quantize")
 
 _vp = ctypes.c_void_p
 _i64 = ctypes.c_int64
@@ -65,6 +66,7 @@ _SIGS = {
     "mh3_preattn_run_e4m3": (_i32, [_vp, _vp, _i64, _vp, _vp, _vp, _i64, _vp, _i64, _i64, _vp, _vp,
                                     _vp, _vp, _vp, _i64, _vp, _i32, _f32, _f32, _vp, _vp, _vp]),
     "mh3_preattn_out_e4m3_bytes": (ctypes.c_size_t, [_i64]),
+    "mh3_e4m3_quantize": (_i32, [_vp, _i64, _vp, _vp, _vp]),
     "mh3_preattn_run_noalloc": (_i32, [_vp, _i64, _vp, _vp, _vp, _i64, _vp, _i64, _i64, _vp, _vp,
                                        _vp, _vp, _vp, _i64, _vp, _i32, _f32, _f32, _vp, _vp]),
 }
@@ -314,6 +316,17 @@ def mh3_preattn_run_e4m3(handle: Handle, stream, M, x, x_norm_weight, adaln_scal
         _ptr(qkv_weight), _ptr(q_norm_weight), _ptr(k_norm_weight), _ptr(rope_cos_sin), S,
         _ptr(rope_positions), P, float(eps), _qk_eps_arg(qk_eps), _ptr(qkv_descale),
         _ptr(workspace), _ptr(out)), "mh3_preattn_run_e4m3")
+
+
+def mh3_e4m3_quantize(stream, values, descale, codes) -> None:
+    """codes[i] = e4m3(values[i] / descale[0]) for a device bf16 tensor
+    `values`, a device float32 tensor `descale` [1] and a device uint8 tensor
+    `codes` of the same number of elements."""
+    n = values.numel()
+    if codes.numel() != n:
+        raise ValueError("codes must have as many elements as values")
+    _check(load().mh3_e4m3_quantize(_stream_ptr(stream), n, _ptr(values), _ptr(descale),
+                                    _ptr(codes)), "mh3_e4m3_quantize")
 
 
 def mh3_preattn_norm_adaln(handle: Handle, stream, M, x, x_norm_weight, adaln_scale,

@@ -130,6 +130,10 @@ cudaError_t qkv_e4m3_prepare_device(int* max_clusters);
 cudaError_t launch_qkv_e4m3(const QkvMaps& maps, const QkvParams& p, int clusters,
                             cudaStream_t stream);
 
+// Standalone per-tensor e4m3 quantiser: out[i] = e4m3_sat(RN32(in[i] / *descale)).
+cudaError_t launch_e4m3_quantize(const __nv_bfloat16* in, const float* descale, uint8_t* out,
+                                 int64_t n, int num_sms, cudaStream_t stream);
+
 // Single-CTA form (128 x 256 tiles), used for M <= 128.
 int qkv_smem_bytes();
 cudaError_t qkv_prepare_device();  // raise the dynamic shared-memory limit

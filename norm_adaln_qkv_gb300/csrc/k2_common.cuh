@@ -21,6 +21,7 @@
 #pragma once
 
 #include "common.cuh"
+#include "e4m3.cuh"
 #include "ptx.cuh"
 
 namespace mh3 {
@@ -226,31 +227,29 @@ __device__ __forceinline__ void epi_qk_head(uint32_t tcol, uint32_t stg, int lan
 }
 
 // e4m3 output mode: turn this thread's staged bf16 row (16 chunks over both
-// halves) into 128 e4m3 codes, value / descale, written in place over the
-// first half as one 128-byte swizzled row (the layout of a 128 x 32 byte box).
-// Only this thread's row is read or written.
-__device__ __forceinline__ void stage_to_e4m3(uint32_t stg, int lane, float descale) {
+// halves) into 128 e4m3 codes (the quantiser of e4m3.cuh), written in place
+// over the first half as one 128-byte swizzled row (the layout of a
+// 128 x 32 byte box).  Only this thread's row is read or written.
+template <bool kFast>
+__device__ __forceinline__ void stage_row_to_e4m3(uint32_t stg, int lane,
+                                                  const e4m3q::Divisor& dv) {
   uint4 w[16];
 #pragma unroll
   for (int c = 0; c < 16; ++c) w[c] = ld_shared_v4(stg_addr(stg, lane, c));
 #pragma unroll
   for (int c = 0; c < 8; ++c) {  // e4m3 chunk c = bf16 chunks 2c, 2c+1
-    uint32_t o[4];
-#pragma unroll
-    for (int h = 0; h < 2; ++h) {
-      const uint4 b = w[2 * c + h];
-      const uint32_t words[4] = {b.x, b.y, b.z, b.w};
-#pragma unroll
-      for (int e = 0; e < 2; ++e) {
-        const uint32_t lo = e4m3x2_satfinite(__fdiv_rn(bf16_lo(words[2 * e]), descale),
-                                             __fdiv_rn(bf16_hi(words[2 * e]), descale));
-        const uint32_t hi = e4m3x2_satfinite(__fdiv_rn(bf16_lo(words[2 * e + 1]), descale),
-                                             __fdiv_rn(bf16_hi(words[2 * e + 1]), descale));
-        o[2 * h + e] = lo | (hi << 16);
-      }
-    }
-    st_shared_v4(stg_addr(stg, lane, c), make_uint4(o[0], o[1], o[2], o[3]));
+    const uint2 a = e4m3q::quantize8<kFast>(w[2 * c], dv);
+    const uint2 b = e4m3q::quantize8<kFast>(w[2 * c + 1], dv);
+    st_shared_v4(stg_addr(stg, lane, c), make_uint4(a.x, a.y, b.x, b.y));
   }
+}
+
+__device__ __forceinline__ void stage_to_e4m3(uint32_t stg, int lane, float descale) {
+  const e4m3q::Divisor dv = e4m3q::make_divisor(descale);
+  if (dv.fast)
+    stage_row_to_e4m3<true>(stg, lane, dv);
+  else
+    stage_row_to_e4m3<false>(stg, lane, dv);
 }
 
 // The epilogue of one 128-row x 256-column accumulator block.

@@ -546,6 +546,27 @@ extern "C" size_t mh3_preattn_out_e4m3_bytes(int64_t M) {
   return M <= 0 ? 0 : static_cast<size_t>(M) * kQkvRows;
 }
 
+extern "C" int mh3_e4m3_quantize(void* stream, int64_t n, const mh3_bf16* values,
+                                 const float* descale, uint8_t* codes) {
+  if (n < 0) return fail(MH3_ERR_INVALID_ARG, "n must be >= 0 (got %lld)", (long long)n);
+  if (n == 0) return MH3_OK;
+  int rc;
+  if ((rc = check_ptr(values, "values", 2))) return rc;
+  if ((rc = check_ptr(descale, "descale", 4))) return rc;
+  if ((rc = check_ptr(codes, "codes", 1))) return rc;
+  const uintptr_t v0 = reinterpret_cast<uintptr_t>(values), c0 = reinterpret_cast<uintptr_t>(codes);
+  const uintptr_t v1 = v0 + static_cast<uintptr_t>(n) * 2, c1 = c0 + static_cast<uintptr_t>(n);
+  if (v0 < c1 && c0 < v1) return fail(MH3_ERR_INVALID_ARG, "codes overlaps values");
+  int dev = 0, sms = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e == cudaSuccess) e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+  if (e != cudaSuccess) return cuda_fail(e, "device query");
+  e = launch_e4m3_quantize(reinterpret_cast<const __nv_bfloat16*>(values), descale, codes, n, sms,
+                           static_cast<cudaStream_t>(stream));
+  if (e != cudaSuccess) return cuda_fail(e, "e4m3 quantiser launch");
+  return MH3_OK;
+}
+
 extern "C" int mh3_preattn_run_e4m3(
     mh3_preattn_t h, void* stream, int64_t M, const mh3_bf16* x, const mh3_bf16* x_norm_weight,
     const mh3_bf16* adaln_scale, int64_t scale_row_stride, const mh3_bf16* adaln_shift,

@@ -95,3 +95,57 @@ def test_saturation_and_guard_rows(handle):
     assert len(bad) > 0
     tok = oracle.ulysses_unpack_rows(vals, bad.tolist())
     assert bool((tok == 0).all())
+
+
+# ---------------------------------------------------------- the quantiser alone
+QUANT_DESCALES = [1 / 64, 1 / 48, 1 / 128, 0.3, 7.0, 1e-3, 1234.5, 1.0, -0.5, 2.0 ** -60,
+                  2.0 ** 60, 1e-30, 1e30, 3e-39] + \
+    [float(v) for v in torch.exp2(torch.empty(24).uniform_(-40, 40,
+                                                           generator=torch.Generator().manual_seed(9)))]
+
+
+def _all_bf16():
+    return torch.arange(-32768, 32768, dtype=torch.int32).to(torch.int16).view(torch.bfloat16)
+
+
+@pytest.mark.parametrize("descale", QUANT_DESCALES)
+def test_quantiser_all_bf16_patterns(cuda_lib, descale):
+    """Every bf16 bit pattern, bit-exact against the oracle's FP32 division
+    (NaN inputs: a NaN code).  Descales outside [2^-60, 2^60] take the true
+    division; the rest the Markstein quotient."""
+    v = _all_bf16()
+    ds = torch.tensor([descale], dtype=torch.float32)
+    codes = torch.empty(v.numel(), dtype=torch.uint8, device="cuda")
+    binding.mh3_e4m3_quantize(None, v.cuda(), ds.cuda(), codes)
+    got = codes.cpu()
+    exp = e4m3.quantize_e4m3(v, float(ds))
+    nan_in = torch.isnan(v.float() / ds)
+    assert torch.equal(got[~nan_in], exp[~nan_in]), int((got[~nan_in] != exp[~nan_in]).sum())
+    assert bool(((got[nan_in] & 0x7F) == 0x7F).all())
+
+
+@pytest.mark.parametrize("offset,n", [(0, 1 << 20), (1, 1000003), (3, 7), (0, 9)])
+def test_quantiser_vector_and_scalar_paths(cuda_lib, offset, n):
+    g = torch.Generator().manual_seed(10 + offset)
+    base = (torch.randn(n + 8, generator=g) * 30).to(torch.bfloat16).cuda()
+    v = base[offset:offset + n]
+    codes_buf = torch.full((n + 8,), 0xAB, dtype=torch.uint8, device="cuda")
+    codes = codes_buf[offset:offset + n]
+    ds = torch.tensor([1 / 48], dtype=torch.float32, device="cuda")
+    binding.mh3_e4m3_quantize(None, v, ds, codes)
+    torch.cuda.synchronize()
+    assert torch.equal(codes.cpu(), e4m3.quantize_e4m3(v.cpu(), 1 / 48))
+    # nothing written outside [offset, offset + n)
+    assert bool((codes_buf[:offset] == 0xAB).all()) and bool((codes_buf[offset + n:] == 0xAB).all())
+
+
+def test_quantiser_rejects_bad_arguments(cuda_lib):
+    v = torch.zeros(16, dtype=torch.bfloat16, device="cuda")
+    ds = torch.ones(1, dtype=torch.float32, device="cuda")
+    with pytest.raises(RuntimeError, match="overlaps"):
+        binding.mh3_e4m3_quantize(None, v, ds, v.view(torch.uint8)[:16])
+    lib = binding.load()
+    assert lib.mh3_e4m3_quantize(None, -1, None, None, None) == 1
+    assert lib.mh3_e4m3_quantize(None, 0, None, None, None) == 0
+    assert lib.mh3_e4m3_quantize(None, 4, v.data_ptr() + 1, ds.data_ptr(),
+                                 v.data_ptr() + 64) == 2
