@@ -30,3 +30,4 @@ from .preattn import (  # noqa: F401
 from . import out_proj  # noqa: F401  (attention output projection + gated residual)
 from . import mlp  # noqa: F401  (MLP block)
 from . import e4m3  # noqa: F401  (e4m3 output mode)
+from . import nvfp4  # noqa: F401  (NVFP4 pre-attention)

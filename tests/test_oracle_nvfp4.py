@@ -1,0 +1,187 @@
+"""Pins of the NVFP4 oracle (oracle/nvfp4.py) to facts that do not come from
+the oracle (flashinfer.diffusion_ops.minimax_h3_nvfp4_pre_attention, summary
+and Parameters): hand-derived E2M1 and UE4M3 roundings, worked quantisation
+examples, the E2M1 rounding bound, one-hot weights, and the bf16 stage's
+oracle on inputs that NVFP4 represents exactly."""
+from fractions import Fraction
+
+import pytest
+import torch
+
+import oracle
+from oracle import nvfp4 as f
+
+BF16 = torch.bfloat16
+
+
+def test_e2m1_hand_table():
+    # value -> code, worked by hand: nearest of {0,.5,1,1.5,2,3,4,6}, ties to
+    # the even code (0, 1.0, 2.0, 4.0 have even codes 0, 2, 4, 6), saturating
+    cases = [(0.0, 0), (0.2, 0), (0.25, 0), (0.3, 1), (0.74, 1), (0.75, 2), (1.25, 2), (1.26, 3),
+             (1.75, 4), (2.5, 4), (2.6, 5), (3.5, 6), (5.0, 6), (5.01, 7), (6.0, 7), (1e9, 7),
+             (-0.25, 8), (-0.26, 9), (-1.75, 12), (-6.5, 15)]
+    x = torch.tensor([c[0] for c in cases], dtype=torch.float64)
+    assert f.e2m1_codes(x).tolist() == [c[1] for c in cases]
+    assert f.e2m1_codes(torch.tensor([-0.0])).item() == 8  # sign kept on zero
+
+
+def test_e2m1_is_the_nearest_value_brute_force():
+    vals = [Fraction(v).limit_denominator() for v in f.E2M1_VALUES]
+    g = torch.Generator().manual_seed(3)
+    xs = torch.cat([torch.rand(400, generator=g, dtype=torch.float64) * 8,
+                    torch.arange(0, 7.0, 0.125, dtype=torch.float64)])
+    codes = f.e2m1_codes(xs)
+    for x, c in zip(xs.tolist(), codes.tolist()):
+        fx = Fraction(x)
+        dist = [abs(fx - v) for v in vals]
+        best = min(dist)
+        near = [i for i, d in enumerate(dist) if d == best]
+        want = near[0] if len(near) == 1 else [i for i in near if i % 2 == 0][0]
+        if fx > 6:
+            want = 7
+        assert c == want, (x, c, want)
+
+
+def test_ue4m3_brute_force():
+    # all positive finite e4m3 values, enumerated from the format definition
+    vals = []
+    for code in range(0, 127):
+        e, m = code >> 3, code & 7
+        vals.append(Fraction(m, 8) * Fraction(1, 2 ** 6) if e == 0 else (1 + Fraction(m, 8)) * Fraction(2) ** (e - 7))
+    g = torch.Generator().manual_seed(4)
+    xs = torch.cat([torch.exp2(torch.rand(300, generator=g) * 20 - 11), torch.tensor([0.0, 448.0, 460.0, 1e6])])
+    codes = f.ue4m3_codes(xs)
+    for x, c in zip(xs.tolist(), codes.tolist()):
+        fx = min(Fraction(x), Fraction(448))
+        dist = [abs(fx - v) for v in vals]
+        best = min(dist)
+        near = [i for i, d in enumerate(dist) if d == best]
+        want = near[0] if len(near) == 1 else [i for i in near if i % 2 == 0][0]
+        assert c == want, (x, c, want)
+
+
+def test_quantize_worked_examples():
+    # block 0: amax 6, gs 1 -> t = 1, s = 1.0 (0x38), enc 1: codes are the values
+    # block 1: amax 12, gs 1 -> s = 2.0 (0x40), enc 0.5: 12 -> 6 (7), -6 -> -3 (13), 1 -> 0.5 (1)
+    b0 = [6.0, -3.0, 1.5, 0.5, -0.5, 2.0, 4.0, -1.0] + [0.0] * 8
+    b1 = [12.0, -6.0, 1.0, 0.0] + [0.0] * 12
+    a = torch.tensor([b0 + b1], dtype=BF16)
+    q, s = f.fp4_quantize(a, 1.0)
+    assert s.tolist() == [[0x38, 0x40]]
+    codes = f.unpack_codes(q)[0].tolist()
+    assert codes[:8] == [7, 13, 3, 1, 9, 4, 6, 10]
+    assert codes[16:20] == [7, 13, 1, 0]
+    # packing: element 0 in the low nibble
+    assert q[0, 0].item() == 7 | (13 << 4)
+    # gs = 336 (448 * 6 / 8), amax 8: t = 8/6 * 336 = 448 -> s = 448 (0x7E),
+    # enc = 336/448 = 0.75; 8 -> 6 (7); 1 -> 0.75 -> tie .5/1 -> 1.0 (2)
+    a2 = torch.tensor([[8.0, 1.0] + [0.0] * 14], dtype=BF16)
+    q2, s2 = f.fp4_quantize(a2, 336.0)
+    assert s2.item() == 0x7E and f.unpack_codes(q2)[0, :2].tolist() == [7, 2]
+    # an all-zero block: scale 0, codes 0
+    q3, s3 = f.fp4_quantize(torch.zeros(1, 32, dtype=BF16), 100.0)
+    assert s3.tolist() == [[0, 0]] and int(q3.sum()) == 0
+
+
+def test_quantize_error_bound():
+    """Each element lands within half an E2M1 step of a * enc (or saturates)."""
+    g = torch.Generator().manual_seed(5)
+    a = (torch.randn(64, 256, generator=g) * 3).to(BF16)
+    gs = 448.0 * 6 / 12.0
+    q, s = f.fp4_quantize(a, gs)
+    sv = f.ue4m3_values(s).to(torch.float64).repeat_interleave(16, dim=1)
+    enc = torch.where(sv == 0, 0.0, torch.tensor(gs, dtype=torch.float32).double() / sv)
+    scaled = a.double() * enc
+    v = f.e2m1_values(f.unpack_codes(q))
+    step = torch.where(v.abs() < 2, 0.5, torch.where(v.abs() < 4, 1.0, 2.0))
+    err = (scaled - v).abs()
+    sat = scaled.abs() > 6
+    assert bool(((err <= step / 2 + 1e-6) | sat).all())
+    # saturation only by the rounding of the block scale (at most 1/16 above 6)
+    assert float(scaled.abs().max()) <= 6 * (1 + 1 / 16) + 1e-6
+
+
+def test_alpha_closed_form():
+    assert f.alpha_from_scales(2.0, 4.0) == 0.125
+    assert f.alpha_from_scales(448.0 * 6, 1.0) == float(torch.tensor(1 / 2688.0, dtype=torch.float32))
+
+
+def test_projection_one_hot_weight():
+    g = torch.Generator().manual_seed(6)
+    a = (torch.randn(5, 64, generator=g) * 2).to(BF16)
+    aq, asf = f.fp4_quantize(a, 50.0)
+    # weight row c: code 2 (1.0) at element k(c), scale 1.0 (0x38)
+    N, K = 8, 64
+    ks = torch.tensor([0, 1, 17, 33, 63, 5, 16, 48])
+    codes = torch.zeros(N, K, dtype=torch.uint8)
+    codes[torch.arange(N), ks] = 2
+    wq = (codes[:, 0::2] | (codes[:, 1::2] << 4)).to(torch.uint8)
+    wsf = torch.full((N, K // 16), 0x38, dtype=torch.uint8)
+    y = f.nvfp4_projection(aq, asf, wq, wsf, 0.25)
+    qa = f.e2m1_values(f.unpack_codes(aq))
+    sa = f.ue4m3_values(asf).double()
+    exp = torch.stack([qa[:, k] * sa[:, k // 16] for k in ks.tolist()], dim=1)
+    assert torch.equal(y, (exp.float() * 0.25).to(BF16))
+
+
+def _representable_inputs(M=6, H=64, N=12, seed=7):
+    """bf16 a whose every 16-block has amax 6 and E2M1 values, and an E2M1
+    weight with the same property: NVFP4 with unit global scales is exact."""
+    g = torch.Generator().manual_seed(seed)
+    def grid(rows, cols):
+        c = torch.randint(0, 16, (rows, cols), generator=g, dtype=torch.uint8)
+        c[:, ::16] = 7  # amax 6 in every block
+        return f.e2m1_values(c).float()
+    return grid(M, H), grid(N, H)
+
+
+def test_projection_matches_bf16_oracle_on_exact_inputs():
+    a, w = _representable_inputs()
+    aq, asf = f.fp4_quantize(a.to(BF16), 1.0)
+    wq, wsf = f.fp4_quantize(w.to(BF16), 1.0)
+    assert torch.equal(f.dequantize(aq, asf, 1.0), a.double())
+    assert asf.unique().tolist() == [0x38]
+    y = f.nvfp4_projection(aq, asf, wq, wsf, 1.0)
+    assert torch.equal(y.view(torch.int16), oracle.qkv_projection(a.to(BF16), w.to(BF16)).view(torch.int16))
+
+
+def test_stage_matches_bf16_oracle_when_nvfp4_is_exact():
+    """The NVFP4 stage composes the bf16 stage's oracle steps: its GEMM equals
+    the bf16 GEMM of the dequantised operands (with an exactly representable
+    weight), and its tail is the bf16 Q/K norm (eps) and RoPE (token-index
+    positions)."""
+    g = torch.Generator().manual_seed(8)
+    M, H = 3, 5376
+    # zero AdaLN tables: a = n
+    codes = torch.randint(0, 16, (M, H), generator=g, dtype=torch.uint8)
+    codes[:, ::16] = 7
+    x = f.e2m1_values(codes).float()
+    x = x.to(BF16)
+    xw = torch.ones(H, dtype=BF16)
+    sc = torch.zeros(1, H, dtype=BF16)
+    sh = torch.zeros(1, H, dtype=BF16)
+    idx = torch.zeros(M, dtype=torch.int32)
+    n = oracle.input_rmsnorm(x, xw, 1e-30)
+    wc = torch.randint(0, 16, (21504, H), generator=g, dtype=torch.uint8)
+    wc[:, ::16] = 7
+    w = f.e2m1_values(wc).to(BF16)
+    wq, wsf = f.fp4_quantize(w, 1.0)
+    cs = torch.randn(M, 96, generator=g).to(BF16)
+    qn = (1 + 0.1 * torch.randn(128, generator=g)).to(BF16)
+    kn = (1 + 0.1 * torch.randn(128, generator=g)).to(BF16)
+    got = f.pre_attention_nvfp4_tokens(x, xw, sc, sh, idx, wq, wsf, 1.0, 1.0, qn, kn, cs,
+                                       eps=1e-30)
+    # zero tables: a = n (by value; shift 0 turns -0 into +0)
+    assert torch.equal(got.a.float(), n.float())
+    # the NVFP4 GEMM equals the bf16 oracle's GEMM of the dequantised operands
+    # (e2m1 * ue4m3 values are exact in bf16; the weight dequantises to w)
+    a_deq = f.dequantize(got.act_q, got.act_sf, 1.0).to(BF16)
+    assert torch.equal(f.dequantize(wq, wsf, 1.0).to(BF16).view(torch.int16), w.view(torch.int16))
+    y_ref = oracle.qkv_projection(a_deq, w)
+    assert torch.equal(got.y.view(torch.int16), y_ref.view(torch.int16))
+    # the norm/RoPE tail: the bf16 oracle's own functions, eps for the Q/K norm
+    y4 = y_ref.view(M, 3, 56, 128)
+    for kind, wn in ((0, qn), (1, kn)):
+        t = oracle.rope_split_half(oracle.head_rmsnorm(y4[:, kind], wn, 1e-30), cs, torch.arange(M))
+        assert torch.equal(got.qkv[:, :, kind].view(torch.int16), t.view(torch.int16))
+    assert torch.equal(got.qkv[:, :, 2].view(torch.int16), y4[:, 2].view(torch.int16))
