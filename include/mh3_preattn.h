@@ -325,6 +325,98 @@ int mh3_mlp_validate(int64_t M, const mh3_bf16* x, const mh3_bf16* x_norm_weight
 /* Bytes of the MLP intermediate y, [M, 14336] bf16: M * 14336 * 2 (0 for M <= 0). */
 size_t mh3_mlp_workspace_y_bytes(int64_t M);
 
+/* ------------------------------------------------------------ NVFP4 stage
+ * The pre-attention stage with NVFP4 operands (page
+ * "flashinfer.diffusion_ops.minimax_h3_nvfp4_pre_attention", summary and
+ * Parameters).  NVFP4 here: E2M1 element codes packed two per byte (element
+ * 2j in the low nibble of byte j), one UE4M3 scale per block of 16
+ * consecutive elements of a row, and an FP32 global scale gs:
+ *   s    = ue4m3(RN(RN(amax / 6) * gs))    amax = max |v| of the block
+ *   code = e2m1(RN(v * RN(gs / s)))         (0 when s = 0); v ~ code * s / gs
+ * both roundings to nearest even and saturating (448, 6).
+ * Scale layouts: row-major [rows, cols/16] (tiled = 0), or tiled (tiled = 1):
+ * 512-byte atoms of 128 rows x 4 scales (one 64-element step), row r of an
+ * atom at byte (r % 32) * 16 + (r / 32) * 4, atoms ordered [rows/128][cols/64]
+ * (rows padded up to a multiple of 128; padding bytes are not written).  The
+ * tiled layout is what the block-scaled GEMM reads, and is this library's
+ * reading of the page's "128x4 swizzled" weight scales. */
+
+/* Bytes of packed codes, rows * cols / 2, and of the scales of a rows x cols
+ * matrix in the given layout (0 for rows <= 0 or cols <= 0). */
+size_t mh3_nvfp4_codes_bytes(int64_t rows, int64_t cols);
+size_t mh3_nvfp4_scales_bytes(int64_t rows, int64_t cols, int tiled);
+
+/* Quantise a bf16 matrix (the weight preparation of the NVFP4 stage, in the
+ * role of the page's quantize_minimax_h3_qkv_weight_nvfp4, and a standalone
+ * activation quantiser):
+ *   rows, cols     rows >= 0; cols a positive multiple of 64 (<= 2^24)
+ *   values         DEVICE bf16 [rows, cols] row-major, 16-byte aligned
+ *   global_scale   DEVICE pointer to one float gs, read on the device
+ *   codes          DEVICE, rows * cols / 2 bytes, 16-byte aligned
+ *   scales         DEVICE, mh3_nvfp4_scales_bytes(rows, cols, tiled) bytes
+ * Returns MH3_ERR_INVALID_ARG / MH3_ERR_ALIGNMENT for bad arguments,
+ * MH3_ERR_CUDA for a failed launch.  Needs no handle. */
+int mh3_nvfp4_quantize(void* stream, int64_t rows, int64_t cols, const mh3_bf16* values,
+                       const float* global_scale, uint8_t* codes, uint8_t* scales, int tiled);
+
+/* Kernel 1 of the NVFP4 stage alone: the bf16 stage's n and a (input
+ * RMSNorm, indexed AdaLN with the guard) quantised per token with the
+ * activation global scale.  adaln_index is INT32 [M] here (Parameters:
+ * adaln_index); a bad index gives zero codes and zero scales.
+ *   act_global_scale  DEVICE pointer to one float (Parameters:
+ *                     act_global_scale, read on the device)
+ *   act_q             DEVICE [M, 2688] bytes, 16-byte aligned
+ *   act_sf            DEVICE, mh3_nvfp4_scales_bytes(M, 5376, tiled) bytes
+ * Other arguments as in mh3_preattn_norm_adaln. */
+int mh3_nvfp4_norm_quant(mh3_preattn_t handle, void* stream, int64_t M, const mh3_bf16* x,
+                         const mh3_bf16* x_norm_weight, const mh3_bf16* adaln_scale,
+                         int64_t scale_row_stride, const mh3_bf16* adaln_shift,
+                         int64_t shift_row_stride, int64_t rows, const int32_t* adaln_index,
+                         float eps, const float* act_global_scale, uint8_t* act_q,
+                         uint8_t* act_sf, int tiled);
+
+/* The whole NVFP4 stage: kernel 1 (norm, AdaLN, activation quantisation)
+ * then the block-scaled FP4 GEMM (tcgen05 kind::mxf4nvf4) with
+ *   y = bf16(RN(alpha * acc)),  acc = sum_k (qa sa)(qw sw)  (FP32)
+ * and the bf16 stage's epilogue: per-head RMSNorm of q and k with eps (the
+ * op has one eps), split-half RoPE of dims [0, 96) with row m of
+ * rope_cos_sin for token m, and the destination-major pack.
+ *   adaln_index          INT32 [M]
+ *   weight_q             DEVICE [21504, 2688] codes of qkv_weight (rows in
+ *                        [kind, head, d] order), 16-byte aligned
+ *   weight_sf            DEVICE tiled scales of qkv_weight,
+ *                        mh3_nvfp4_scales_bytes(21504, 5376, 1) bytes,
+ *                        16-byte aligned
+ *   weight_global_scale  host float: the weight's gs
+ *   act_global_scale     DEVICE pointer to one float
+ *   alpha                host float; finite and > 0 is used as given, any
+ *                        other value (e.g. NaN) means alpha is derived on the
+ *                        device as RN(1 / RN(act_gs * weight_global_scale))
+ *                        (Parameters: alpha)
+ *   rope_cos_sin         DEVICE bf16 [M, 96], 16-byte aligned
+ *   P                    ulysses degree 1, 2, 4 or 8
+ *   qkv_descale          NULL: bf16 out [P, M, 56/P, 3, 128]; else DEVICE
+ *                        float [3] and out holds e4m3 codes of the same
+ *                        shape (the conversion of mh3_preattn_run_e4m3)
+ *   act_q, act_sf        stage-1 workspaces ([M, 2688] bytes and the tiled
+ *                        scales of [M, 5376], each 16-byte aligned) or NULL
+ *                        for handle-owned buffers (grown with
+ *                        cudaMallocAsync on `stream`)
+ *   out                  DEVICE, 16-byte aligned
+ * The output shapes of the page's q, k, v are defined on the FP8 stage's
+ * page, which is not available; this call writes the bf16 stage's packed
+ * layout.  Returns as mh3_preattn_run; MH3_ERR_UNSUPPORTED when no CTA pair
+ * of the GEMM fits the device. */
+int mh3_nvfp4_preattn_run(mh3_preattn_t handle, void* stream, int64_t M, const mh3_bf16* x,
+                          const mh3_bf16* x_norm_weight, const mh3_bf16* adaln_scale,
+                          int64_t scale_row_stride, const mh3_bf16* adaln_shift,
+                          int64_t shift_row_stride, int64_t rows, const int32_t* adaln_index,
+                          const uint8_t* weight_q, const uint8_t* weight_sf,
+                          float weight_global_scale, const float* act_global_scale, float alpha,
+                          const mh3_bf16* q_norm_weight, const mh3_bf16* k_norm_weight,
+                          const mh3_bf16* rope_cos_sin, int P, float eps,
+                          const float* qkv_descale, uint8_t* act_q, uint8_t* act_sf, void* out);
+
 /* Message of the calling thread's last failed call ("" if none). */
 const char* mh3_preattn_last_error(void);
 

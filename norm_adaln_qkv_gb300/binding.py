@@ -35,7 +35,8 @@ EXPORTS = ("mh3_preattn_create", "mh3_preattn_destroy", "mh3_preattn_workspace_b
            "mh3_preattn_last_error", "mh3_preattn_run_noalloc", "mh3_out_proj_run",
            "mh3_out_proj_validate", "mh3_mlp_run", "mh3_mlp_validate",
            "mh3_mlp_workspace_y_bytes", "mh3_preattn_run_e4m3", "mh3_preattn_out_e4m3_bytes",
-           "mh3_e4m3_quantize")
+           "mh3_e4m3_quantize", "mh3_nvfp4_codes_bytes", "mh3_nvfp4_scales_bytes",
+           "mh3_nvfp4_quantize", "mh3_nvfp4_norm_quant", "mh3_nvfp4_preattn_run")
 
 _vp = ctypes.c_void_p
 _i64 = ctypes.c_int64
@@ -67,6 +68,14 @@ _SIGS = {
                                     _vp, _vp, _vp, _i64, _vp, _i32, _f32, _f32, _vp, _vp, _vp]),
     "mh3_preattn_out_e4m3_bytes": (ctypes.c_size_t, [_i64]),
     "mh3_e4m3_quantize": (_i32, [_vp, _i64, _vp, _vp, _vp]),
+    "mh3_nvfp4_codes_bytes": (ctypes.c_size_t, [_i64, _i64]),
+    "mh3_nvfp4_scales_bytes": (ctypes.c_size_t, [_i64, _i64, _i32]),
+    "mh3_nvfp4_quantize": (_i32, [_vp, _i64, _i64, _vp, _vp, _vp, _vp, _i32]),
+    "mh3_nvfp4_norm_quant": (_i32, [_vp, _vp, _i64, _vp, _vp, _vp, _i64, _vp, _i64, _i64, _vp,
+                                    _f32, _vp, _vp, _vp, _i32]),
+    "mh3_nvfp4_preattn_run": (_i32, [_vp, _vp, _i64, _vp, _vp, _vp, _i64, _vp, _i64, _i64, _vp,
+                                     _vp, _vp, _f32, _vp, _f32, _vp, _vp, _vp, _i32, _f32, _vp,
+                                     _vp, _vp, _vp]),
     "mh3_preattn_run_noalloc": (_i32, [_vp, _i64, _vp, _vp, _vp, _i64, _vp, _i64, _i64, _vp, _vp,
                                        _vp, _vp, _vp, _i64, _vp, _i32, _f32, _f32, _vp, _vp]),
 }
@@ -327,6 +336,41 @@ def mh3_e4m3_quantize(stream, values, descale, codes) -> None:
         raise ValueError("codes must have as many elements as values")
     _check(load().mh3_e4m3_quantize(_stream_ptr(stream), n, _ptr(values), _ptr(descale),
                                     _ptr(codes)), "mh3_e4m3_quantize")
+
+
+def mh3_nvfp4_quantize(stream, values, global_scale, codes, scales, tiled: bool = True) -> None:
+    """NVFP4 codes and block scales of a device bf16 matrix [rows, cols]
+    (cols a multiple of 64); global_scale is a device float32 tensor [1]."""
+    rows, cols = values.shape
+    _check(load().mh3_nvfp4_quantize(_stream_ptr(stream), rows, cols, _ptr(values),
+                                     _ptr(global_scale), _ptr(codes), _ptr(scales),
+                                     1 if tiled else 0), "mh3_nvfp4_quantize")
+
+
+def mh3_nvfp4_norm_quant(handle: Handle, stream, M, x, x_norm_weight, adaln_scale,
+                         scale_row_stride, adaln_shift, shift_row_stride, rows, adaln_index, eps,
+                         act_global_scale, act_q, act_sf, tiled: bool = True) -> None:
+    _check(load().mh3_nvfp4_norm_quant(
+        handle.ptr, _stream_ptr(stream), M, _ptr(x), _ptr(x_norm_weight), _ptr(adaln_scale),
+        scale_row_stride, _ptr(adaln_shift), shift_row_stride, rows, _ptr(adaln_index),
+        float(eps), _ptr(act_global_scale), _ptr(act_q), _ptr(act_sf), 1 if tiled else 0),
+        "mh3_nvfp4_norm_quant")
+
+
+def mh3_nvfp4_preattn_run(handle: Handle, stream, M, x, x_norm_weight, adaln_scale,
+                          scale_row_stride, adaln_shift, shift_row_stride, rows, adaln_index,
+                          weight_q, weight_sf, weight_global_scale, act_global_scale, alpha,
+                          q_norm_weight, k_norm_weight, rope_cos_sin, P, eps, qkv_descale,
+                          act_q, act_sf, out) -> None:
+    """The NVFP4 stage; alpha None derives it on the device from the global
+    scales; qkv_descale None writes bf16 out, else e4m3 codes."""
+    _check(load().mh3_nvfp4_preattn_run(
+        handle.ptr, _stream_ptr(stream), M, _ptr(x), _ptr(x_norm_weight), _ptr(adaln_scale),
+        scale_row_stride, _ptr(adaln_shift), shift_row_stride, rows, _ptr(adaln_index),
+        _ptr(weight_q), _ptr(weight_sf), float(weight_global_scale), _ptr(act_global_scale),
+        float("nan") if alpha is None else float(alpha), _ptr(q_norm_weight),
+        _ptr(k_norm_weight), _ptr(rope_cos_sin), P, float(eps), _ptr(qkv_descale), _ptr(act_q),
+        _ptr(act_sf), _ptr(out)), "mh3_nvfp4_preattn_run")
 
 
 def mh3_preattn_norm_adaln(handle: Handle, stream, M, x, x_norm_weight, adaln_scale,

@@ -19,7 +19,8 @@ CSRC = os.path.join(PKG, "csrc")
 BUILD = os.path.join(PKG, "_build")
 LIB = os.path.join(PKG, "libmh3_preattn.so")
 SOURCES = ["mh3_preattn.cu", "k1_norm_adaln.cu", "k2_qkv_gemm.cu", "k2_qkv_gemm_pair.cu",
-           "out_proj.cu", "mlp.cu", "e4m3_quantize.cu"]
+           "out_proj.cu", "mlp.cu", "e4m3_quantize.cu",
+           "k2_nvfp4_pair.cu", "nvfp4_quantize.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 
 

@@ -45,6 +45,13 @@ struct NormAdalnParams {
   int64_t M;
   float eps;
   int* status;  // device status word (bounded-wait timeouts)
+  // NVFP4 form (act_q != nullptr): int32 indices; the quantised activation
+  // replaces the bf16 workspace
+  const int32_t* index32 = nullptr;
+  uint8_t* act_q = nullptr;      // [M, 2688] packed E2M1
+  uint8_t* act_sf = nullptr;     // UE4M3 scales, tiled atoms or row-major [M, 336]
+  const float* act_gs = nullptr; // device [1]: activation global scale
+  int sf_tiled = 1;
 };
 
 struct QkvParams {
@@ -60,6 +67,11 @@ struct QkvParams {
   int num_tiles;    // num_m_tiles * 84
   const float* descales;  // e4m3 output mode: q, k, v dequantisation scales (device)
   int* status;  // device status word
+  // NVFP4 stage: y = bf16(RN(alpha * acc)); alpha given (finite, > 0) or
+  // derived on the device as RN(1 / RN(act_gs * w_gs))
+  float alpha = 1.0f;
+  const float* act_gs = nullptr;  // device [1]
+  float w_gs = 0.0f;
 };
 
 // num_sms: SM count of the device (the kernel is persistent over rows).
@@ -71,6 +83,25 @@ struct QkvMaps {
   CUtensorMap b;    // qkv_weight [21504, 5376], box 64 x 256 (single) / 64 x 128 (pair)
   CUtensorMap out;  // out as 4-D (d 128, slot 168/P, m M, dst P), box 64x1x32x1
 };
+
+// NVFP4 pre-attention, kernel 2: block-scaled FP4 CTA-pair GEMM with the
+// QKV epilogue (one head per 256 x 128 tile).
+struct Nvfp4Maps {
+  CUtensorMap a;    // act_q [M, 2688] bytes, box 128 B x 128 rows, 128-B swizzle
+  CUtensorMap b;    // weight codes [21504, 2688] bytes, box 128 B x 64 rows, 128-B swizzle
+  CUtensorMap sfa;  // act scales, tiled atoms as u32 (128, 84, ceil(M/128)), box 128 x 4 x 1
+  CUtensorMap sfb;  // weight scales, tiled atoms as u32 (128, 84, 168), box 128 x 4 x 1
+  CUtensorMap out;  // as QkvMaps::out (bf16) or the e4m3 byte map
+};
+cudaError_t nvfp4_qkv_prepare_device(int* max_clusters, int* max_clusters_e4m3);
+cudaError_t launch_nvfp4_qkv(const Nvfp4Maps& maps, const QkvParams& p, int clusters, bool e4m3,
+                             cudaStream_t stream);
+
+// Standalone NVFP4 quantiser: rows x cols bf16 (cols a multiple of 64) ->
+// packed codes [rows, cols/2] and scales (tiled atoms or row-major).
+cudaError_t launch_nvfp4_quantize(const __nv_bfloat16* in, int64_t rows, int cols, const float* gs,
+                                  uint8_t* codes, uint8_t* scales, bool tiled, int num_sms,
+                                  cudaStream_t stream);
 
 // ----------------------------------------- attention output projection
 // out = bf16(residual + bf16(gate[gate_index[m]] * bf16(attn_out @ o_weight^T)))

@@ -24,7 +24,15 @@
 // write-back policy so the GEMM that follows finds the rows in L2 when they
 // fit.  The ring wait is bounded (2 s) and records a status code instead of
 // hanging.
+//
+// NVFP4 form (flashinfer.diffusion_ops.minimax_h3_nvfp4_pre_attention,
+// summary): int32 indices, and instead of the bf16 workspace the activation
+// quantised per token in blocks of 16 (nvfp4.cuh): E2M1 codes [M, 2688] and
+// UE4M3 scales.  A block is two neighbouring lanes' chunks (one shuffle for
+// the amax); a 64-element step's four scales are gathered from eight aligned
+// lanes into one 4-byte store.  A guarded row gets zero codes and scales.
 #include "common.cuh"
+#include "nvfp4.cuh"
 #include "ptx.cuh"
 
 namespace mh3 {
@@ -76,6 +84,25 @@ __device__ __forceinline__ uint32_t adaln_pair(uint64_t x2, uint32_t w, uint32_t
   return f2_to_bf16x2(f2_fma(f2_from_bf16x2(n), f2_from_bf16x2(g), f2_from_bf16x2(sh)));
 }
 
+// NVFP4 outputs of one 8-element chunk c of row m (a in `o`): the block of
+// 16 is this thread's chunk and its neighbour's (lanes 2b, 2b+1), the scale
+// word of one 64-element step is gathered from 8 aligned lanes.
+__device__ __forceinline__ void fp4_chunk(const uint4& o, int lane, int c, int64_t m, float gs,
+                                          const NormAdalnParams& p) {
+  float amax = fp4::amax8(o);
+  amax = fmaxf(amax, __shfl_xor_sync(0xFFFFFFFFu, amax, 1));
+  const fp4::BlockScale bs = fp4::block_scale(amax, gs);
+  *reinterpret_cast<uint32_t*>(p.act_q + m * (kHidden / 2) + 4 * c) = fp4::encode8(o, bs.enc);
+  uint32_t word = (lane & 1) ? 0u : bs.code << (8 * ((lane & 7) >> 1));
+  word |= __shfl_xor_sync(0xFFFFFFFFu, word, 1);
+  word |= __shfl_xor_sync(0xFFFFFFFFu, word, 2);
+  word |= __shfl_xor_sync(0xFFFFFFFFu, word, 4);
+  if ((lane & 7) == 0)
+    *reinterpret_cast<uint32_t*>(p.act_sf + fp4::scale_offset(m, c >> 3, kHidden / 64,
+                                                               p.sf_tiled != 0)) = word;
+}
+
+template <bool kFp4>
 __global__ void __launch_bounds__(kThreads, kCtasPerSm) norm_adaln_kernel(const NormAdalnParams p) {
   __shared__ __align__(128) uint8_t rows_buf[kStages][kRowBytes];
   __shared__ __align__(8) uint64_t full[kStages];
@@ -93,6 +120,7 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm) norm_adaln_kernel(const 
   // kernel 2 may start its prologue (barriers, TMEM, tensor maps) now; it
   // waits for this grid's completion before it reads the workspace
   griddep_launch_dependents();
+  const float gs = kFp4 ? __ldg(p.act_gs) : 0.0f;
 
   uint64_t policy = 0;
   if (tid == 0) {
@@ -112,7 +140,7 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm) norm_adaln_kernel(const 
     const int s = static_cast<int>(i % kStages);
     const uint32_t parity = static_cast<uint32_t>((i / kStages) & 1);
     const int64_t m = first + i * G;
-    const int64_t idx = __ldg(p.index + m);
+    const int64_t idx = kFp4 ? static_cast<int64_t>(__ldg(p.index32 + m)) : __ldg(p.index + m);
     if (tid == 0) go = wait_row(bar0 + 8 * s, parity, p.status) ? 1 : 0;
     __syncthreads();
     if (!go) break;
@@ -157,7 +185,12 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm) norm_adaln_kernel(const 
     if (idx < 0 || idx >= p.rows) {
       const uint4 z = make_uint4(0u, 0u, 0u, 0u);
 #pragma unroll
-      for (int j = 0; j < kVecPerThread; ++j) wr[tid + kThreads * j] = z;
+      for (int j = 0; j < kVecPerThread; ++j) {
+        if (kFp4)
+          fp4_chunk(z, lane, tid + kThreads * j, m, 0.0f, p);  // codes 0, scale 0
+        else
+          wr[tid + kThreads * j] = z;
+      }
       continue;
     }
     const float r =
@@ -177,7 +210,10 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm) norm_adaln_kernel(const 
       o.y = adaln_pair(f2_from_bf16x2(v[j].y), w.y, sc.y, sh.y, r2);
       o.z = adaln_pair(f2_from_bf16x2(v[j].z), w.z, sc.z, sh.z, r2);
       o.w = adaln_pair(f2_from_bf16x2(v[j].w), w.w, sc.w, sh.w, r2);
-      wr[c] = o;
+      if (kFp4)
+        fp4_chunk(o, lane, c, m, gs, p);
+      else
+        wr[c] = o;
     }
   }
 
@@ -196,7 +232,10 @@ cudaError_t launch_norm_adaln(const NormAdalnParams& p, int num_sms, cudaStream_
   if (p.M <= 0) return cudaSuccess;
   const int64_t want = static_cast<int64_t>(num_sms) * kCtasPerSm;
   const int64_t grid = p.M < want ? p.M : want;
-  norm_adaln_kernel<<<static_cast<unsigned>(grid), kThreads, 0, stream>>>(p);
+  if (p.act_q != nullptr)
+    norm_adaln_kernel<true><<<static_cast<unsigned>(grid), kThreads, 0, stream>>>(p);
+  else
+    norm_adaln_kernel<false><<<static_cast<unsigned>(grid), kThreads, 0, stream>>>(p);
   return cudaGetLastError();
 }
 

@@ -124,8 +124,20 @@ __device__ __forceinline__ uint32_t stg_addr(uint32_t stg, int row, int chunk) {
 
 __device__ __forceinline__ float acc_to_y(uint32_t bits) { return round_bf16(__uint_as_float(bits)); }
 
-// V head: o = bf16(acc).
-__device__ __forceinline__ void epi_v_head(uint32_t tcol, uint32_t stg, int lane) {
+// y = bf16(acc), or bf16(RN(alpha * acc)) for a scaled (block-scaled FP4) accumulator.
+template <bool kScaled>
+__device__ __forceinline__ float acc_to_y_s(uint32_t bits, float alpha) {
+  return kScaled ? round_bf16(__fmul_rn(__uint_as_float(bits), alpha)) : acc_to_y(bits);
+}
+template <bool kScaled>
+__device__ __forceinline__ float acc_value(uint32_t bits, float alpha) {
+  return kScaled ? __fmul_rn(__uint_as_float(bits), alpha) : __uint_as_float(bits);
+}
+
+// V head: o = bf16(acc) (bf16(RN(alpha * acc)) when kScaled).
+template <bool kScaled = false>
+__device__ __forceinline__ void epi_v_head(uint32_t tcol, uint32_t stg, int lane,
+                                           float alpha = 1.0f) {
 #pragma unroll
   for (int c = 0; c < 4; ++c) {
     uint32_t v[32];
@@ -134,10 +146,10 @@ __device__ __forceinline__ void epi_v_head(uint32_t tcol, uint32_t stg, int lane
 #pragma unroll
     for (int g = 0; g < 4; ++g) {
       uint4 w;
-      w.x = pack_bf16x2(__uint_as_float(v[8 * g + 0]), __uint_as_float(v[8 * g + 1]));
-      w.y = pack_bf16x2(__uint_as_float(v[8 * g + 2]), __uint_as_float(v[8 * g + 3]));
-      w.z = pack_bf16x2(__uint_as_float(v[8 * g + 4]), __uint_as_float(v[8 * g + 5]));
-      w.w = pack_bf16x2(__uint_as_float(v[8 * g + 6]), __uint_as_float(v[8 * g + 7]));
+      w.x = pack_bf16x2(acc_value<kScaled>(v[8 * g + 0], alpha), acc_value<kScaled>(v[8 * g + 1], alpha));
+      w.y = pack_bf16x2(acc_value<kScaled>(v[8 * g + 2], alpha), acc_value<kScaled>(v[8 * g + 3], alpha));
+      w.z = pack_bf16x2(acc_value<kScaled>(v[8 * g + 4], alpha), acc_value<kScaled>(v[8 * g + 5], alpha));
+      w.w = pack_bf16x2(acc_value<kScaled>(v[8 * g + 6], alpha), acc_value<kScaled>(v[8 * g + 7], alpha));
       st_shared_v4(stg_addr(stg, lane, 4 * c + g), w);
     }
   }
@@ -145,8 +157,9 @@ __device__ __forceinline__ void epi_v_head(uint32_t tcol, uint32_t stg, int lane
 
 // Q or K head: RMSNorm over the 128 columns, rotation of [0, 96), pass-through
 // of [96, 128).
+template <bool kScaled = false>
 __device__ __forceinline__ void epi_qk_head(uint32_t tcol, uint32_t stg, int lane, const float* nw,
-                                            const uint4* cs_row, float qk_eps) {
+                                            const uint4* cs_row, float qk_eps, float alpha = 1.0f) {
   // Pass 1: FP32 sum of squares of the bf16-rounded projection.
   float s0 = 0.f, s1 = 0.f, s2 = 0.f, s3 = 0.f;
 #pragma unroll
@@ -156,8 +169,8 @@ __device__ __forceinline__ void epi_qk_head(uint32_t tcol, uint32_t stg, int lan
     tmem_wait_ld();
 #pragma unroll
     for (int i = 0; i < 32; i += 4) {
-      const float y0 = acc_to_y(v[i]), y1 = acc_to_y(v[i + 1]);
-      const float y2 = acc_to_y(v[i + 2]), y3 = acc_to_y(v[i + 3]);
+      const float y0 = acc_to_y_s<kScaled>(v[i], alpha), y1 = acc_to_y_s<kScaled>(v[i + 1], alpha);
+      const float y2 = acc_to_y_s<kScaled>(v[i + 2], alpha), y3 = acc_to_y_s<kScaled>(v[i + 3], alpha);
       s0 = __fmaf_rn(y0, y0, s0);
       s1 = __fmaf_rn(y1, y1, s1);
       s2 = __fmaf_rn(y2, y2, s2);
@@ -189,9 +202,9 @@ __device__ __forceinline__ void epi_qk_head(uint32_t tcol, uint32_t stg, int lan
         const int j = 16 * g + i + e;
         const float c = e ? bf16_hi(cw) : bf16_lo(cw);
         const float s = e ? bf16_hi(sw) : bf16_lo(sw);
-        const float t1 = round_bf16(__fmul_rn(__fmul_rn(acc_to_y(lo[i + e]), rr), nw[j]));
+        const float t1 = round_bf16(__fmul_rn(__fmul_rn(acc_to_y_s<kScaled>(lo[i + e], alpha), rr), nw[j]));
         const float t2 =
-            round_bf16(__fmul_rn(__fmul_rn(acc_to_y(hi[i + e]), rr), nw[j + kRopeHalf]));
+            round_bf16(__fmul_rn(__fmul_rn(acc_to_y_s<kScaled>(hi[i + e], alpha), rr), nw[j + kRopeHalf]));
         r1[e] = __fsub_rn(__fmul_rn(t1, c), __fmul_rn(t2, s));
         r2[e] = __fadd_rn(__fmul_rn(t2, c), __fmul_rn(t1, s));
       }
@@ -217,8 +230,8 @@ __device__ __forceinline__ void epi_qk_head(uint32_t tcol, uint32_t stg, int lan
       for (int e = 0; e < 4; ++e) {
         const int i = 8 * g + 2 * e;
         const int d = kRopeDims + i;
-        const float t0 = __fmul_rn(__fmul_rn(acc_to_y(v[i]), rr), nw[d]);
-        const float t1 = __fmul_rn(__fmul_rn(acc_to_y(v[i + 1]), rr), nw[d + 1]);
+        const float t0 = __fmul_rn(__fmul_rn(acc_to_y_s<kScaled>(v[i], alpha), rr), nw[d]);
+        const float t1 = __fmul_rn(__fmul_rn(acc_to_y_s<kScaled>(v[i + 1], alpha), rr), nw[d + 1]);
         o[e] = pack_bf16x2(t0, t1);
       }
       st_shared_v4(stg_addr(stg, lane, 12 + g), make_uint4(o[0], o[1], o[2], o[3]));
@@ -252,6 +265,58 @@ __device__ __forceinline__ void stage_to_e4m3(uint32_t stg, int lane, float desc
     stage_row_to_e4m3<false>(stg, lane, dv);
 }
 
+// cos/sin row of token m for kind (q or k); v needs none.
+__device__ __forceinline__ const uint4* rope_row(const QkvParams& p, int64_t m, int kind) {
+  int64_t prow = 0;
+  if (kind < 2 && m < p.M) {
+    if (p.positions) {
+      const int64_t pv = __ldg(p.positions + m);
+      prow = pv < 0 ? 0 : (pv >= p.S ? p.S - 1 : pv);
+    } else {
+      prow = m;
+    }
+  }
+  return reinterpret_cast<const uint4*>(p.cos_sin + prow * kRopeDims);
+}
+
+// The epilogue of one 128-column head for this warp's 32 accumulator rows.
+//   tcol      TMEM address of the warp's lanes, first column of the head
+//   m0        token row of the warp's first lane
+// The previous store from the staging buffer is waited for first; the new
+// one may still be in flight on return (bulk group of lane 0).
+template <bool kE4m3, bool kScaled = false>
+__device__ __forceinline__ void epilogue_head(uint32_t tcol, int lane, uint32_t stg,
+                                              const float* nw_all, const QkvParams& p, int64_t m0,
+                                              int kind, int head, const uint4* cs_row, float alpha,
+                                              const CUtensorMap* tm_out) {
+  if (lane == 0) bulk_wait_group_read0();
+  __syncwarp();
+  if (kind == 2)
+    epi_v_head<kScaled>(tcol, stg, lane, alpha);
+  else
+    epi_qk_head<kScaled>(tcol, stg, lane, nw_all + kind * kHeadDim, cs_row, p.qk_eps, alpha);
+  if (kE4m3) stage_to_e4m3(stg, lane, __ldg(p.descales + kind));
+  fence_proxy_async_smem();
+  __syncwarp();
+  if (lane == 0 && m0 < p.M) {
+    const int dst = head / p.heads_per_dst;
+    const int slot = (head % p.heads_per_dst) * 3 + kind;
+    if (kE4m3) {
+      tma_store_4d_hint(tm_out, stg, 0, slot, static_cast<int32_t>(m0), dst, policy_evict_first());
+    } else if (MH3_OUT_EVICT_FIRST) {
+      // out is written once and read by the next operation, not by this
+      // one: evict-first keeps it from lingering dirty in L2
+      const uint64_t pol = policy_evict_first();
+      tma_store_4d_hint(tm_out, stg, 0, slot, static_cast<int32_t>(m0), dst, pol);
+      tma_store_4d_hint(tm_out, stg + kStgHalfBytes, 64, slot, static_cast<int32_t>(m0), dst, pol);
+    } else {
+      tma_store_4d(tm_out, stg, 0, slot, static_cast<int32_t>(m0), dst);
+      tma_store_4d(tm_out, stg + kStgHalfBytes, 64, slot, static_cast<int32_t>(m0), dst);
+    }
+    bulk_commit_group();
+  }
+}
+
 // The epilogue of one 128-row x 256-column accumulator block.
 //   tmem_acc  TMEM address of the block (lane 0, first column)
 //   quad      TMEM lane quadrant this warp may read (warp index % 4)
@@ -266,54 +331,13 @@ __device__ __forceinline__ void epilogue_block(uint32_t tmem_acc, int quad, int 
   const int kind = n_blk / kNTilesPerKind;
   const int head0 = (n_blk % kNTilesPerKind) * 2;
   const int64_t m = row0 + quad * 32 + lane;
-  int64_t prow = 0;
-  if (kind < 2 && m < p.M) {
-    if (p.positions) {
-      const int64_t pv = __ldg(p.positions + m);
-      prow = pv < 0 ? 0 : (pv >= p.S ? p.S - 1 : pv);
-    } else {
-      prow = m;
-    }
-  }
-  const uint4* cs_row = reinterpret_cast<const uint4*>(p.cos_sin + prow * kRopeDims);
+  const uint4* cs_row = rope_row(p, m, kind);
   const int64_t m0 = row0 + quad * 32;
 #pragma unroll 1
   for (int j = 0; j < 2; ++j) {
     const uint32_t tcol = tmem_acc + (static_cast<uint32_t>(quad * 32) << 16) +
                           static_cast<uint32_t>(j * kHeadDim);
-    // the previous store from this staging buffer must have read it
-    if (lane == 0) bulk_wait_group_read0();
-    __syncwarp();
-    if (kind == 2)
-      epi_v_head(tcol, stg, lane);
-    else
-      epi_qk_head(tcol, stg, lane, nw_all + kind * kHeadDim, cs_row, p.qk_eps);
-    if (kE4m3) stage_to_e4m3(stg, lane, __ldg(p.descales + kind));
-    fence_proxy_async_smem();
-    __syncwarp();
-    if (kE4m3 && lane == 0 && m0 < p.M) {
-      const int head = head0 + j;
-      const int slot = (head % p.heads_per_dst) * 3 + kind;
-      tma_store_4d_hint(tm_out, stg, 0, slot, static_cast<int32_t>(m0), head / p.heads_per_dst,
-                        policy_evict_first());
-      bulk_commit_group();
-    } else if (!kE4m3 && lane == 0 && m0 < p.M) {
-      const int head = head0 + j;
-      const int dst = head / p.heads_per_dst;
-      const int slot = (head % p.heads_per_dst) * 3 + kind;
-      if (MH3_OUT_EVICT_FIRST) {
-        // out is written once and read by the next operation, not by this
-        // one: evict-first keeps it from lingering dirty in L2
-        const uint64_t pol = policy_evict_first();
-        tma_store_4d_hint(tm_out, stg, 0, slot, static_cast<int32_t>(m0), dst, pol);
-        tma_store_4d_hint(tm_out, stg + kStgHalfBytes, 64, slot, static_cast<int32_t>(m0), dst,
-                          pol);
-      } else {
-        tma_store_4d(tm_out, stg, 0, slot, static_cast<int32_t>(m0), dst);
-        tma_store_4d(tm_out, stg + kStgHalfBytes, 64, slot, static_cast<int32_t>(m0), dst);
-      }
-      bulk_commit_group();
-    }
+    epilogue_head<kE4m3>(tcol, lane, stg, nw_all, p, m0, kind, head0 + j, cs_row, 1.0f, tm_out);
   }
 }
 

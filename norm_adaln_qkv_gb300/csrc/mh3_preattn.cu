@@ -36,6 +36,12 @@ struct mh3_preattn_ctx {
   int* d_status = nullptr;
   void* ws = nullptr;  // handle-owned workspace (grown on demand)
   size_t ws_bytes = 0;
+  int nvfp4_clusters = 0;       // resident clusters of the NVFP4 GEMM (bf16 out)
+  int nvfp4_e4m3_clusters = 0;  // ... and its e4m3-output form
+  void* act_q = nullptr;        // handle-owned NVFP4 stage-1 workspaces
+  size_t act_q_bytes = 0;
+  void* act_sf = nullptr;
+  size_t act_sf_bytes = 0;
 };
 
 namespace {
@@ -78,7 +84,8 @@ int check_M(int64_t M) {
 
 int check_norm_adaln_args(int64_t M, const mh3_bf16* x, const mh3_bf16* xw, const mh3_bf16* sc,
                           int64_t sc_stride, const mh3_bf16* sh, int64_t sh_stride, int64_t rows,
-                          const int64_t* idx, float eps, const mh3_bf16* ws, bool ws_required) {
+                          const void* idx, float eps, const mh3_bf16* ws, bool ws_required,
+                          uintptr_t idx_align = 8) {
   int rc;
   if ((rc = check_M(M))) return rc;
   if (rows < 1) return fail(MH3_ERR_INVALID_ARG, "rows must be >= 1 (got %lld)", (long long)rows);
@@ -98,7 +105,7 @@ int check_norm_adaln_args(int64_t M, const mh3_bf16* x, const mh3_bf16* xw, cons
   if ((rc = check_ptr(sh, "adaln_shift", 16))) return rc;
   if (M == 0) return MH3_OK;
   if ((rc = check_ptr(x, "x", 16))) return rc;
-  if ((rc = check_ptr(idx, "adaln_index", 8))) return rc;
+  if ((rc = check_ptr(idx, "adaln_index", idx_align))) return rc;
   if (ws_required || ws != nullptr)
     if ((rc = check_ptr(ws, "workspace", 16))) return rc;
   return MH3_OK;
@@ -327,8 +334,13 @@ int mh3_preattn_create(mh3_preattn_t* handle, int device) {
   e = mlp_fc1_prepare_device(&fc1_clusters);
   if (e == cudaSuccess) e = mlp_fc2_prepare_device(&fc2_clusters);
   if (e != cudaSuccess) return cuda_fail(e, "preparing the MLP GEMMs");
+  int nvfp4_clusters = 0, nvfp4_e4m3_clusters = 0;
+  e = nvfp4_qkv_prepare_device(&nvfp4_clusters, &nvfp4_e4m3_clusters);
+  if (e != cudaSuccess) return cuda_fail(e, "preparing the NVFP4 GEMM");
   mh3_preattn_ctx* h = new mh3_preattn_ctx();
   h->device = device;
+  h->nvfp4_clusters = nvfp4_clusters;
+  h->nvfp4_e4m3_clusters = nvfp4_e4m3_clusters;
   h->fc1_clusters = fc1_clusters;
   h->e4m3_clusters = e4m3_clusters;
   h->fc2_clusters = fc2_clusters;
@@ -353,8 +365,9 @@ int mh3_preattn_destroy(mh3_preattn_t h) {
     cudaError_t e = cudaFree(h->ws);
     if (e != cudaSuccess) rc = cuda_fail(e, "freeing the handle workspace");
   }
-  if (h->ws_y) {
-    cudaError_t e = cudaFree(h->ws_y);
+  for (void* buf : {h->ws_y, h->act_q, h->act_sf}) {
+    if (buf == nullptr) continue;
+    cudaError_t e = cudaFree(buf);
     if (e != cudaSuccess && rc == MH3_OK) rc = cuda_fail(e, "freeing the handle workspace");
   }
   if (h->d_status) {
@@ -544,6 +557,244 @@ extern "C" int mh3_out_proj_run(mh3_preattn_t h, void* stream, int64_t M, const 
 // ------------------------------------------------------- e4m3 output mode
 extern "C" size_t mh3_preattn_out_e4m3_bytes(int64_t M) {
   return M <= 0 ? 0 : static_cast<size_t>(M) * kQkvRows;
+}
+
+// ------------------------------------------------------------ NVFP4 stage
+namespace {
+
+constexpr int kFp4KSteps = kHidden / 64;  // 84 scale words per token
+
+int encode_tiled(CUtensorMap* map, CUtensorMapDataType type, uint32_t rank, const void* base,
+                 const cuuint64_t* dims, const cuuint64_t* strides, const cuuint32_t* box,
+                 CUtensorMapSwizzle swz, const char* what) {
+  PFN_cuTensorMapEncodeTiled_v12000 enc = encode_fn();
+  if (enc == nullptr) return fail(MH3_ERR_CUDA, "cuTensorMapEncodeTiled entry point not found");
+  const cuuint32_t unit[5] = {1, 1, 1, 1, 1};
+  CUresult r = enc(map, type, rank, const_cast<void*>(base), dims, strides, box, unit,
+                   CU_TENSOR_MAP_INTERLEAVE_NONE, swz, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                   CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  if (r != CUDA_SUCCESS) return fail(MH3_ERR_CUDA, "tensor map (%s) failed: %d", what, (int)r);
+  return MH3_OK;
+}
+
+// out[P, M, 56/P, 3, 128] as (d, slot, m, dst): bf16 (two 64-column boxes
+// per head) or e4m3 bytes (one 128-byte box).
+int encode_out_map(CUtensorMap* map, void* out, int64_t M, int P, bool e4m3) {
+  const int64_t slots = 3 * (kHeads / P);
+  const cuuint64_t es = e4m3 ? 1 : 2;
+  const cuuint64_t dims[4] = {static_cast<cuuint64_t>(kHeadDim), static_cast<cuuint64_t>(slots),
+                              static_cast<cuuint64_t>(M), static_cast<cuuint64_t>(P)};
+  const cuuint64_t strides[3] = {kHeadDim * es, static_cast<cuuint64_t>(slots) * kHeadDim * es,
+                                 static_cast<cuuint64_t>(M) * slots * kHeadDim * es};
+  const cuuint32_t box[4] = {e4m3 ? 128u : 64u, 1, 32, 1};
+  PFN_cuTensorMapEncodeTiled_v12000 enc = encode_fn();
+  if (enc == nullptr) return fail(MH3_ERR_CUDA, "cuTensorMapEncodeTiled entry point not found");
+  const cuuint32_t unit[4] = {1, 1, 1, 1};
+  CUresult r = enc(map, e4m3 ? CU_TENSOR_MAP_DATA_TYPE_UINT8 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4,
+                   out, dims, strides, box, unit, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                   CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_NONE,
+                   CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  if (r != CUDA_SUCCESS) return fail(MH3_ERR_CUDA, "tensor map (out) failed: %d", (int)r);
+  return MH3_OK;
+}
+
+int check_fp4_stage1(int64_t M, const mh3_bf16* x, const mh3_bf16* xw, const mh3_bf16* sc,
+                     int64_t sc_stride, const mh3_bf16* sh, int64_t sh_stride, int64_t rows,
+                     const int32_t* idx, float eps, const float* act_gs) {
+  int rc = check_norm_adaln_args(M, x, xw, sc, sc_stride, sh, sh_stride, rows, idx, eps, nullptr,
+                                 false, 4);
+  if (rc) return rc;
+  if (M > 0 && (rc = check_ptr(act_gs, "act_global_scale", 4))) return rc;
+  return MH3_OK;
+}
+
+int launch_fp4_stage1(cudaStream_t s, int num_sms, int* status, int64_t M, const mh3_bf16* x,
+                      const mh3_bf16* xw, const mh3_bf16* sc, int64_t sc_stride,
+                      const mh3_bf16* sh, int64_t sh_stride, int64_t rows, const int32_t* idx,
+                      float eps, const float* act_gs, uint8_t* act_q, uint8_t* act_sf,
+                      bool tiled) {
+  NormAdalnParams p;
+  p.x = reinterpret_cast<const __nv_bfloat16*>(x);
+  p.x_norm_weight = reinterpret_cast<const __nv_bfloat16*>(xw);
+  p.scale = reinterpret_cast<const __nv_bfloat16*>(sc);
+  p.shift = reinterpret_cast<const __nv_bfloat16*>(sh);
+  p.scale_stride = sc_stride;
+  p.shift_stride = sh_stride;
+  p.rows = rows;
+  p.index = nullptr;
+  p.workspace = nullptr;
+  p.M = M;
+  p.eps = eps;
+  p.status = status;
+  p.index32 = idx;
+  p.act_q = act_q;
+  p.act_sf = act_sf;
+  p.act_gs = act_gs;
+  p.sf_tiled = tiled ? 1 : 0;
+  cudaError_t e = launch_norm_adaln(p, num_sms, s);
+  if (e != cudaSuccess) return cuda_fail(e, "NVFP4 norm/AdaLN/quantisation launch");
+  return MH3_OK;
+}
+
+}  // namespace
+
+extern "C" size_t mh3_nvfp4_codes_bytes(int64_t rows, int64_t cols) {
+  return rows <= 0 || cols <= 0 ? 0 : static_cast<size_t>(rows) * static_cast<size_t>(cols) / 2;
+}
+
+extern "C" size_t mh3_nvfp4_scales_bytes(int64_t rows, int64_t cols, int tiled) {
+  if (rows <= 0 || cols <= 0) return 0;
+  if (!tiled) return static_cast<size_t>(rows) * static_cast<size_t>(cols / 16);
+  return static_cast<size_t>((rows + 127) / 128) * static_cast<size_t>(cols / 64) * 512;
+}
+
+extern "C" int mh3_nvfp4_quantize(void* stream, int64_t rows, int64_t cols, const mh3_bf16* values,
+                                  const float* global_scale, uint8_t* codes, uint8_t* scales,
+                                  int tiled) {
+  if (rows < 0) return fail(MH3_ERR_INVALID_ARG, "rows must be >= 0 (got %lld)", (long long)rows);
+  if (cols <= 0 || cols % 64 != 0 || cols > (int64_t(1) << 24))
+    return fail(MH3_ERR_INVALID_ARG, "cols must be a positive multiple of 64 up to 2^24 (got %lld)",
+                (long long)cols);
+  if (rows > (int64_t(1) << 40) / cols)
+    return fail(MH3_ERR_INVALID_ARG, "rows x cols too large");
+  if (rows == 0) return MH3_OK;
+  int rc;
+  if ((rc = check_ptr(values, "values", 16))) return rc;
+  if ((rc = check_ptr(global_scale, "global_scale", 4))) return rc;
+  if ((rc = check_ptr(codes, "codes", 16))) return rc;
+  if ((rc = check_ptr(scales, "scales", 4))) return rc;
+  int dev = 0, sms = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e == cudaSuccess) e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+  if (e != cudaSuccess) return cuda_fail(e, "device query");
+  e = launch_nvfp4_quantize(reinterpret_cast<const __nv_bfloat16*>(values), rows,
+                            static_cast<int>(cols), global_scale, codes, scales, tiled != 0, sms,
+                            static_cast<cudaStream_t>(stream));
+  if (e != cudaSuccess) return cuda_fail(e, "NVFP4 quantiser launch");
+  return MH3_OK;
+}
+
+extern "C" int mh3_nvfp4_norm_quant(mh3_preattn_t h, void* stream, int64_t M, const mh3_bf16* x,
+                                    const mh3_bf16* x_norm_weight, const mh3_bf16* adaln_scale,
+                                    int64_t scale_row_stride, const mh3_bf16* adaln_shift,
+                                    int64_t shift_row_stride, int64_t rows,
+                                    const int32_t* adaln_index, float eps,
+                                    const float* act_global_scale, uint8_t* act_q,
+                                    uint8_t* act_sf, int tiled) {
+  int rc = check_handle(h);
+  if (rc) return rc;
+  rc = check_fp4_stage1(M, x, x_norm_weight, adaln_scale, scale_row_stride, adaln_shift,
+                        shift_row_stride, rows, adaln_index, eps, act_global_scale);
+  if (rc) return rc;
+  if (M == 0) return MH3_OK;
+  if ((rc = check_ptr(act_q, "act_q", 16))) return rc;
+  if ((rc = check_ptr(act_sf, "act_sf", 4))) return rc;
+  return launch_fp4_stage1(static_cast<cudaStream_t>(stream), h->num_sms, h->d_status, M, x,
+                           x_norm_weight, adaln_scale, scale_row_stride, adaln_shift,
+                           shift_row_stride, rows, adaln_index, eps, act_global_scale, act_q,
+                           act_sf, tiled != 0);
+}
+
+extern "C" int mh3_nvfp4_preattn_run(
+    mh3_preattn_t h, void* stream, int64_t M, const mh3_bf16* x, const mh3_bf16* x_norm_weight,
+    const mh3_bf16* adaln_scale, int64_t scale_row_stride, const mh3_bf16* adaln_shift,
+    int64_t shift_row_stride, int64_t rows, const int32_t* adaln_index, const uint8_t* weight_q,
+    const uint8_t* weight_sf, float weight_global_scale, const float* act_global_scale,
+    float alpha, const mh3_bf16* q_norm_weight, const mh3_bf16* k_norm_weight,
+    const mh3_bf16* rope_cos_sin, int P, float eps, const float* qkv_descale, uint8_t* act_q,
+    uint8_t* act_sf, void* out) {
+  int rc = check_handle(h);
+  if (rc) return rc;
+  rc = check_fp4_stage1(M, x, x_norm_weight, adaln_scale, scale_row_stride, adaln_shift,
+                        shift_row_stride, rows, adaln_index, eps, act_global_scale);
+  if (rc) return rc;
+  if (!(P == 1 || P == 2 || P == 4 || P == 8))
+    return fail(MH3_ERR_INVALID_ARG, "P (ulysses_degree) must be 1, 2, 4 or 8 (got %d)", P);
+  const bool alpha_given = std::isfinite(alpha) && alpha > 0.0f;
+  if (!alpha_given && !(std::isfinite(weight_global_scale) && weight_global_scale > 0.0f))
+    return fail(MH3_ERR_INVALID_ARG,
+                "without alpha, weight_global_scale must be finite and > 0 (alpha is derived)");
+  if ((rc = check_ptr(weight_q, "qkv_weight_q", 16))) return rc;
+  if ((rc = check_ptr(weight_sf, "qkv_weight_sf", 16))) return rc;
+  if ((rc = check_ptr(q_norm_weight, "q_norm_weight", 2))) return rc;
+  if ((rc = check_ptr(k_norm_weight, "k_norm_weight", 2))) return rc;
+  if (M == 0) return MH3_OK;
+  if ((rc = check_ptr(rope_cos_sin, "rope_cos_sin", 16))) return rc;
+  if ((rc = check_ptr(out, "out", 16))) return rc;
+  if (qkv_descale != nullptr && (rc = check_ptr(qkv_descale, "qkv_descale", 4))) return rc;
+  if (act_q != nullptr && (rc = check_ptr(act_q, "act_q", 16))) return rc;
+  if (act_sf != nullptr && (rc = check_ptr(act_sf, "act_sf", 16))) return rc;
+  const bool e4m3 = qkv_descale != nullptr;
+  const int max_clusters = e4m3 ? h->nvfp4_e4m3_clusters : h->nvfp4_clusters;
+  if (max_clusters <= 0)
+    return fail(MH3_ERR_UNSUPPORTED, "no 2-CTA cluster of the NVFP4 GEMM fits this device");
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  if (act_q == nullptr) {
+    if ((rc = grow_buffer(&h->act_q, &h->act_q_bytes, mh3_nvfp4_codes_bytes(M, kHidden), s)))
+      return rc;
+    act_q = static_cast<uint8_t*>(h->act_q);
+  }
+  if (act_sf == nullptr) {
+    if ((rc = grow_buffer(&h->act_sf, &h->act_sf_bytes, mh3_nvfp4_scales_bytes(M, kHidden, 1), s)))
+      return rc;
+    act_sf = static_cast<uint8_t*>(h->act_sf);
+  }
+  Nvfp4Maps maps;
+  {
+    const cuuint64_t dims[2] = {kHidden / 2, static_cast<cuuint64_t>(M)};
+    const cuuint64_t strides[1] = {kHidden / 2};
+    const cuuint32_t box[2] = {128, 128};
+    if ((rc = encode_tiled(&maps.a, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, act_q, dims, strides, box,
+                           CU_TENSOR_MAP_SWIZZLE_128B, "act_q")))
+      return rc;
+  }
+  {
+    const cuuint64_t dims[2] = {kHidden / 2, kQkvRows};
+    const cuuint64_t strides[1] = {kHidden / 2};
+    const cuuint32_t box[2] = {128, 64};
+    if ((rc = encode_tiled(&maps.b, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, weight_q, dims, strides, box,
+                           CU_TENSOR_MAP_SWIZZLE_128B, "qkv_weight_q")))
+      return rc;
+  }
+  {
+    // tiled scales as u32: (128 words of an atom, 84 steps, row groups)
+    const cuuint64_t groups_a = static_cast<cuuint64_t>((M + 127) / 128);
+    const cuuint64_t dims_a[3] = {128, kFp4KSteps, groups_a};
+    const cuuint64_t dims_b[3] = {128, kFp4KSteps, kQkvRows / 128};
+    const cuuint64_t strides[2] = {512, 512 * kFp4KSteps};
+    const cuuint32_t box[3] = {128, 4, 1};
+    if ((rc = encode_tiled(&maps.sfa, CU_TENSOR_MAP_DATA_TYPE_UINT32, 3, act_sf, dims_a, strides,
+                           box, CU_TENSOR_MAP_SWIZZLE_NONE, "act_sf")))
+      return rc;
+    if ((rc = encode_tiled(&maps.sfb, CU_TENSOR_MAP_DATA_TYPE_UINT32, 3, weight_sf, dims_b,
+                           strides, box, CU_TENSOR_MAP_SWIZZLE_NONE, "qkv_weight_sf")))
+      return rc;
+  }
+  if ((rc = encode_out_map(&maps.out, out, M, P, e4m3))) return rc;
+  rc = launch_fp4_stage1(s, h->num_sms, h->d_status, M, x, x_norm_weight, adaln_scale,
+                         scale_row_stride, adaln_shift, shift_row_stride, rows, adaln_index, eps,
+                         act_global_scale, act_q, act_sf, true);
+  if (rc) return rc;
+  QkvParams p;
+  p.positions = nullptr;  // one cos/sin row per token
+  p.cos_sin = reinterpret_cast<const __nv_bfloat16*>(rope_cos_sin);
+  p.q_norm_weight = reinterpret_cast<const __nv_bfloat16*>(q_norm_weight);
+  p.k_norm_weight = reinterpret_cast<const __nv_bfloat16*>(k_norm_weight);
+  p.M = M;
+  p.S = M;
+  p.heads_per_dst = kHeads / P;
+  p.qk_eps = eps;
+  p.status = h->d_status;
+  p.descales = qkv_descale;
+  p.num_m_tiles = static_cast<int>((M + 255) / 256);
+  p.num_tiles = p.num_m_tiles * (kQkvRows / 128);
+  p.alpha = alpha_given ? alpha : -1.0f;
+  p.act_gs = act_global_scale;
+  p.w_gs = weight_global_scale;
+  const int clusters = p.num_tiles < max_clusters ? p.num_tiles : max_clusters;
+  cudaError_t e = launch_nvfp4_qkv(maps, p, clusters, e4m3, s);
+  if (e != cudaSuccess) return cuda_fail(e, "NVFP4 GEMM launch");
+  return MH3_OK;
 }
 
 extern "C" int mh3_e4m3_quantize(void* stream, int64_t n, const mh3_bf16* values,

@@ -131,6 +131,17 @@ __device__ __forceinline__ void tma_load_2d_pair(uint32_t dst, const CUtensorMap
       : "memory");
 }
 
+// 3-D tiled load into this CTA's shared memory counted on an mbarrier of
+// either CTA of a pair.  c0 is the innermost coordinate (elements).
+__device__ __forceinline__ void tma_load_3d_pair(uint32_t dst, const CUtensorMap* m, uint32_t bar,
+                                                 int32_t c0, int32_t c1, int32_t c2) {
+  asm volatile(
+      "cp.async.bulk.tensor.3d.cta_group::2.shared::cluster.global.mbarrier::complete_tx::bytes"
+      " [%0], [%1, {%3, %4, %5}], [%2];" ::"r"(dst),
+      "l"(reinterpret_cast<uint64_t>(m)), "r"(bar), "r"(c0), "r"(c1), "r"(c2)
+      : "memory");
+}
+
 // Same, with an L2 eviction-priority policy from createpolicy.
 __device__ __forceinline__ void tma_load_2d_hint(uint32_t dst, const CUtensorMap* m, uint32_t bar,
                                                  int32_t c0, int32_t c1, uint64_t policy) {
@@ -380,6 +391,45 @@ __device__ __forceinline__ void umma_bf16_pair(uint32_t d_tmem, uint64_t a_desc,
       "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(accumulate)
       : "memory");
 }
+// Block-scaled pair MMA, kind::mxf4nvf4 with scale_vec::4X (E2M1 A and B in
+// shared memory, one UE4M3 scale per 16 elements, FP32 accumulator): each
+// CTA reads the A scales of its own rows and the B scales of all N rows from
+// its own TMEM at sfa / sfb.  Per K=64 step the A scales take 4 columns
+// (row m: lane m, column sfa + m / 32, byte = block) and the B scales N / 32
+// columns (row n: lane 32 * (reader's quadrant) + n % 32, column
+// sfb + n / 32), so both addresses advance in whole 4-column groups.
+__device__ __forceinline__ void umma_fp4_pair(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc,
+                                              uint32_t idesc, uint32_t sfa, uint32_t sfb,
+                                              uint32_t accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "setp.ne.b32 p, %6, 0;\n\t"
+      "tcgen05.mma.cta_group::2.kind::mxf4nvf4.block_scale.scale_vec::4X [%0], %1, %2, %3, [%4], "
+      "[%5], p;\n\t}" ::"r"(d_tmem),
+      "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(sfa), "r"(sfb), "r"(accumulate)
+      : "memory");
+}
+
+// Shared memory -> TMEM copy, pair form: each CTA copies its own 32 rows x
+// 16 bytes at `sdesc` to TMEM columns [taddr, taddr + 4) of all four lane
+// quadrants (lane l receives row l % 32).  Ordered with the pair MMAs that
+// the same thread issues after it.
+__device__ __forceinline__ void tmem_cp_pair_32x128b_x4(uint32_t taddr, uint64_t sdesc) {
+  asm volatile("tcgen05.cp.cta_group::2.32x128b.warpx4 [%0], %1;" ::"r"(taddr), "l"(sdesc)
+               : "memory");
+}
+
+// Shared-memory descriptor of an unswizzled tile of 16-byte rows stored
+// contiguously (8-row core matrices 128 B apart), the source of tcgen05.cp.
+__device__ __forceinline__ uint64_t rows16_desc(uint32_t smem_addr) {
+  uint64_t d = 0;
+  d |= static_cast<uint64_t>((smem_addr & 0x3FFFFu) >> 4);
+  d |= static_cast<uint64_t>(16 >> 4) << 16;
+  d |= static_cast<uint64_t>(128 >> 4) << 32;
+  d |= static_cast<uint64_t>(1) << 46;
+  return d;
+}
+
 // Arrive on the mbarrier at offset `bar` in every CTA of `cta_mask` once all
 // previously issued pair MMAs of this thread have completed.
 __device__ __forceinline__ void umma_commit_pair_multicast(uint32_t bar, uint16_t cta_mask) {
@@ -444,6 +494,14 @@ __device__ __forceinline__ uint64_t sw128_kmajor_desc(uint32_t smem_addr) {
 // N >> 3 in bits 17-22, M >> 4 in bits 24-28.
 __host__ __device__ constexpr uint32_t idesc_bf16_f32(int m, int n) {
   return (1u << 4) | (1u << 7) | (1u << 10) | (static_cast<uint32_t>(n >> 3) << 17) |
+         (static_cast<uint32_t>(m >> 4) << 24);
+}
+
+// Instruction descriptor of kind::mxf4nvf4: A and B E2M1 (bits 7-9 = 1,
+// 10-12 = 1), K-major, N >> 3 in bits 17-22, UE4M3 scales (bit 23 = 0),
+// M >> 4 in bits 24-28; FP32 accumulation is implied by the kind.
+__host__ __device__ constexpr uint32_t idesc_fp4_f32(int m, int n) {
+  return (1u << 7) | (1u << 10) | (static_cast<uint32_t>(n >> 3) << 17) |
          (static_cast<uint32_t>(m >> 4) << 24);
 }
 

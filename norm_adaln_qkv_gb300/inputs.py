@@ -379,3 +379,46 @@ def make_mlp_workload(M: int, seed: int = SEED_BASE + 200, rows: int = 9,
     fc2 = (_normal(gen, (HIDDEN, MLP_INTER)) / math.sqrt(MLP_INTER)).to(torch.bfloat16)
     return MlpWorkload(M=M, x=x, x_norm_weight=xw, adaln_mod=mod, adaln_index=idx, residual=res,
                        fc1_weight=fc1, fc2_weight=fc2)
+
+
+# ---------------------------------------------------------------- NVFP4 stage
+# The NVFP4 op takes int32 AdaLN indices and one cos/sin row per token
+# (flashinfer.diffusion_ops.minimax_h3_nvfp4_pre_attention, Parameters).
+BAD_INDEX32_CYCLE = (-1, 9, 2 ** 30)
+NVFP4_ACT_AMAX = 8.0  # calibration amax of the normalised activation
+
+
+@dataclass
+class Nvfp4Workload:
+    """A bf16-stage workload re-cut for the NVFP4 op: the same x, tables,
+    weights and norm weights; int32 indices (out-of-range values -1, 9, 2^30);
+    rope_cos_sin [M, 96] with row m for token m; global scales 448 * 6 / amax
+    with the calibration amax 8 for the activation and 6 sigma of the weight
+    distribution (N(0, 1/5376)) for the weight."""
+
+    base: Workload
+    adaln_index: torch.Tensor  # int32 [M]
+    rope_cos_sin: torch.Tensor  # bf16 [M, 96]
+    act_global_scale: float
+    weight_global_scale: float
+
+    @property
+    def M(self) -> int:
+        return self.base.M
+
+    @property
+    def eps(self) -> float:
+        return self.base.spec.eps
+
+
+def make_nvfp4_workload(key: str, M: Optional[int] = None) -> Nvfp4Workload:
+    wl = make_workload(key, M)
+    idx = wl.adaln_index.clone()
+    bad = (idx < 0) | (idx >= wl.spec.rows)
+    for j, t in enumerate(torch.nonzero(bad).flatten().tolist()):
+        idx[t] = BAD_INDEX32_CYCLE[j % len(BAD_INDEX32_CYCLE)]
+    cs = rope_cos_sin_cache(max(wl.M, 1), wl.spec.grid)[:wl.M].contiguous()
+    w_amax = 6.0 / math.sqrt(HIDDEN)
+    return Nvfp4Workload(base=wl, adaln_index=idx.to(torch.int32), rope_cos_sin=cs,
+                         act_global_scale=448.0 * 6.0 / NVFP4_ACT_AMAX,
+                         weight_global_scale=448.0 * 6.0 / w_amax)

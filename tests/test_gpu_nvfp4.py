@@ -1,0 +1,235 @@
+"""GPU parity of the NVFP4 pre-attention stage against the oracle
+(flashinfer.diffusion_ops.minimax_h3_nvfp4_pre_attention): the quantiser
+and kernel 1's quantised activation bit for bit; the whole stage against the
+oracle's GEMM and tail run on the GPU's own activation codes (same inputs to
+the contraction, so only the FP32 summation order differs), and against the
+oracle's whole pipeline within the bf16 stage's output bar."""
+import pytest
+import torch
+
+from oracle import e4m3, nvfp4 as f
+import oracle
+from norm_adaln_qkv_gb300 import binding
+from norm_adaln_qkv_gb300.inputs import make_nvfp4_workload
+
+from parity_utils import check_outputs
+
+pytestmark = pytest.mark.gpu
+BF16 = torch.bfloat16
+
+
+def untile(tiled: torch.Tensor, rows: int, cols: int) -> torch.Tensor:
+    """Tiled scale atoms -> row-major [rows, cols/16] (the layout stated in
+    the header: row r of an atom at byte (r % 32) * 16 + (r / 32) * 4)."""
+    ks = cols // 64
+    r = torch.arange(rows).view(-1, 1, 1)
+    k = torch.arange(ks).view(1, -1, 1)
+    j = torch.arange(4).view(1, 1, -1)
+    off = ((r // 128) * ks + k) * 512 + (r % 32) * 16 + ((r // 32) % 4) * 4 + j
+    return tiled.view(-1)[off.reshape(-1)].view(rows, ks * 4)
+
+
+@pytest.fixture(scope="module")
+def handle(cuda_lib):
+    h = binding.Handle(torch.cuda.current_device())
+    yield h
+    torch.cuda.synchronize()
+    h.close()
+
+
+def gpu_quantize(x: torch.Tensor, gs: float, tiled=True):
+    rows, cols = x.shape
+    codes = torch.empty(rows, cols // 2, dtype=torch.uint8, device="cuda")
+    nsc = binding.load().mh3_nvfp4_scales_bytes(rows, cols, 1 if tiled else 0)
+    scales = torch.full((nsc,), 0xEE, dtype=torch.uint8, device="cuda")
+    g = torch.tensor([gs], dtype=torch.float32, device="cuda")
+    binding.mh3_nvfp4_quantize(None, x, g, codes, scales, tiled)
+    torch.cuda.synchronize()
+    sc = scales.cpu()
+    return codes.cpu(), (untile(sc, rows, cols) if tiled else sc.view(rows, cols // 16))
+
+
+# ------------------------------------------------------------------ quantiser
+def _quant_input(rows, cols, seed):
+    g = torch.Generator().manual_seed(seed)
+    x = torch.randn(rows, cols, generator=g) * torch.exp2(torch.randint(-6, 6, (rows, 1), generator=g).float())
+    x[0, :16] = 0.0                      # an all-zero block
+    x[0, 16:32] = -0.0                   # signed zeros
+    x[min(1, rows - 1), 32:64] = 1e-30   # scale underflows to 0 for small gs
+    x[rows - 1, ::7] *= 1000             # saturation after the scale's rounding
+    return x.to(BF16)
+
+
+@pytest.mark.parametrize("rows,cols,gs,tiled", [(300, 5376, 336.0, True), (129, 64, 1.0, True),
+                                                (300, 5376, 2.5e4, False), (1, 128, 7.0, False),
+                                                (513, 256, 448.0 * 6, True)])
+def test_quantiser_matches_oracle(cuda_lib, rows, cols, gs, tiled):
+    x = _quant_input(rows, cols, rows + cols)
+    codes, scales = gpu_quantize(x.cuda(), gs, tiled)
+    ref_q, ref_s = f.fp4_quantize(x, gs)
+    assert torch.equal(scales, ref_s), int((scales != ref_s).sum())
+    bad = codes != ref_q
+    assert not bool(bad.any()), (int(bad.sum()), torch.nonzero(bad)[:4].tolist())
+
+
+def test_quantiser_e2m1_rounding_all_ties(cuda_lib):
+    """Block amax 6 with gs 1 (scale 1.0, enc 1.0): every element is rounded
+    by the e2m1 conversion itself; a sweep over [-7, 7] in steps of 1/64
+    covers every tie and the saturation."""
+    v = torch.arange(-7 * 64, 7 * 64 + 1, dtype=torch.float32) / 64
+    n = (v.numel() + 14) // 15
+    rows = torch.zeros(n, 16)
+    rows[:, 0] = 6.0
+    flat = rows[:, 1:].reshape(-1)
+    flat[:v.numel()] = v
+    x = rows.reshape(-1, 64 if (n * 16) % 64 == 0 else 16)
+    if x.shape[1] != 64:
+        pad = (-x.numel()) % 64
+        x = torch.cat([x.reshape(-1), torch.full((pad,), 6.0)]).reshape(-1, 64)
+    codes, _ = gpu_quantize(x.to(BF16).cuda(), 1.0, True)
+    ref_q, _ = f.fp4_quantize(x.to(BF16), 1.0)
+    assert torch.equal(codes, ref_q)
+
+
+# ------------------------------------------------------------- kernel 1 form
+def _dev(w):
+    b = w.base
+    mod = b.adaln_mod.cuda()
+    sc, sh = b.table_views(mod)
+    return dict(x=b.x.cuda(), xw=b.x_norm_weight.cuda(), mod=mod, sc=sc, sh=sh,
+                idx32=w.adaln_index.cuda(), idx64=w.adaln_index.long().cuda(),
+                qw=b.q_norm_weight.cuda(), kw=b.k_norm_weight.cuda(), cs=w.rope_cos_sin.cuda(),
+                gs=torch.tensor([w.act_global_scale], dtype=torch.float32, device="cuda"))
+
+
+@pytest.mark.parametrize("key,M", [("c2", 300), ("c3", 257), ("c0", None)])
+def test_kernel1_quantises_its_own_activation(handle, key, M):
+    w = make_nvfp4_workload(key, M)
+    d = _dev(w)
+    M = w.M
+    act_q = torch.empty(M, 2688, dtype=torch.uint8, device="cuda")
+    act_sf = torch.empty(binding.load().mh3_nvfp4_scales_bytes(M, 5376, 1), dtype=torch.uint8,
+                         device="cuda")
+    binding.mh3_nvfp4_norm_quant(handle, None, M, d["x"], d["xw"], d["sc"], d["sc"].stride(0),
+                                 d["sh"], d["sh"].stride(0), d["sc"].shape[0], d["idx32"],
+                                 w.eps, d["gs"], act_q, act_sf, True)
+    # the bf16 kernel 1 computes the same a (same code, int64 indices)
+    ws = torch.empty(M, 5376, dtype=BF16, device="cuda")
+    binding.mh3_preattn_norm_adaln(handle, None, M, d["x"], d["xw"], d["sc"], d["sc"].stride(0),
+                                   d["sh"], d["sh"].stride(0), d["sc"].shape[0], d["idx64"],
+                                   w.eps, ws)
+    torch.cuda.synchronize()
+    assert handle.device_status() == 0
+    ref_q, ref_s = f.fp4_quantize(ws.cpu(), w.act_global_scale)
+    assert torch.equal(untile(act_sf.cpu(), M, 5376), ref_s)
+    assert torch.equal(act_q.cpu(), ref_q)
+    bad = (w.adaln_index < 0) | (w.adaln_index >= w.base.spec.rows)
+    if bool(bad.any()):
+        assert int(act_q.cpu()[bad].sum()) == 0
+
+
+# ----------------------------------------------------------------- the stage
+@pytest.fixture(scope="module")
+def weight(cuda_lib):
+    w = make_nvfp4_workload("c2", 16)
+    W = w.base.qkv_weight
+    codes, scales = gpu_quantize(W.cuda(), w.weight_global_scale, True)
+    ref_q, ref_s = f.fp4_quantize(W, w.weight_global_scale)
+    assert torch.equal(codes, ref_q) and torch.equal(scales, ref_s)
+    # device copies in the GEMM's (tiled) layout
+    tiled = torch.empty(binding.load().mh3_nvfp4_scales_bytes(21504, 5376, 1), dtype=torch.uint8,
+                        device="cuda")
+    q_dev = torch.empty(21504, 2688, dtype=torch.uint8, device="cuda")
+    g = torch.tensor([w.weight_global_scale], dtype=torch.float32, device="cuda")
+    binding.mh3_nvfp4_quantize(None, W.cuda(), g, q_dev, tiled, True)
+    torch.cuda.synchronize()
+    return dict(q=ref_q, sf=ref_s, q_dev=q_dev, sf_dev=tiled, gs=w.weight_global_scale,
+                products=f.block_products(ref_q, ref_s))
+
+
+def run_stage(h, w, d, weight, out, alpha=None, descale=None, act_q=None, act_sf=None, P=None):
+    P = w.base.spec.P if P is None else P
+    binding.mh3_nvfp4_preattn_run(
+        h, None, w.M, d["x"], d["xw"], d["sc"], d["sc"].stride(0), d["sh"], d["sh"].stride(0),
+        d["sc"].shape[0], d["idx32"], weight["q_dev"], weight["sf_dev"], weight["gs"], d["gs"],
+        alpha, d["qw"], d["kw"], d["cs"], P, w.eps, descale, act_q, act_sf, out)
+
+
+def oracle_tail(w, weight, act_q, act_sf, tokens):
+    """The oracle's GEMM, alpha, Q/K norm and RoPE on given activation codes."""
+    al = f.alpha_from_scales(w.act_global_scale, weight["gs"])
+    acc = f.block_products(act_q[tokens], act_sf[tokens]) @ weight["products"].T
+    y = torch.mul(acc.to(torch.float32), torch.tensor(al, dtype=torch.float32)).to(BF16)
+    T = len(tokens)
+    y4 = y.view(T, 3, 56, 128)
+    tok = torch.as_tensor(tokens)
+    b = w.base
+    q = oracle.rope_split_half(oracle.head_rmsnorm(y4[:, 0], b.q_norm_weight, w.eps), w.rope_cos_sin, tok)
+    k = oracle.rope_split_half(oracle.head_rmsnorm(y4[:, 1], b.k_norm_weight, w.eps), w.rope_cos_sin, tok)
+    return torch.stack([q, k, y4[:, 2]], dim=2)
+
+
+@pytest.mark.parametrize("key,M", [("c2", 300), ("c3", 520), ("c0", None), ("c2", 1), ("c3", 257)])
+def test_stage_parity(handle, weight, key, M):
+    w = make_nvfp4_workload(key, M)
+    d = _dev(w)
+    M, P = w.M, w.base.spec.P
+    act_q = torch.empty(M, 2688, dtype=torch.uint8, device="cuda")
+    act_sf = torch.empty(binding.load().mh3_nvfp4_scales_bytes(M, 5376, 1), dtype=torch.uint8,
+                         device="cuda")
+    out = torch.full((P, M, 56 // P, 3, 128), float("nan"), dtype=BF16, device="cuda")
+    run_stage(handle, w, d, weight, out, act_q=act_q, act_sf=act_sf)
+    torch.cuda.synchronize()
+    assert handle.device_status() == 0
+    got = oracle.ulysses_unpack_rows(out.cpu(), list(range(M)))
+    # 1. same activation codes: only the FP32 summation order differs
+    aq, asf = act_q.cpu(), untile(act_sf.cpu(), M, 5376)
+    ref = oracle_tail(w, weight, aq, asf, list(range(M)))
+    st = check_outputs(got, ref, f"nvfp4 {key} M={M} (own codes)")
+    assert st["exact"] > 0.99, st
+    # 2. the oracle's whole pipeline
+    b = w.base
+    sc, sh = b.table_views()
+    full = f.pre_attention_nvfp4_tokens(b.x, b.x_norm_weight, sc, sh, w.adaln_index,
+                                        weight["q"], weight["sf"], weight["gs"],
+                                        w.act_global_scale, b.q_norm_weight, b.k_norm_weight,
+                                        w.rope_cos_sin, eps=w.eps)
+    st2 = check_outputs(got, full.qkv, f"nvfp4 {key} M={M} (oracle pipeline)")
+    print(key, M, st, st2)
+
+
+def test_e4m3_output_and_alpha(handle, weight):
+    w = make_nvfp4_workload("c2", 300)
+    d = _dev(w)
+    M, P = w.M, w.base.spec.P
+    out = torch.empty((P, M, 56 // P, 3, 128), dtype=BF16, device="cuda")
+    run_stage(handle, w, d, weight, out)                       # alpha derived on the device
+    out2 = torch.empty_like(out)
+    run_stage(handle, w, d, weight, out2, alpha=f.alpha_from_scales(w.act_global_scale, weight["gs"]))
+    ds = (1 / 64, 1 / 48, 1 / 128)
+    codes = torch.empty(out.shape, dtype=torch.uint8, device="cuda")
+    run_stage(handle, w, d, weight, codes, descale=torch.tensor(ds, device="cuda"))
+    torch.cuda.synchronize()
+    assert handle.device_status() == 0
+    assert torch.equal(out.view(torch.int16), out2.view(torch.int16))
+    assert torch.equal(codes.cpu(), e4m3.quantize_packed(out.cpu(), ds))
+
+
+def test_invalid_arguments(handle, weight):
+    w = make_nvfp4_workload("c2", 8)
+    d = _dev(w)
+    out = torch.empty((w.base.spec.P, 8, 56 // w.base.spec.P, 3, 128), dtype=BF16, device="cuda")
+    with pytest.raises(RuntimeError, match="P"):
+        run_stage(handle, w, d, weight, out, P=3)
+    bad = dict(weight, gs=-1.0)
+    with pytest.raises(RuntimeError, match="weight_global_scale"):
+        run_stage(handle, w, d, bad, out)
+    lib = binding.load()
+    x = torch.zeros(4, 64, dtype=BF16, device="cuda")
+    g = torch.ones(1, device="cuda")
+    c = torch.empty(4, 32, dtype=torch.uint8, device="cuda")
+    s = torch.empty(512, dtype=torch.uint8, device="cuda")
+    assert lib.mh3_nvfp4_quantize(None, 4, 48, x.data_ptr(), g.data_ptr(), c.data_ptr(), s.data_ptr(), 1) == 1
+    assert lib.mh3_nvfp4_quantize(None, 4, 64, x.data_ptr() + 2, g.data_ptr(), c.data_ptr(), s.data_ptr(), 1) == 2
+    torch.cuda.synchronize()
+    assert handle.device_status() == 0
