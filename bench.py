@@ -444,6 +444,69 @@ def run_ours(args, world, rank, local):
                                  "v 1/128)", "stage_us": q_ms * 1e3,
                      "out_bytes": int(codes.numel()), "launches_per_call": 2}
         del codes
+    # ---- the NVFP4 stage (FP4 operands, block-scaled tcgen05 GEMM), same x,
+    # tables and weight; the weight is quantised once, outside the timing
+    nvfp4_line = None
+    if not args.skip_also:
+        from norm_adaln_qkv_gb300.inputs import nvfp4_from_workload
+        wf = nvfp4_from_workload(wl)
+        lib = binding.load()
+        Mf = wf.M
+        idx32 = wf.adaln_index.to(dev)
+        csf = wf.rope_cos_sin.to(dev)
+        gsa = torch.tensor([wf.act_global_scale], dtype=torch.float32, device=dev)
+        gsw = torch.tensor([wf.weight_global_scale], dtype=torch.float32, device=dev)
+        wq = torch.empty(21504, 2688, dtype=torch.uint8, device=dev)
+        wsf = torch.empty(lib.mh3_nvfp4_scales_bytes(21504, 5376, 1), dtype=torch.uint8, device=dev)
+        binding.mh3_nvfp4_quantize(stream, d["W"], gsw, wq, wsf, True)
+        aq = torch.empty(Mf, 2688, dtype=torch.uint8, device=dev)
+        asf = torch.empty(lib.mh3_nvfp4_scales_bytes(Mf, 5376, 1), dtype=torch.uint8, device=dev)
+        Pf = wl.spec.P
+
+        def f_stage():
+            binding.mh3_nvfp4_preattn_run(h, stream, Mf, d["x"], d["xw"], d["sc"], d["sc"].stride(0),
+                                          d["sh"], d["sh"].stride(0), wl.spec.rows, idx32, wq, wsf,
+                                          wf.weight_global_scale, gsa, None, d["qw"], d["kw"], csf,
+                                          Pf, wl.spec.eps, None, aq, asf, d["out"])
+
+        def f_k1():
+            binding.mh3_nvfp4_norm_quant(h, stream, Mf, d["x"], d["xw"], d["sc"], d["sc"].stride(0),
+                                         d["sh"], d["sh"].stride(0), wl.spec.rows, idx32,
+                                         wl.spec.eps, gsa, aq, asf, True)
+
+        def f_k2():
+            binding.mh3_nvfp4_qkv(h, stream, Mf, aq, asf, wq, wsf, wf.weight_global_scale, gsa, None,
+                                  d["qw"], d["kw"], csf, Pf, wl.spec.eps, None, d["out"])
+
+        def timed(fn, n):
+            for _ in range(3):
+                fn()
+            torch.cuda.synchronize()
+            t0, t1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            t0.record(stream)
+            for _ in range(n):
+                fn()
+            t1.record(stream)
+            torch.cuda.synchronize()
+            return t0.elapsed_time(t1) / n
+
+        st_ms = timed(f_stage, args.steps)
+        k1f_ms = timed(f_k1, args.steps)
+        k2f_ms = timed(f_k2, args.steps)
+        tf4 = FLOP_PER_TOKEN * Mf / (k2f_ms * 1e-3) / 1e12
+        k1f_bytes = Mf * 10752 + Mf * 4 + Mf * 2688 + Mf * 336
+        nvfp4_line = {
+            "workload": f"{wl.spec.name}, NVFP4 operands (W4A4, block 16, UE4M3 scales)",
+            "stage_us": st_ms * 1e3, "k1_us": k1f_ms * 1e3, "k2_us": k2f_ms * 1e3,
+            "k2_tflops": tf4,
+            "k2_frac_of_bf16x4": tf4 / (4 * peaks["bf16"]),
+            "k2_frac_of_bf16x6": tf4 / (6 * peaks["bf16"]),
+            "fp4_peak_note": "FP4 peak = measured bf16 burst x 4 (the per-clock FP4/bf16 ratio "
+                             "measured for this MMA shape) or x 6 (nominal 13.5/2.25)",
+            "k1_gbs": k1f_bytes / (k1f_ms * 1e-3) / 1e9,
+            "k1_frac_of_measured_hbm": k1f_bytes / (k1f_ms * 1e-3) / 1e9 / peaks["hbm"],
+            "launches_per_call": 2}
+        del wq, wsf, aq, asf, idx32, csf
     # ---- the attention output projection with the gated residual (the
     # step after attention, same GEMM machinery), at the bench's M
     out_proj = None
@@ -558,6 +621,7 @@ def run_ours(args, world, rank, local):
         "clocks": clk,
         "also": also,
         "e4m3": e4m3_line,
+        "nvfp4": nvfp4_line,
         "out_proj": out_proj,
         "mlp": mlp_line,
     }

@@ -417,6 +417,18 @@ int mh3_nvfp4_preattn_run(mh3_preattn_t handle, void* stream, int64_t M, const m
                           const mh3_bf16* rope_cos_sin, int P, float eps,
                           const float* qkv_descale, uint8_t* act_q, uint8_t* act_sf, void* out);
 
+/* Kernel 2 of the NVFP4 stage alone, on act_q / act_sf already filled by
+ * mh3_nvfp4_norm_quant (tiled scales) or mh3_nvfp4_quantize (tiled).  act_q
+ * and act_sf must be 16-byte aligned; act_global_scale is only read when
+ * alpha is not given (finite and > 0).  Other arguments and rules as in
+ * mh3_nvfp4_preattn_run. */
+int mh3_nvfp4_qkv(mh3_preattn_t handle, void* stream, int64_t M, const uint8_t* act_q,
+                  const uint8_t* act_sf, const uint8_t* weight_q, const uint8_t* weight_sf,
+                  float weight_global_scale, const float* act_global_scale, float alpha,
+                  const mh3_bf16* q_norm_weight, const mh3_bf16* k_norm_weight,
+                  const mh3_bf16* rope_cos_sin, int P, float eps, const float* qkv_descale,
+                  void* out);
+
 /* Message of the calling thread's last failed call ("" if none). */
 const char* mh3_preattn_last_error(void);
 

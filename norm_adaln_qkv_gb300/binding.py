@@ -36,7 +36,7 @@ EXPORTS = ("mh3_preattn_create", "mh3_preattn_destroy", "mh3_preattn_workspace_b
            "mh3_out_proj_validate", "mh3_mlp_run", "mh3_mlp_validate",
            "mh3_mlp_workspace_y_bytes", "mh3_preattn_run_e4m3", "mh3_preattn_out_e4m3_bytes",
            "mh3_e4m3_quantize", "mh3_nvfp4_codes_bytes", "mh3_nvfp4_scales_bytes",
-           "mh3_nvfp4_quantize", "mh3_nvfp4_norm_quant", "mh3_nvfp4_preattn_run")
+           "mh3_nvfp4_quantize", "mh3_nvfp4_norm_quant", "mh3_nvfp4_preattn_run", "mh3_nvfp4_qkv")
 
 _vp = ctypes.c_void_p
 _i64 = ctypes.c_int64
@@ -73,6 +73,8 @@ _SIGS = {
     "mh3_nvfp4_quantize": (_i32, [_vp, _i64, _i64, _vp, _vp, _vp, _vp, _i32]),
     "mh3_nvfp4_norm_quant": (_i32, [_vp, _vp, _i64, _vp, _vp, _vp, _i64, _vp, _i64, _i64, _vp,
                                     _f32, _vp, _vp, _vp, _i32]),
+    "mh3_nvfp4_qkv": (_i32, [_vp, _vp, _i64, _vp, _vp, _vp, _vp, _f32, _vp, _f32, _vp, _vp, _vp,
+                             _i32, _f32, _vp, _vp]),
     "mh3_nvfp4_preattn_run": (_i32, [_vp, _vp, _i64, _vp, _vp, _vp, _i64, _vp, _i64, _i64, _vp,
                                      _vp, _vp, _f32, _vp, _f32, _vp, _vp, _vp, _i32, _f32, _vp,
                                      _vp, _vp, _vp]),
@@ -371,6 +373,16 @@ def mh3_nvfp4_preattn_run(handle: Handle, stream, M, x, x_norm_weight, adaln_sca
         float("nan") if alpha is None else float(alpha), _ptr(q_norm_weight),
         _ptr(k_norm_weight), _ptr(rope_cos_sin), P, float(eps), _ptr(qkv_descale), _ptr(act_q),
         _ptr(act_sf), _ptr(out)), "mh3_nvfp4_preattn_run")
+
+
+def mh3_nvfp4_qkv(handle: Handle, stream, M, act_q, act_sf, weight_q, weight_sf,
+                  weight_global_scale, act_global_scale, alpha, q_norm_weight, k_norm_weight,
+                  rope_cos_sin, P, eps, qkv_descale, out) -> None:
+    _check(load().mh3_nvfp4_qkv(
+        handle.ptr, _stream_ptr(stream), M, _ptr(act_q), _ptr(act_sf), _ptr(weight_q),
+        _ptr(weight_sf), float(weight_global_scale), _ptr(act_global_scale),
+        float("nan") if alpha is None else float(alpha), _ptr(q_norm_weight), _ptr(k_norm_weight),
+        _ptr(rope_cos_sin), P, float(eps), _ptr(qkv_descale), _ptr(out)), "mh3_nvfp4_qkv")
 
 
 def mh3_preattn_norm_adaln(handle: Handle, stream, M, x, x_norm_weight, adaln_scale,

@@ -636,6 +636,72 @@ int launch_fp4_stage1(cudaStream_t s, int num_sms, int* status, int64_t M, const
   return MH3_OK;
 }
 
+// Kernel 2 of the NVFP4 stage on filled act_q / act_sf (tiled) buffers.
+int launch_fp4_gemm(mh3_preattn_ctx* h, cudaStream_t s, int64_t M, const uint8_t* act_q,
+                    const uint8_t* act_sf, const uint8_t* weight_q, const uint8_t* weight_sf,
+                    float weight_global_scale, const float* act_global_scale, float alpha,
+                    bool alpha_given, const mh3_bf16* q_norm_weight, const mh3_bf16* k_norm_weight,
+                    const mh3_bf16* rope_cos_sin, int P, float eps, const float* qkv_descale,
+                    void* out) {
+  const bool e4m3 = qkv_descale != nullptr;
+  const int max_clusters = e4m3 ? h->nvfp4_e4m3_clusters : h->nvfp4_clusters;
+  if (max_clusters <= 0)
+    return fail(MH3_ERR_UNSUPPORTED, "no 2-CTA cluster of the NVFP4 GEMM fits this device");
+  int rc;
+  Nvfp4Maps maps;
+  {
+    const cuuint64_t dims[2] = {kHidden / 2, static_cast<cuuint64_t>(M)};
+    const cuuint64_t strides[1] = {kHidden / 2};
+    const cuuint32_t box[2] = {128, 128};
+    if ((rc = encode_tiled(&maps.a, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, act_q, dims, strides, box,
+                           CU_TENSOR_MAP_SWIZZLE_128B, "act_q")))
+      return rc;
+  }
+  {
+    const cuuint64_t dims[2] = {kHidden / 2, kQkvRows};
+    const cuuint64_t strides[1] = {kHidden / 2};
+    const cuuint32_t box[2] = {128, 64};
+    if ((rc = encode_tiled(&maps.b, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, weight_q, dims, strides, box,
+                           CU_TENSOR_MAP_SWIZZLE_128B, "qkv_weight_q")))
+      return rc;
+  }
+  {
+    // tiled scales as u32: (128 words of an atom, 84 steps, row groups)
+    const cuuint64_t groups_a = static_cast<cuuint64_t>((M + 127) / 128);
+    const cuuint64_t dims_a[3] = {128, kFp4KSteps, groups_a};
+    const cuuint64_t dims_b[3] = {128, kFp4KSteps, kQkvRows / 128};
+    const cuuint64_t strides[2] = {512, 512 * kFp4KSteps};
+    const cuuint32_t box[3] = {128, 4, 1};
+    if ((rc = encode_tiled(&maps.sfa, CU_TENSOR_MAP_DATA_TYPE_UINT32, 3, act_sf, dims_a, strides,
+                           box, CU_TENSOR_MAP_SWIZZLE_NONE, "act_sf")))
+      return rc;
+    if ((rc = encode_tiled(&maps.sfb, CU_TENSOR_MAP_DATA_TYPE_UINT32, 3, weight_sf, dims_b,
+                           strides, box, CU_TENSOR_MAP_SWIZZLE_NONE, "qkv_weight_sf")))
+      return rc;
+  }
+  if ((rc = encode_out_map(&maps.out, out, M, P, e4m3))) return rc;
+  QkvParams p;
+  p.positions = nullptr;  // one cos/sin row per token
+  p.cos_sin = reinterpret_cast<const __nv_bfloat16*>(rope_cos_sin);
+  p.q_norm_weight = reinterpret_cast<const __nv_bfloat16*>(q_norm_weight);
+  p.k_norm_weight = reinterpret_cast<const __nv_bfloat16*>(k_norm_weight);
+  p.M = M;
+  p.S = M;
+  p.heads_per_dst = kHeads / P;
+  p.qk_eps = eps;
+  p.status = h->d_status;
+  p.descales = qkv_descale;
+  p.num_m_tiles = static_cast<int>((M + 255) / 256);
+  p.num_tiles = p.num_m_tiles * (kQkvRows / 128);
+  p.alpha = alpha_given ? alpha : -1.0f;
+  p.act_gs = act_global_scale;
+  p.w_gs = weight_global_scale;
+  const int clusters = p.num_tiles < max_clusters ? p.num_tiles : max_clusters;
+  cudaError_t e = launch_nvfp4_qkv(maps, p, clusters, e4m3, s);
+  if (e != cudaSuccess) return cuda_fail(e, "NVFP4 GEMM launch");
+  return MH3_OK;
+}
+
 }  // namespace
 
 extern "C" size_t mh3_nvfp4_codes_bytes(int64_t rows, int64_t cols) {
@@ -724,10 +790,6 @@ extern "C" int mh3_nvfp4_preattn_run(
   if (qkv_descale != nullptr && (rc = check_ptr(qkv_descale, "qkv_descale", 4))) return rc;
   if (act_q != nullptr && (rc = check_ptr(act_q, "act_q", 16))) return rc;
   if (act_sf != nullptr && (rc = check_ptr(act_sf, "act_sf", 16))) return rc;
-  const bool e4m3 = qkv_descale != nullptr;
-  const int max_clusters = e4m3 ? h->nvfp4_e4m3_clusters : h->nvfp4_clusters;
-  if (max_clusters <= 0)
-    return fail(MH3_ERR_UNSUPPORTED, "no 2-CTA cluster of the NVFP4 GEMM fits this device");
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   if (act_q == nullptr) {
     if ((rc = grow_buffer(&h->act_q, &h->act_q_bytes, mh3_nvfp4_codes_bytes(M, kHidden), s)))
@@ -739,62 +801,46 @@ extern "C" int mh3_nvfp4_preattn_run(
       return rc;
     act_sf = static_cast<uint8_t*>(h->act_sf);
   }
-  Nvfp4Maps maps;
-  {
-    const cuuint64_t dims[2] = {kHidden / 2, static_cast<cuuint64_t>(M)};
-    const cuuint64_t strides[1] = {kHidden / 2};
-    const cuuint32_t box[2] = {128, 128};
-    if ((rc = encode_tiled(&maps.a, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, act_q, dims, strides, box,
-                           CU_TENSOR_MAP_SWIZZLE_128B, "act_q")))
-      return rc;
-  }
-  {
-    const cuuint64_t dims[2] = {kHidden / 2, kQkvRows};
-    const cuuint64_t strides[1] = {kHidden / 2};
-    const cuuint32_t box[2] = {128, 64};
-    if ((rc = encode_tiled(&maps.b, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, weight_q, dims, strides, box,
-                           CU_TENSOR_MAP_SWIZZLE_128B, "qkv_weight_q")))
-      return rc;
-  }
-  {
-    // tiled scales as u32: (128 words of an atom, 84 steps, row groups)
-    const cuuint64_t groups_a = static_cast<cuuint64_t>((M + 127) / 128);
-    const cuuint64_t dims_a[3] = {128, kFp4KSteps, groups_a};
-    const cuuint64_t dims_b[3] = {128, kFp4KSteps, kQkvRows / 128};
-    const cuuint64_t strides[2] = {512, 512 * kFp4KSteps};
-    const cuuint32_t box[3] = {128, 4, 1};
-    if ((rc = encode_tiled(&maps.sfa, CU_TENSOR_MAP_DATA_TYPE_UINT32, 3, act_sf, dims_a, strides,
-                           box, CU_TENSOR_MAP_SWIZZLE_NONE, "act_sf")))
-      return rc;
-    if ((rc = encode_tiled(&maps.sfb, CU_TENSOR_MAP_DATA_TYPE_UINT32, 3, weight_sf, dims_b,
-                           strides, box, CU_TENSOR_MAP_SWIZZLE_NONE, "qkv_weight_sf")))
-      return rc;
-  }
-  if ((rc = encode_out_map(&maps.out, out, M, P, e4m3))) return rc;
   rc = launch_fp4_stage1(s, h->num_sms, h->d_status, M, x, x_norm_weight, adaln_scale,
                          scale_row_stride, adaln_shift, shift_row_stride, rows, adaln_index, eps,
                          act_global_scale, act_q, act_sf, true);
   if (rc) return rc;
-  QkvParams p;
-  p.positions = nullptr;  // one cos/sin row per token
-  p.cos_sin = reinterpret_cast<const __nv_bfloat16*>(rope_cos_sin);
-  p.q_norm_weight = reinterpret_cast<const __nv_bfloat16*>(q_norm_weight);
-  p.k_norm_weight = reinterpret_cast<const __nv_bfloat16*>(k_norm_weight);
-  p.M = M;
-  p.S = M;
-  p.heads_per_dst = kHeads / P;
-  p.qk_eps = eps;
-  p.status = h->d_status;
-  p.descales = qkv_descale;
-  p.num_m_tiles = static_cast<int>((M + 255) / 256);
-  p.num_tiles = p.num_m_tiles * (kQkvRows / 128);
-  p.alpha = alpha_given ? alpha : -1.0f;
-  p.act_gs = act_global_scale;
-  p.w_gs = weight_global_scale;
-  const int clusters = p.num_tiles < max_clusters ? p.num_tiles : max_clusters;
-  cudaError_t e = launch_nvfp4_qkv(maps, p, clusters, e4m3, s);
-  if (e != cudaSuccess) return cuda_fail(e, "NVFP4 GEMM launch");
-  return MH3_OK;
+  return launch_fp4_gemm(h, s, M, act_q, act_sf, weight_q, weight_sf, weight_global_scale,
+                         act_global_scale, alpha, alpha_given, q_norm_weight, k_norm_weight,
+                         rope_cos_sin, P, eps, qkv_descale, out);
+}
+
+extern "C" int mh3_nvfp4_qkv(mh3_preattn_t h, void* stream, int64_t M, const uint8_t* act_q,
+                             const uint8_t* act_sf, const uint8_t* weight_q,
+                             const uint8_t* weight_sf, float weight_global_scale,
+                             const float* act_global_scale, float alpha,
+                             const mh3_bf16* q_norm_weight, const mh3_bf16* k_norm_weight,
+                             const mh3_bf16* rope_cos_sin, int P, float eps,
+                             const float* qkv_descale, void* out) {
+  int rc = check_handle(h);
+  if (rc) return rc;
+  if ((rc = check_M(M))) return rc;
+  if (!valid_eps(eps)) return fail(MH3_ERR_INVALID_ARG, "eps must be finite and > 0");
+  if (!(P == 1 || P == 2 || P == 4 || P == 8))
+    return fail(MH3_ERR_INVALID_ARG, "P (ulysses_degree) must be 1, 2, 4 or 8 (got %d)", P);
+  const bool alpha_given = std::isfinite(alpha) && alpha > 0.0f;
+  if (!alpha_given && !(std::isfinite(weight_global_scale) && weight_global_scale > 0.0f))
+    return fail(MH3_ERR_INVALID_ARG,
+                "without alpha, weight_global_scale must be finite and > 0 (alpha is derived)");
+  if ((rc = check_ptr(weight_q, "qkv_weight_q", 16))) return rc;
+  if ((rc = check_ptr(weight_sf, "qkv_weight_sf", 16))) return rc;
+  if ((rc = check_ptr(q_norm_weight, "q_norm_weight", 2))) return rc;
+  if ((rc = check_ptr(k_norm_weight, "k_norm_weight", 2))) return rc;
+  if (M == 0) return MH3_OK;
+  if (!alpha_given && (rc = check_ptr(act_global_scale, "act_global_scale", 4))) return rc;
+  if ((rc = check_ptr(act_q, "act_q", 16))) return rc;
+  if ((rc = check_ptr(act_sf, "act_sf", 16))) return rc;
+  if ((rc = check_ptr(rope_cos_sin, "rope_cos_sin", 16))) return rc;
+  if ((rc = check_ptr(out, "out", 16))) return rc;
+  if (qkv_descale != nullptr && (rc = check_ptr(qkv_descale, "qkv_descale", 4))) return rc;
+  return launch_fp4_gemm(h, static_cast<cudaStream_t>(stream), M, act_q, act_sf, weight_q,
+                         weight_sf, weight_global_scale, act_global_scale, alpha, alpha_given,
+                         q_norm_weight, k_norm_weight, rope_cos_sin, P, eps, qkv_descale, out);
 }
 
 extern "C" int mh3_e4m3_quantize(void* stream, int64_t n, const mh3_bf16* values,

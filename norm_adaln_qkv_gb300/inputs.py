@@ -412,7 +412,11 @@ class Nvfp4Workload:
 
 
 def make_nvfp4_workload(key: str, M: Optional[int] = None) -> Nvfp4Workload:
-    wl = make_workload(key, M)
+    return nvfp4_from_workload(make_workload(key, M))
+
+
+def nvfp4_from_workload(wl: Workload) -> Nvfp4Workload:
+    """Re-cut an already drawn bf16-stage workload for the NVFP4 op."""
     idx = wl.adaln_index.clone()
     bad = (idx < 0) | (idx >= wl.spec.rows)
     for j, t in enumerate(torch.nonzero(bad).flatten().tolist()):
