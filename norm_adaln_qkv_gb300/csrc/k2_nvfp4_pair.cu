@@ -13,20 +13,26 @@
 //
 // A cluster of two CTAs owns a 256-row x 128-column tile (one head of one
 // kind).  Per k-block CTA r loads its 128 A rows (16 KB), its 64 of the 128
-// B rows (8 KB), the 4 A-scale atoms of its rows (2 KB) and the 4 B-scale
-// atoms of all 128 B rows (2 KB) into a 6-stage ring, counted on the even
-// CTA's barrier.  One thread of the even CTA copies the stage's scale atoms
-// into both CTAs' TMEM (tcgen05.cp pair form, 32x128b.warpx4: each copy is
-// one K=64 step's 4 columns) and issues four M=256 N=128 K=64 block-scaled
-// MMAs.  With FP4 at four times the bf16 rate per clock, a 256 x 128 tile
+// B rows (8 KB), and the 4 A-scale atoms of its rows (2 KB) and the 4
+// B-scale atoms of all 128 B rows (2 KB), into a 6-stage ring, counted on
+// two barriers of the even CTA (operands, scales).  The scales go from
+// shared memory to both CTAs' TMEM by
+// tcgen05.cp (pair form, 32x128b.warpx4: one copy = one K=64 step's 4
+// columns of A or B scales).  A copy stalls the thread that issues it for
+// over a hundred clocks, so four copy warps of the even CTA issue two copies
+// each per k-block; once they have also seen the stage's operands land they
+// commit to a per-stage "ready" barrier, the only one the MMA thread waits
+// on (every wait or commit in that thread costs MMA issue time) before it
+// issues four M=256 N=128 K=64 block-scaled MMAs.  With FP4 at four times the bf16 rate per clock a 256 x 128 tile
 // reads 96 B of shared memory per clock per SM, inside the 128 B/clk budget,
 // and two 128-column accumulators plus six 32-column scale slots fit the 512
 // TMEM columns, so the epilogue of one tile overlaps the next tile's MMAs.
 //
-// Roles per CTA (192 threads): warp 0 TMA producer, warp 1 TMEM allocation
-// and (even CTA) tcgen05.cp + MMA issue, warps 2..5 the epilogue of the
-// CTA's 128 rows.  Bounded waits, abort flags and draining as in
-// gemm_pair.cuh.
+// Roles per CTA (352 threads): warp 0 operand TMA producer, warp 1 TMEM
+// allocation
+// and (even CTA) MMA issue, warps 2..5 the epilogue of the CTA's 128 rows,
+// warps 6..9 (even CTA) the scale copies, warp 10 the scale TMA producer.  Bounded waits, abort flags and
+// draining as in gemm_pair.cuh.
 #include "gemm_pair.cuh"
 
 namespace mh3 {
@@ -49,22 +55,30 @@ constexpr int kFStageBytes = kFABytes + kFBBytes + 2 * kFSfBytes;  // 28 KB
 constexpr uint32_t kFIdesc = idesc_fp4_f32(2 * FBM, kFTileN);
 constexpr uint32_t kFTmemSf = 2 * kFTileN;     // scale slots start after the accumulators
 constexpr uint32_t kFSfCols = 32;              // per slot: A scales 16 + B scales 16
+constexpr int kFSfSlots = kFStages;            // scale slots (shared memory and TMEM), one per stage
 
 constexpr int kFOffA = 0;
 constexpr int kFOffB = kFOffA + kFStages * kFABytes;
 constexpr int kFOffSfa = kFOffB + kFStages * kFBBytes;
-constexpr int kFOffSfb = kFOffSfa + kFStages * kFSfBytes;
-constexpr int kFOffStg = kFOffSfb + kFStages * kFSfBytes;
+constexpr int kFOffSfb = kFOffSfa + kFSfSlots * kFSfBytes;
+constexpr int kFOffStg = kFOffSfb + kFSfSlots * kFSfBytes;
 constexpr int kFOffBar = kFOffStg + kEpiWarps * kStgWarpBytes;
-constexpr int kFNumBars = 2 * kFStages + 4 + 1;
+// per stage: operands full, empty, scales full, ready (scales in TMEM and
+// operands landed); tmem full x2, tmem empty x2, drain, copy drain
+constexpr int kFNumBars = 4 * kFStages + 4 + 1 + 1;
 constexpr int kFOffTmemPtr = kFOffBar + kFNumBars * 8;
 constexpr int kFOffAbort = kFOffTmemPtr + 4;
-constexpr int kFOffScratch = kFOffBar + 256;
+constexpr int kFOffScratch = kFOffBar + 512;
+constexpr int kCpWarps = 4;  // scale-copy warps of the even CTA, one K step each
+constexpr int kSfWarp = 2 + kEpiWarps + kCpWarps;                    // warp 10: scale loads
+constexpr int kFThreads = 64 + kEpiWarps * 32 + kCpWarps * 32 + 32;  // 352
 constexpr int kFSmemUsed = kFOffScratch + 1024;
 constexpr int kFSmemAlloc = kFSmemUsed + 1024;
 static_assert(kFOffAbort + 4 <= kFOffScratch, "barrier block overflow");
+static_assert(kCpWarps == 4, "one copy warp per K=64 step of a k-block");
 static_assert(kFSmemAlloc <= 232448, "exceeds the 227 KB per-CTA limit");
-static_assert(kFTmemSf + kFStages * kFSfCols <= kTmemCols, "TMEM budget");
+static_assert(kFTmemSf + kFSfSlots * kFSfCols <= kTmemCols, "TMEM budget");
+
 static_assert(kHidden % 256 == 0 && kQkvRows % kFTileN == 0, "shapes must tile");
 
 struct FSmem {
@@ -79,6 +93,9 @@ struct FSmem {
   __device__ uint32_t tfull(int b) const { return base + kFOffBar + (2 * kFStages + b) * 8; }
   __device__ uint32_t tempty(int b) const { return base + kFOffBar + (2 * kFStages + 2 + b) * 8; }
   __device__ uint32_t drain() const { return base + kFOffBar + (2 * kFStages + 4) * 8; }
+  __device__ uint32_t cpdrain() const { return base + kFOffBar + (2 * kFStages + 5) * 8; }
+  __device__ uint32_t sffull(int s) const { return base + kFOffBar + (2 * kFStages + 6 + s) * 8; }
+  __device__ uint32_t ready(int s) const { return base + kFOffBar + (3 * kFStages + 6 + s) * 8; }
   __device__ uint32_t stg(int ew) const { return base + kFOffStg + ew * kStgWarpBytes; }
   __device__ uint32_t tmem_ptr_addr() const { return base + kFOffTmemPtr; }
   __device__ uint32_t* tmem_ptr() const { return reinterpret_cast<uint32_t*>(ptr + kFOffTmemPtr); }
@@ -90,7 +107,7 @@ struct FSmem {
 };
 
 template <bool kE4m3>
-__global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(gp::kThreads, 1)
+__global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kFThreads, 1)
     nvfp4_qkv_kernel(const __grid_constant__ CUtensorMap tm_a,
                      const __grid_constant__ CUtensorMap tm_b,
                      const __grid_constant__ CUtensorMap tm_sfa,
@@ -105,7 +122,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(gp::kThreads, 1)
   }
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
-  const uint32_t rank = cluster_ctarank();  // 0: issues copies and MMAs
+  const uint32_t rank = cluster_ctarank();  // 0: issues the scale copies and MMAs
   const int cid = static_cast<int>(cluster_id_x());
   const int ncl = static_cast<int>(cluster_count_x());
 
@@ -114,6 +131,11 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(gp::kThreads, 1)
       mbar_init(sm.full(s), 1);
       mbar_init(sm.empty(s), 1);
     }
+    for (int s = 0; s < kFStages; ++s) {
+      mbar_init(sm.sffull(s), 1);
+      mbar_init(sm.ready(s), kCpWarps);
+    }
+    mbar_init(sm.cpdrain(), kCpWarps);
     for (int b = 0; b < 2; ++b) {
       mbar_init(sm.tfull(b), 1);
       mbar_init(sm.tempty(b), 2 * kEpiWarps);
@@ -128,7 +150,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(gp::kThreads, 1)
     prefetch_tmap(&tm_out);
   }
   // q then k norm weights as FP32
-  for (int i = threadIdx.x; i < 2 * kHeadDim; i += gp::kThreads) {
+  for (int i = threadIdx.x; i < 2 * kHeadDim; i += kFThreads) {
     const __nv_bfloat16 w = i < kHeadDim ? p.q_norm_weight[i] : p.k_norm_weight[i - kHeadDim];
     sm.scratch()[i] = __bfloat162float(w);
   }
@@ -143,7 +165,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(gp::kThreads, 1)
   gp::PairCtx ctx{sm.abort_flag(), mapa_shared(sm.abort_addr(), rank ^ 1u), p.status};
 
   if (warp == 0) {
-    // ------------------------------------------------- producer (both CTAs)
+    // ------------------------------------ operand producer (both CTAs)
     if (lane == 0) {
       griddep_wait();  // act_q / act_sf come from the kernel before this one
       int stage = 0;
@@ -161,11 +183,9 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(gp::kThreads, 1)
             break;
           }
           const uint32_t leader_full = mapa_shared(sm.full(stage), 0);
-          if (rank == 0) mbar_arrive_expect_tx(sm.full(stage), 2 * kFStageBytes);
+          if (rank == 0) mbar_arrive_expect_tx(sm.full(stage), 2 * (kFABytes + kFBBytes));
           tma_load_2d_pair(sm.a(stage), &tm_a, leader_full, kb * kFBytesPerRow, a_rg * FBM);
           tma_load_2d_pair(sm.b(stage), &tm_b, leader_full, kb * kFBytesPerRow, b_row);
-          tma_load_3d_pair(sm.sfa(stage), &tm_sfa, leader_full, 0, 4 * kb, a_rg);
-          tma_load_3d_pair(sm.sfb(stage), &tm_sfb, leader_full, 0, 4 * kb, n_blk);
           issued_any = true;
           if (++stage == kFStages) {
             stage = 0;
@@ -193,18 +213,14 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(gp::kThreads, 1)
         tc_fence_after();
         const uint32_t d_tmem = tmem_base + static_cast<uint32_t>(buf * kFTileN);
         for (int kb = 0; kb < kFKBlocks; ++kb) {
-          if (!gp::pair_wait(ctx, sm.full(stage), phase, kStatusMmaFull)) {
+          // the operands have landed and the scales are in both CTAs' TMEM
+          // (the copy warps commit to `ready` only after seeing `full`)
+          if (!gp::pair_wait(ctx, sm.ready(stage), phase, kStatusMmaFull)) {
             ok = false;
             break;
           }
           tc_fence_after();
           const uint32_t sf_cols = tmem_base + kFTmemSf + static_cast<uint32_t>(stage) * kFSfCols;
-#pragma unroll
-          for (int k = 0; k < 4; ++k) {
-            // one K=64 step's scales: A in columns [4k, 4k+4), B in [16+4k, 16+4k+4)
-            tmem_cp_pair_32x128b_x4(sf_cols + 4 * k, rows16_desc(sm.sfa(stage) + 512 * k));
-            tmem_cp_pair_32x128b_x4(sf_cols + 16 + 4 * k, rows16_desc(sm.sfb(stage) + 512 * k));
-          }
           const uint64_t a_desc = sw128_kmajor_desc(sm.a(stage));
           const uint64_t b_desc = sw128_kmajor_desc(sm.b(stage));
 #pragma unroll
@@ -226,6 +242,75 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(gp::kThreads, 1)
         umma_commit_pair_multicast(sm.drain(), 0x1);
         drain_wait(sm.drain(), 0, p.status);
       }
+    }
+    __syncwarp();
+  } else if (warp == kSfWarp) {
+    // ---------------------- scale producer (both CTAs), on the stage ring
+    if (lane == 0) {
+      griddep_wait();
+      int stage = 0;
+      uint32_t phase = 0;
+      bool ok = true;
+      bool issued_any = false;
+      for (int t = cid; t < p.num_tiles && ok; t += ncl) {
+        int pr, n_blk;
+        tile_coords<gp::kGroupPairs, kFNTiles>(t, p.num_m_tiles, pr, n_blk);
+        const int a_rg = pr * 2 + static_cast<int>(rank);
+        for (int kb = 0; kb < kFKBlocks; ++kb) {
+          if (!gp::pair_wait(ctx, sm.empty(stage), phase ^ 1u, kStatusProducerEmpty)) {
+            ok = false;
+            break;
+          }
+          const uint32_t leader_sffull = mapa_shared(sm.sffull(stage), 0);
+          if (rank == 0) mbar_arrive_expect_tx(sm.sffull(stage), 4 * kFSfBytes);
+          tma_load_3d_pair(sm.sfa(stage), &tm_sfa, leader_sffull, 0, 4 * kb, a_rg);
+          tma_load_3d_pair(sm.sfb(stage), &tm_sfb, leader_sffull, 0, 4 * kb, n_blk);
+          issued_any = true;
+          if (++stage == kFStages) {
+            stage = 0;
+            phase ^= 1u;
+          }
+        }
+      }
+      if (!ok && issued_any) gp::grace_period();
+    }
+    __syncwarp();
+  } else if (warp >= 2 + kEpiWarps && warp < kSfWarp) {
+    // ---------------------------------------- scale copies (even CTA only)
+    // Copy warp k moves K step k's A-scale atom to columns [4k, 4k+4) and its
+    // B-scale atom to [16+4k, 16+4k+4) of the stage's slot, in both CTAs.
+    if (lane == 0 && rank == 0) {
+      const int k = warp - 2 - kEpiWarps;
+      int stage = 0;
+      uint32_t phase = 0;
+      bool ok = true;
+      for (int t = cid; t < p.num_tiles && ok; t += ncl) {
+        for (int kb = 0; kb < kFKBlocks; ++kb) {
+          if (!gp::pair_wait(ctx, sm.sffull(stage), phase, kStatusMmaFull)) {
+            ok = false;
+            break;
+          }
+          tc_fence_after();
+          const uint32_t sf_cols =
+              tmem_base + kFTmemSf + static_cast<uint32_t>(stage) * kFSfCols;
+          tmem_cp_pair_32x128b_x4(sf_cols + 4 * k, rows16_desc(sm.sfa(stage) + 512 * k));
+          tmem_cp_pair_32x128b_x4(sf_cols + 16 + 4 * k, rows16_desc(sm.sfb(stage) + 512 * k));
+          // the MMA thread waits on `ready` alone: report only once the
+          // operands of the stage have landed too
+          if (!gp::pair_wait(ctx, sm.full(stage), phase, kStatusMmaFull)) {
+            ok = false;
+            break;
+          }
+          umma_commit_pair_multicast(sm.ready(stage), 0x1);
+          if (++stage == kFStages) {
+            stage = 0;
+            phase ^= 1u;
+          }
+        }
+      }
+      // every copy this warp issued has landed before TMEM can be released
+      umma_commit_pair_multicast(sm.cpdrain(), 0x1);
+      drain_wait(sm.cpdrain(), 0, p.status);
     }
     __syncwarp();
   } else {
@@ -280,7 +365,7 @@ cudaError_t prepare_one(int* max_clusters) {
   if (e != cudaSuccess) return e;
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(2, 1, 1);
-  cfg.blockDim = dim3(gp::kThreads, 1, 1);
+  cfg.blockDim = dim3(kFThreads, 1, 1);
   cfg.dynamicSmemBytes = kFSmemAlloc;
   return cudaOccupancyMaxActiveClusters(max_clusters, nvfp4_qkv_kernel<kE4m3>, &cfg);
 }
@@ -289,7 +374,7 @@ template <bool kE4m3>
 cudaError_t launch_one(const Nvfp4Maps& m, const QkvParams& p, int clusters, cudaStream_t stream) {
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(static_cast<unsigned>(2 * clusters), 1, 1);
-  cfg.blockDim = dim3(gp::kThreads, 1, 1);
+  cfg.blockDim = dim3(kFThreads, 1, 1);
   cfg.dynamicSmemBytes = kFSmemAlloc;
   cfg.stream = stream;
   cudaLaunchAttribute attr[1];
