@@ -201,6 +201,15 @@ int mh3_preattn_qkv(mh3_preattn_t handle, void* stream, int64_t M, const mh3_bf1
                     const mh3_bf16* k_norm_weight, const mh3_bf16* rope_cos_sin, int64_t S,
                     const int64_t* rope_positions, int P, float qk_eps, mh3_bf16* out);
 
+/* Test hook for failure detection: when `stall` is nonzero, the next launch
+ * of the CTA-pair QKV GEMM through this handle (mh3_preattn_run or
+ * mh3_preattn_qkv with M > 128) issues no operand loads.  Its consumers'
+ * bounded waits then run out (about 2 s), the kernel records a nonzero code
+ * in the device status word, drains and returns: the launch completes and the
+ * context stays usable; `out` is not written.  The flag clears itself after
+ * that launch.  No fault, trap or endless wait is involved. */
+int mh3_preattn_set_test_stall(mh3_preattn_t handle, int stall);
+
 /* Synchronise `stream`, then read and clear the handle's device status word.
  * *device_code receives 0 when no kernel recorded a timeout since the last
  * read, else a nonzero code (which wait gave up).  Returns MH3_OK, or

@@ -36,7 +36,8 @@ EXPORTS = ("mh3_preattn_create", "mh3_preattn_destroy", "mh3_preattn_workspace_b
            "mh3_out_proj_validate", "mh3_mlp_run", "mh3_mlp_validate",
            "mh3_mlp_workspace_y_bytes", "mh3_preattn_run_e4m3", "mh3_preattn_out_e4m3_bytes",
            "mh3_e4m3_quantize", "mh3_nvfp4_codes_bytes", "mh3_nvfp4_scales_bytes",
-           "mh3_nvfp4_quantize", "mh3_nvfp4_norm_quant", "mh3_nvfp4_preattn_run", "mh3_nvfp4_qkv")
+           "mh3_nvfp4_quantize", "mh3_nvfp4_norm_quant", "mh3_nvfp4_preattn_run", "mh3_nvfp4_qkv",
+           "mh3_preattn_set_test_stall")
 
 _vp = ctypes.c_void_p
 _i64 = ctypes.c_int64
@@ -73,6 +74,7 @@ _SIGS = {
     "mh3_nvfp4_quantize": (_i32, [_vp, _i64, _i64, _vp, _vp, _vp, _vp, _i32]),
     "mh3_nvfp4_norm_quant": (_i32, [_vp, _vp, _i64, _vp, _vp, _vp, _i64, _vp, _i64, _i64, _vp,
                                     _f32, _vp, _vp, _vp, _i32]),
+    "mh3_preattn_set_test_stall": (_i32, [_vp, _i32]),
     "mh3_nvfp4_qkv": (_i32, [_vp, _vp, _i64, _vp, _vp, _vp, _vp, _f32, _vp, _f32, _vp, _vp, _vp,
                              _i32, _f32, _vp, _vp]),
     "mh3_nvfp4_preattn_run": (_i32, [_vp, _vp, _i64, _vp, _vp, _vp, _i64, _vp, _i64, _i64, _vp,
@@ -163,6 +165,12 @@ class Handle:
         _check(load().mh3_preattn_device_status(self._h, _stream_ptr(stream), ctypes.byref(code)),
                "mh3_preattn_device_status")
         return code.value
+
+    def set_test_stall(self, stall: bool = True) -> None:
+        """Test hook: the next CTA-pair QKV GEMM launch issues no loads, so its
+        bounded waits run out and it reports a status code."""
+        _check(load().mh3_preattn_set_test_stall(self._h, 1 if stall else 0),
+               "mh3_preattn_set_test_stall")
 
 
 _handles = {}

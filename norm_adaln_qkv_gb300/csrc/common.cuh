@@ -72,6 +72,7 @@ struct QkvParams {
   float alpha = 1.0f;
   const float* act_gs = nullptr;  // device [1]
   float w_gs = 0.0f;
+  int test_stall = 0;  // test hook: the producer issues no loads (bounded waits run out)
 };
 
 // num_sms: SM count of the device (the kernel is persistent over rows).
@@ -119,6 +120,7 @@ struct GatedResidualParams {
   int num_m_tiles;  // 256-row blocks
   int num_tiles;    // num_m_tiles * 21
   int* status;
+  int test_stall = 0;  // test hook: the producer issues no loads (bounded waits run out)
 };
 using OutProjParams = GatedResidualParams<int32_t>;
 
@@ -141,6 +143,7 @@ struct SwigluParams {
   int num_m_tiles;  // 256-row blocks
   int num_tiles;    // num_m_tiles * 112
   int* status;
+  int test_stall = 0;  // test hook: the producer issues no loads (bounded waits run out)
 };
 
 // fc1 + SwiGLU: y = bf16(bf16(silu(h_gate)) * h_up), h = bf16(a @ fc1^T).

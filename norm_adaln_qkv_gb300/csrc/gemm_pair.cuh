@@ -195,7 +195,9 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
       griddep_wait();
       int stage = 0;
       uint32_t phase = 0;
-      bool ok = true;
+      // test hook: issue nothing, so that the consumers' bounded waits run
+      // out and the kernel reports a status code instead of hanging
+      bool ok = p.test_stall == 0;
       bool issued_any = false;
       for (int t = cid; t < p.num_tiles && ok; t += ncl) {
         int pr, n_blk;

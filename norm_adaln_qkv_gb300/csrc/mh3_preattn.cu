@@ -42,6 +42,7 @@ struct mh3_preattn_ctx {
   size_t act_q_bytes = 0;
   void* act_sf = nullptr;
   size_t act_sf_bytes = 0;
+  int test_stall_next = 0;  // test hook for the next CTA-pair QKV GEMM launch
 };
 
 namespace {
@@ -259,7 +260,7 @@ int launch_stage1(cudaStream_t s, int num_sms, int* status, int64_t M, const mh3
 int launch_stage2(cudaStream_t s, int num_sms, int max_clusters, int* status, int64_t M,
                   const mh3_bf16* ws, const mh3_bf16* W, const mh3_bf16* qw, const mh3_bf16* kw,
                   const mh3_bf16* cs, int64_t S, const int64_t* pos, int P, float qk_eps,
-                  mh3_bf16* out) {
+                  mh3_bf16* out, int* test_stall = nullptr) {
   const bool pair = M > 128 && max_clusters > 0;
   QkvMaps maps;
   int rc = encode_maps(maps, M, ws, W, P, out, pair ? 128u : 256u);
@@ -280,6 +281,10 @@ int launch_stage2(cudaStream_t s, int num_sms, int max_clusters, int* status, in
     p.num_m_tiles = static_cast<int>((M + 255) / 256);
     p.num_tiles = p.num_m_tiles * (kQkvRows / 256);
     const int clusters = p.num_tiles < max_clusters ? p.num_tiles : max_clusters;
+    if (test_stall != nullptr) {
+      p.test_stall = *test_stall;
+      *test_stall = 0;
+    }
     e = launch_qkv_pair(maps, p, clusters, s);
   } else {
     p.num_m_tiles = static_cast<int>((M + 127) / 128);
@@ -437,7 +442,8 @@ int mh3_preattn_run(mh3_preattn_t h, void* stream, int64_t M, const mh3_bf16* x,
                      workspace);
   if (rc) return rc;
   return launch_stage2(s, h->num_sms, h->max_clusters, h->d_status, M, workspace, qkv_weight,
-                       q_norm_weight, k_norm_weight, rope_cos_sin, S, rope_positions, P, qk, out);
+                       q_norm_weight, k_norm_weight, rope_cos_sin, S, rope_positions, P, qk, out,
+                       &h->test_stall_next);
 }
 
 int mh3_preattn_norm_adaln(mh3_preattn_t h, void* stream, int64_t M, const mh3_bf16* x,
@@ -470,7 +476,14 @@ int mh3_preattn_qkv(mh3_preattn_t h, void* stream, int64_t M, const mh3_bf16* wo
   if ((rc = check_ptr(workspace, "workspace", 16))) return rc;
   return launch_stage2(static_cast<cudaStream_t>(stream), h->num_sms, h->max_clusters,
                        h->d_status, M, workspace, qkv_weight, q_norm_weight, k_norm_weight,
-                       rope_cos_sin, S, rope_positions, P, qk_eps, out);
+                       rope_cos_sin, S, rope_positions, P, qk_eps, out, &h->test_stall_next);
+}
+
+int mh3_preattn_set_test_stall(mh3_preattn_t h, int stall) {
+  int rc = check_handle(h);
+  if (rc) return rc;
+  h->test_stall_next = stall != 0 ? 1 : 0;
+  return MH3_OK;
 }
 
 int mh3_preattn_device_status(mh3_preattn_t h, void* stream, int* device_code) {
