@@ -86,12 +86,12 @@ struct QkvMaps {
 };
 
 // NVFP4 pre-attention, kernel 2: block-scaled FP4 CTA-pair GEMM with the
-// QKV epilogue (one head per 256 x 128 tile).
+// QKV epilogue (two heads per 256 x 256 tile).
 struct Nvfp4Maps {
   CUtensorMap a;    // act_q [M, 2688] bytes, box 128 B x 128 rows, 128-B swizzle
-  CUtensorMap b;    // weight codes [21504, 2688] bytes, box 128 B x 64 rows, 128-B swizzle
+  CUtensorMap b;    // weight codes [21504, 2688] bytes, box 128 B x 128 rows, 128-B swizzle
   CUtensorMap sfa;  // act scales, tiled atoms as u32 (128, 84, ceil(M/128)), box 128 x 4 x 1
-  CUtensorMap sfb;  // weight scales, tiled atoms as u32 (128, 84, 168), box 128 x 4 x 1
+  CUtensorMap sfb;  // weight scales, tiled atoms as u32 (128, 84, 168), box 128 x 4 x 2
   CUtensorMap out;  // as QkvMaps::out (bf16) or the e4m3 byte map
 };
 cudaError_t nvfp4_qkv_prepare_device(int* max_clusters, int* max_clusters_e4m3);

@@ -317,6 +317,94 @@ __device__ __forceinline__ void epilogue_head(uint32_t tcol, int lane, uint32_t 
   }
 }
 
+// The epilogue of one head whose bf16 projection y is already in registers
+// (y[i] holds columns 2i (low half) and 2i + 1): the same operations, in the
+// same order, as epilogue_head on an accumulator in TMEM.
+template <bool kE4m3>
+__device__ __forceinline__ void epilogue_head_regs(const uint32_t (&y)[64], int lane, uint32_t stg,
+                                                   const float* nw_all, const QkvParams& p,
+                                                   int64_t m0, int kind, int head,
+                                                   const uint4* cs_row,
+                                                   const CUtensorMap* tm_out) {
+  if (lane == 0) bulk_wait_group_read0();
+  __syncwarp();
+  auto yv = [&](int d) { return (d & 1) ? bf16_hi(y[d >> 1]) : bf16_lo(y[d >> 1]); };
+  if (kind == 2) {
+#pragma unroll
+    for (int c = 0; c < 16; ++c)
+      st_shared_v4(stg_addr(stg, lane, c), make_uint4(y[4 * c], y[4 * c + 1], y[4 * c + 2], y[4 * c + 3]));
+  } else {
+    const float* nw = nw_all + kind * kHeadDim;
+    // FP32 sum of squares in epi_qk_head's order: four partial sums over
+    // columns d % 4, d increasing
+    float s0 = 0.f, s1 = 0.f, s2 = 0.f, s3 = 0.f;
+#pragma unroll
+    for (int d = 0; d < kHeadDim; d += 4) {
+      const float y0 = yv(d), y1 = yv(d + 1), y2 = yv(d + 2), y3 = yv(d + 3);
+      s0 = __fmaf_rn(y0, y0, s0);
+      s1 = __fmaf_rn(y1, y1, s1);
+      s2 = __fmaf_rn(y2, y2, s2);
+      s3 = __fmaf_rn(y3, y3, s3);
+    }
+    const float ss = __fadd_rn(__fadd_rn(s0, s1), __fadd_rn(s2, s3));
+    const float rr = __fdiv_rn(1.0f, __fsqrt_rn(__fadd_rn(__fdiv_rn(ss, 128.0f), p.qk_eps)));
+    // rotated dims: chunk c (columns 8c..8c+7, c < 6) pairs with chunk c + 6
+#pragma unroll
+    for (int c = 0; c < 6; ++c) {
+      const uint4 cv = __ldg(cs_row + c);
+      const uint4 sv = __ldg(cs_row + 6 + c);
+      const uint32_t cw[4] = {cv.x, cv.y, cv.z, cv.w};
+      const uint32_t sw[4] = {sv.x, sv.y, sv.z, sv.w};
+      uint32_t o1[4], o2[4];
+#pragma unroll
+      for (int e2 = 0; e2 < 4; ++e2) {
+        float r1[2], r2[2];
+#pragma unroll
+        for (int e = 0; e < 2; ++e) {
+          const int j = 8 * c + 2 * e2 + e;
+          const float cs = e ? bf16_hi(cw[e2]) : bf16_lo(cw[e2]);
+          const float sn = e ? bf16_hi(sw[e2]) : bf16_lo(sw[e2]);
+          const float t1 = round_bf16(__fmul_rn(__fmul_rn(yv(j), rr), nw[j]));
+          const float t2 = round_bf16(__fmul_rn(__fmul_rn(yv(j + kRopeHalf), rr), nw[j + kRopeHalf]));
+          r1[e] = __fsub_rn(__fmul_rn(t1, cs), __fmul_rn(t2, sn));
+          r2[e] = __fadd_rn(__fmul_rn(t2, cs), __fmul_rn(t1, sn));
+        }
+        o1[e2] = pack_bf16x2(r1[0], r1[1]);
+        o2[e2] = pack_bf16x2(r2[0], r2[1]);
+      }
+      st_shared_v4(stg_addr(stg, lane, c), make_uint4(o1[0], o1[1], o1[2], o1[3]));
+      st_shared_v4(stg_addr(stg, lane, c + 6), make_uint4(o2[0], o2[1], o2[2], o2[3]));
+    }
+    // dims [96, 128) pass through the rotation
+#pragma unroll
+    for (int c = 12; c < 16; ++c) {
+      uint32_t o[4];
+#pragma unroll
+      for (int e = 0; e < 4; ++e) {
+        const int d = 8 * c + 2 * e;
+        o[e] = pack_bf16x2(__fmul_rn(__fmul_rn(yv(d), rr), nw[d]),
+                           __fmul_rn(__fmul_rn(yv(d + 1), rr), nw[d + 1]));
+      }
+      st_shared_v4(stg_addr(stg, lane, c), make_uint4(o[0], o[1], o[2], o[3]));
+    }
+  }
+  if (kE4m3) stage_to_e4m3(stg, lane, __ldg(p.descales + kind));
+  fence_proxy_async_smem();
+  __syncwarp();
+  if (lane == 0 && m0 < p.M) {
+    const int dst = head / p.heads_per_dst;
+    const int slot = (head % p.heads_per_dst) * 3 + kind;
+    const uint64_t pol = policy_evict_first();
+    if (kE4m3) {
+      tma_store_4d_hint(tm_out, stg, 0, slot, static_cast<int32_t>(m0), dst, pol);
+    } else {
+      tma_store_4d_hint(tm_out, stg, 0, slot, static_cast<int32_t>(m0), dst, pol);
+      tma_store_4d_hint(tm_out, stg + kStgHalfBytes, 64, slot, static_cast<int32_t>(m0), dst, pol);
+    }
+    bulk_commit_group();
+  }
+}
+
 // The epilogue of one 128-row x 256-column accumulator block.
 //   tmem_acc  TMEM address of the block (lane 0, first column)
 //   quad      TMEM lane quadrant this warp may read (warp index % 4)

@@ -1,7 +1,7 @@
 // k2_nvfp4_pair.cu -- kernel 2 of the NVFP4 pre-attention stage: the QKV
 // projection with block-scaled FP4 operands on the CTA-pair tcgen05 MMA,
-// with the Q/K RMSNorm, RoPE and destination-major pack epilogue of
-// k2_common.cuh applied to y = bf16(RN(alpha * acc))
+// with the Q/K RMSNorm, RoPE and destination-major pack epilogue applied to
+// y = bf16(RN(alpha * acc))
 // (flashinfer.diffusion_ops.minimax_h3_nvfp4_pre_attention, summary:
 // NVFP4 operands, accumulator rescaled by alpha; Parameters: qkv_weight_q,
 // qkv_weight_sf, qkv_weight_global_scale, act_global_scale, alpha).
@@ -11,27 +11,32 @@
 // elements = one k-block (21 k-blocks).  Scales: 512-byte atoms of 128 rows
 // x one 64-element step (row r at byte (r % 32) * 16 + (r / 32) * 4).
 //
-// A cluster of two CTAs owns a 256-row x 128-column tile (one head of one
-// kind).  Per k-block CTA r loads its 128 A rows (16 KB), its 64 of the 128
-// B rows (8 KB), and the 4 A-scale atoms of its rows (2 KB) and the 4
-// B-scale atoms of all 128 B rows (2 KB), into a 6-stage ring, counted on
-// two barriers of the even CTA (operands, scales).  The scales go from
-// shared memory to both CTAs' TMEM by
-// tcgen05.cp (pair form, 32x128b.warpx4: one copy = one K=64 step's 4
-// columns of A or B scales).  A copy stalls the thread that issues it for
-// over a hundred clocks, so four copy warps of the even CTA issue two copies
-// each per k-block; once they have also seen the stage's operands land they
-// commit to a per-stage "ready" barrier, the only one the MMA thread waits
-// on (every wait or commit in that thread costs MMA issue time) before it
-// issues four M=256 N=128 K=64 block-scaled MMAs.  With FP4 at four times the bf16 rate per clock a 256 x 128 tile
-// reads 96 B of shared memory per clock per SM, inside the 128 B/clk budget,
-// and two 128-column accumulators plus six 32-column scale slots fit the 512
-// TMEM columns, so the epilogue of one tile overlaps the next tile's MMAs.
+// A cluster of two CTAs owns a 256-row x 256-column tile (two heads of one
+// kind).  Per k-block CTA r loads its 128 A rows (16 KB), its 128 of the 256
+// B rows (16 KB), the 4 A-scale atoms of its rows (2 KB) and the 8 B-scale
+// atoms of all 256 B rows (4 KB) into a 5-stage ring, counted on two
+// barriers of the even CTA (scales, operands).  The scales go from shared
+// memory to both CTAs' TMEM by tcgen05.cp (pair form, 32x128b.warpx4: one
+// copy = one K=64 step's A scales, or half of its B scales).  A copy stalls
+// the thread that issues it for over a hundred clocks, so two copy warps of
+// the even CTA issue six copies each per k-block; once they have also seen
+// the stage's operands land they commit to a per-stage "ready" barrier, the
+// only one the MMA thread waits on (every wait or commit in that thread costs
+// MMA issue time) before it issues four M=256 N=256 K=64 block-scaled MMAs
+// (512 clocks of tensor work per k-block).
 //
-// Roles per CTA (352 threads): warp 0 operand TMA producer, warp 1 TMEM
-// allocation
+// TMEM: one 256-column accumulator plus five 48-column scale slots (496 of
+// 512 columns).  The epilogue drains its 32 lanes x 256 columns into
+// registers at once, as packed bf16(RN(alpha * acc)) (128 registers), and
+// releases the accumulator before it computes the two heads, so the next
+// tile's MMAs overlap the epilogue's arithmetic and stores.
+//
+// Roles per CTA (256 threads): warp 0 TMA producer, warp 1 TMEM allocation
 // and (even CTA) MMA issue, warps 2..5 the epilogue of the CTA's 128 rows,
-// warps 6..9 (even CTA) the scale copies, warp 10 the scale TMA producer.  Bounded waits, abort flags and
+// warps 6..7 (even CTA) the scale copies.  Eight warps keep at most two warps
+// on each SM sub-partition, whose register file (16K) then allows the 256
+// registers per thread the epilogue's live row of y needs without spilling
+// (ten warps would cap a thread at 168).  Bounded waits, abort flags and
 // draining as in gemm_pair.cuh.
 #include "gemm_pair.cuh"
 
@@ -42,60 +47,59 @@ namespace {
 using namespace k2;
 
 constexpr int FBM = 128;                       // A rows per CTA
-constexpr int kFTileN = 128;                   // one head
+constexpr int kFTileN = 256;                   // two heads
 constexpr int kFBRows = kFTileN / 2;           // B rows per CTA
 constexpr int kFBytesPerRow = 128;             // one k-block of one row
 constexpr int kFKBlocks = kHidden / 256;       // 21
-constexpr int kFNTiles = kQkvRows / kFTileN;   // 168
-constexpr int kFStages = 6;
+constexpr int kFNTiles = kQkvRows / kFTileN;   // 84
+constexpr int kFNTilesPerKind = kKindCols / kFTileN;  // 28
+constexpr int kFStages = 5;
 constexpr int kFABytes = FBM * kFBytesPerRow;       // 16 KB
-constexpr int kFBBytes = kFBRows * kFBytesPerRow;   // 8 KB
-constexpr int kFSfBytes = 4 * 512;                  // 4 atoms = 2 KB
-constexpr int kFStageBytes = kFABytes + kFBBytes + 2 * kFSfBytes;  // 28 KB
+constexpr int kFBBytes = kFBRows * kFBytesPerRow;   // 16 KB
+constexpr int kFSfaBytes = 4 * 512;                 // 4 atoms = 2 KB
+constexpr int kFSfbBytes = 8 * 512;                 // 8 atoms = 4 KB
 constexpr uint32_t kFIdesc = idesc_fp4_f32(2 * FBM, kFTileN);
-constexpr uint32_t kFTmemSf = 2 * kFTileN;     // scale slots start after the accumulators
-constexpr uint32_t kFSfCols = 32;              // per slot: A scales 16 + B scales 16
-constexpr int kFSfSlots = kFStages;            // scale slots (shared memory and TMEM), one per stage
+constexpr uint32_t kFTmemSf = kFTileN;         // scale slots start after the accumulator
+constexpr uint32_t kFSfCols = 48;              // per slot: A scales 16 + B scales 32
+constexpr int kCpWarps = 2;                    // scale-copy warps of the even CTA, two K steps each
+constexpr int kFThreads = 64 + kEpiWarps * 32 + kCpWarps * 32;  // 256
 
 constexpr int kFOffA = 0;
 constexpr int kFOffB = kFOffA + kFStages * kFABytes;
 constexpr int kFOffSfa = kFOffB + kFStages * kFBBytes;
-constexpr int kFOffSfb = kFOffSfa + kFSfSlots * kFSfBytes;
-constexpr int kFOffStg = kFOffSfb + kFSfSlots * kFSfBytes;
+constexpr int kFOffSfb = kFOffSfa + kFStages * kFSfaBytes;
+constexpr int kFOffStg = kFOffSfb + kFStages * kFSfbBytes;
 constexpr int kFOffBar = kFOffStg + kEpiWarps * kStgWarpBytes;
 // per stage: operands full, empty, scales full, ready (scales in TMEM and
-// operands landed); tmem full x2, tmem empty x2, drain, copy drain
-constexpr int kFNumBars = 4 * kFStages + 4 + 1 + 1;
+// operands landed); tmem full, tmem empty, drain, copy drain
+constexpr int kFNumBars = 4 * kFStages + 4;
 constexpr int kFOffTmemPtr = kFOffBar + kFNumBars * 8;
 constexpr int kFOffAbort = kFOffTmemPtr + 4;
-constexpr int kFOffScratch = kFOffBar + 512;
-constexpr int kCpWarps = 4;  // scale-copy warps of the even CTA, one K step each
-constexpr int kSfWarp = 2 + kEpiWarps + kCpWarps;                    // warp 10: scale loads
-constexpr int kFThreads = 64 + kEpiWarps * 32 + kCpWarps * 32 + 32;  // 352
+constexpr int kFOffScratch = kFOffBar + 256;
 constexpr int kFSmemUsed = kFOffScratch + 1024;
 constexpr int kFSmemAlloc = kFSmemUsed + 1024;
 static_assert(kFOffAbort + 4 <= kFOffScratch, "barrier block overflow");
-static_assert(kCpWarps == 4, "one copy warp per K=64 step of a k-block");
+static_assert(4 % kCpWarps == 0, "copy warps split a k-block's four K=64 steps evenly");
 static_assert(kFSmemAlloc <= 232448, "exceeds the 227 KB per-CTA limit");
-static_assert(kFTmemSf + kFSfSlots * kFSfCols <= kTmemCols, "TMEM budget");
-
+static_assert(kFTmemSf + kFStages * kFSfCols <= kTmemCols, "TMEM budget");
 static_assert(kHidden % 256 == 0 && kQkvRows % kFTileN == 0, "shapes must tile");
+static_assert(kKindCols % kFTileN == 0, "a tile must not straddle q/k/v");
 
 struct FSmem {
   uint32_t base;
   uint8_t* ptr;
   __device__ uint32_t a(int s) const { return base + kFOffA + s * kFABytes; }
   __device__ uint32_t b(int s) const { return base + kFOffB + s * kFBBytes; }
-  __device__ uint32_t sfa(int s) const { return base + kFOffSfa + s * kFSfBytes; }
-  __device__ uint32_t sfb(int s) const { return base + kFOffSfb + s * kFSfBytes; }
+  __device__ uint32_t sfa(int s) const { return base + kFOffSfa + s * kFSfaBytes; }
+  __device__ uint32_t sfb(int s) const { return base + kFOffSfb + s * kFSfbBytes; }
   __device__ uint32_t full(int s) const { return base + kFOffBar + s * 8; }
   __device__ uint32_t empty(int s) const { return base + kFOffBar + (kFStages + s) * 8; }
-  __device__ uint32_t tfull(int b) const { return base + kFOffBar + (2 * kFStages + b) * 8; }
-  __device__ uint32_t tempty(int b) const { return base + kFOffBar + (2 * kFStages + 2 + b) * 8; }
-  __device__ uint32_t drain() const { return base + kFOffBar + (2 * kFStages + 4) * 8; }
-  __device__ uint32_t cpdrain() const { return base + kFOffBar + (2 * kFStages + 5) * 8; }
-  __device__ uint32_t sffull(int s) const { return base + kFOffBar + (2 * kFStages + 6 + s) * 8; }
-  __device__ uint32_t ready(int s) const { return base + kFOffBar + (3 * kFStages + 6 + s) * 8; }
+  __device__ uint32_t sffull(int s) const { return base + kFOffBar + (2 * kFStages + s) * 8; }
+  __device__ uint32_t ready(int s) const { return base + kFOffBar + (3 * kFStages + s) * 8; }
+  __device__ uint32_t tfull() const { return base + kFOffBar + (4 * kFStages) * 8; }
+  __device__ uint32_t tempty() const { return base + kFOffBar + (4 * kFStages + 1) * 8; }
+  __device__ uint32_t drain() const { return base + kFOffBar + (4 * kFStages + 2) * 8; }
+  __device__ uint32_t cpdrain() const { return base + kFOffBar + (4 * kFStages + 3) * 8; }
   __device__ uint32_t stg(int ew) const { return base + kFOffStg + ew * kStgWarpBytes; }
   __device__ uint32_t tmem_ptr_addr() const { return base + kFOffTmemPtr; }
   __device__ uint32_t* tmem_ptr() const { return reinterpret_cast<uint32_t*>(ptr + kFOffTmemPtr); }
@@ -105,6 +109,21 @@ struct FSmem {
   }
   __device__ float* scratch() const { return reinterpret_cast<float*>(ptr + kFOffScratch); }
 };
+
+// This warp's 32 accumulator rows x 256 columns -> y = bf16(RN(alpha * acc)),
+// two columns per register (y[i] = columns 2i, 2i + 1).
+__device__ __forceinline__ void drain_accumulator(uint32_t tcol, float alpha, uint32_t (&y)[128]) {
+#pragma unroll
+  for (int c = 0; c < 8; ++c) {
+    uint32_t v[32];
+    tmem_ld_x32(tcol + 32 * c, v);
+    tmem_wait_ld();
+#pragma unroll
+    for (int i = 0; i < 16; ++i)
+      y[16 * c + i] = pack_bf16x2(__fmul_rn(__uint_as_float(v[2 * i]), alpha),
+                                  __fmul_rn(__uint_as_float(v[2 * i + 1]), alpha));
+  }
+}
 
 template <bool kE4m3>
 __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kFThreads, 1)
@@ -130,17 +149,13 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kFThreads, 1)
     for (int s = 0; s < kFStages; ++s) {
       mbar_init(sm.full(s), 1);
       mbar_init(sm.empty(s), 1);
-    }
-    for (int s = 0; s < kFStages; ++s) {
       mbar_init(sm.sffull(s), 1);
       mbar_init(sm.ready(s), kCpWarps);
     }
-    mbar_init(sm.cpdrain(), kCpWarps);
-    for (int b = 0; b < 2; ++b) {
-      mbar_init(sm.tfull(b), 1);
-      mbar_init(sm.tempty(b), 2 * kEpiWarps);
-    }
+    mbar_init(sm.tfull(), 1);
+    mbar_init(sm.tempty(), 2 * kEpiWarps);
     mbar_init(sm.drain(), 1);
+    mbar_init(sm.cpdrain(), kCpWarps);
     *sm.abort_flag() = 0;
     fence_mbar_init();
     prefetch_tmap(&tm_a);
@@ -165,12 +180,12 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kFThreads, 1)
   gp::PairCtx ctx{sm.abort_flag(), mapa_shared(sm.abort_addr(), rank ^ 1u), p.status};
 
   if (warp == 0) {
-    // ------------------------------------ operand producer (both CTAs)
+    // ------------------------------------------------- producer (both CTAs)
     if (lane == 0) {
       griddep_wait();  // act_q / act_sf come from the kernel before this one
       int stage = 0;
       uint32_t phase = 0;
-      bool ok = true;
+      bool ok = p.test_stall == 0;
       bool issued_any = false;
       for (int t = cid; t < p.num_tiles && ok; t += ncl) {
         int pr, n_blk;
@@ -182,8 +197,16 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kFThreads, 1)
             ok = false;
             break;
           }
+          // scales first, on their own barrier: the copy warps can move them
+          // into TMEM while the operands are still in flight
           const uint32_t leader_full = mapa_shared(sm.full(stage), 0);
-          if (rank == 0) mbar_arrive_expect_tx(sm.full(stage), 2 * (kFABytes + kFBBytes));
+          const uint32_t leader_sffull = mapa_shared(sm.sffull(stage), 0);
+          if (rank == 0) {
+            mbar_arrive_expect_tx(sm.sffull(stage), 2 * (kFSfaBytes + kFSfbBytes));
+            mbar_arrive_expect_tx(sm.full(stage), 2 * (kFABytes + kFBBytes));
+          }
+          tma_load_3d_pair(sm.sfa(stage), &tm_sfa, leader_sffull, 0, 4 * kb, a_rg);
+          tma_load_3d_pair(sm.sfb(stage), &tm_sfb, leader_sffull, 0, 4 * kb, 2 * n_blk);
           tma_load_2d_pair(sm.a(stage), &tm_a, leader_full, kb * kFBytesPerRow, a_rg * FBM);
           tma_load_2d_pair(sm.b(stage), &tm_b, leader_full, kb * kFBytesPerRow, b_row);
           issued_any = true;
@@ -197,21 +220,20 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kFThreads, 1)
     }
     __syncwarp();
   } else if (warp == 1) {
-    // --------------------------------- scale copies + MMA issue (even CTA)
+    // ------------------------------------------------ MMA issue (even CTA)
     if (lane == 0 && rank == 0) {
       int stage = 0;
       uint32_t phase = 0;
       bool ok = true;
       int it = 0;
       for (int t = cid; t < p.num_tiles && ok; t += ncl, ++it) {
-        const int buf = it & 1;
-        const uint32_t use = static_cast<uint32_t>(it >> 1);
-        if (!gp::pair_wait(ctx, sm.tempty(buf), (use & 1u) ^ 1u, kStatusMmaTmemEmpty)) {
+        // the epilogue has drained the accumulator of the previous tile
+        if (!gp::pair_wait(ctx, sm.tempty(), (static_cast<uint32_t>(it) & 1u) ^ 1u,
+                           kStatusMmaTmemEmpty)) {
           ok = false;
           break;
         }
         tc_fence_after();
-        const uint32_t d_tmem = tmem_base + static_cast<uint32_t>(buf * kFTileN);
         for (int kb = 0; kb < kFKBlocks; ++kb) {
           // the operands have landed and the scales are in both CTAs' TMEM
           // (the copy warps commit to `ready` only after seeing `full`)
@@ -225,9 +247,10 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kFThreads, 1)
           const uint64_t b_desc = sw128_kmajor_desc(sm.b(stage));
 #pragma unroll
           for (int k = 0; k < 4; ++k) {
-            // 64 elements = 32 B along K inside the swizzle atom
-            umma_fp4_pair(d_tmem, a_desc + 2 * k, b_desc + 2 * k, kFIdesc, sf_cols + 4 * k,
-                          sf_cols + 16 + 4 * k, (kb | k) != 0 ? 1u : 0u);
+            // 64 elements = 32 B along K inside the swizzle atom; A scales of
+            // step k in columns [4k, 4k+4), B scales in [16+8k, 16+8k+8)
+            umma_fp4_pair(tmem_base, a_desc + 2 * k, b_desc + 2 * k, kFIdesc, sf_cols + 4 * k,
+                          sf_cols + 16 + 8 * k, (kb | k) != 0 ? 1u : 0u);
           }
           umma_commit_pair_multicast(sm.empty(stage), gp::kBothCtas);
           if (++stage == kFStages) {
@@ -236,7 +259,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kFThreads, 1)
           }
         }
         if (!ok) break;
-        umma_commit_pair_multicast(sm.tfull(buf), gp::kBothCtas);
+        umma_commit_pair_multicast(sm.tfull(), gp::kBothCtas);
       }
       if (!ok) {
         umma_commit_pair_multicast(sm.drain(), 0x1);
@@ -244,43 +267,13 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kFThreads, 1)
       }
     }
     __syncwarp();
-  } else if (warp == kSfWarp) {
-    // ---------------------- scale producer (both CTAs), on the stage ring
-    if (lane == 0) {
-      griddep_wait();
-      int stage = 0;
-      uint32_t phase = 0;
-      bool ok = true;
-      bool issued_any = false;
-      for (int t = cid; t < p.num_tiles && ok; t += ncl) {
-        int pr, n_blk;
-        tile_coords<gp::kGroupPairs, kFNTiles>(t, p.num_m_tiles, pr, n_blk);
-        const int a_rg = pr * 2 + static_cast<int>(rank);
-        for (int kb = 0; kb < kFKBlocks; ++kb) {
-          if (!gp::pair_wait(ctx, sm.empty(stage), phase ^ 1u, kStatusProducerEmpty)) {
-            ok = false;
-            break;
-          }
-          const uint32_t leader_sffull = mapa_shared(sm.sffull(stage), 0);
-          if (rank == 0) mbar_arrive_expect_tx(sm.sffull(stage), 4 * kFSfBytes);
-          tma_load_3d_pair(sm.sfa(stage), &tm_sfa, leader_sffull, 0, 4 * kb, a_rg);
-          tma_load_3d_pair(sm.sfb(stage), &tm_sfb, leader_sffull, 0, 4 * kb, n_blk);
-          issued_any = true;
-          if (++stage == kFStages) {
-            stage = 0;
-            phase ^= 1u;
-          }
-        }
-      }
-      if (!ok && issued_any) gp::grace_period();
-    }
-    __syncwarp();
-  } else if (warp >= 2 + kEpiWarps && warp < kSfWarp) {
+  } else if (warp >= 2 + kEpiWarps) {
     // ---------------------------------------- scale copies (even CTA only)
-    // Copy warp k moves K step k's A-scale atom to columns [4k, 4k+4) and its
-    // B-scale atom to [16+4k, 16+4k+4) of the stage's slot, in both CTAs.
+    // For each of its K steps k, a copy warp moves the A-scale atom to
+    // columns [4k, 4k+4) and the two B-scale atoms (rows 0-127, 128-255) to
+    // [16+8k, 16+8k+8) of the stage's slot, in both CTAs.
     if (lane == 0 && rank == 0) {
-      const int k = warp - 2 - kEpiWarps;
+      const int k0 = warp - 2 - kEpiWarps;
       int stage = 0;
       uint32_t phase = 0;
       bool ok = true;
@@ -293,8 +286,14 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kFThreads, 1)
           tc_fence_after();
           const uint32_t sf_cols =
               tmem_base + kFTmemSf + static_cast<uint32_t>(stage) * kFSfCols;
-          tmem_cp_pair_32x128b_x4(sf_cols + 4 * k, rows16_desc(sm.sfa(stage) + 512 * k));
-          tmem_cp_pair_32x128b_x4(sf_cols + 16 + 4 * k, rows16_desc(sm.sfb(stage) + 512 * k));
+          // B-scale atoms arrive as [row group][step][512 B]
+#pragma unroll
+          for (int k = k0; k < 4; k += kCpWarps) {
+            tmem_cp_pair_32x128b_x4(sf_cols + 4 * k, rows16_desc(sm.sfa(stage) + 512 * k));
+            tmem_cp_pair_32x128b_x4(sf_cols + 16 + 8 * k, rows16_desc(sm.sfb(stage) + 512 * k));
+            tmem_cp_pair_32x128b_x4(sf_cols + 16 + 8 * k + 4,
+                                    rows16_desc(sm.sfb(stage) + 2048 + 512 * k));
+          }
           // the MMA thread waits on `ready` alone: report only once the
           // operands of the stage have landed too
           if (!gp::pair_wait(ctx, sm.full(stage), phase, kStatusMmaFull)) {
@@ -323,27 +322,31 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kFThreads, 1)
                             : __frcp_rn(__fmul_rn(__ldg(p.act_gs), p.w_gs));
     int it = 0;
     for (int t = cid; t < p.num_tiles; t += ncl, ++it) {
-      const int buf = it & 1;
-      const uint32_t use = static_cast<uint32_t>(it >> 1);
-      bool ok = gp::pair_wait(ctx, sm.tfull(buf), use & 1u, kStatusEpiTmemFull);
+      bool ok = gp::pair_wait(ctx, sm.tfull(), static_cast<uint32_t>(it) & 1u, kStatusEpiTmemFull);
       ok = __all_sync(0xFFFFFFFFu, ok);
       if (!ok) break;
       tc_fence_after();
+      uint32_t y[128];
+      drain_accumulator(tmem_base + (static_cast<uint32_t>(quad * 32) << 16), alpha, y);
+      // every TMEM read of the accumulator is complete: the next tile may start
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive_cluster(mapa_shared(sm.tempty(), 0));
       int pr, n_blk;
       tile_coords<gp::kGroupPairs, kFNTiles>(t, p.num_m_tiles, pr, n_blk);
-      const int kind = n_blk / kHeads;
-      const int head = n_blk % kHeads;
+      const int kind = n_blk / kFNTilesPerKind;
+      const int head0 = (n_blk % kFNTilesPerKind) * 2;
       const int64_t m0 = static_cast<int64_t>(pr) * (2 * FBM) + static_cast<int64_t>(rank) * FBM +
                          quad * 32;
       const uint4* cs_row = rope_row(p, m0 + lane, kind);
-      const uint32_t tcol = tmem_base + static_cast<uint32_t>(buf * kFTileN) +
-                            (static_cast<uint32_t>(quad * 32) << 16);
-      epilogue_head<kE4m3, true>(tcol, lane, stg, sm.scratch(), p, m0, kind, head, cs_row, alpha,
-                                 &tm_out);
-      // all TMEM reads of this accumulator are complete (tcgen05.wait::ld)
-      tc_fence_before();
-      __syncwarp();
-      if (lane == 0) mbar_arrive_cluster(mapa_shared(sm.tempty(buf), 0));
+#pragma unroll
+      for (int j = 0; j < 2; ++j) {
+        uint32_t yh[64];
+#pragma unroll
+        for (int i = 0; i < 64; ++i) yh[i] = y[64 * j + i];
+        epilogue_head_regs<kE4m3>(yh, lane, stg, sm.scratch(), p, m0, kind, head0 + j, cs_row,
+                                  &tm_out);
+      }
     }
     if (lane == 0) bulk_wait_group0();
     __syncwarp();

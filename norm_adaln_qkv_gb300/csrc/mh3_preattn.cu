@@ -673,7 +673,7 @@ int launch_fp4_gemm(mh3_preattn_ctx* h, cudaStream_t s, int64_t M, const uint8_t
   {
     const cuuint64_t dims[2] = {kHidden / 2, kQkvRows};
     const cuuint64_t strides[1] = {kHidden / 2};
-    const cuuint32_t box[2] = {128, 64};
+    const cuuint32_t box[2] = {128, 128};  // 128 of a tile's 256 B rows per CTA
     if ((rc = encode_tiled(&maps.b, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, weight_q, dims, strides, box,
                            CU_TENSOR_MAP_SWIZZLE_128B, "qkv_weight_q")))
       return rc;
@@ -684,12 +684,13 @@ int launch_fp4_gemm(mh3_preattn_ctx* h, cudaStream_t s, int64_t M, const uint8_t
     const cuuint64_t dims_a[3] = {128, kFp4KSteps, groups_a};
     const cuuint64_t dims_b[3] = {128, kFp4KSteps, kQkvRows / 128};
     const cuuint64_t strides[2] = {512, 512 * kFp4KSteps};
-    const cuuint32_t box[3] = {128, 4, 1};
+    const cuuint32_t box_a[3] = {128, 4, 1};  // one k-block: 4 steps of one row group
+    const cuuint32_t box_b[3] = {128, 4, 2};  // ... of the tile's two row groups
     if ((rc = encode_tiled(&maps.sfa, CU_TENSOR_MAP_DATA_TYPE_UINT32, 3, act_sf, dims_a, strides,
-                           box, CU_TENSOR_MAP_SWIZZLE_NONE, "act_sf")))
+                           box_a, CU_TENSOR_MAP_SWIZZLE_NONE, "act_sf")))
       return rc;
     if ((rc = encode_tiled(&maps.sfb, CU_TENSOR_MAP_DATA_TYPE_UINT32, 3, weight_sf, dims_b,
-                           strides, box, CU_TENSOR_MAP_SWIZZLE_NONE, "qkv_weight_sf")))
+                           strides, box_b, CU_TENSOR_MAP_SWIZZLE_NONE, "qkv_weight_sf")))
       return rc;
   }
   if ((rc = encode_out_map(&maps.out, out, M, P, e4m3))) return rc;
@@ -705,7 +706,7 @@ int launch_fp4_gemm(mh3_preattn_ctx* h, cudaStream_t s, int64_t M, const uint8_t
   p.status = h->d_status;
   p.descales = qkv_descale;
   p.num_m_tiles = static_cast<int>((M + 255) / 256);
-  p.num_tiles = p.num_m_tiles * (kQkvRows / 128);
+  p.num_tiles = p.num_m_tiles * (kQkvRows / 256);  // 256 x 256 pair tiles
   p.alpha = alpha_given ? alpha : -1.0f;
   p.act_gs = act_global_scale;
   p.w_gs = weight_global_scale;
