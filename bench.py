@@ -393,6 +393,21 @@ def run_ours(args, world, rank, local):
     torch.cuda.synchronize()
     barrier()
     e2e_ms = max_over_ranks(s0.elapsed_time(s1), dev) / n_e2e
+    # the host link itself: one pinned copy each way of the step's bytes
+    # (the e2e step moves h2d + d2h bytes; its floor is the slower direction)
+    lk = torch.empty(d2h // 2, dtype=torch.bfloat16, device=dev)
+    lh = torch.empty(d2h // 2, dtype=torch.bfloat16).pin_memory()
+    torch.cuda.synchronize()
+    l0, l1, l2 = (torch.cuda.Event(enable_timing=True) for _ in range(3))
+    l0.record(stream)
+    lh.copy_(lk, non_blocking=True)
+    l1.record(stream)
+    lk.copy_(lh, non_blocking=True)
+    l2.record(stream)
+    torch.cuda.synchronize()
+    d2h_gbs = d2h / (l0.elapsed_time(l1) * 1e-3) / 1e9
+    h2d_gbs = d2h / (l1.elapsed_time(l2) * 1e-3) / 1e9
+    del lk, lh
     # the result of the last step really came back
     assert torch.equal(houts[(n_e2e - 1) % 2].view(torch.int16)[0, :4],
                        sets[(n_e2e - 1) % 2]["out"].view(torch.int16)[0, :4].cpu())
@@ -614,6 +629,8 @@ def run_ours(args, world, rank, local):
         "cpu_baseline": cpu,
         "e2e": {"value": e2e_ms * 1e3 / world, "unit": UNIT, "h2d_bytes_per_step": h2d,
                 "d2h_bytes_per_step": d2h,
+                "link_gbs": {"d2h": d2h_gbs, "h2d": h2d_gbs},
+                "link_floor_us": max(d2h / d2h_gbs, h2d / h2d_gbs) * 1e-3,
                 "how": "pinned host inputs in and out back every step; copies of neighbouring "
                        "steps overlap the kernels (2 buffer sets; input, compute and "
                        f"{n_out} read-back streams)"},
