@@ -88,10 +88,10 @@ __device__ __forceinline__ uint32_t adaln_pair(uint64_t x2, uint32_t w, uint32_t
 // 16 is this thread's chunk and its neighbour's (lanes 2b, 2b+1), the scale
 // word of one 64-element step is gathered from 8 aligned lanes.
 __device__ __forceinline__ void fp4_chunk(const uint4& o, int lane, int c, int64_t m, float gs,
-                                          const NormAdalnParams& p) {
+                                          const float* enc_lut, const NormAdalnParams& p) {
   float amax = fp4::amax8(o);
   amax = fmaxf(amax, __shfl_xor_sync(0xFFFFFFFFu, amax, 1));
-  const fp4::BlockScale bs = fp4::block_scale(amax, gs);
+  const fp4::BlockScale bs = fp4::block_scale(amax, gs, enc_lut);
   *reinterpret_cast<uint32_t*>(p.act_q + m * (kHidden / 2) + 4 * c) = fp4::encode8(o, bs.enc);
   uint32_t word = (lane & 1) ? 0u : bs.code << (8 * ((lane & 7) >> 1));
   word |= __shfl_xor_sync(0xFFFFFFFFu, word, 1);
@@ -108,6 +108,7 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm) norm_adaln_kernel(const 
   __shared__ __align__(8) uint64_t full[kStages];
   __shared__ float warp_ss[kWarps];
   __shared__ int go;
+  __shared__ float enc_lut[kFp4 ? fp4::kEncLut : 1];
 
   const int tid = threadIdx.x;
   const int lane = tid & 31;
@@ -121,6 +122,7 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm) norm_adaln_kernel(const 
   // waits for this grid's completion before it reads the workspace
   griddep_launch_dependents();
   const float gs = kFp4 ? __ldg(p.act_gs) : 0.0f;
+  if (kFp4) fp4::init_enc_lut(enc_lut, gs, tid, kThreads);  // visible after the first barrier
 
   uint64_t policy = 0;
   if (tid == 0) {
@@ -187,7 +189,7 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm) norm_adaln_kernel(const 
 #pragma unroll
       for (int j = 0; j < kVecPerThread; ++j) {
         if (kFp4)
-          fp4_chunk(z, lane, tid + kThreads * j, m, 0.0f, p);  // codes 0, scale 0
+          fp4_chunk(z, lane, tid + kThreads * j, m, 0.0f, enc_lut, p);  // codes 0, scale 0
         else
           wr[tid + kThreads * j] = z;
       }
@@ -211,7 +213,7 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm) norm_adaln_kernel(const 
       o.z = adaln_pair(f2_from_bf16x2(v[j].z), w.z, sc.z, sh.z, r2);
       o.w = adaln_pair(f2_from_bf16x2(v[j].w), w.w, sc.w, sh.w, r2);
       if (kFp4)
-        fp4_chunk(o, lane, c, m, gs, p);
+        fp4_chunk(o, lane, c, m, gs, enc_lut, p);
       else
         wr[c] = o;
     }

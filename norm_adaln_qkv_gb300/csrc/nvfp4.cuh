@@ -5,7 +5,7 @@
 // fp4_quantize(a, act_global_scale, sf_vec_size=16)):
 //
 //   s    = ue4m3(RN(RN(amax / 6) * gs))       amax = max |v| over the block
-//   enc  = s == 0 ? 0 : RN(gs / s)
+//   enc  = s == 0 ? 0 : RN(gs / s)            (a 128-entry table per block)
 //   code = e2m1(RN(v * enc))                  nearest even, saturating at 6
 //
 // Codes are packed two per byte, element 2j in the low nibble.  Scales are
@@ -31,17 +31,38 @@ __device__ __forceinline__ float ue4m3_value(uint32_t code) {
   return e == 0 ? __uint2float_rn(m) * 0x1p-9f : __uint_as_float(((e + 120u) << 23) | (m << 20));
 }
 
+// RN(v / 6) for v >= 0: Markstein's quotient with the constant r = RN(1/6)
+// (one multiply, two FMAs), exact whenever no step leaves the normal range,
+// i.e. for v in [2^-100, 2^127) (checked for every bf16 value there); outside
+// that range (tiny, huge, infinite or NaN) a true division.
+__device__ __forceinline__ float div6_rn(float v) {
+  if (!(v >= 0x1p-100f && v < 0x1p127f)) return __fdiv_rn(v, 6.0f);
+  const float r = 0x1.555556p-3f;  // RN(1/6)
+  const float q = __fmul_rn(v, r);
+  return __fmaf_rn(__fmaf_rn(-q, 6.0f, v), r, q);
+}
+
+// enc[c] = RN(gs / s_c) for every UE4M3 code c (0 for c = 0): the per-block
+// division of the encode multiplier, done once per code.  Fill with all
+// threads of the block, then synchronise.
+constexpr int kEncLut = 128;
+__device__ __forceinline__ void init_enc_lut(float* lut, float gs, int tid, int nthreads) {
+  for (int c = tid; c < kEncLut; c += nthreads) {
+    const float s = c < 127 ? ue4m3_value(static_cast<uint32_t>(c)) : 0.0f;
+    lut[c] = s == 0.0f ? 0.0f : __fdiv_rn(gs, s);
+  }
+}
+
 struct BlockScale {
   uint32_t code;  // UE4M3 scale code
   float enc;      // multiplier that maps the block onto the E2M1 range
 };
 
-__device__ __forceinline__ BlockScale block_scale(float amax, float gs) {
-  const float t = __fmul_rn(__fdiv_rn(amax, 6.0f), gs);
+__device__ __forceinline__ BlockScale block_scale(float amax, float gs, const float* enc_lut) {
+  const float t = __fmul_rn(div6_rn(amax), gs);
   BlockScale b;
   b.code = e4m3x2_satfinite(t, 0.0f) & 0xFFu;  // t >= 0: nearest even, <= 448
-  const float s = ue4m3_value(b.code);
-  b.enc = s == 0.0f ? 0.0f : __fdiv_rn(gs, s);
+  b.enc = enc_lut[b.code];
   return b;
 }
 
@@ -59,25 +80,29 @@ __device__ __forceinline__ uint32_t e2m1x8(const float (&v)[8]) {
   return r;
 }
 
-// Eight bf16 values (uint4) and the block's encode multiplier -> 8 codes.
+// Eight bf16 values (uint4) and the block's encode multiplier -> 8 codes;
+// the products are packed two-lane FP32 multiplies (each lane one IEEE
+// round-to-nearest multiply).
 __device__ __forceinline__ uint32_t encode8(const uint4& w, float enc) {
-  float v[8];
+  const uint64_t e2 = f2_pack(enc, enc);
   const uint32_t ws[4] = {w.x, w.y, w.z, w.w};
+  float v[8];
 #pragma unroll
-  for (int i = 0; i < 4; ++i) {
-    v[2 * i] = __fmul_rn(bf16_lo(ws[i]), enc);
-    v[2 * i + 1] = __fmul_rn(bf16_hi(ws[i]), enc);
-  }
+  for (int i = 0; i < 4; ++i) f2_unpack(f2_mul(f2_from_bf16x2(ws[i]), e2), v[2 * i], v[2 * i + 1]);
   return e2m1x8(v);
 }
 
-// max |v| of eight bf16 values (exact).
+__device__ __forceinline__ uint32_t bf16x2_max(uint32_t a, uint32_t b) {
+  uint32_t r;
+  asm("max.bf16x2 %0, %1, %2;" : "=r"(r) : "r"(a), "r"(b));
+  return r;
+}
+
+// max |v| of eight bf16 values (exact): sign bits cleared, packed bf16 max.
 __device__ __forceinline__ float amax8(const uint4& w) {
-  const uint32_t ws[4] = {w.x, w.y, w.z, w.w};
-  float m = 0.0f;
-#pragma unroll
-  for (int i = 0; i < 4; ++i) m = fmaxf(m, fmaxf(fabsf(bf16_lo(ws[i])), fabsf(bf16_hi(ws[i]))));
-  return m;
+  const uint32_t m = bf16x2_max(bf16x2_max(w.x & 0x7FFF7FFFu, w.y & 0x7FFF7FFFu),
+                                bf16x2_max(w.z & 0x7FFF7FFFu, w.w & 0x7FFF7FFFu));
+  return fmaxf(bf16_lo(m), bf16_hi(m));
 }
 
 // Byte offset of the 4 scales of (row, 64-element K step `kstep`).

@@ -18,6 +18,9 @@ __global__ void __launch_bounds__(256) nvfp4_quantize_kernel(const __nv_bfloat16
                                                              uint8_t* __restrict__ scales,
                                                              int tiled) {
   const float gs = __ldg(gs_ptr);
+  __shared__ float enc_lut[fp4::kEncLut];
+  fp4::init_enc_lut(enc_lut, gs, threadIdx.x, blockDim.x);
+  __syncthreads();
   const int ksteps = cols / 64;
   const int64_t total = rows * ksteps;
   const int64_t stride = static_cast<int64_t>(gridDim.x) * blockDim.x;
@@ -34,7 +37,7 @@ __global__ void __launch_bounds__(256) nvfp4_quantize_kernel(const __nv_bfloat16
 #pragma unroll
     for (int b = 0; b < 4; ++b) {
       const float amax = fmaxf(fp4::amax8(v[2 * b]), fp4::amax8(v[2 * b + 1]));
-      const fp4::BlockScale bs = fp4::block_scale(amax, gs);
+      const fp4::BlockScale bs = fp4::block_scale(amax, gs, enc_lut);
       q[2 * b] = fp4::encode8(v[2 * b], bs.enc);
       q[2 * b + 1] = fp4::encode8(v[2 * b + 1], bs.enc);
       word |= bs.code << (8 * b);

@@ -85,3 +85,17 @@ def test_markstein_quotient_equals_ieee_division():
         ref = (V / D).astype(np.float32)
         bad = np.nonzero(got != ref)[0]
         assert bad.size == 0, (V[bad[0]], D[bad[0]], got[bad[0]], ref[bad[0]])
+
+
+def test_markstein_division_by_six_for_every_bf16_value():
+    """The NVFP4 block scale's RN(amax / 6) on the GPU: the Markstein quotient
+    with the constant r = RN(1/6), used for amax in [2^-100, 2^127) (outside,
+    a true division).  Every positive bf16 value in that range."""
+    bits = np.arange(0x0001, 0x7F80, dtype=np.uint32)          # positive finite bf16
+    v = (bits << 16).view(np.float32)
+    v = v[(v >= np.float32(2.0 ** -100)) & (v < np.float32(2.0 ** 127))]
+    d = np.full(v.shape, 6.0, dtype=np.float32)
+    got = markstein(v, d)
+    ref = (v / d).astype(np.float32)
+    bad = np.nonzero(got != ref)[0]
+    assert bad.size == 0, (v[bad[0]], got[bad[0]], ref[bad[0]])
