@@ -35,6 +35,7 @@ METRIC = ("pre-attn µs/call & GEMM TFLOP/s at M=4096/32760; "
 UNIT = "us/call"
 WORKLOAD = "c3"
 ALSO = "c2"
+SMALL_CALLS = 50
 FLOP_PER_TOKEN = 2 * 5376 * 21504
 # kernel 2 at the bench size is the CTA-pair form; its traffic figure is tied
 # to these sources
@@ -223,6 +224,18 @@ def cpu_baseline(wl, rows: int, chunk: int = 4096):
             f"first {rows} tokens of M={wl.M}, scaled by M/{rows}")
     return {"value": el * (wl.M / rows) * 1e6, "unit": UNIT, "cores": torch.get_num_threads(),
             "kind": "oracle", "sample": f"{what}, {el:.1f} s of CPU time"}
+
+
+def stage_roofline_us(wl, peaks) -> float:
+    """max(FLOP / bf16 peak, compulsory bytes / HBM peak) for one stage call:
+    x, W, out, indices, explicit positions, the cache rows used, both tables'
+    rows and the norm weights."""
+    M = wl.M
+    flop_time = FLOP_PER_TOKEN * M / (peaks["bf16"] * 1e12)
+    comp_bytes = (M * 10752 + 21504 * 5376 * 2 + M * 43008 + 8 * M +
+                  (8 * M if wl.rope_positions is not None else 0) + min(wl.spec.S, M) * 192 +
+                  wl.spec.rows * 2 * 5376 * 2 + 5376 * 2 + 2 * 128 * 2)
+    return max(flop_time, comp_bytes / (peaks["hbm"] * 1e9)) * 1e6
 
 
 def run_ours(args, world, rank, local):
@@ -597,6 +610,36 @@ def run_ours(args, world, rank, local):
                     "us": mlp_ms * 1e3, "tflops": mlp_tf,
                     "frac_of_measured_bf16": mlp_tf / peaks["bf16"], "launches_per_call": 3}
         del xm, f1, f2, wam, wym, outm, rm
+    # ---- the small configurations (M = 16, 1024): per-call medians of the
+    # whole stage, back to back (warm) and after writing 320 MB (> 2x L2)
+    small = None
+    if not args.skip_also:
+        flush = torch.empty(80 * 2**20, dtype=torch.float32, device=dev)
+        small = {}
+        for key in ("c0", "c1"):
+            ws_ = make_workload(key)
+            ds_ = prepare(ws_)
+            for _ in range(3):
+                stage(ws_, ds_)
+            per = {}
+            for mode in ("warm", "cold"):
+                evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+                       for _ in range(SMALL_CALLS)]
+                for i, (s0, s1) in enumerate(evs):
+                    if mode == "cold":
+                        flush.fill_(float(i))
+                    s0.record(stream)
+                    stage(ws_, ds_)
+                    s1.record(stream)
+                torch.cuda.synchronize()
+                per[mode] = statistics.median(s0.elapsed_time(s1) for s0, s1 in evs) * 1e3
+            roof = stage_roofline_us(ws_, peaks)
+            small[key] = {"workload": ws_.spec.name, "stage_us_warm": per["warm"],
+                          "stage_us_cold": per["cold"], "stage_roofline_us": roof,
+                          "roofline_frac_cold": roof / per["cold"],
+                          "timed": f"median of {SMALL_CALLS} calls, CUDA events around each"}
+            del ds_
+        del flush
     clk = clocks.stop()
     assert h.device_status(stream) == 0, "a kernel recorded a timeout"
 
@@ -610,12 +653,7 @@ def run_ours(args, world, rank, local):
     k1_gbs = k1_bytes / (k1_first_ms * 1e-3) / 1e9
     k1_gbs_after = k1_bytes / (k1_alone_ms * 1e-3) / 1e9
     k1_gbs_stage = k1_bytes / (k1_ms * 1e-3) / 1e9
-    flop_time = FLOP_PER_TOKEN * M / (peaks["bf16"] * 1e12)
-    comp_bytes = (M * 10752 + 21504 * 5376 * 2 + M * 43008 + 8 * M +
-                  (8 * M if wl.rope_positions is not None else 0) + min(wl.spec.S, M) * 192 +
-                  wl.spec.rows * 2 * 5376 * 2)
-    bytes_time = comp_bytes / (peaks["hbm"] * 1e9)
-    stage_roof_us = max(flop_time, bytes_time) * 1e6
+    stage_roof_us = stage_roofline_us(wl, peaks)
     line = {
         "metric": METRIC, "value": value_us, "unit": UNIT, "n_gpus": world,
         "steps": args.steps, "warmup": max(args.warmup, 3), "ms_per_step": ms_step,
@@ -660,6 +698,7 @@ def run_ours(args, world, rank, local):
         "nvfp4": nvfp4_line,
         "out_proj": out_proj,
         "mlp": mlp_line,
+        "small": small,
     }
     print(json.dumps(line), flush=True)
 

@@ -108,13 +108,21 @@ __device__ __forceinline__ bool pair_wait(const PairCtx& c, uint32_t bar, uint32
   st_shared_cluster_u32(c.peer_abort, 1u);
   return false;
 }
+// The same without a subroutine call (for kernels with a register split).
+__device__ __forceinline__ bool pair_wait_inl(const PairCtx& c, uint32_t bar, uint32_t parity,
+                                              int code) {
+  if (wait_phase_inl<true>(bar, parity, c.abort_flag, c.status, code)) return true;
+  st_shared_cluster_u32(c.peer_abort, 1u);
+  return false;
+}
 
 // Fixed grace period for asynchronous work this thread cannot observe.
-__device__ __noinline__ inline void grace_period() {
+__device__ __forceinline__ void grace_period_inl() {
   const uint64_t t0 = globaltimer_ns();
   while (globaltimer_ns() - t0 < kGraceNs) {
   }
 }
+__device__ __noinline__ inline void grace_period() { grace_period_inl(); }
 
 // The usual B split: the tile's 256 B rows, 128 per CTA of the pair.
 __device__ __forceinline__ int contiguous_b_row(int n_blk, int rank) {

@@ -67,9 +67,11 @@ inline cudaError_t launch_k2(Kernel kernel, int grid, int threads, int smem, cud
 }
 
 // Bounded wait on one mbarrier phase; false when this CTA is aborting.
+// (Inline form, for kernels whose warps hold different register budgets and
+// so may not call shared subroutines; wait_phase is the out-of-line form.)
 template <bool kClusterScope>
-__device__ __noinline__ bool wait_phase(uint32_t bar, uint32_t parity, volatile int* abort_flag,
-                                        int* status, int code) {
+__device__ __forceinline__ bool wait_phase_inl(uint32_t bar, uint32_t parity,
+                                               volatile int* abort_flag, int* status, int code) {
   auto poll = [&]() {
     return kClusterScope ? mbar_try_wait_cluster(bar, parity) : mbar_try_wait(bar, parity);
   };
@@ -87,9 +89,14 @@ __device__ __noinline__ bool wait_phase(uint32_t bar, uint32_t parity, volatile 
     }
   }
 }
+template <bool kClusterScope>
+__device__ __noinline__ bool wait_phase(uint32_t bar, uint32_t parity, volatile int* abort_flag,
+                                        int* status, int code) {
+  return wait_phase_inl<kClusterScope>(bar, parity, abort_flag, status, code);
+}
 
 // Short bounded wait used only while draining after an abort.
-__device__ __noinline__ inline void drain_wait(uint32_t bar, uint32_t parity, int* status) {
+__device__ __forceinline__ void drain_wait_inl(uint32_t bar, uint32_t parity, int* status) {
   const uint64_t t0 = globaltimer_ns();
   while (!mbar_try_wait(bar, parity)) {
     if (globaltimer_ns() - t0 > kWaitLimitNs) {
@@ -97,6 +104,9 @@ __device__ __noinline__ inline void drain_wait(uint32_t bar, uint32_t parity, in
       return;
     }
   }
+}
+__device__ __noinline__ inline void drain_wait(uint32_t bar, uint32_t parity, int* status) {
+  drain_wait_inl(bar, parity, status);
 }
 
 // Tile t -> (row block, column block): groups of kGroup row blocks, row

@@ -18,12 +18,14 @@
 // barriers of the even CTA (scales, operands).  The scales go from shared
 // memory to both CTAs' TMEM by tcgen05.cp (pair form, 32x128b.warpx4: one
 // copy = one K=64 step's A scales, or half of its B scales).  A copy stalls
-// the thread that issues it for over a hundred clocks, so two copy warps of
-// the even CTA issue six copies each per k-block; once they have also seen
-// the stage's operands land they commit to a per-stage "ready" barrier, the
-// only one the MMA thread waits on (every wait or commit in that thread costs
-// MMA issue time) before it issues four M=256 N=256 K=64 block-scaled MMAs
-// (512 clocks of tensor work per k-block).
+// the thread that issues it for over a hundred clocks, while copies issued
+// by different warps overlap: the twelve copies of a k-block take about 1800
+// clocks from one warp, 950 from two, 660 from three, against 512 clocks of
+// MMA.  So kCpWarps copy warps of the even CTA share them; once they have
+// also seen the stage's operands land they commit to a per-stage "ready"
+// barrier, the only one the MMA thread waits on (every wait or commit in that
+// thread costs MMA issue time) before it issues four M=256 N=256 K=64
+// block-scaled MMAs.
 //
 // TMEM: one 256-column accumulator plus five 48-column scale slots (496 of
 // 512 columns).  The epilogue drains its 32 lanes x 256 columns into
@@ -31,13 +33,15 @@
 // releases the accumulator before it computes the two heads, so the next
 // tile's MMAs overlap the epilogue's arithmetic and stores.
 //
-// Roles per CTA (256 threads): warp 0 TMA producer, warp 1 TMEM allocation
-// and (even CTA) MMA issue, warps 2..5 the epilogue of the CTA's 128 rows,
-// warps 6..7 (even CTA) the scale copies.  Eight warps keep at most two warps
-// on each SM sub-partition, whose register file (16K) then allows the 256
-// registers per thread the epilogue's live row of y needs without spilling
-// (ten warps would cap a thread at 168).  Bounded waits, abort flags and
-// draining as in gemm_pair.cuh.
+// Roles per CTA (12 warps, three warpgroups): warp 0 TMA producer, warp 1
+// TMEM allocation and (even CTA) MMA issue, warps 4..7 (warpgroup 1) the
+// epilogue of the CTA's 128 rows (warp w reads TMEM lanes 32 (w % 4) ...),
+// warps 8..11 and, with six copy warps, 2..3 the scale copies (even CTA).
+// Launched at 168 registers per thread; warpgroups 0 and 2 then give theirs
+// down to 120 and the epilogue warpgroup takes 256, which its live row of y
+// needs (each SM sub-partition holds one warp of each warpgroup: 256 + 2 x
+// 120 <= 3 x 168).  Bounded waits, abort flags and draining as in
+// gemm_pair.cuh.
 #include "gemm_pair.cuh"
 
 namespace mh3 {
@@ -61,8 +65,21 @@ constexpr int kFSfbBytes = 8 * 512;                 // 8 atoms = 4 KB
 constexpr uint32_t kFIdesc = idesc_fp4_f32(2 * FBM, kFTileN);
 constexpr uint32_t kFTmemSf = kFTileN;         // scale slots start after the accumulator
 constexpr uint32_t kFSfCols = 48;              // per slot: A scales 16 + B scales 32
-constexpr int kCpWarps = 2;                    // scale-copy warps of the even CTA, two K steps each
-constexpr int kFThreads = 64 + kEpiWarps * 32 + kCpWarps * 32;  // 256
+#ifndef MH3_FP4_CP_WARPS
+#define MH3_FP4_CP_WARPS 6
+#endif
+constexpr int kCpWarps = MH3_FP4_CP_WARPS;     // scale-copy warps of the even CTA
+constexpr int kFCopies = 12;                   // per k-block: 4 K steps x (A, B rows 0-127, 128-255)
+constexpr int kFWarps = 12;
+constexpr int kFThreads = kFWarps * 32;        // 384
+constexpr int kFEpiWarp0 = 4;                  // warpgroup 1
+constexpr int kRegsLaunch = 168;               // 65536 / 384, rounded down to 8
+constexpr int kRegsEpi = 256;
+constexpr int kRegsOther = 120;
+static_assert(kCpWarps == 4 || kCpWarps == 6, "copy warps: 8..11, plus 2..3");
+static_assert(kEpiWarps == 4 && kFEpiWarp0 % 4 == 0, "the epilogue is one whole warpgroup");
+static_assert(kRegsEpi + 2 * kRegsOther <= 3 * kRegsLaunch, "per sub-partition register budget");
+static_assert(128 * kRegsEpi + 256 * kRegsOther <= kFThreads * kRegsLaunch, "CTA register budget");
 
 constexpr int kFOffA = 0;
 constexpr int kFOffB = kFOffA + kFStages * kFABytes;
@@ -79,7 +96,6 @@ constexpr int kFOffScratch = kFOffBar + 256;
 constexpr int kFSmemUsed = kFOffScratch + 1024;
 constexpr int kFSmemAlloc = kFSmemUsed + 1024;
 static_assert(kFOffAbort + 4 <= kFOffScratch, "barrier block overflow");
-static_assert(4 % kCpWarps == 0, "copy warps split a k-block's four K=64 steps evenly");
 static_assert(kFSmemAlloc <= 232448, "exceeds the 227 KB per-CTA limit");
 static_assert(kFTmemSf + kFStages * kFSfCols <= kTmemCols, "TMEM budget");
 static_assert(kHidden % 256 == 0 && kQkvRows % kFTileN == 0, "shapes must tile");
@@ -122,6 +138,20 @@ __device__ __forceinline__ void drain_accumulator(uint32_t tcol, float alpha, ui
     for (int i = 0; i < 16; ++i)
       y[16 * c + i] = pack_bf16x2(__fmul_rn(__uint_as_float(v[2 * i]), alpha),
                                   __fmul_rn(__uint_as_float(v[2 * i + 1]), alpha));
+  }
+}
+
+// End of a role: neither CTA may leave while the other can still reach its
+// shared memory (MMA operand reads, barrier arrivals, copies counted on the
+// even CTA); warp 1 then releases TMEM.  Each role runs this copy of the tail
+// itself, so that no code is shared by warps holding different register
+// budgets.
+__device__ __forceinline__ void finish_role(bool tmem_owner, uint32_t tmem_base) {
+  tc_fence_before();
+  cluster_sync_all();
+  if (tmem_owner) {
+    tc_fence_after();
+    tmem_dealloc_pair(tmem_base, kTmemCols);
   }
 }
 
@@ -179,142 +209,13 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kFThreads, 1)
   const uint32_t tmem_base = *sm.tmem_ptr();
   gp::PairCtx ctx{sm.abort_flag(), mapa_shared(sm.abort_addr(), rank ^ 1u), p.status};
 
-  if (warp == 0) {
-    // ------------------------------------------------- producer (both CTAs)
-    if (lane == 0) {
-      griddep_wait();  // act_q / act_sf come from the kernel before this one
-      int stage = 0;
-      uint32_t phase = 0;
-      bool ok = p.test_stall == 0;
-      bool issued_any = false;
-      for (int t = cid; t < p.num_tiles && ok; t += ncl) {
-        int pr, n_blk;
-        tile_coords<gp::kGroupPairs, kFNTiles>(t, p.num_m_tiles, pr, n_blk);
-        const int a_rg = pr * 2 + static_cast<int>(rank);  // 128-row group of A
-        const int b_row = n_blk * kFTileN + static_cast<int>(rank) * kFBRows;
-        for (int kb = 0; kb < kFKBlocks; ++kb) {
-          if (!gp::pair_wait(ctx, sm.empty(stage), phase ^ 1u, kStatusProducerEmpty)) {
-            ok = false;
-            break;
-          }
-          // scales first, on their own barrier: the copy warps can move them
-          // into TMEM while the operands are still in flight
-          const uint32_t leader_full = mapa_shared(sm.full(stage), 0);
-          const uint32_t leader_sffull = mapa_shared(sm.sffull(stage), 0);
-          if (rank == 0) {
-            mbar_arrive_expect_tx(sm.sffull(stage), 2 * (kFSfaBytes + kFSfbBytes));
-            mbar_arrive_expect_tx(sm.full(stage), 2 * (kFABytes + kFBBytes));
-          }
-          tma_load_3d_pair(sm.sfa(stage), &tm_sfa, leader_sffull, 0, 4 * kb, a_rg);
-          tma_load_3d_pair(sm.sfb(stage), &tm_sfb, leader_sffull, 0, 4 * kb, 2 * n_blk);
-          tma_load_2d_pair(sm.a(stage), &tm_a, leader_full, kb * kFBytesPerRow, a_rg * FBM);
-          tma_load_2d_pair(sm.b(stage), &tm_b, leader_full, kb * kFBytesPerRow, b_row);
-          issued_any = true;
-          if (++stage == kFStages) {
-            stage = 0;
-            phase ^= 1u;
-          }
-        }
-      }
-      if (!ok && issued_any) gp::grace_period();  // copies signal the even CTA
-    }
-    __syncwarp();
-  } else if (warp == 1) {
-    // ------------------------------------------------ MMA issue (even CTA)
-    if (lane == 0 && rank == 0) {
-      int stage = 0;
-      uint32_t phase = 0;
-      bool ok = true;
-      int it = 0;
-      for (int t = cid; t < p.num_tiles && ok; t += ncl, ++it) {
-        // the epilogue has drained the accumulator of the previous tile
-        if (!gp::pair_wait(ctx, sm.tempty(), (static_cast<uint32_t>(it) & 1u) ^ 1u,
-                           kStatusMmaTmemEmpty)) {
-          ok = false;
-          break;
-        }
-        tc_fence_after();
-        for (int kb = 0; kb < kFKBlocks; ++kb) {
-          // the operands have landed and the scales are in both CTAs' TMEM
-          // (the copy warps commit to `ready` only after seeing `full`)
-          if (!gp::pair_wait(ctx, sm.ready(stage), phase, kStatusMmaFull)) {
-            ok = false;
-            break;
-          }
-          tc_fence_after();
-          const uint32_t sf_cols = tmem_base + kFTmemSf + static_cast<uint32_t>(stage) * kFSfCols;
-          const uint64_t a_desc = sw128_kmajor_desc(sm.a(stage));
-          const uint64_t b_desc = sw128_kmajor_desc(sm.b(stage));
-#pragma unroll
-          for (int k = 0; k < 4; ++k) {
-            // 64 elements = 32 B along K inside the swizzle atom; A scales of
-            // step k in columns [4k, 4k+4), B scales in [16+8k, 16+8k+8)
-            umma_fp4_pair(tmem_base, a_desc + 2 * k, b_desc + 2 * k, kFIdesc, sf_cols + 4 * k,
-                          sf_cols + 16 + 8 * k, (kb | k) != 0 ? 1u : 0u);
-          }
-          umma_commit_pair_multicast(sm.empty(stage), gp::kBothCtas);
-          if (++stage == kFStages) {
-            stage = 0;
-            phase ^= 1u;
-          }
-        }
-        if (!ok) break;
-        umma_commit_pair_multicast(sm.tfull(), gp::kBothCtas);
-      }
-      if (!ok) {
-        umma_commit_pair_multicast(sm.drain(), 0x1);
-        drain_wait(sm.drain(), 0, p.status);
-      }
-    }
-    __syncwarp();
-  } else if (warp >= 2 + kEpiWarps) {
-    // ---------------------------------------- scale copies (even CTA only)
-    // For each of its K steps k, a copy warp moves the A-scale atom to
-    // columns [4k, 4k+4) and the two B-scale atoms (rows 0-127, 128-255) to
-    // [16+8k, 16+8k+8) of the stage's slot, in both CTAs.
-    if (lane == 0 && rank == 0) {
-      const int k0 = warp - 2 - kEpiWarps;
-      int stage = 0;
-      uint32_t phase = 0;
-      bool ok = true;
-      for (int t = cid; t < p.num_tiles && ok; t += ncl) {
-        for (int kb = 0; kb < kFKBlocks; ++kb) {
-          if (!gp::pair_wait(ctx, sm.sffull(stage), phase, kStatusMmaFull)) {
-            ok = false;
-            break;
-          }
-          tc_fence_after();
-          const uint32_t sf_cols =
-              tmem_base + kFTmemSf + static_cast<uint32_t>(stage) * kFSfCols;
-          // B-scale atoms arrive as [row group][step][512 B]
-#pragma unroll
-          for (int k = k0; k < 4; k += kCpWarps) {
-            tmem_cp_pair_32x128b_x4(sf_cols + 4 * k, rows16_desc(sm.sfa(stage) + 512 * k));
-            tmem_cp_pair_32x128b_x4(sf_cols + 16 + 8 * k, rows16_desc(sm.sfb(stage) + 512 * k));
-            tmem_cp_pair_32x128b_x4(sf_cols + 16 + 8 * k + 4,
-                                    rows16_desc(sm.sfb(stage) + 2048 + 512 * k));
-          }
-          // the MMA thread waits on `ready` alone: report only once the
-          // operands of the stage have landed too
-          if (!gp::pair_wait(ctx, sm.full(stage), phase, kStatusMmaFull)) {
-            ok = false;
-            break;
-          }
-          umma_commit_pair_multicast(sm.ready(stage), 0x1);
-          if (++stage == kFStages) {
-            stage = 0;
-            phase ^= 1u;
-          }
-        }
-      }
-      // every copy this warp issued has landed before TMEM can be released
-      umma_commit_pair_multicast(sm.cpdrain(), 0x1);
-      drain_wait(sm.cpdrain(), 0, p.status);
-    }
-    __syncwarp();
-  } else {
+  // register split: the epilogue warpgroup takes what the others give up;
+  // each side's roles sit inside its own branch
+  __syncwarp();
+  if ((warp >> 2) == kFEpiWarp0 / 4) {
+    setmaxnreg_inc<kRegsEpi>();
     // ------------------------------------------------- epilogue (both CTAs)
-    const int ew = warp - 2;
+    const int ew = warp - kFEpiWarp0;
     const int quad = warp & 3;
     const uint32_t stg = sm.stg(ew);
     const float alpha = isfinite(p.alpha) && p.alpha > 0.0f
@@ -322,7 +223,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kFThreads, 1)
                             : __frcp_rn(__fmul_rn(__ldg(p.act_gs), p.w_gs));
     int it = 0;
     for (int t = cid; t < p.num_tiles; t += ncl, ++it) {
-      bool ok = gp::pair_wait(ctx, sm.tfull(), static_cast<uint32_t>(it) & 1u, kStatusEpiTmemFull);
+      bool ok = gp::pair_wait_inl(ctx, sm.tfull(), static_cast<uint32_t>(it) & 1u, kStatusEpiTmemFull);
       ok = __all_sync(0xFFFFFFFFu, ok);
       if (!ok) break;
       tc_fence_after();
@@ -350,21 +251,167 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kFThreads, 1)
     }
     if (lane == 0) bulk_wait_group0();
     __syncwarp();
+    finish_role(false, tmem_base);
+    return;
   }
+  setmaxnreg_dec<kRegsOther>();
+  const int cw = warp >= 8 ? warp - 8 : warp + 2;  // copy warp index: 8..11 -> 0..3, 2..3 -> 4..5
 
-  tc_fence_before();
-  cluster_sync_all();
-  if (warp == 1) {
-    tc_fence_after();
-    tmem_dealloc_pair(tmem_base, kTmemCols);
+  if (warp == 0) {
+    // ------------------------------------------------- producer (both CTAs)
+    if (lane == 0) {
+      griddep_wait();  // act_q / act_sf come from the kernel before this one
+      int stage = 0;
+      uint32_t phase = 0;
+      bool ok = p.test_stall == 0;
+      bool issued_any = false;
+      for (int t = cid; t < p.num_tiles && ok; t += ncl) {
+        int pr, n_blk;
+        tile_coords<gp::kGroupPairs, kFNTiles>(t, p.num_m_tiles, pr, n_blk);
+        const int a_rg = pr * 2 + static_cast<int>(rank);  // 128-row group of A
+        const int b_row = n_blk * kFTileN + static_cast<int>(rank) * kFBRows;
+        for (int kb = 0; kb < kFKBlocks; ++kb) {
+          if (!gp::pair_wait_inl(ctx, sm.empty(stage), phase ^ 1u, kStatusProducerEmpty)) {
+            ok = false;
+            break;
+          }
+          // scales first, on their own barrier: the copy warps can move them
+          // into TMEM while the operands are still in flight
+          const uint32_t leader_full = mapa_shared(sm.full(stage), 0);
+          const uint32_t leader_sffull = mapa_shared(sm.sffull(stage), 0);
+          if (rank == 0) {
+            mbar_arrive_expect_tx(sm.sffull(stage), 2 * (kFSfaBytes + kFSfbBytes));
+            mbar_arrive_expect_tx(sm.full(stage), 2 * (kFABytes + kFBBytes));
+          }
+          tma_load_3d_pair(sm.sfa(stage), &tm_sfa, leader_sffull, 0, 4 * kb, a_rg);
+          tma_load_3d_pair(sm.sfb(stage), &tm_sfb, leader_sffull, 0, 4 * kb, 2 * n_blk);
+          tma_load_2d_pair(sm.a(stage), &tm_a, leader_full, kb * kFBytesPerRow, a_rg * FBM);
+          tma_load_2d_pair(sm.b(stage), &tm_b, leader_full, kb * kFBytesPerRow, b_row);
+          issued_any = true;
+          if (++stage == kFStages) {
+            stage = 0;
+            phase ^= 1u;
+          }
+        }
+      }
+      if (!ok && issued_any) gp::grace_period_inl();  // copies signal the even CTA
+    }
+    __syncwarp();
+    finish_role(false, tmem_base);
+    return;
+  } else if (warp == 1) {
+    // ------------------------------------------------ MMA issue (even CTA)
+    if (lane == 0 && rank == 0) {
+      int stage = 0;
+      uint32_t phase = 0;
+      bool ok = true;
+      int it = 0;
+      for (int t = cid; t < p.num_tiles && ok; t += ncl, ++it) {
+        // the epilogue has drained the accumulator of the previous tile
+        if (!gp::pair_wait_inl(ctx, sm.tempty(), (static_cast<uint32_t>(it) & 1u) ^ 1u,
+                           kStatusMmaTmemEmpty)) {
+          ok = false;
+          break;
+        }
+        tc_fence_after();
+        for (int kb = 0; kb < kFKBlocks; ++kb) {
+          // the operands have landed and the scales are in both CTAs' TMEM
+          // (the copy warps commit to `ready` only after seeing `full`)
+          if (!gp::pair_wait_inl(ctx, sm.ready(stage), phase, kStatusMmaFull)) {
+            ok = false;
+            break;
+          }
+          tc_fence_after();
+          const uint32_t sf_cols = tmem_base + kFTmemSf + static_cast<uint32_t>(stage) * kFSfCols;
+          const uint64_t a_desc = sw128_kmajor_desc(sm.a(stage));
+          const uint64_t b_desc = sw128_kmajor_desc(sm.b(stage));
+#pragma unroll
+          for (int k = 0; k < 4; ++k) {
+            // 64 elements = 32 B along K inside the swizzle atom; A scales of
+            // step k in columns [4k, 4k+4), B scales in [16+8k, 16+8k+8)
+            umma_fp4_pair(tmem_base, a_desc + 2 * k, b_desc + 2 * k, kFIdesc, sf_cols + 4 * k,
+                          sf_cols + 16 + 8 * k, (kb | k) != 0 ? 1u : 0u);
+          }
+          umma_commit_pair_multicast(sm.empty(stage), gp::kBothCtas);
+          if (++stage == kFStages) {
+            stage = 0;
+            phase ^= 1u;
+          }
+        }
+        if (!ok) break;
+        umma_commit_pair_multicast(sm.tfull(), gp::kBothCtas);
+      }
+      if (!ok) {
+        umma_commit_pair_multicast(sm.drain(), 0x1);
+        drain_wait_inl(sm.drain(), 0, p.status);
+      }
+    }
+    __syncwarp();
+    finish_role(true, tmem_base);
+    return;
+  } else {
+    // ---------------------------------------- scale copies (even CTA only)
+    // Copy c of a k-block (K step k = c / 3) moves the A-scale atom of step k
+    // to columns [4k, 4k+4), or one of its two B-scale atoms (rows 0-127,
+    // 128-255) to [16+8k, 16+8k+4) or [16+8k+4, 16+8k+8), of the stage's
+    // slot in both CTAs; copy warp cw issues copies cw, cw + kCpWarps, ...
+    if (lane == 0 && rank == 0 && cw < kCpWarps) {
+      int stage = 0;
+      uint32_t phase = 0;
+      bool ok = true;
+      for (int t = cid; t < p.num_tiles && ok; t += ncl) {
+        for (int kb = 0; kb < kFKBlocks; ++kb) {
+          if (!gp::pair_wait_inl(ctx, sm.sffull(stage), phase, kStatusMmaFull)) {
+            ok = false;
+            break;
+          }
+          tc_fence_after();
+          const uint32_t sf_cols =
+              tmem_base + kFTmemSf + static_cast<uint32_t>(stage) * kFSfCols;
+          // B-scale atoms arrive as [row group][step][512 B]
+          for (int c = cw; c < kFCopies; c += kCpWarps) {
+            const int k = c / 3, part = c - 3 * (c / 3);
+            const uint32_t col = part == 0 ? 4u * k : 16u + 8u * k + 4u * (part - 1);
+            const uint32_t src = part == 0 ? sm.sfa(stage) + 512 * k
+                                           : sm.sfb(stage) + 2048 * (part - 1) + 512 * k;
+            tmem_cp_pair_32x128b_x4(sf_cols + col, rows16_desc(src));
+          }
+          // the MMA thread waits on `ready` alone: report only once the
+          // operands of the stage have landed too
+          if (!gp::pair_wait_inl(ctx, sm.full(stage), phase, kStatusMmaFull)) {
+            ok = false;
+            break;
+          }
+          umma_commit_pair_multicast(sm.ready(stage), 0x1);
+          if (++stage == kFStages) {
+            stage = 0;
+            phase ^= 1u;
+          }
+        }
+      }
+      // every copy this warp issued has landed before TMEM can be released
+      umma_commit_pair_multicast(sm.cpdrain(), 0x1);
+      drain_wait_inl(sm.cpdrain(), 0, p.status);
+    }
+    __syncwarp();
+    finish_role(false, tmem_base);
+    return;
   }
 }
 
 template <bool kE4m3>
 cudaError_t prepare_one(int* max_clusters) {
   *max_clusters = 0;
-  cudaError_t e = cudaFuncSetAttribute(nvfp4_qkv_kernel<kE4m3>,
-                                       cudaFuncAttributeMaxDynamicSharedMemorySize, kFSmemAlloc);
+  // The register split (setmaxnreg) is sized for a launch at exactly
+  // kRegsLaunch registers per thread; with any other entry allocation an
+  // `inc` could wait forever, so such a build is refused here.
+  cudaFuncAttributes fa;
+  cudaError_t e = cudaFuncGetAttributes(&fa, nvfp4_qkv_kernel<kE4m3>);
+  if (e != cudaSuccess) return e;
+  if (fa.numRegs != kRegsLaunch || fa.maxThreadsPerBlock < kFThreads)
+    return cudaErrorInvalidConfiguration;
+  e = cudaFuncSetAttribute(nvfp4_qkv_kernel<kE4m3>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                           kFSmemAlloc);
   if (e != cudaSuccess) return e;
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(2, 1, 1);

@@ -364,6 +364,21 @@ __device__ __forceinline__ void tc_fence_after() {
   asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
 }
 
+// Per-warpgroup register budget (all four warps of a warpgroup execute the
+// same instruction).  `inc` waits until other warpgroups' `dec` have returned
+// enough registers to the CTA's allocation, so the shares must add up to at
+// most what the CTA was launched with.
+template <uint32_t kRegs>
+__device__ __forceinline__ void setmaxnreg_inc() {
+  static_assert(kRegs >= 24 && kRegs <= 256 && kRegs % 8 == 0, "register count");
+  asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(kRegs));
+}
+template <uint32_t kRegs>
+__device__ __forceinline__ void setmaxnreg_dec() {
+  static_assert(kRegs >= 24 && kRegs <= 256 && kRegs % 8 == 0, "register count");
+  asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(kRegs));
+}
+
 // D[tmem] (+)= A[smem] * B[smem]^T, kind::f16 (bf16 inputs, FP32 accumulator),
 // issued by one thread.  `accumulate` = 0 overwrites D.
 __device__ __forceinline__ void umma_bf16(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc,
