@@ -338,26 +338,37 @@ __device__ __forceinline__ void epilogue_head_regs(const uint32_t (&y)[64], int 
                                                    const CUtensorMap* tm_out) {
   if (lane == 0) bulk_wait_group_read0();
   __syncwarp();
-  auto yv = [&](int d) { return (d & 1) ? bf16_hi(y[d >> 1]) : bf16_lo(y[d >> 1]); };
   if (kind == 2) {
 #pragma unroll
     for (int c = 0; c < 16; ++c)
       st_shared_v4(stg_addr(stg, lane, c), make_uint4(y[4 * c], y[4 * c + 1], y[4 * c + 2], y[4 * c + 3]));
   } else {
+    // Packed two-lane FP32 (each lane one IEEE round-to-nearest operation, in
+    // epi_qk_head's order): lane pairs are neighbouring columns (d, d + 1).
     const float* nw = nw_all + kind * kHeadDim;
-    // FP32 sum of squares in epi_qk_head's order: four partial sums over
-    // columns d % 4, d increasing
-    float s0 = 0.f, s1 = 0.f, s2 = 0.f, s3 = 0.f;
+    auto nw2 = [&](int d) {
+      const float2 w = *reinterpret_cast<const float2*>(nw + d);
+      return f2_pack(w.x, w.y);
+    };
+    // FP32 sum of squares: four partial sums over columns d % 4, d increasing
+    uint64_t s01 = 0, s23 = 0;  // (+0.0, +0.0)
 #pragma unroll
-    for (int d = 0; d < kHeadDim; d += 4) {
-      const float y0 = yv(d), y1 = yv(d + 1), y2 = yv(d + 2), y3 = yv(d + 3);
-      s0 = __fmaf_rn(y0, y0, s0);
-      s1 = __fmaf_rn(y1, y1, s1);
-      s2 = __fmaf_rn(y2, y2, s2);
-      s3 = __fmaf_rn(y3, y3, s3);
+    for (int i = 0; i < kHeadDim / 4; ++i) {
+      const uint64_t y01 = f2_from_bf16x2(y[2 * i]);
+      const uint64_t y23 = f2_from_bf16x2(y[2 * i + 1]);
+      s01 = f2_fma(y01, y01, s01);
+      s23 = f2_fma(y23, y23, s23);
     }
+    float s0, s1, s2, s3;
+    f2_unpack(s01, s0, s1);
+    f2_unpack(s23, s2, s3);
     const float ss = __fadd_rn(__fadd_rn(s0, s1), __fadd_rn(s2, s3));
     const float rr = __fdiv_rn(1.0f, __fsqrt_rn(__fadd_rn(__fdiv_rn(ss, 128.0f), p.qk_eps)));
+    const uint64_t rr2 = f2_pack(rr, rr);
+    // t = bf16((y * rr) * w) for the column pair (d, d + 1), back as FP32
+    auto t2 = [&](int d) {
+      return f2_from_bf16x2(f2_to_bf16x2(f2_mul(f2_mul(f2_from_bf16x2(y[d >> 1]), rr2), nw2(d))));
+    };
     // rotated dims: chunk c (columns 8c..8c+7, c < 6) pairs with chunk c + 6
 #pragma unroll
     for (int c = 0; c < 6; ++c) {
@@ -368,19 +379,12 @@ __device__ __forceinline__ void epilogue_head_regs(const uint32_t (&y)[64], int 
       uint32_t o1[4], o2[4];
 #pragma unroll
       for (int e2 = 0; e2 < 4; ++e2) {
-        float r1[2], r2[2];
-#pragma unroll
-        for (int e = 0; e < 2; ++e) {
-          const int j = 8 * c + 2 * e2 + e;
-          const float cs = e ? bf16_hi(cw[e2]) : bf16_lo(cw[e2]);
-          const float sn = e ? bf16_hi(sw[e2]) : bf16_lo(sw[e2]);
-          const float t1 = round_bf16(__fmul_rn(__fmul_rn(yv(j), rr), nw[j]));
-          const float t2 = round_bf16(__fmul_rn(__fmul_rn(yv(j + kRopeHalf), rr), nw[j + kRopeHalf]));
-          r1[e] = __fsub_rn(__fmul_rn(t1, cs), __fmul_rn(t2, sn));
-          r2[e] = __fadd_rn(__fmul_rn(t2, cs), __fmul_rn(t1, sn));
-        }
-        o1[e2] = pack_bf16x2(r1[0], r1[1]);
-        o2[e2] = pack_bf16x2(r2[0], r2[1]);
+        const int j = 8 * c + 2 * e2;
+        const uint64_t c2 = f2_from_bf16x2(cw[e2]);
+        const uint64_t s2 = f2_from_bf16x2(sw[e2]);
+        const uint64_t ta = t2(j), tb = t2(j + kRopeHalf);
+        o1[e2] = f2_to_bf16x2(f2_sub(f2_mul(ta, c2), f2_mul(tb, s2)));
+        o2[e2] = f2_to_bf16x2(f2_add(f2_mul(tb, c2), f2_mul(ta, s2)));
       }
       st_shared_v4(stg_addr(stg, lane, c), make_uint4(o1[0], o1[1], o1[2], o1[3]));
       st_shared_v4(stg_addr(stg, lane, c + 6), make_uint4(o2[0], o2[1], o2[2], o2[3]));
@@ -392,8 +396,7 @@ __device__ __forceinline__ void epilogue_head_regs(const uint32_t (&y)[64], int 
 #pragma unroll
       for (int e = 0; e < 4; ++e) {
         const int d = 8 * c + 2 * e;
-        o[e] = pack_bf16x2(__fmul_rn(__fmul_rn(yv(d), rr), nw[d]),
-                           __fmul_rn(__fmul_rn(yv(d + 1), rr), nw[d + 1]));
+        o[e] = f2_to_bf16x2(f2_mul(f2_mul(f2_from_bf16x2(y[d >> 1]), rr2), nw2(d)));
       }
       st_shared_v4(stg_addr(stg, lane, c), make_uint4(o[0], o[1], o[2], o[3]));
     }
