@@ -165,13 +165,30 @@ __device__ __forceinline__ void epi_v_head(uint32_t tcol, uint32_t stg, int lane
   }
 }
 
+// Two accumulator words -> the bf16-rounded projection y of both columns, as
+// packed FP32 (bf16(RN(alpha * acc)) when kScaled).
+template <bool kScaled>
+__device__ __forceinline__ uint64_t acc2_to_y2(uint32_t a, uint32_t b, uint64_t alpha2) {
+  uint64_t v = f2_pack(__uint_as_float(a), __uint_as_float(b));
+  if (kScaled) v = f2_mul(v, alpha2);
+  return f2_from_bf16x2(f2_to_bf16x2(v));
+}
+
 // Q or K head: RMSNorm over the 128 columns, rotation of [0, 96), pass-through
-// of [96, 128).
+// of [96, 128).  Packed two-lane FP32 over neighbouring columns (d, d + 1):
+// each lane is one IEEE round-to-nearest operation, in the order of the
+// formulas (sum of squares in four partial sums over d % 4, d increasing;
+// t = bf16((y * rr) * w); o = bf16(t_j c - t_{j+48} s), bf16(t_{j+48} c + t_j s)).
 template <bool kScaled = false>
 __device__ __forceinline__ void epi_qk_head(uint32_t tcol, uint32_t stg, int lane, const float* nw,
                                             const uint4* cs_row, float qk_eps, float alpha = 1.0f) {
+  const uint64_t alpha2 = f2_pack(alpha, alpha);
+  auto nw2 = [&](int d) {
+    const float2 w = *reinterpret_cast<const float2*>(nw + d);
+    return f2_pack(w.x, w.y);
+  };
   // Pass 1: FP32 sum of squares of the bf16-rounded projection.
-  float s0 = 0.f, s1 = 0.f, s2 = 0.f, s3 = 0.f;
+  uint64_t s01 = 0, s23 = 0;  // (+0.0, +0.0)
 #pragma unroll
   for (int c = 0; c < 4; ++c) {
     uint32_t v[32];
@@ -179,16 +196,18 @@ __device__ __forceinline__ void epi_qk_head(uint32_t tcol, uint32_t stg, int lan
     tmem_wait_ld();
 #pragma unroll
     for (int i = 0; i < 32; i += 4) {
-      const float y0 = acc_to_y_s<kScaled>(v[i], alpha), y1 = acc_to_y_s<kScaled>(v[i + 1], alpha);
-      const float y2 = acc_to_y_s<kScaled>(v[i + 2], alpha), y3 = acc_to_y_s<kScaled>(v[i + 3], alpha);
-      s0 = __fmaf_rn(y0, y0, s0);
-      s1 = __fmaf_rn(y1, y1, s1);
-      s2 = __fmaf_rn(y2, y2, s2);
-      s3 = __fmaf_rn(y3, y3, s3);
+      const uint64_t y01 = acc2_to_y2<kScaled>(v[i], v[i + 1], alpha2);
+      const uint64_t y23 = acc2_to_y2<kScaled>(v[i + 2], v[i + 3], alpha2);
+      s01 = f2_fma(y01, y01, s01);
+      s23 = f2_fma(y23, y23, s23);
     }
   }
+  float s0, s1, s2, s3;
+  f2_unpack(s01, s0, s1);
+  f2_unpack(s23, s2, s3);
   const float ss = __fadd_rn(__fadd_rn(s0, s1), __fadd_rn(s2, s3));
   const float rr = __fdiv_rn(1.0f, __fsqrt_rn(__fadd_rn(__fdiv_rn(ss, 128.0f), qk_eps)));
+  const uint64_t rr2 = f2_pack(rr, rr);
 
   // Pass 2a: the rotated dims, 16 pairs (j, j + 48) at a time.
 #pragma unroll
@@ -204,22 +223,15 @@ __device__ __forceinline__ void epi_qk_head(uint32_t tcol, uint32_t stg, int lan
     uint32_t o1[8], o2[8];
 #pragma unroll
     for (int i = 0; i < 16; i += 2) {
-      const uint32_t cw = (&cv[i >> 3].x)[(i & 7) >> 1];
-      const uint32_t sw = (&sv[i >> 3].x)[(i & 7) >> 1];
-      float r1[2], r2[2];
-#pragma unroll
-      for (int e = 0; e < 2; ++e) {
-        const int j = 16 * g + i + e;
-        const float c = e ? bf16_hi(cw) : bf16_lo(cw);
-        const float s = e ? bf16_hi(sw) : bf16_lo(sw);
-        const float t1 = round_bf16(__fmul_rn(__fmul_rn(acc_to_y_s<kScaled>(lo[i + e], alpha), rr), nw[j]));
-        const float t2 =
-            round_bf16(__fmul_rn(__fmul_rn(acc_to_y_s<kScaled>(hi[i + e], alpha), rr), nw[j + kRopeHalf]));
-        r1[e] = __fsub_rn(__fmul_rn(t1, c), __fmul_rn(t2, s));
-        r2[e] = __fadd_rn(__fmul_rn(t2, c), __fmul_rn(t1, s));
-      }
-      o1[i >> 1] = pack_bf16x2(r1[0], r1[1]);
-      o2[i >> 1] = pack_bf16x2(r2[0], r2[1]);
+      const int j = 16 * g + i;
+      const uint64_t c2 = f2_from_bf16x2((&cv[i >> 3].x)[(i & 7) >> 1]);
+      const uint64_t s2 = f2_from_bf16x2((&sv[i >> 3].x)[(i & 7) >> 1]);
+      const uint64_t ta = f2_from_bf16x2(
+          f2_to_bf16x2(f2_mul(f2_mul(acc2_to_y2<kScaled>(lo[i], lo[i + 1], alpha2), rr2), nw2(j))));
+      const uint64_t tb = f2_from_bf16x2(f2_to_bf16x2(
+          f2_mul(f2_mul(acc2_to_y2<kScaled>(hi[i], hi[i + 1], alpha2), rr2), nw2(j + kRopeHalf))));
+      o1[i >> 1] = f2_to_bf16x2(f2_sub(f2_mul(ta, c2), f2_mul(tb, s2)));
+      o2[i >> 1] = f2_to_bf16x2(f2_add(f2_mul(tb, c2), f2_mul(ta, s2)));
     }
     // columns [16g, 16g+16) are chunks 2g, 2g+1; [48+16g, ...) are 6+2g, 7+2g
     st_shared_v4(stg_addr(stg, lane, 2 * g), make_uint4(o1[0], o1[1], o1[2], o1[3]));
@@ -239,10 +251,8 @@ __device__ __forceinline__ void epi_qk_head(uint32_t tcol, uint32_t stg, int lan
 #pragma unroll
       for (int e = 0; e < 4; ++e) {
         const int i = 8 * g + 2 * e;
-        const int d = kRopeDims + i;
-        const float t0 = __fmul_rn(__fmul_rn(acc_to_y_s<kScaled>(v[i], alpha), rr), nw[d]);
-        const float t1 = __fmul_rn(__fmul_rn(acc_to_y_s<kScaled>(v[i + 1], alpha), rr), nw[d + 1]);
-        o[e] = pack_bf16x2(t0, t1);
+        o[e] = f2_to_bf16x2(
+            f2_mul(f2_mul(acc2_to_y2<kScaled>(v[i], v[i + 1], alpha2), rr2), nw2(kRopeDims + i)));
       }
       st_shared_v4(stg_addr(stg, lane, 12 + g), make_uint4(o[0], o[1], o[2], o[3]));
     }
