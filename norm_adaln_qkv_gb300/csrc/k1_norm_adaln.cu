@@ -29,8 +29,8 @@
 // summary): int32 indices, and instead of the bf16 workspace the activation
 // quantised per token in blocks of 16 (nvfp4.cuh): E2M1 codes [M, 2688] and
 // UE4M3 scales.  A block is two neighbouring lanes' chunks (one shuffle for
-// the amax); a 64-element step's four scales are gathered from eight aligned
-// lanes into one 4-byte store.  A guarded row gets zero codes and scales.
+// the amax), whose even lane stores the scale byte.  A guarded row gets zero
+// codes and scales.
 #include "common.cuh"
 #include "nvfp4.cuh"
 #include "ptx.cuh"
@@ -85,21 +85,17 @@ __device__ __forceinline__ uint32_t adaln_pair(uint64_t x2, uint32_t w, uint32_t
 }
 
 // NVFP4 outputs of one 8-element chunk c of row m (a in `o`): the block of
-// 16 is this thread's chunk and its neighbour's (lanes 2b, 2b+1), the scale
-// word of one 64-element step is gathered from 8 aligned lanes.
+// 16 is this thread's chunk and its neighbour's (lanes 2b, 2b+1); the even
+// lane stores the block's scale byte.
 __device__ __forceinline__ void fp4_chunk(const uint4& o, int lane, int c, int64_t m, float gs,
                                           const float* enc_lut, const NormAdalnParams& p) {
   float amax = fp4::amax8(o);
   amax = fmaxf(amax, __shfl_xor_sync(0xFFFFFFFFu, amax, 1));
   const fp4::BlockScale bs = fp4::block_scale(amax, gs, enc_lut);
   *reinterpret_cast<uint32_t*>(p.act_q + m * (kHidden / 2) + 4 * c) = fp4::encode8(o, bs.enc);
-  uint32_t word = (lane & 1) ? 0u : bs.code << (8 * ((lane & 7) >> 1));
-  word |= __shfl_xor_sync(0xFFFFFFFFu, word, 1);
-  word |= __shfl_xor_sync(0xFFFFFFFFu, word, 2);
-  word |= __shfl_xor_sync(0xFFFFFFFFu, word, 4);
-  if ((lane & 7) == 0)
-    *reinterpret_cast<uint32_t*>(p.act_sf + fp4::scale_offset(m, c >> 3, kHidden / 64,
-                                                               p.sf_tiled != 0)) = word;
+  if ((lane & 1) == 0)
+    p.act_sf[fp4::scale_offset(m, c >> 3, kHidden / 64, p.sf_tiled != 0) + ((lane & 7) >> 1)] =
+        static_cast<uint8_t>(bs.code);
 }
 
 template <bool kFp4>

@@ -92,16 +92,15 @@ __device__ __forceinline__ uint32_t encode8(const uint4& w, float enc) {
   return e2m1x8(v);
 }
 
-__device__ __forceinline__ uint32_t bf16x2_max(uint32_t a, uint32_t b) {
+// max |v| of eight bf16 values (exact): packed magnitude maxima
+// (max.xorsign.abs keeps the larger magnitude), then the sign bits cleared.
+__device__ __forceinline__ uint32_t bf16x2_absmax(uint32_t a, uint32_t b) {
   uint32_t r;
-  asm("max.bf16x2 %0, %1, %2;" : "=r"(r) : "r"(a), "r"(b));
+  asm("max.xorsign.abs.bf16x2 %0, %1, %2;" : "=r"(r) : "r"(a), "r"(b));
   return r;
 }
-
-// max |v| of eight bf16 values (exact): sign bits cleared, packed bf16 max.
 __device__ __forceinline__ float amax8(const uint4& w) {
-  const uint32_t m = bf16x2_max(bf16x2_max(w.x & 0x7FFF7FFFu, w.y & 0x7FFF7FFFu),
-                                bf16x2_max(w.z & 0x7FFF7FFFu, w.w & 0x7FFF7FFFu));
+  const uint32_t m = bf16x2_absmax(bf16x2_absmax(w.x, w.y), bf16x2_absmax(w.z, w.w)) & 0x7FFF7FFFu;
   return fmaxf(bf16_lo(m), bf16_hi(m));
 }
 
