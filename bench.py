@@ -36,6 +36,7 @@ UNIT = "us/call"
 WORKLOAD = "c3"
 ALSO = "c2"
 SMALL_CALLS = 50
+E2E_PASSES = 3
 FLOP_PER_TOKEN = 2 * 5376 * 21504
 # kernel 2 at the bench size is the CTA-pair form; its traffic figure is tied
 # to these sources
@@ -409,16 +410,22 @@ def run_ours(args, world, rank, local):
         e2e_step(i)
     torch.cuda.synchronize()
     barrier()
-    s0, s1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    s0.record(s_in)
-    for i in range(n_e2e):
-        e2e_step(i)
-    for so in s_outs:
-        s_in.wait_stream(so)
-    s1.record(s_in)
-    torch.cuda.synchronize()
-    barrier()
-    e2e_ms = max_over_ranks(s0.elapsed_time(s1), dev) / n_e2e
+    # E2E_PASSES timed passes of n_e2e steps each; the median pass is the
+    # number (the host link is shared with other tenants of the machine, so
+    # single passes vary), all passes are reported beside it
+    e2e_passes = []
+    for _ in range(E2E_PASSES):
+        s0, s1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        s0.record(s_in)
+        for i in range(n_e2e):
+            e2e_step(i)
+        for so in s_outs:
+            s_in.wait_stream(so)
+        s1.record(s_in)
+        torch.cuda.synchronize()
+        barrier()
+        e2e_passes.append(max_over_ranks(s0.elapsed_time(s1), dev) / n_e2e)
+    e2e_ms = statistics.median(e2e_passes)
     # the host link itself: one pinned copy each way of the step's bytes
     # (the e2e step moves h2d + d2h bytes; its floor is the slower direction)
     lk = torch.empty(d2h // 2, dtype=torch.bfloat16, device=dev)
@@ -688,6 +695,7 @@ def run_ours(args, world, rank, local):
                 "d2h_bytes_per_step": d2h,
                 "link_gbs": {"d2h": d2h_gbs, "h2d": h2d_gbs},
                 "link_floor_us": max(d2h / d2h_gbs, h2d / h2d_gbs) * 1e-3,
+                "passes_us": [v * 1e3 / world for v in e2e_passes],
                 "how": "pinned host inputs in and out back every step; copies of neighbouring "
                        "steps overlap the kernels (2 buffer sets; input, compute and "
                        f"{n_out} read-back streams)"},
