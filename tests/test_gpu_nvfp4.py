@@ -285,3 +285,61 @@ def test_production_size_sampled_parity(handle, weight):
     assert bool((out.permute(1, 0, 2, 3, 4)[bad_d] == 0).all())
     assert bool(torch.isfinite(out).all())
     print("c3", len(tokens), st, st2, code_eq, sf_eq)
+
+
+def test_repacking_is_bit_identical_across_P(handle, weight):
+    """The pack is a pure relabelling: every P gives the same per-token values."""
+    w = make_nvfp4_workload("c2", 300)
+    d = _dev(w)
+    M = w.M
+    outs = {}
+    for P in (1, 2, 4, 8):
+        o = torch.empty((P, M, 56 // P, 3, 128), dtype=BF16, device="cuda")
+        run_stage(handle, w, d, weight, o, P=P)
+        outs[P] = o
+    torch.cuda.synchronize()
+    assert handle.device_status() == 0
+    base = outs[1][0]
+    for P in (2, 4, 8):
+        rep = outs[P].permute(1, 0, 2, 3, 4).reshape(M, 56, 3, 128)
+        assert torch.equal(rep.view(torch.int16), base.view(torch.int16)), P
+
+
+def test_guard_bands_untouched(handle, weight):
+    """Nothing is written outside out, act_q and act_sf (M = 200: a ragged
+    256-row tile and a ragged 128-row scale atom)."""
+    w = make_nvfp4_workload("c3", 200)
+    d = _dev(w)
+    M, P = w.M, w.base.spec.P
+    pad = 4096
+    n_out = M * 21504
+    nq = M * 2688
+    ns = binding.load().mh3_nvfp4_scales_bytes(M, 5376, 1)
+    obuf = torch.full((n_out + 2 * pad,), 7.0, dtype=BF16, device="cuda")
+    qbuf = torch.full((nq + 2 * pad,), 0xA5, dtype=torch.uint8, device="cuda")
+    sbuf = torch.full((ns + 2 * pad,), 0x5A, dtype=torch.uint8, device="cuda")
+    out = obuf[pad:pad + n_out].view(P, M, 56 // P, 3, 128)
+    act_q = qbuf[pad:pad + nq].view(M, 2688)
+    act_sf = sbuf[pad:pad + ns]
+    run_stage(handle, w, d, weight, out, act_q=act_q, act_sf=act_sf)
+    torch.cuda.synchronize()
+    assert handle.device_status() == 0
+    for b, v in ((obuf, 7.0), (qbuf, 0xA5), (sbuf, 0x5A)):
+        assert bool((b[:pad] == v).all()) and bool((b[-pad:] == v).all())
+    tokens = list(range(M))
+    got = oracle.ulysses_unpack_rows(out.cpu(), tokens)
+    aq, asf = act_q.cpu(), untile(act_sf.cpu(), M, 5376)
+    st = check_outputs(got, oracle_tail(w, weight, aq, asf, tokens), "nvfp4 guard-band case")
+    assert st["exact"] > 0.99, st
+
+
+def test_zero_tokens_is_a_no_op(handle, weight):
+    w = make_nvfp4_workload("c0")
+    d = _dev(w)
+    empty = torch.empty(0, dtype=BF16, device="cuda")
+    binding.mh3_nvfp4_preattn_run(
+        handle, None, 0, None, d["xw"], d["sc"], d["sc"].stride(0), d["sh"], d["sh"].stride(0),
+        d["sc"].shape[0], None, weight["q_dev"], weight["sf_dev"], weight["gs"], None, None,
+        d["qw"], d["kw"], d["cs"], 1, w.eps, None, None, None, empty)
+    torch.cuda.synchronize()
+    assert handle.device_status() == 0
