@@ -202,8 +202,9 @@ int mh3_preattn_qkv(mh3_preattn_t handle, void* stream, int64_t M, const mh3_bf1
                     const int64_t* rope_positions, int P, float qk_eps, mh3_bf16* out);
 
 /* Test hook for failure detection: when `stall` is nonzero, the next launch
- * of the CTA-pair QKV GEMM through this handle (mh3_preattn_run or
- * mh3_preattn_qkv with M > 128) issues no operand loads.  Its consumers'
+ * of a CTA-pair QKV GEMM through this handle (mh3_preattn_run or
+ * mh3_preattn_qkv with M > 128, or the NVFP4 GEMM of mh3_nvfp4_preattn_run
+ * or mh3_nvfp4_qkv) issues no operand loads.  Its consumers'
  * bounded waits then run out (about 2 s), the kernel records a nonzero code
  * in the device status word, drains and returns: the launch completes and the
  * context stays usable; `out` is not written.  The flag clears itself after

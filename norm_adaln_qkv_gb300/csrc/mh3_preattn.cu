@@ -42,7 +42,7 @@ struct mh3_preattn_ctx {
   size_t act_q_bytes = 0;
   void* act_sf = nullptr;
   size_t act_sf_bytes = 0;
-  int test_stall_next = 0;  // test hook for the next CTA-pair QKV GEMM launch
+  int test_stall_next = 0;  // test hook for the next CTA-pair QKV GEMM launch (bf16 or NVFP4)
 };
 
 namespace {
@@ -710,6 +710,8 @@ int launch_fp4_gemm(mh3_preattn_ctx* h, cudaStream_t s, int64_t M, const uint8_t
   p.alpha = alpha_given ? alpha : -1.0f;
   p.act_gs = act_global_scale;
   p.w_gs = weight_global_scale;
+  p.test_stall = h->test_stall_next;  // test hook: consumed by this launch
+  h->test_stall_next = 0;
   const int clusters = p.num_tiles < max_clusters ? p.num_tiles : max_clusters;
   cudaError_t e = launch_nvfp4_qkv(maps, p, clusters, e4m3, s);
   if (e != cudaSuccess) return cuda_fail(e, "NVFP4 GEMM launch");

@@ -56,3 +56,57 @@ def test_stalled_gemm_reports_a_status_code_and_the_next_call_is_correct(cuda_li
     finally:
         torch.cuda.synchronize()
         h.close()
+
+
+def test_stalled_nvfp4_gemm_reports_a_status_code_and_the_next_call_is_correct(cuda_lib):
+    """The same for the NVFP4 GEMM (12 warps with a register split, scale-copy
+    warps): every role gives up through a bounded wait and the CTA pair
+    exits cleanly."""
+    from norm_adaln_qkv_gb300.inputs import make_nvfp4_workload
+    h = binding.Handle(torch.cuda.current_device())
+    try:
+        w = make_nvfp4_workload("c2", 300)
+        b = w.base
+        M, P = w.M, b.spec.P
+        dev = "cuda"
+        mod = b.adaln_mod.to(dev)
+        sc, sh = b.table_views(mod)
+        gsa = torch.tensor([w.act_global_scale], dtype=torch.float32, device=dev)
+        gsw = torch.tensor([w.weight_global_scale], dtype=torch.float32, device=dev)
+        lib = binding.load()
+        wq = torch.empty(21504, 2688, dtype=torch.uint8, device=dev)
+        wsf = torch.empty(lib.mh3_nvfp4_scales_bytes(21504, 5376, 1), dtype=torch.uint8, device=dev)
+        binding.mh3_nvfp4_quantize(None, b.qkv_weight.to(dev), gsw, wq, wsf, True)
+        aq = torch.empty(M, 2688, dtype=torch.uint8, device=dev)
+        asf = torch.empty(lib.mh3_nvfp4_scales_bytes(M, 5376, 1), dtype=torch.uint8, device=dev)
+        binding.mh3_nvfp4_norm_quant(h, None, M, b.x.to(dev), b.x_norm_weight.to(dev), sc,
+                                     sc.stride(0), sh, sh.stride(0), sc.shape[0],
+                                     w.adaln_index.to(dev), w.eps, gsa, aq, asf, True)
+        torch.cuda.synchronize()
+        assert h.device_status() == 0
+        qw, kw, cs = b.q_norm_weight.to(dev), b.k_norm_weight.to(dev), w.rope_cos_sin.to(dev)
+
+        def gemm(o):
+            binding.mh3_nvfp4_qkv(h, None, M, aq, asf, wq, wsf, w.weight_global_scale, gsa, None,
+                                  qw, kw, cs, P, w.eps, None, o)
+        good = torch.empty((P, M, 56 // P, 3, 128), dtype=torch.bfloat16, device=dev)
+        gemm(good)  # a normal launch (its parity is covered by the NVFP4 tests)
+        torch.cuda.synchronize()
+        assert h.device_status() == 0
+        out = torch.full((P, M, 56 // P, 3, 128), 7.0, dtype=torch.bfloat16, device=dev)
+        h.set_test_stall(True)
+        t0 = time.time()
+        gemm(out)
+        torch.cuda.synchronize()
+        elapsed = time.time() - t0
+        code = h.device_status()
+        assert code in STALL_CODES, hex(code)
+        assert 1.5 < elapsed < 30.0, elapsed          # the 2 s limit, not a hang
+        assert bool((out == 7.0).all())               # nothing was stored
+        gemm(out)
+        torch.cuda.synchronize()
+        assert h.device_status() == 0
+        assert torch.equal(out.view(torch.int16), good.view(torch.int16))
+    finally:
+        torch.cuda.synchronize()
+        h.close()
