@@ -335,9 +335,12 @@ def run_ours(args, world, rank, local):
         torch.cuda.synchronize()
         t1 = [e[0].elapsed_time(e[1]) for e in ev]
         t2 = [e[1].elapsed_time(e[2]) for e in ev]
+        breakdown.medians = (statistics.median(t1), statistics.median(t2),
+                             statistics.median(a + b for a, b in zip(t1, t2)))
         return sum(t1) / n, sum(t2) / n
 
     k1_ms, k2_ms = breakdown(wl, d, args.steps)
+    k1_med, k2_med, pair_med = breakdown.medians
 
     # kernel 1 alone, back to back (no GEMM between launches)
     a0, a1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
@@ -675,6 +678,10 @@ def run_ours(args, world, rank, local):
         "kernels_us": {"k1_norm_adaln": k1_ms * 1e3, "k2_qkv_gemm": k2_ms * 1e3,
                        "k1_norm_adaln_alone": k1_first_ms * 1e3,
                        "k1_norm_adaln_alone_after_gemm": k1_alone_ms * 1e3},
+        "kernels_us_median": {"k1_norm_adaln": k1_med * 1e3, "k2_qkv_gemm": k2_med * 1e3,
+                              "k1_plus_k2": pair_med * 1e3,
+                              "timed": f"median of {args.steps} calls, CUDA events around each "
+                                       "kernel on the launching stream"},
         "roofline": {"bound": "tensor", "achieved": k2_tflops, "peak": peaks["bf16"],
                      "unit": "TFLOP/s", "frac": k2_tflops / peaks["bf16"],
                      "traffic": _k2_traffic(M),
