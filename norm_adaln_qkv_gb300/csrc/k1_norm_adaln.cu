@@ -18,9 +18,11 @@
 // one fixed order by every thread.  r = 1 / sqrt(ss/H + eps) uses IEEE
 // division and square root; the elementwise steps are packed two-lane FP32
 // operations (each lane one IEEE round-to-nearest operation, in the
-// formula's order; the one fused multiply-add computes shift + n * g, whose
-// product is exact) and one bf16x2 add for bf16(1 + scale).  The guard is an int64 compare: a bad index writes +0.0
-// and never forms a table address.  Workspace stores keep the default
+// formula's order) and one bf16x2 add for bf16(1 + scale).  The squares and
+// shift + n * g (whose product is exact) are fused multiply-adds that take
+// their bf16 operands directly (fma.rn.f32.bf16: exact widening, one
+// rounding), which saves the unpacking instructions.  The guard is an int64
+// compare: a bad index writes +0.0 and never forms a table address.  Workspace stores keep the default
 // write-back policy so the GEMM that follows finds the rows in L2 when they
 // fit.  The ring wait is bounded (2 s) and records a status code instead of
 // hanging.
@@ -81,7 +83,7 @@ __device__ __forceinline__ uint32_t adaln_pair(uint64_t x2, uint32_t w, uint32_t
   // a = bf16(shift + n * g).  n and g are bf16, so n * g (at most 16
   // significant bits) is exact in FP32 and one fused multiply-add rounds
   // exactly as the multiply followed by the rounded add.
-  return f2_to_bf16x2(f2_fma(f2_from_bf16x2(n), f2_from_bf16x2(g), f2_from_bf16x2(sh)));
+  return pack_bf16x2(fma_bf16_lo(n, g, bf16_lo(sh)), fma_bf16_hi(n, g, bf16_hi(sh)));
 }
 
 // NVFP4 outputs of one 8-element chunk c of row m (a in `o`): the block of
@@ -147,22 +149,19 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm) norm_adaln_kernel(const 
 
     const uint32_t row = buf0 + s * kRowBytes;
     uint4 v[kVecPerThread];
-    uint64_t acc = 0;  // two FP32 partial sums (+0.0, +0.0)
+    float lo = 0.0f, hi = 0.0f;  // two FP32 partial sums
 #pragma unroll
     for (int j = 0; j < kVecPerThread; ++j) {
       v[j] = ld_shared_v4(row + 16 * (tid + kThreads * j));
-      // bf16 squares are exact in FP32, so the fused form equals mul-then-add
-      uint64_t q = f2_from_bf16x2(v[j].x);
-      acc = f2_fma(q, q, acc);
-      q = f2_from_bf16x2(v[j].y);
-      acc = f2_fma(q, q, acc);
-      q = f2_from_bf16x2(v[j].z);
-      acc = f2_fma(q, q, acc);
-      q = f2_from_bf16x2(v[j].w);
-      acc = f2_fma(q, q, acc);
+      lo = fma_bf16_lo(v[j].x, v[j].x, lo);
+      hi = fma_bf16_hi(v[j].x, v[j].x, hi);
+      lo = fma_bf16_lo(v[j].y, v[j].y, lo);
+      hi = fma_bf16_hi(v[j].y, v[j].y, hi);
+      lo = fma_bf16_lo(v[j].z, v[j].z, lo);
+      hi = fma_bf16_hi(v[j].z, v[j].z, hi);
+      lo = fma_bf16_lo(v[j].w, v[j].w, lo);
+      hi = fma_bf16_hi(v[j].w, v[j].w, hi);
     }
-    float lo, hi;
-    f2_unpack(acc, lo, hi);
     float ss = __fadd_rn(lo, hi);
 #pragma unroll
     for (int o = 16; o > 0; o >>= 1) ss = __fadd_rn(ss, __shfl_xor_sync(0xFFFFFFFFu, ss, o));

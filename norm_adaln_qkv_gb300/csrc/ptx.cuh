@@ -247,6 +247,21 @@ __device__ __forceinline__ uint32_t f2_to_bf16x2(uint64_t v) {
   asm("cvt.rn.bf16x2.f32 %0, %1, %2;" : "=r"(r) : "f"(hi), "f"(lo));
   return r;
 }
+// d = a * b + c with a, b the low (or high) bf16 halves of packed words
+// (exact widening) and c, d FP32: one IEEE fused multiply-add.
+__device__ __forceinline__ float fma_bf16_lo(uint32_t a, uint32_t b, float c) {
+  float d;
+  asm("{\n\t.reg .b16 a0, a1, b0, b1;\n\tmov.b32 {a0, a1}, %1;\n\tmov.b32 {b0, b1}, %2;\n\t"
+      "fma.rn.f32.bf16 %0, a0, b0, %3;\n\t}" : "=f"(d) : "r"(a), "r"(b), "f"(c));
+  return d;
+}
+__device__ __forceinline__ float fma_bf16_hi(uint32_t a, uint32_t b, float c) {
+  float d;
+  asm("{\n\t.reg .b16 a0, a1, b0, b1;\n\tmov.b32 {a0, a1}, %1;\n\tmov.b32 {b0, b1}, %2;\n\t"
+      "fma.rn.f32.bf16 %0, a1, b1, %3;\n\t}" : "=f"(d) : "r"(a), "r"(b), "f"(c));
+  return d;
+}
+
 // bf16x2 addition, each lane rounded once to bf16 (nearest-even).
 __device__ __forceinline__ uint32_t bf16x2_add(uint32_t a, uint32_t b) {
   uint32_t d;
