@@ -1,7 +1,7 @@
 """The stage is stream-ordered and allocation-free when the caller passes the
-workspaces, so it can be captured in a CUDA graph and replayed: the replayed
-outputs equal a direct call bit for bit (bf16 stage, e4m3 outputs and the
-NVFP4 stage)."""
+workspaces, or once the handle's own buffers have grown to the call's M, so
+it can be captured in a CUDA graph and replayed: the replayed outputs equal
+a direct call bit for bit (bf16 stage, e4m3 outputs and the NVFP4 stage)."""
 import pytest
 import torch
 
@@ -106,3 +106,64 @@ def test_nvfp4_stage_replays_from_a_cuda_graph(handle):
     torch.cuda.synchronize()
     assert torch.equal(out.view(torch.int16), ref.view(torch.int16))
     assert handle.device_status() == 0
+
+
+def test_handle_workspace_is_capturable_once_grown(cuda_lib):
+    """With workspace NULL the handle's own buffer serves; once a call has
+    grown it to at least M, a captured call allocates nothing and replays
+    bit-identically (a fresh handle, so the first call does the growing)."""
+    h = binding.Handle(torch.cuda.current_device())
+    try:
+        wl = make_workload("c2", M=300)
+        d = to_device(wl)
+        ref = new_out(d.M, d.P)
+        run_stage(h, d, ref)  # grows the handle workspace to M
+        torch.cuda.synchronize()
+        out = new_out(d.M, d.P)
+        g = _capture_and_replay(lambda s: run_stage(h, d, out, stream=s))
+        out.fill_(0.0)
+        g.replay()
+        torch.cuda.synchronize()
+        assert torch.equal(out.view(torch.int16), ref.view(torch.int16))
+        assert h.device_status() == 0
+    finally:
+        torch.cuda.synchronize()
+        h.close()
+
+
+def test_nvfp4_handle_buffers_are_capturable_once_grown(cuda_lib):
+    h = binding.Handle(torch.cuda.current_device())
+    try:
+        w = make_nvfp4_workload("c2", 300)
+        b = w.base
+        mod = b.adaln_mod.cuda()
+        sc, sh = b.table_views(mod)
+        x, xw, idx = b.x.cuda(), b.x_norm_weight.cuda(), w.adaln_index.cuda()
+        qw, kw, cs = b.q_norm_weight.cuda(), b.k_norm_weight.cuda(), w.rope_cos_sin.cuda()
+        gsa = torch.tensor([w.act_global_scale], dtype=torch.float32, device="cuda")
+        gsw = torch.tensor([w.weight_global_scale], dtype=torch.float32, device="cuda")
+        lib = binding.load()
+        wq = torch.empty(21504, 2688, dtype=torch.uint8, device="cuda")
+        wsf = torch.empty(lib.mh3_nvfp4_scales_bytes(21504, 5376, 1), dtype=torch.uint8,
+                          device="cuda")
+        binding.mh3_nvfp4_quantize(None, b.qkv_weight.cuda(), gsw, wq, wsf, True)
+        M, P = w.M, b.spec.P
+
+        def call(out, stream):
+            binding.mh3_nvfp4_preattn_run(h, stream, M, x, xw, sc, sc.stride(0), sh, sh.stride(0),
+                                          sc.shape[0], idx, wq, wsf, w.weight_global_scale, gsa,
+                                          None, qw, kw, cs, P, w.eps, None, None, None, out)
+
+        ref = new_out(M, P)
+        call(ref, None)  # grows the handle's activation codes and scales
+        torch.cuda.synchronize()
+        out = new_out(M, P)
+        g = _capture_and_replay(lambda s: call(out, s))
+        out.fill_(0.0)
+        g.replay()
+        torch.cuda.synchronize()
+        assert torch.equal(out.view(torch.int16), ref.view(torch.int16))
+        assert h.device_status() == 0
+    finally:
+        torch.cuda.synchronize()
+        h.close()
