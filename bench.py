@@ -36,7 +36,7 @@ UNIT = "us/call"
 WORKLOAD = "c3"
 ALSO = "c2"
 SMALL_CALLS = 50
-E2E_PASSES = 3
+E2E_PASSES = 5
 FLOP_PER_TOKEN = 2 * 5376 * 21504
 # kernel 2 at the bench size is the CTA-pair form; its traffic figure is tied
 # to these sources
