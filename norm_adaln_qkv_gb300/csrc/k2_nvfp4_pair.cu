@@ -70,16 +70,24 @@ constexpr uint32_t kFSfCols = 48;              // per slot: A scales 16 + B scal
 #endif
 constexpr int kCpWarps = MH3_FP4_CP_WARPS;     // scale-copy warps of the even CTA
 constexpr int kFCopies = 12;                   // per k-block: 4 K steps x (A, B rows 0-127, 128-255)
-constexpr int kFWarps = 12;
-constexpr int kFThreads = kFWarps * 32;        // 384
+#ifndef MH3_FP4_WARPS
+#define MH3_FP4_WARPS 12
+#endif
+constexpr int kFWarps = MH3_FP4_WARPS;         // 12 (three warpgroups) or 16 (four)
+constexpr int kFThreads = kFWarps * 32;
 constexpr int kFEpiWarp0 = 4;                  // warpgroup 1
-constexpr int kRegsLaunch = 168;               // 65536 / 384, rounded down to 8
+constexpr int kRegsLaunch = (65536 / kFThreads) / 8 * 8;  // 168 (12 warps), 128 (16)
 constexpr int kRegsEpi = 256;
-constexpr int kRegsOther = 120;
-static_assert(kCpWarps == 4 || kCpWarps == 6, "copy warps: 8..11, plus 2..3");
+constexpr int kRegsOther = kFWarps == 12 ? 120 : 80;
+constexpr int kWgs = kFWarps / 4;
+static_assert(kFWarps == 12 || kFWarps == 16, "three or four warpgroups");
+static_assert(kCpWarps >= 4 && kCpWarps <= kFWarps - 6 && kCpWarps <= kFCopies,
+              "copy warps: 8.., plus 2..3");
 static_assert(kEpiWarps == 4 && kFEpiWarp0 % 4 == 0, "the epilogue is one whole warpgroup");
-static_assert(kRegsEpi + 2 * kRegsOther <= 3 * kRegsLaunch, "per sub-partition register budget");
-static_assert(128 * kRegsEpi + 256 * kRegsOther <= kFThreads * kRegsLaunch, "CTA register budget");
+static_assert(kRegsEpi + (kWgs - 1) * kRegsOther <= kWgs * kRegsLaunch,
+              "per sub-partition register budget");
+static_assert(128 * kRegsEpi + 128 * (kWgs - 1) * kRegsOther <= kFThreads * kRegsLaunch,
+              "CTA register budget");
 
 constexpr int kFOffA = 0;
 constexpr int kFOffB = kFOffA + kFStages * kFABytes;
@@ -255,7 +263,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kFThreads, 1)
     return;
   }
   setmaxnreg_dec<kRegsOther>();
-  const int cw = warp >= 8 ? warp - 8 : warp + 2;  // copy warp index: 8..11 -> 0..3, 2..3 -> 4..5
+  // copy warp index: 8.. -> 0.., then 2..3
+  const int cw = warp >= 8 ? warp - 8 : warp + (kFWarps - 8) - 2;
 
   if (warp == 0) {
     // ------------------------------------------------- producer (both CTAs)
