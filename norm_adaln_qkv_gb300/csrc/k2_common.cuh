@@ -134,20 +134,8 @@ __device__ __forceinline__ uint32_t stg_addr(uint32_t stg, int row, int chunk) {
 
 __device__ __forceinline__ float acc_to_y(uint32_t bits) { return round_bf16(__uint_as_float(bits)); }
 
-// y = bf16(acc), or bf16(RN(alpha * acc)) for a scaled (block-scaled FP4) accumulator.
-template <bool kScaled>
-__device__ __forceinline__ float acc_to_y_s(uint32_t bits, float alpha) {
-  return kScaled ? round_bf16(__fmul_rn(__uint_as_float(bits), alpha)) : acc_to_y(bits);
-}
-template <bool kScaled>
-__device__ __forceinline__ float acc_value(uint32_t bits, float alpha) {
-  return kScaled ? __fmul_rn(__uint_as_float(bits), alpha) : __uint_as_float(bits);
-}
-
-// V head: o = bf16(acc) (bf16(RN(alpha * acc)) when kScaled).
-template <bool kScaled = false>
-__device__ __forceinline__ void epi_v_head(uint32_t tcol, uint32_t stg, int lane,
-                                           float alpha = 1.0f) {
+// V head: o = bf16(acc).
+__device__ __forceinline__ void epi_v_head(uint32_t tcol, uint32_t stg, int lane) {
 #pragma unroll
   for (int c = 0; c < 4; ++c) {
     uint32_t v[32];
@@ -156,22 +144,19 @@ __device__ __forceinline__ void epi_v_head(uint32_t tcol, uint32_t stg, int lane
 #pragma unroll
     for (int g = 0; g < 4; ++g) {
       uint4 w;
-      w.x = pack_bf16x2(acc_value<kScaled>(v[8 * g + 0], alpha), acc_value<kScaled>(v[8 * g + 1], alpha));
-      w.y = pack_bf16x2(acc_value<kScaled>(v[8 * g + 2], alpha), acc_value<kScaled>(v[8 * g + 3], alpha));
-      w.z = pack_bf16x2(acc_value<kScaled>(v[8 * g + 4], alpha), acc_value<kScaled>(v[8 * g + 5], alpha));
-      w.w = pack_bf16x2(acc_value<kScaled>(v[8 * g + 6], alpha), acc_value<kScaled>(v[8 * g + 7], alpha));
+      w.x = pack_bf16x2(__uint_as_float(v[8 * g + 0]), __uint_as_float(v[8 * g + 1]));
+      w.y = pack_bf16x2(__uint_as_float(v[8 * g + 2]), __uint_as_float(v[8 * g + 3]));
+      w.z = pack_bf16x2(__uint_as_float(v[8 * g + 4]), __uint_as_float(v[8 * g + 5]));
+      w.w = pack_bf16x2(__uint_as_float(v[8 * g + 6]), __uint_as_float(v[8 * g + 7]));
       st_shared_v4(stg_addr(stg, lane, 4 * c + g), w);
     }
   }
 }
 
 // Two accumulator words -> the bf16-rounded projection y of both columns, as
-// packed FP32 (bf16(RN(alpha * acc)) when kScaled).
-template <bool kScaled>
-__device__ __forceinline__ uint64_t acc2_to_y2(uint32_t a, uint32_t b, uint64_t alpha2) {
-  uint64_t v = f2_pack(__uint_as_float(a), __uint_as_float(b));
-  if (kScaled) v = f2_mul(v, alpha2);
-  return f2_from_bf16x2(f2_to_bf16x2(v));
+// packed FP32.
+__device__ __forceinline__ uint64_t acc2_to_y2(uint32_t a, uint32_t b) {
+  return f2_from_bf16x2(f2_to_bf16x2(f2_pack(__uint_as_float(a), __uint_as_float(b))));
 }
 
 // Q or K head: RMSNorm over the 128 columns, rotation of [0, 96), pass-through
@@ -179,10 +164,8 @@ __device__ __forceinline__ uint64_t acc2_to_y2(uint32_t a, uint32_t b, uint64_t 
 // each lane is one IEEE round-to-nearest operation, in the order of the
 // formulas (sum of squares in four partial sums over d % 4, d increasing;
 // t = bf16((y * rr) * w); o = bf16(t_j c - t_{j+48} s), bf16(t_{j+48} c + t_j s)).
-template <bool kScaled = false>
 __device__ __forceinline__ void epi_qk_head(uint32_t tcol, uint32_t stg, int lane, const float* nw,
-                                            const uint4* cs_row, float qk_eps, float alpha = 1.0f) {
-  const uint64_t alpha2 = f2_pack(alpha, alpha);
+                                            const uint4* cs_row, float qk_eps) {
   auto nw2 = [&](int d) {
     const float2 w = *reinterpret_cast<const float2*>(nw + d);
     return f2_pack(w.x, w.y);
@@ -196,8 +179,8 @@ __device__ __forceinline__ void epi_qk_head(uint32_t tcol, uint32_t stg, int lan
     tmem_wait_ld();
 #pragma unroll
     for (int i = 0; i < 32; i += 4) {
-      const uint64_t y01 = acc2_to_y2<kScaled>(v[i], v[i + 1], alpha2);
-      const uint64_t y23 = acc2_to_y2<kScaled>(v[i + 2], v[i + 3], alpha2);
+      const uint64_t y01 = acc2_to_y2(v[i], v[i + 1]);
+      const uint64_t y23 = acc2_to_y2(v[i + 2], v[i + 3]);
       s01 = f2_fma(y01, y01, s01);
       s23 = f2_fma(y23, y23, s23);
     }
@@ -227,9 +210,9 @@ __device__ __forceinline__ void epi_qk_head(uint32_t tcol, uint32_t stg, int lan
       const uint64_t c2 = f2_from_bf16x2((&cv[i >> 3].x)[(i & 7) >> 1]);
       const uint64_t s2 = f2_from_bf16x2((&sv[i >> 3].x)[(i & 7) >> 1]);
       const uint64_t ta = f2_from_bf16x2(
-          f2_to_bf16x2(f2_mul(f2_mul(acc2_to_y2<kScaled>(lo[i], lo[i + 1], alpha2), rr2), nw2(j))));
+          f2_to_bf16x2(f2_mul(f2_mul(acc2_to_y2(lo[i], lo[i + 1]), rr2), nw2(j))));
       const uint64_t tb = f2_from_bf16x2(f2_to_bf16x2(
-          f2_mul(f2_mul(acc2_to_y2<kScaled>(hi[i], hi[i + 1], alpha2), rr2), nw2(j + kRopeHalf))));
+          f2_mul(f2_mul(acc2_to_y2(hi[i], hi[i + 1]), rr2), nw2(j + kRopeHalf))));
       o1[i >> 1] = f2_to_bf16x2(f2_sub(f2_mul(ta, c2), f2_mul(tb, s2)));
       o2[i >> 1] = f2_to_bf16x2(f2_add(f2_mul(tb, c2), f2_mul(ta, s2)));
     }
@@ -252,7 +235,7 @@ __device__ __forceinline__ void epi_qk_head(uint32_t tcol, uint32_t stg, int lan
       for (int e = 0; e < 4; ++e) {
         const int i = 8 * g + 2 * e;
         o[e] = f2_to_bf16x2(
-            f2_mul(f2_mul(acc2_to_y2<kScaled>(v[i], v[i + 1], alpha2), rr2), nw2(kRopeDims + i)));
+            f2_mul(f2_mul(acc2_to_y2(v[i], v[i + 1]), rr2), nw2(kRopeDims + i)));
       }
       st_shared_v4(stg_addr(stg, lane, 12 + g), make_uint4(o[0], o[1], o[2], o[3]));
     }
@@ -304,17 +287,17 @@ __device__ __forceinline__ const uint4* rope_row(const QkvParams& p, int64_t m, 
 //   m0        token row of the warp's first lane
 // The previous store from the staging buffer is waited for first; the new
 // one may still be in flight on return (bulk group of lane 0).
-template <bool kE4m3, bool kScaled = false>
+template <bool kE4m3>
 __device__ __forceinline__ void epilogue_head(uint32_t tcol, int lane, uint32_t stg,
                                               const float* nw_all, const QkvParams& p, int64_t m0,
-                                              int kind, int head, const uint4* cs_row, float alpha,
+                                              int kind, int head, const uint4* cs_row,
                                               const CUtensorMap* tm_out) {
   if (lane == 0) bulk_wait_group_read0();
   __syncwarp();
   if (kind == 2)
-    epi_v_head<kScaled>(tcol, stg, lane, alpha);
+    epi_v_head(tcol, stg, lane);
   else
-    epi_qk_head<kScaled>(tcol, stg, lane, nw_all + kind * kHeadDim, cs_row, p.qk_eps, alpha);
+    epi_qk_head(tcol, stg, lane, nw_all + kind * kHeadDim, cs_row, p.qk_eps);
   if (kE4m3) stage_to_e4m3(stg, lane, __ldg(p.descales + kind));
   fence_proxy_async_smem();
   __syncwarp();
@@ -448,7 +431,7 @@ __device__ __forceinline__ void epilogue_block(uint32_t tmem_acc, int quad, int 
   for (int j = 0; j < 2; ++j) {
     const uint32_t tcol = tmem_acc + (static_cast<uint32_t>(quad * 32) << 16) +
                           static_cast<uint32_t>(j * kHeadDim);
-    epilogue_head<kE4m3>(tcol, lane, stg, nw_all, p, m0, kind, head0 + j, cs_row, 1.0f, tm_out);
+    epilogue_head<kE4m3>(tcol, lane, stg, nw_all, p, m0, kind, head0 + j, cs_row, tm_out);
   }
 }
 
