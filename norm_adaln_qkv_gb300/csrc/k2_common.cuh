@@ -132,8 +132,6 @@ __device__ __forceinline__ uint32_t stg_addr(uint32_t stg, int row, int chunk) {
   return stg + half * kStgHalfBytes + row * 128 + ((c ^ (row & 7)) << 4);
 }
 
-__device__ __forceinline__ float acc_to_y(uint32_t bits) { return round_bf16(__uint_as_float(bits)); }
-
 // V head: o = bf16(acc).
 __device__ __forceinline__ void epi_v_head(uint32_t tcol, uint32_t stg, int lane) {
 #pragma unroll
