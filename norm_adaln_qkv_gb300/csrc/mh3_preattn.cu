@@ -650,6 +650,35 @@ int launch_fp4_stage1(cudaStream_t s, int num_sms, int* status, int64_t M, const
 }
 
 // Kernel 2 of the NVFP4 stage on filled act_q / act_sf (tiled) buffers.
+// The NVFP4 GEMM's arguments checked for any M: P, alpha (or the weight
+// global scale it is derived from), the quantised weight and the norm
+// weights.  *alpha_given reports whether alpha is used as given.
+int check_fp4_gemm_fixed(int P, float alpha, float weight_global_scale, const uint8_t* weight_q,
+                         const uint8_t* weight_sf, const mh3_bf16* q_norm_weight,
+                         const mh3_bf16* k_norm_weight, bool* alpha_given) {
+  if (!(P == 1 || P == 2 || P == 4 || P == 8))
+    return fail(MH3_ERR_INVALID_ARG, "P (ulysses_degree) must be 1, 2, 4 or 8 (got %d)", P);
+  *alpha_given = std::isfinite(alpha) && alpha > 0.0f;
+  if (!*alpha_given && !(std::isfinite(weight_global_scale) && weight_global_scale > 0.0f))
+    return fail(MH3_ERR_INVALID_ARG,
+                "without alpha, weight_global_scale must be finite and > 0 (alpha is derived)");
+  int rc;
+  if ((rc = check_ptr(weight_q, "qkv_weight_q", 16))) return rc;
+  if ((rc = check_ptr(weight_sf, "qkv_weight_sf", 16))) return rc;
+  if ((rc = check_ptr(q_norm_weight, "q_norm_weight", 2))) return rc;
+  if ((rc = check_ptr(k_norm_weight, "k_norm_weight", 2))) return rc;
+  return MH3_OK;
+}
+
+// The NVFP4 GEMM's per-token arguments, checked when M > 0.
+int check_fp4_gemm_rows(const mh3_bf16* rope_cos_sin, const void* out, const float* qkv_descale) {
+  int rc;
+  if ((rc = check_ptr(rope_cos_sin, "rope_cos_sin", 16))) return rc;
+  if ((rc = check_ptr(out, "out", 16))) return rc;
+  if (qkv_descale != nullptr && (rc = check_ptr(qkv_descale, "qkv_descale", 4))) return rc;
+  return MH3_OK;
+}
+
 int launch_fp4_gemm(mh3_preattn_ctx* h, cudaStream_t s, int64_t M, const uint8_t* act_q,
                     const uint8_t* act_sf, const uint8_t* weight_q, const uint8_t* weight_sf,
                     float weight_global_scale, const float* act_global_scale, float alpha,
@@ -790,20 +819,12 @@ extern "C" int mh3_nvfp4_preattn_run(
   rc = check_fp4_stage1(M, x, x_norm_weight, adaln_scale, scale_row_stride, adaln_shift,
                         shift_row_stride, rows, adaln_index, eps, act_global_scale);
   if (rc) return rc;
-  if (!(P == 1 || P == 2 || P == 4 || P == 8))
-    return fail(MH3_ERR_INVALID_ARG, "P (ulysses_degree) must be 1, 2, 4 or 8 (got %d)", P);
-  const bool alpha_given = std::isfinite(alpha) && alpha > 0.0f;
-  if (!alpha_given && !(std::isfinite(weight_global_scale) && weight_global_scale > 0.0f))
-    return fail(MH3_ERR_INVALID_ARG,
-                "without alpha, weight_global_scale must be finite and > 0 (alpha is derived)");
-  if ((rc = check_ptr(weight_q, "qkv_weight_q", 16))) return rc;
-  if ((rc = check_ptr(weight_sf, "qkv_weight_sf", 16))) return rc;
-  if ((rc = check_ptr(q_norm_weight, "q_norm_weight", 2))) return rc;
-  if ((rc = check_ptr(k_norm_weight, "k_norm_weight", 2))) return rc;
+  bool alpha_given = false;
+  if ((rc = check_fp4_gemm_fixed(P, alpha, weight_global_scale, weight_q, weight_sf, q_norm_weight,
+                                 k_norm_weight, &alpha_given)))
+    return rc;
   if (M == 0) return MH3_OK;
-  if ((rc = check_ptr(rope_cos_sin, "rope_cos_sin", 16))) return rc;
-  if ((rc = check_ptr(out, "out", 16))) return rc;
-  if (qkv_descale != nullptr && (rc = check_ptr(qkv_descale, "qkv_descale", 4))) return rc;
+  if ((rc = check_fp4_gemm_rows(rope_cos_sin, out, qkv_descale))) return rc;
   if (act_q != nullptr && (rc = check_ptr(act_q, "act_q", 16))) return rc;
   if (act_sf != nullptr && (rc = check_ptr(act_sf, "act_sf", 16))) return rc;
   cudaStream_t s = static_cast<cudaStream_t>(stream);
@@ -837,23 +858,15 @@ extern "C" int mh3_nvfp4_qkv(mh3_preattn_t h, void* stream, int64_t M, const uin
   if (rc) return rc;
   if ((rc = check_M(M))) return rc;
   if (!valid_eps(eps)) return fail(MH3_ERR_INVALID_ARG, "eps must be finite and > 0");
-  if (!(P == 1 || P == 2 || P == 4 || P == 8))
-    return fail(MH3_ERR_INVALID_ARG, "P (ulysses_degree) must be 1, 2, 4 or 8 (got %d)", P);
-  const bool alpha_given = std::isfinite(alpha) && alpha > 0.0f;
-  if (!alpha_given && !(std::isfinite(weight_global_scale) && weight_global_scale > 0.0f))
-    return fail(MH3_ERR_INVALID_ARG,
-                "without alpha, weight_global_scale must be finite and > 0 (alpha is derived)");
-  if ((rc = check_ptr(weight_q, "qkv_weight_q", 16))) return rc;
-  if ((rc = check_ptr(weight_sf, "qkv_weight_sf", 16))) return rc;
-  if ((rc = check_ptr(q_norm_weight, "q_norm_weight", 2))) return rc;
-  if ((rc = check_ptr(k_norm_weight, "k_norm_weight", 2))) return rc;
+  bool alpha_given = false;
+  if ((rc = check_fp4_gemm_fixed(P, alpha, weight_global_scale, weight_q, weight_sf, q_norm_weight,
+                                 k_norm_weight, &alpha_given)))
+    return rc;
   if (M == 0) return MH3_OK;
   if (!alpha_given && (rc = check_ptr(act_global_scale, "act_global_scale", 4))) return rc;
   if ((rc = check_ptr(act_q, "act_q", 16))) return rc;
   if ((rc = check_ptr(act_sf, "act_sf", 16))) return rc;
-  if ((rc = check_ptr(rope_cos_sin, "rope_cos_sin", 16))) return rc;
-  if ((rc = check_ptr(out, "out", 16))) return rc;
-  if (qkv_descale != nullptr && (rc = check_ptr(qkv_descale, "qkv_descale", 4))) return rc;
+  if ((rc = check_fp4_gemm_rows(rope_cos_sin, out, qkv_descale))) return rc;
   return launch_fp4_gemm(h, static_cast<cudaStream_t>(stream), M, act_q, act_sf, weight_q,
                          weight_sf, weight_global_scale, act_global_scale, alpha, alpha_given,
                          q_norm_weight, k_norm_weight, rope_cos_sin, P, eps, qkv_descale, out);
@@ -911,22 +924,7 @@ extern "C" int mh3_preattn_run_e4m3(
   QkvMaps maps;
   if ((rc = encode_2d(&maps.a, workspace, kHidden, M, 64, 128, "workspace"))) return rc;
   if ((rc = encode_2d(&maps.b, qkv_weight, kHidden, kQkvRows, 64, 128, "qkv_weight"))) return rc;
-  {
-    PFN_cuTensorMapEncodeTiled_v12000 enc = encode_fn();
-    if (enc == nullptr) return fail(MH3_ERR_CUDA, "cuTensorMapEncodeTiled entry point not found");
-    const int64_t slots = 3 * (kHeads / P);
-    const cuuint64_t dims[4] = {static_cast<cuuint64_t>(kHeadDim), static_cast<cuuint64_t>(slots),
-                                static_cast<cuuint64_t>(M), static_cast<cuuint64_t>(P)};
-    const cuuint64_t strides[3] = {static_cast<cuuint64_t>(kHeadDim),
-                                   static_cast<cuuint64_t>(slots) * kHeadDim,
-                                   static_cast<cuuint64_t>(M) * slots * kHeadDim};
-    const cuuint32_t box[4] = {128, 1, 32, 1};
-    const cuuint32_t unit[4] = {1, 1, 1, 1};
-    CUresult r = enc(&maps.out, CU_TENSOR_MAP_DATA_TYPE_UINT8, 4, out, dims, strides, box, unit,
-                     CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
-                     CU_TENSOR_MAP_L2_PROMOTION_NONE, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
-    if (r != CUDA_SUCCESS) return fail(MH3_ERR_CUDA, "tensor map (e4m3 out) failed: %d", (int)r);
-  }
+  if ((rc = encode_out_map(&maps.out, out, M, P, true))) return rc;
   QkvParams p;
   p.positions = rope_positions;
   p.cos_sin = reinterpret_cast<const __nv_bfloat16*>(rope_cos_sin);
