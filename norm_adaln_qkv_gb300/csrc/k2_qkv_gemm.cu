@@ -31,54 +31,78 @@ using namespace k2;
 
 constexpr int BM = 128;
 constexpr int BN = kTileN;
-constexpr int kStages = 4;
 #ifndef MH3_GROUP_M
 #define MH3_GROUP_M 16
 #endif
 constexpr int kGroupM = MH3_GROUP_M;
-constexpr int kABytes = BM * BK * 2;  // 16 KB
-constexpr int kBBytes = BN * BK * 2;  // 32 KB
-constexpr int kStageBytes = kABytes + kBBytes;
 constexpr int kThreads = 64 + kEpiWarps * 32;  // 192
 constexpr uint32_t kIdesc = idesc_bf16_f32(BM, BN);
 
-// Shared-memory layout (offsets from a 1024-B aligned base).
-constexpr int kOffA = 0;
-constexpr int kOffB = kOffA + kStages * kABytes;
-constexpr int kOffStg = kOffB + kStages * kBBytes;
-constexpr int kOffBar = kOffStg + kEpiWarps * kStgWarpBytes;
-constexpr int kNumBars = 2 * kStages + 4 + 1;  // full, empty, tmem full x2, tmem empty x2, drain
-constexpr int kOffTmemPtr = kOffBar + kNumBars * 8;
-constexpr int kOffAbort = kOffTmemPtr + 4;
-constexpr int kOffNormW = kOffBar + 256;  // 256 floats: q weights then k weights
-constexpr int kSmemUsed = kOffNormW + 2 * kHeadDim * 4;
-constexpr int kSmemAlloc = kSmemUsed + 1024;  // slack for aligning the base
-static_assert(kOffAbort + 4 <= kOffNormW, "barrier block overflow");
-static_assert(kSmemAlloc <= 232448, "exceeds the 227 KB per-CTA limit");
+// Shared-memory layout (offsets from a 1024-B aligned base) for a ring of
+// kStagesT stages whose A box holds kARowsT workspace rows.  The MMA always
+// reads 128 A rows from a stage's A address; with kARowsT < 128 (the tiny-M
+// layout, M <= kARowsT) the rows past the box lie in the following stages'
+// A regions or in the B region, hold stale data, and produce accumulator
+// rows >= M, which are never stored.  The shared memory freed this way buys
+// one more stage of weight in flight.
+template <int kStagesT, int kARowsT>
+struct Layout {
+  static constexpr int kStages = kStagesT;
+  static constexpr int kARows = kARowsT;
+  static constexpr int kABytes = kARowsT * BK * 2;
+  static constexpr int kBBytes = BN * BK * 2;  // 32 KB
+  static constexpr int kStageBytes = kABytes + kBBytes;
+  static constexpr int kOffA = 0;
+  static constexpr int kOffB = kOffA + kStages * kABytes;
+  static constexpr int kOffStg = kOffB + kStages * kBBytes;
+  static constexpr int kOffBar = kOffStg + kEpiWarps * kStgWarpBytes;
+  // full, empty, tmem full x2, tmem empty x2, drain
+  static constexpr int kNumBars = 2 * kStages + 4 + 1;
+  static constexpr int kOffTmemPtr = kOffBar + kNumBars * 8;
+  static constexpr int kOffAbort = kOffTmemPtr + 4;
+  static constexpr int kOffNormW = kOffBar + 256;  // 256 floats: q weights then k weights
+  static constexpr int kSmemUsed = kOffNormW + 2 * kHeadDim * 4;
+  static constexpr int kSmemAlloc = kSmemUsed + 1024;  // slack for aligning the base
+  static_assert(kOffAbort + 4 <= kOffNormW, "barrier block overflow");
+  static_assert(kSmemAlloc <= 232448, "exceeds the 227 KB per-CTA limit");
+  static_assert(kARowsT % 8 == 0 && kARowsT <= BM, "A box: whole 8-row swizzle atoms");
+  static_assert(kOffA + (kStages - 1) * kABytes + BM * BK * 2 <= kSmemUsed,
+                "the MMA's 128-row A reads stay inside the allocation");
+};
+using FullLayout = Layout<4, BM>;  // M <= 128
+using TinyLayout = Layout<5, 16>;  // M <= 16
+constexpr int kTinyRows = TinyLayout::kARows;
 
+template <class L>
 struct Smem {
   uint32_t base;  // shared address of the aligned base
   uint8_t* ptr;
-  __device__ uint32_t a(int s) const { return base + kOffA + s * kABytes; }
-  __device__ uint32_t b(int s) const { return base + kOffB + s * kBBytes; }
-  __device__ uint32_t full(int s) const { return base + kOffBar + s * 8; }
-  __device__ uint32_t empty(int s) const { return base + kOffBar + (kStages + s) * 8; }
-  __device__ uint32_t tfull(int b) const { return base + kOffBar + (2 * kStages + b) * 8; }
-  __device__ uint32_t tempty(int b) const { return base + kOffBar + (2 * kStages + 2 + b) * 8; }
-  __device__ uint32_t drain() const { return base + kOffBar + (2 * kStages + 4) * 8; }
-  __device__ uint32_t stg(int ew) const { return base + kOffStg + ew * kStgWarpBytes; }
-  __device__ uint32_t* tmem_ptr() const { return reinterpret_cast<uint32_t*>(ptr + kOffTmemPtr); }
-  __device__ volatile int* abort_flag() const {
-    return reinterpret_cast<volatile int*>(ptr + kOffAbort);
+  __device__ uint32_t a(int s) const { return base + L::kOffA + s * L::kABytes; }
+  __device__ uint32_t b(int s) const { return base + L::kOffB + s * L::kBBytes; }
+  __device__ uint32_t full(int s) const { return base + L::kOffBar + s * 8; }
+  __device__ uint32_t empty(int s) const { return base + L::kOffBar + (L::kStages + s) * 8; }
+  __device__ uint32_t tfull(int b) const { return base + L::kOffBar + (2 * L::kStages + b) * 8; }
+  __device__ uint32_t tempty(int b) const {
+    return base + L::kOffBar + (2 * L::kStages + 2 + b) * 8;
   }
-  __device__ float* norm_w() const { return reinterpret_cast<float*>(ptr + kOffNormW); }
+  __device__ uint32_t drain() const { return base + L::kOffBar + (2 * L::kStages + 4) * 8; }
+  __device__ uint32_t stg(int ew) const { return base + L::kOffStg + ew * kStgWarpBytes; }
+  __device__ uint32_t* tmem_ptr() const {
+    return reinterpret_cast<uint32_t*>(ptr + L::kOffTmemPtr);
+  }
+  __device__ volatile int* abort_flag() const {
+    return reinterpret_cast<volatile int*>(ptr + L::kOffAbort);
+  }
+  __device__ float* norm_w() const { return reinterpret_cast<float*>(ptr + L::kOffNormW); }
 };
 
+template <class L>
 __global__ void __launch_bounds__(kThreads, 1)
     qkv_gemm_kernel(const __grid_constant__ CUtensorMap tm_a, const __grid_constant__ CUtensorMap tm_b,
                     const __grid_constant__ CUtensorMap tm_out, const QkvParams p) {
   extern __shared__ uint8_t smem_raw[];
-  Smem sm;
+  constexpr int kStages = L::kStages;
+  Smem<L> sm;
   {
     const uint32_t raw = smem_u32(smem_raw);
     sm.base = (raw + 1023u) & ~1023u;
@@ -135,7 +159,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             ok = false;
             break;
           }
-          mbar_arrive_expect_tx(sm.full(stage), kStageBytes);
+          mbar_arrive_expect_tx(sm.full(stage), L::kStageBytes);
           tma_load_2d(sm.a(stage), &tm_a, sm.full(stage), kb * BK, m_blk * BM);
           tma_load_2d(sm.b(stage), &tm_b, sm.full(stage), kb * BK, n_blk * BN);
           issued_mask |= 1u << stage;
@@ -233,16 +257,30 @@ __global__ void __launch_bounds__(kThreads, 1)
 
 }  // namespace
 
-int qkv_smem_bytes() { return kSmemAlloc; }
+int qkv_smem_bytes() {
+  return FullLayout::kSmemAlloc > TinyLayout::kSmemAlloc ? FullLayout::kSmemAlloc
+                                                         : TinyLayout::kSmemAlloc;
+}
+
+int qkv_a_box_rows(int64_t M) { return M <= kTinyRows ? kTinyRows : BM; }
 
 cudaError_t qkv_prepare_device() {
-  return cudaFuncSetAttribute(qkv_gemm_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                              kSmemAlloc);
+  cudaError_t e = cudaFuncSetAttribute(qkv_gemm_kernel<FullLayout>,
+                                       cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                       FullLayout::kSmemAlloc);
+  if (e != cudaSuccess) return e;
+  return cudaFuncSetAttribute(qkv_gemm_kernel<TinyLayout>,
+                              cudaFuncAttributeMaxDynamicSharedMemorySize, TinyLayout::kSmemAlloc);
 }
 
 cudaError_t launch_qkv(const QkvMaps& maps, const QkvParams& p, int grid, cudaStream_t stream) {
   if (p.M <= 0) return cudaSuccess;
-  return launch_k2(qkv_gemm_kernel, grid, kThreads, kSmemAlloc, stream, maps, p);
+  // the A map's box height must be qkv_a_box_rows(p.M)
+  if (p.M <= kTinyRows)
+    return launch_k2(qkv_gemm_kernel<TinyLayout>, grid, kThreads, TinyLayout::kSmemAlloc, stream,
+                     maps, p);
+  return launch_k2(qkv_gemm_kernel<FullLayout>, grid, kThreads, FullLayout::kSmemAlloc, stream,
+                   maps, p);
 }
 
 }  // namespace mh3

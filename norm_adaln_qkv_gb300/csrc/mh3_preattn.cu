@@ -21,6 +21,12 @@
 #include "mh3_preattn.h"
 #include "common.cuh"
 
+namespace mh3 {
+// Workspace rows per stage of the single-CTA GEMM's A box for this M (its
+// tiny-M ring loads fewer rows); defined with that kernel.
+int qkv_a_box_rows(int64_t M);
+}  // namespace mh3
+
 using namespace mh3;
 
 struct mh3_preattn_ctx {
@@ -159,14 +165,14 @@ PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
 }
 
 int encode_maps(QkvMaps& maps, int64_t M, const mh3_bf16* ws, const mh3_bf16* W, int P,
-                mh3_bf16* out, unsigned b_box_rows) {
+                mh3_bf16* out, unsigned b_box_rows, unsigned a_box_rows) {
   PFN_cuTensorMapEncodeTiled_v12000 enc = encode_fn();
   if (enc == nullptr) return fail(MH3_ERR_CUDA, "cuTensorMapEncodeTiled entry point not found");
   const cuuint32_t unit[4] = {1, 1, 1, 1};
   {
     const cuuint64_t dims[2] = {static_cast<cuuint64_t>(kHidden), static_cast<cuuint64_t>(M)};
     const cuuint64_t strides[1] = {static_cast<cuuint64_t>(kHidden) * 2};
-    const cuuint32_t box[2] = {64, 128};
+    const cuuint32_t box[2] = {64, a_box_rows};
     CUresult r = enc(&maps.a, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<mh3_bf16*>(ws), dims,
                      strides, box, unit, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
                      CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
@@ -263,7 +269,8 @@ int launch_stage2(cudaStream_t s, int num_sms, int max_clusters, int* status, in
                   mh3_bf16* out, int* test_stall = nullptr) {
   const bool pair = M > 128 && max_clusters > 0;
   QkvMaps maps;
-  int rc = encode_maps(maps, M, ws, W, P, out, pair ? 128u : 256u);
+  int rc = encode_maps(maps, M, ws, W, P, out, pair ? 128u : 256u,
+                       pair ? 128u : static_cast<unsigned>(qkv_a_box_rows(M)));
   if (rc) return rc;
   QkvParams p;
   p.positions = pos;
