@@ -40,11 +40,11 @@ constexpr uint32_t kIdesc = idesc_bf16_f32(BM, BN);
 
 // Shared-memory layout (offsets from a 1024-B aligned base) for a ring of
 // kStagesT stages whose A box holds kARowsT workspace rows.  The MMA always
-// reads 128 A rows from a stage's A address; with kARowsT < 128 (the tiny-M
-// layout, M <= kARowsT) the rows past the box lie in the following stages'
-// A regions or in the B region, hold stale data, and produce accumulator
-// rows >= M, which are never stored.  The shared memory freed this way buys
-// one more stage of weight in flight.
+// reads 128 A rows from a stage's A address; with kARowsT < 128 (the small-
+// and tiny-M layouts, M <= kARowsT) the rows past the box lie in the
+// following stages' A regions or in the B region, hold stale data, and
+// produce accumulator rows >= M, which are never stored.  The shared memory
+// freed this way buys one more stage of weight in flight.
 template <int kStagesT, int kARowsT>
 struct Layout {
   static constexpr int kStages = kStagesT;
@@ -65,13 +65,15 @@ struct Layout {
   static constexpr int kSmemAlloc = kSmemUsed + 1024;  // slack for aligning the base
   static_assert(kOffAbort + 4 <= kOffNormW, "barrier block overflow");
   static_assert(kSmemAlloc <= 232448, "exceeds the 227 KB per-CTA limit");
-  static_assert(kARowsT % 8 == 0 && kARowsT <= BM, "A box: whole 8-row swizzle atoms");
+  static_assert(kARows % 8 == 0 && kARows <= BM, "A box: whole 8-row swizzle atoms");
   static_assert(kOffA + (kStages - 1) * kABytes + BM * BK * 2 <= kSmemUsed,
                 "the MMA's 128-row A reads stay inside the allocation");
 };
-using FullLayout = Layout<4, BM>;  // M <= 128
-using TinyLayout = Layout<5, 16>;  // M <= 16
+using FullLayout = Layout<4, BM>;   // M <= 128
+using SmallLayout = Layout<5, 48>;  // M <= 48
+using TinyLayout = Layout<5, 16>;   // M <= 16
 constexpr int kTinyRows = TinyLayout::kARows;
+constexpr int kSmallRows = SmallLayout::kARows;
 
 template <class L>
 struct Smem {
@@ -258,16 +260,23 @@ __global__ void __launch_bounds__(kThreads, 1)
 }  // namespace
 
 int qkv_smem_bytes() {
-  return FullLayout::kSmemAlloc > TinyLayout::kSmemAlloc ? FullLayout::kSmemAlloc
-                                                         : TinyLayout::kSmemAlloc;
+  int m = FullLayout::kSmemAlloc;
+  if (SmallLayout::kSmemAlloc > m) m = SmallLayout::kSmemAlloc;
+  if (TinyLayout::kSmemAlloc > m) m = TinyLayout::kSmemAlloc;
+  return m;
 }
 
-int qkv_a_box_rows(int64_t M) { return M <= kTinyRows ? kTinyRows : BM; }
+int qkv_a_box_rows(int64_t M) {
+  return M <= kTinyRows ? kTinyRows : (M <= kSmallRows ? kSmallRows : BM);
+}
 
 cudaError_t qkv_prepare_device() {
   cudaError_t e = cudaFuncSetAttribute(qkv_gemm_kernel<FullLayout>,
                                        cudaFuncAttributeMaxDynamicSharedMemorySize,
                                        FullLayout::kSmemAlloc);
+  if (e != cudaSuccess) return e;
+  e = cudaFuncSetAttribute(qkv_gemm_kernel<SmallLayout>,
+                           cudaFuncAttributeMaxDynamicSharedMemorySize, SmallLayout::kSmemAlloc);
   if (e != cudaSuccess) return e;
   return cudaFuncSetAttribute(qkv_gemm_kernel<TinyLayout>,
                               cudaFuncAttributeMaxDynamicSharedMemorySize, TinyLayout::kSmemAlloc);
@@ -278,6 +287,9 @@ cudaError_t launch_qkv(const QkvMaps& maps, const QkvParams& p, int grid, cudaSt
   // the A map's box height must be qkv_a_box_rows(p.M)
   if (p.M <= kTinyRows)
     return launch_k2(qkv_gemm_kernel<TinyLayout>, grid, kThreads, TinyLayout::kSmemAlloc, stream,
+                     maps, p);
+  if (p.M <= kSmallRows)
+    return launch_k2(qkv_gemm_kernel<SmallLayout>, grid, kThreads, SmallLayout::kSmemAlloc, stream,
                      maps, p);
   return launch_k2(qkv_gemm_kernel<FullLayout>, grid, kThreads, FullLayout::kSmemAlloc, stream,
                    maps, p);

@@ -37,7 +37,8 @@ def _unpacked(out, tokens):
 
 # ----------------------------------------------------------- every token
 @pytest.mark.parametrize("key,M", [("c0", None), ("c1", None), ("c2", None),
-                                   ("c2", 300), ("c2", 129), ("c3", 127), ("c0", 1)])
+                                   ("c2", 300), ("c2", 129), ("c3", 127), ("c0", 1),
+                                   ("c3", 40), ("c2", 17)])
 def test_full_parity(handle, key, M):
     wl = make_workload(key, M=M)
     d = to_device(wl)
