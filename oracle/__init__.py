@@ -5,17 +5,23 @@ CPU-baseline / reference arm may import this package.  The product path (the
 CUDA library and its Python binding) never imports, calls or links it, and
 the oracle shares no code with the CUDA path.
 
-Plain, slow, shape-generic PyTorch CPU code: FP32 elementwise steps with the
-BF16 rounding points the pages name, and float64 reductions rounded once to
-FP32 (the ideal FP32 accumulator; the pages fix FP32 accumulation but no
-summation order).
+The stage's oracle is plain C++ (``cpp/mh3_oracle.cpp``, compiled by
+``build.py`` with g++, loaded by ``stage.py``): FP32 elementwise steps with
+the BF16 rounding points the pages name, exact sums of squares rounded once
+to FP32, and a double-accumulated QKV dot product rounded once to FP32.
+``preattn.py`` restates the same steps in PyTorch CPU ops; every pin runs on
+both and the two agree bit for bit.  The neighbouring operations (output
+projection, MLP block, e4m3 and NVFP4 outputs) are PyTorch CPU restatements
+that call the C++ steps they share with the stage.
 
 Pins: every function is pinned by tests that do not re-type its formula
 (closed forms, library routines for special cases, exact integer arithmetic,
-invariants).  No function here is "parity unpinned".
+invariants, and a float64 brute-force recomputation of the whole stage on
+tiny inputs).  No function here is "parity unpinned".
 """
-from .preattn import (  # noqa: F401
+from .stage import (  # noqa: F401
     input_rmsnorm,
+    rmsnorm_apply,
     indexed_adaln,
     qkv_projection,
     head_rmsnorm,
@@ -27,6 +33,7 @@ from .preattn import (  # noqa: F401
     pre_attention,
     PreAttnTokens,
 )
+from . import preattn  # noqa: F401  (PyTorch restatement of the same steps)
 from . import out_proj  # noqa: F401  (attention output projection + gated residual)
 from . import mlp  # noqa: F401  (MLP block)
 from . import e4m3  # noqa: F401  (e4m3 output mode)

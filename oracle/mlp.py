@@ -24,7 +24,7 @@ from __future__ import annotations
 import torch
 
 from .out_proj import gated_residual, out_projection
-from .preattn import indexed_adaln, input_rmsnorm
+from .stage import indexed_adaln, input_rmsnorm
 
 F32 = torch.float32
 F64 = torch.float64

@@ -31,8 +31,8 @@ from typing import Optional, Sequence
 
 import torch
 
-from .preattn import (PreAttnTokens, head_rmsnorm, indexed_adaln, input_rmsnorm,
-                      rope_split_half)
+from .stage import (PreAttnTokens, head_rmsnorm, indexed_adaln, input_rmsnorm,
+                    rope_split_half)
 
 F32 = torch.float32
 F64 = torch.float64

@@ -4,14 +4,10 @@ device, running the stage through the C ABI, and the comparison rules.
 Tolerances (flashinfer.diffusion_ops.minimax_h3_bf16_pre_attention outputs):
 * q/k/v: |gpu - ref| <= 2e-2 * |ref| + 2e-2 elementwise and mean |gpu - ref|
   <= 2e-3 over the compared elements;
-* the bf16 workspace a: within 1 bf16 ulp of the oracle, widened only where
-  the FP32 sum of squares (whose summation order the pages leave open) moves
-  n across a bf16 rounding boundary.  Such a flip changes n by at most
-  u_n = ulp(n_ref), so shift + n*g moves by at most |g|*u_n (g = bf16(1 +
-  scale[i])), and rounding both sides to bf16 adds half an ulp of each
-  result: |gpu - ref| <= |g|*u_n + ulp(a_ref)/2 + ulp(|a_ref| + |g|*u_n)/2.
-  Without a flip the two sides run the same FP32 operations, so nearly
-  every element must be bit-exact and all but a handful within 1 ulp;
+* the bf16 workspace a: every row bit-exact, or bit-exact against the
+  oracle's own norm and AdaLN evaluated with an r = 1/sqrt(ss/H + eps) a few
+  FP32 steps from the oracle's (the only freedom: the pages fix the type of
+  the sum of squares, not its order); see check_workspace;
 * guard rows, clamped positions and the pack are compared bit for bit (zero
   rows by value, since +0 and -0 are both the zero the guard asks for).
 """
@@ -122,30 +118,61 @@ def check_outputs(gpu_tok: torch.Tensor, ref_tok: torch.Tensor, what: str) -> di
     return stats
 
 
+def _nudge(r: float, k: int) -> float:
+    """The FP32 value k representable steps away from r (r > 0)."""
+    b = torch.tensor([r], dtype=torch.float32).view(torch.int32) + k
+    return float(b.view(torch.float32))
+
+
 def check_workspace(gpu_a: torch.Tensor, ref: oracle.PreAttnTokens, wl: Workload,
-                    what: str) -> dict:
-    """gpu_a: [T, H] bf16 (CPU) rows for ref.tokens."""
-    a_ref = ref.a.double()
-    a_gpu = gpu_a.double()
-    sc, _ = wl.table_views()
+                    what: str, max_steps: int = 96) -> dict:
+    """gpu_a: [T, H] bf16 (CPU) rows for ref.tokens.
+
+    Kernel 1 runs the oracle's FP32 operations after the sum of squares, so a
+    row can differ from the oracle only through its FP32 sum of squares (the
+    pages fix its type, not its order), i.e. through r = 1/sqrt(ss/H + eps).
+    Every row must therefore be bit-exact, or equal bit for bit to the
+    oracle's AdaLN applied to bf16((x * r') * w) for one r' a few FP32 steps
+    from the oracle's r.  Guarded rows are +0.0 bit for bit.  Returns counts
+    of exact rows, rows explained by a moved r, and the elements of those
+    rows that lie more than one bf16 step from the oracle (with the largest
+    distance in steps)."""
+    assert torch.isfinite(gpu_a.double()).all(), f"{what}: non-finite workspace"
+    sc, sh = wl.table_views()
     idx = wl.adaln_index[ref.tokens]
     rows = sc.shape[0]
-    valid = (idx >= 0) & (idx < rows)
-    g = torch.ones_like(a_ref)
-    if bool(valid.any()):
-        g[valid] = (sc[idx[valid]].float() + 1.0).to(BF16).double()
-    shift_n = g.abs() * ulp_bf16(ref.n.double())
-    allowed = shift_n + 0.5 * ulp_bf16(a_ref) + 0.5 * ulp_bf16(a_ref.abs() + shift_n)
-    err = (a_gpu - a_ref).abs()
-    assert torch.isfinite(a_gpu).all(), f"{what}: non-finite workspace"
-    bad = err > allowed
-    assert not bool(bad.any()), (
-        f"{what}: {int(bad.sum())} workspace elements beyond the n-flip bound")
-    exact = float((gpu_a.view(torch.int16) == ref.a.view(torch.int16)).double().mean())
-    within1 = float((err <= ulp_bf16(a_ref)).double().mean())
+    g_bits = gpu_a.contiguous().view(torch.int16)
+    r_bits = ref.a.contiguous().view(torch.int16)
+    same = (g_bits == r_bits).all(dim=1)
+    moved = {}
+    beyond, worst = 0, 0.0
+    for t in torch.nonzero(~same).flatten().tolist():
+        i = int(idx[t])
+        assert 0 <= i < rows, f"{what}: guarded token {int(ref.tokens[t])} is not +0"
+        x_row = wl.x[int(ref.tokens[t])].reshape(1, -1)
+        r0 = float(ref.r[t])
+        found = None
+        for step in range(1, max_steps + 1):
+            for k in (step, -step):
+                n_alt = oracle.rmsnorm_apply(x_row, wl.x_norm_weight,
+                                             torch.tensor([_nudge(r0, k)]))
+                a_alt = oracle.indexed_adaln(n_alt, sc, sh, idx[t:t + 1])
+                if torch.equal(a_alt.view(torch.int16)[0], g_bits[t]):
+                    found = k
+                    break
+            if found is not None:
+                break
+        assert found is not None, (
+            f"{what}: workspace row of token {int(ref.tokens[t])} is not the oracle's AdaLN "
+            f"for any r within {max_steps} FP32 steps")
+        moved[found] = moved.get(found, 0) + 1
+        d = (gpu_a[t].double() - ref.a[t].double()).abs() / ulp_bf16(ref.a[t].double())
+        beyond += int((d > 1).sum())
+        worst = max(worst, float(d.max()))
     # guarded rows are +0.0 bit for bit
-    if bool((~valid).any()):
-        assert torch.all(gpu_a[~valid].view(torch.int16) == 0), f"{what}: guard row not +0"
-    assert exact > 0.999, f"{what}: only {exact:.6f} of the workspace is bit-exact"
-    assert within1 > 0.9999, f"{what}: only {within1:.6f} within 1 ulp"
-    return dict(exact=exact, within_1ulp=within1)
+    bad = (idx < 0) | (idx >= rows)
+    if bool(bad.any()):
+        assert torch.all(g_bits[bad] == 0), f"{what}: guard row not +0"
+    return dict(rows=int(len(same)), exact_rows=int(same.sum()),
+                rows_with_moved_r=int((~same).sum()), r_steps=moved,
+                elements_beyond_1ulp=beyond, max_ulps=worst)
