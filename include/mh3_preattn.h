@@ -228,9 +228,11 @@ int mh3_preattn_device_status(mh3_preattn_t handle, void* stream, int* device_co
  * exits.  M > 1024 is rejected with MH3_ERR_INVALID_ARG before anything is
  * launched.  No cudaMalloc, cudaFree or other allocating call is made.
  *
- * The first call on a device does a one-time set-up on that device (it looks
- * up the array's device address, raises the GEMM's shared-memory limit and
- * reads the SM count); make that first call before any stream capture.
+ * The first call on a device does a one-time set-up on that device (it checks
+ * the device as mh3_preattn_create does, looks up the array's device address,
+ * raises the GEMMs' shared-memory limits and reads the SM count); make that
+ * first call before any stream capture.  A set-up that fails is not kept:
+ * the call returns its error and the next call on that device tries again.
  * Every call uses the same array, which keeps the last call's contents;
  * calls that overlap on the GPU (other streams, other threads) race on it.
  *

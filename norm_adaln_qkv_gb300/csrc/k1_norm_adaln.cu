@@ -89,12 +89,13 @@ __device__ __forceinline__ uint32_t adaln_pair(uint64_t x2, uint32_t w, uint32_t
 // NVFP4 outputs of one 8-element chunk c of row m (a in `o`): the block of
 // 16 is this thread's chunk and its neighbour's (lanes 2b, 2b+1); the even
 // lane stores the block's scale byte.
-__device__ __forceinline__ void fp4_chunk(const uint4& o, int lane, int c, int64_t m, float gs,
-                                          const float* enc_lut, const NormAdalnParams& p) {
+__device__ __forceinline__ void fp4_chunk(const uint4& o, int lane, int c, int64_t m,
+                                          const fp4::Quantiser& q, const float2* enc_lut,
+                                          const NormAdalnParams& p) {
   float amax = fp4::amax8(o);
   amax = fmaxf(amax, __shfl_xor_sync(0xFFFFFFFFu, amax, 1));
-  const fp4::BlockScale bs = fp4::block_scale(amax, gs, enc_lut);
-  *reinterpret_cast<uint32_t*>(p.act_q + m * (kHidden / 2) + 4 * c) = fp4::encode8(o, bs.enc);
+  const fp4::BlockScale bs = fp4::block_scale(amax, q, enc_lut);
+  *reinterpret_cast<uint32_t*>(p.act_q + m * (kHidden / 2) + 4 * c) = fp4::encode8(o, bs, q.gs);
   if ((lane & 1) == 0)
     p.act_sf[fp4::scale_offset(m, c >> 3, kHidden / 64, p.sf_tiled != 0) + ((lane & 7) >> 1)] =
         static_cast<uint8_t>(bs.code);
@@ -106,7 +107,7 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm) norm_adaln_kernel(const 
   __shared__ __align__(8) uint64_t full[kStages];
   __shared__ float warp_ss[kWarps];
   __shared__ int go;
-  __shared__ float enc_lut[kFp4 ? fp4::kEncLut : 1];
+  __shared__ float2 enc_lut[kFp4 ? fp4::kEncLut : 1];
 
   const int tid = threadIdx.x;
   const int lane = tid & 31;
@@ -120,6 +121,7 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm) norm_adaln_kernel(const 
   // waits for this grid's completion before it reads the workspace
   griddep_launch_dependents();
   const float gs = kFp4 ? __ldg(p.act_gs) : 0.0f;
+  const fp4::Quantiser quant = fp4::make_quantiser(gs);
   if (kFp4) fp4::init_enc_lut(enc_lut, gs, tid, kThreads);  // visible after the first barrier
 
   uint64_t policy = 0;
@@ -184,7 +186,7 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm) norm_adaln_kernel(const 
 #pragma unroll
       for (int j = 0; j < kVecPerThread; ++j) {
         if (kFp4)
-          fp4_chunk(z, lane, tid + kThreads * j, m, 0.0f, enc_lut, p);  // codes 0, scale 0
+          fp4_chunk(z, lane, tid + kThreads * j, m, quant, enc_lut, p);  // codes 0, scale 0
         else
           wr[tid + kThreads * j] = z;
       }
@@ -208,7 +210,7 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm) norm_adaln_kernel(const 
       o.z = adaln_pair(f2_from_bf16x2(v[j].z), w.z, sc.z, sh.z, r2);
       o.w = adaln_pair(f2_from_bf16x2(v[j].w), w.w, sc.w, sh.w, r2);
       if (kFp4)
-        fp4_chunk(o, lane, c, m, gs, enc_lut, p);
+        fp4_chunk(o, lane, c, m, quant, enc_lut, p);
       else
         wr[c] = o;
     }

@@ -1065,38 +1065,44 @@ static __device__ __align__(256) mh3_bf16 g_noalloc_workspace[kNoAllocMaxM * kHi
 
 constexpr int kNoAllocMaxDevices = 64;
 struct NoAllocDevice {
-  std::once_flag once;
-  int rc = MH3_OK;
-  std::string err;
+  bool ready = false;             // set only after a set-up that succeeded
   mh3_bf16* workspace = nullptr;  // device address of g_noalloc_workspace
   int num_sms = 0;
   int max_clusters = 0;
 };
 NoAllocDevice g_noalloc_dev[kNoAllocMaxDevices];
+std::mutex g_noalloc_mutex;
 
-// Once per device, with that device current: the device address of the
-// array (the host-side name is only a stand-in), the GEMM's shared-memory
-// limit, and the SM count.
-void noalloc_setup(int dev, NoAllocDevice& d) {
+// Per device, with that device current, until it succeeds once: the device
+// address of the array (the host-side name is only a stand-in), the same
+// device checks as mh3_preattn_create (sm_103a, enough opt-in shared memory
+// per block), the GEMMs' shared-memory limits, and the SM count.  A failed
+// set-up is not remembered: the next call tries again.
+int noalloc_setup(int dev, NoAllocDevice& d) {
+  std::lock_guard<std::mutex> lock(g_noalloc_mutex);
+  if (d.ready) return MH3_OK;
   cudaDeviceProp prop;
   cudaError_t e = cudaGetDeviceProperties(&prop, dev);
-  if (e != cudaSuccess) {
-    d.rc = cuda_fail(e, "cudaGetDeviceProperties");
-  } else if (!(prop.major == 10 && prop.minor == 3)) {
-    d.rc = fail(MH3_ERR_UNSUPPORTED, "device %d is sm_%d%d; this library is built for sm_103a",
+  if (e != cudaSuccess) return cuda_fail(e, "cudaGetDeviceProperties");
+  if (!(prop.major == 10 && prop.minor == 3))
+    return fail(MH3_ERR_UNSUPPORTED, "device %d is sm_%d%d; this library is built for sm_103a",
                 dev, prop.major, prop.minor);
-  } else if ((e = cudaGetSymbolAddress(reinterpret_cast<void**>(&d.workspace),
-                                       g_noalloc_workspace)) != cudaSuccess) {
-    d.rc = cuda_fail(e, "cudaGetSymbolAddress (static workspace)");
-  } else if ((e = qkv_prepare_device()) != cudaSuccess) {
-    d.rc = cuda_fail(e, "cudaFuncSetAttribute");
-  } else if ((e = qkv_pair_prepare_device(&d.max_clusters)) != cudaSuccess) {
-    d.rc = cuda_fail(e, "preparing the pair GEMM");
-  } else {
-    d.num_sms = prop.multiProcessorCount;
-    d.rc = MH3_OK;
-  }
-  if (d.rc != MH3_OK) d.err = g_last_error;
+  if (static_cast<int>(prop.sharedMemPerBlockOptin) < qkv_smem_bytes())
+    return fail(MH3_ERR_UNSUPPORTED, "device allows %zu B of shared memory per block, need %d",
+                prop.sharedMemPerBlockOptin, qkv_smem_bytes());
+  mh3_bf16* ws = nullptr;
+  if ((e = cudaGetSymbolAddress(reinterpret_cast<void**>(&ws), g_noalloc_workspace)) !=
+      cudaSuccess)
+    return cuda_fail(e, "cudaGetSymbolAddress (static workspace)");
+  if ((e = qkv_prepare_device()) != cudaSuccess) return cuda_fail(e, "cudaFuncSetAttribute");
+  int clusters = 0;
+  if ((e = qkv_pair_prepare_device(&clusters)) != cudaSuccess)
+    return cuda_fail(e, "preparing the pair GEMM");
+  d.workspace = ws;
+  d.max_clusters = clusters;
+  d.num_sms = prop.multiProcessorCount;
+  d.ready = true;
+  return MH3_OK;
 }
 
 }  // namespace
@@ -1126,8 +1132,7 @@ extern "C" int mh3_preattn_run_noalloc(
   if (dev < 0 || dev >= kNoAllocMaxDevices)
     return fail(MH3_ERR_UNSUPPORTED, "device index %d out of range", dev);
   NoAllocDevice& d = g_noalloc_dev[dev];
-  std::call_once(d.once, noalloc_setup, dev, std::ref(d));
-  if (d.rc != MH3_OK) return fail(d.rc, "%s", d.err.c_str());
+  if ((rc = noalloc_setup(dev, d))) return rc;
 
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   // the timeout code must start at zero for this call

@@ -1,12 +1,31 @@
 // nvfp4.cuh -- NVFP4 block quantisation (E2M1 elements, one UE4M3 scale per
-// 16 elements, an FP32 global scale), shared by the NVFP4 stage's first
-// kernel and the standalone quantiser
-// (flashinfer.diffusion_ops.minimax_h3_nvfp4_pre_attention, summary:
-// fp4_quantize(a, act_global_scale, sf_vec_size=16)):
+// 16 elements, an FP32 global scale gs), shared by the NVFP4 stage's first
+// kernel and the standalone quantiser.  The convention is the FlashInfer
+// block-16 one that flashinfer.diffusion_ops.minimax_h3_nvfp4_out_proj
+// prints in its summary (and that minimax_h3_nvfp4_pre_attention applies to
+// its activation):
 //
-//   s    = ue4m3(RN(RN(amax / 6) * gs))       amax = max |v| over the block
-//   enc  = s == 0 ? 0 : RN(gs / s)            (a 128-entry table per block)
-//   code = e2m1(RN(v * enc))                  nearest even, saturating at 6
+//   sf   = UE4M3(amax * gs / 6)      amax = max |v| over the block
+//   code = RN(v * gs / sf)           E2M1, nearest even, saturating at 6
+//
+// each a single rounding of the exact quotient (UE4M3: nearest even,
+// saturating at 448; where sf = 0 the codes are the signed zeros of v * 0).
+//
+// How one rounding is reached in FP32.  For the scale, directed roundings
+// bracket the exact t = amax * gs / 6: t_lo = RD(amax * RD(gs / 6)) <= t <=
+// t_hi = RU(amax * RU(gs / 6)); rounding is monotonic, so when t_lo and t_hi
+// round to the same code, that is the code of t.  Otherwise the bracket
+// holds one rounding boundary m (the midpoint of the two codes) and the sign
+// of amax * gs - 6m decides; 6m has at most 7 significant bits, so it is an
+// FP32 number, amax * gs is split exactly into hi + lo by one FMA, and
+// hi - 6m is exact (the two are within a factor of 2), so the sign of
+// (hi - 6m) + lo is that of the exact difference.  The elements work the
+// same way with a multiplier just below and one just above gs / sf (a
+// per-code table): when the two code words of eight elements agree they are
+// the codes of the exact quotients; where a pair of codes differs, the sign
+// of |v| * gs - m * sf at the midpoint m between them decides (m * sf has at
+// most 7 significant bits).  Ties (the exact quotient on the midpoint) go to
+// the even code.
 //
 // Codes are packed two per byte, element 2j in the low nibble.  Scales are
 // stored either row-major ([rows, cols/16]) or in the tiled form the
@@ -31,38 +50,82 @@ __device__ __forceinline__ float ue4m3_value(uint32_t code) {
   return e == 0 ? __uint2float_rn(m) * 0x1p-9f : __uint_as_float(((e + 120u) << 23) | (m << 20));
 }
 
-// RN(v / 6) for v >= 0: Markstein's quotient with the constant r = RN(1/6)
-// (one multiply, two FMAs), exact whenever no step leaves the normal range,
-// i.e. for v in [2^-100, 2^127) (checked for every bf16 value there); outside
-// that range (tiny, huge, infinite or NaN) a true division.
-__device__ __forceinline__ float div6_rn(float v) {
-  if (!(v >= 0x1p-100f && v < 0x1p127f)) return __fdiv_rn(v, 6.0f);
-  const float r = 0x1.555556p-3f;  // RN(1/6)
-  const float q = __fmul_rn(v, r);
-  return __fmaf_rn(__fmaf_rn(-q, 6.0f, v), r, q);
+// E2M1 magnitude code (0..7) -> its value: 0, 0.5, 1, 1.5, 2, 3, 4, 6.
+__device__ __forceinline__ float e2m1_value(uint32_t c) {
+  return c < 2 ? 0.5f * static_cast<float>(c)
+               : ldexpf(1.0f + 0.5f * static_cast<float>(c & 1u), static_cast<int>(c >> 1) - 1);
 }
 
-// enc[c] = RN(gs / s_c) for every UE4M3 code c (0 for c = 0): the per-block
-// division of the encode multiplier, done once per code.  Fill with all
-// threads of the block, then synchronise.
+// Per-kernel constants: gs and the bracket RD(gs / 6) <= gs / 6 <= RU(gs / 6).
+struct Quantiser {
+  float gs, c_lo, c_hi;
+};
+__device__ __forceinline__ Quantiser make_quantiser(float gs) {
+  Quantiser q;
+  q.gs = gs;
+  q.c_lo = __fdiv_rd(gs, 6.0f);
+  q.c_hi = __fdiv_ru(gs, 6.0f);
+  return q;
+}
+
+// enc[c] = (multiplier just below gs / s_c, multiplier just above) for every
+// UE4M3 code c ((0, 0) for c = 0).  With e_lo <= (gs / s)(1 - 2^-23) and
+// e_hi >= (gs / s)(1 + 2^-23), one round-to-nearest product |v| * e_lo stays
+// strictly below |v| * gs / s and |v| * e_hi strictly above (for v != 0).
+// Fill with all threads of the block, then synchronise.
 constexpr int kEncLut = 128;
-__device__ __forceinline__ void init_enc_lut(float* lut, float gs, int tid, int nthreads) {
+__device__ __forceinline__ void init_enc_lut(float2* lut, float gs, int tid, int nthreads) {
   for (int c = tid; c < kEncLut; c += nthreads) {
     const float s = c < 127 ? ue4m3_value(static_cast<uint32_t>(c)) : 0.0f;
-    lut[c] = s == 0.0f ? 0.0f : __fdiv_rn(gs, s);
+    float2 e = make_float2(0.0f, 0.0f);
+    if (s != 0.0f) {
+      e.x = __fmul_rd(__fdiv_rd(gs, s), 0x1.fffffep-1f);  // 1 - 2^-23
+      e.y = __fmul_ru(__fdiv_ru(gs, s), 0x1.000002p+0f);  // 1 + 2^-23
+    }
+    lut[c] = e;
   }
 }
 
 struct BlockScale {
   uint32_t code;  // UE4M3 scale code
-  float enc;      // multiplier that maps the block onto the E2M1 range
+  float sf;       // its value
+  float enc_lo;   // multipliers bracketing gs / sf
+  float enc_hi;
 };
 
-__device__ __forceinline__ BlockScale block_scale(float amax, float gs, const float* enc_lut) {
-  const float t = __fmul_rn(div6_rn(amax), gs);
+// Sign of a * b - c for an FP32 number c within a factor of 2 of a * b:
+// a * b = hi + lo exactly (one FMA), hi - c is exact, and (hi - c) + lo has
+// the sign of the exact difference.
+__device__ __forceinline__ float exact_diff_sign(float a, float b, float c) {
+  const float hi = __fmul_rn(a, b);
+  const float lo = __fmaf_rn(a, b, -hi);
+  return __fadd_rn(__fsub_rn(hi, c), lo);
+}
+
+// The bracket [t_lo, t_hi] rounds to the adjacent codes lo < hi: decide at
+// their midpoint m with the exact sign of amax * gs - 6m.
+static __device__ __noinline__ uint32_t scale_code_at_boundary(float amax, float gs, uint32_t lo,
+                                                        uint32_t hi) {
+  const float six_m = __fmul_rn(__fadd_rn(ue4m3_value(lo), ue4m3_value(hi)), 3.0f);  // exact
+  const float d = exact_diff_sign(amax, gs, six_m);
+  if (d > 0.0f) return hi;
+  if (d < 0.0f) return lo;
+  return (lo & 1u) ? hi : lo;  // on the midpoint: the even code
+}
+
+__device__ __forceinline__ BlockScale block_scale(float amax, const Quantiser& q,
+                                                  const float2* enc_lut) {
+  const float t_lo = __fmul_rd(amax, q.c_lo);
+  const float t_hi = __fmul_ru(amax, q.c_hi);
+  const uint32_t both = e4m3x2_satfinite(t_lo, t_hi);  // t >= 0: nearest even, <= 448
+  uint32_t code = both & 0xFFu;
+  if (code != (both >> 8)) code = scale_code_at_boundary(amax, q.gs, code, both >> 8);
   BlockScale b;
-  b.code = e4m3x2_satfinite(t, 0.0f) & 0xFFu;  // t >= 0: nearest even, <= 448
-  b.enc = enc_lut[b.code];
+  b.code = code;
+  b.sf = ue4m3_value(code);
+  const float2 e = enc_lut[code];
+  b.enc_lo = e.x;
+  b.enc_hi = e.y;
   return b;
 }
 
@@ -80,16 +143,44 @@ __device__ __forceinline__ uint32_t e2m1x8(const float (&v)[8]) {
   return r;
 }
 
-// Eight bf16 values (uint4) and the block's encode multiplier -> 8 codes;
-// the products are packed two-lane FP32 multiplies (each lane one IEEE
-// round-to-nearest multiply).
-__device__ __forceinline__ uint32_t encode8(const uint4& w, float enc) {
+// Eight bf16 values (uint4) times one multiplier, packed two-lane FP32
+// multiplies (each lane one IEEE round-to-nearest multiply), to E2M1 codes.
+__device__ __forceinline__ uint32_t codes8(const uint4& w, float enc) {
   const uint64_t e2 = f2_pack(enc, enc);
   const uint32_t ws[4] = {w.x, w.y, w.z, w.w};
   float v[8];
 #pragma unroll
   for (int i = 0; i < 4; ++i) f2_unpack(f2_mul(f2_from_bf16x2(ws[i]), e2), v[2 * i], v[2 * i + 1]);
   return e2m1x8(v);
+}
+
+// The elements whose two bracketing codes differ: decide each at the
+// midpoint m of its two codes with the exact sign of |v| * gs - m * sf.
+static __device__ __noinline__ uint32_t codes8_at_boundary(uint4 w, uint32_t c_lo, uint32_t c_hi, float gs,
+                                                    float sf) {
+  const uint32_t ws[4] = {w.x, w.y, w.z, w.w};
+  uint32_t out = c_lo;
+#pragma unroll 1
+  for (int j = 0; j < 8; ++j) {
+    const uint32_t a = (c_lo >> (4 * j)) & 0xFu, b = (c_hi >> (4 * j)) & 0xFu;
+    if (a == b) continue;
+    const uint32_t ma = a & 7u, mb = b & 7u;  // adjacent magnitudes, same sign
+    const uint32_t lo = ma < mb ? ma : mb, hi = ma < mb ? mb : ma;
+    const uint32_t h = ws[j >> 1] >> (16 * (j & 1));
+    const float mag = __uint_as_float((h & 0x7FFFu) << 16);  // |v|
+    const float m_sf = __fmul_rn(__fmul_rn(__fadd_rn(e2m1_value(lo), e2m1_value(hi)), 0.5f), sf);
+    const float d = exact_diff_sign(mag, gs, m_sf);
+    const uint32_t pick = d > 0.0f ? hi : (d < 0.0f ? lo : ((lo & 1u) ? hi : lo));
+    out = (out & ~(0xFu << (4 * j))) | ((pick | (a & 8u)) << (4 * j));
+  }
+  return out;
+}
+
+// The codes of eight bf16 values of one block.
+__device__ __forceinline__ uint32_t encode8(const uint4& w, const BlockScale& b, float gs) {
+  const uint32_t lo = codes8(w, b.enc_lo);
+  const uint32_t hi = codes8(w, b.enc_hi);
+  return lo == hi ? lo : codes8_at_boundary(w, lo, hi, gs, b.sf);
 }
 
 // max |v| of eight bf16 values (exact): packed magnitude maxima

@@ -18,7 +18,8 @@ __global__ void __launch_bounds__(256) nvfp4_quantize_kernel(const __nv_bfloat16
                                                              uint8_t* __restrict__ scales,
                                                              int tiled) {
   const float gs = __ldg(gs_ptr);
-  __shared__ float enc_lut[fp4::kEncLut];
+  const fp4::Quantiser quant = fp4::make_quantiser(gs);
+  __shared__ float2 enc_lut[fp4::kEncLut];
   fp4::init_enc_lut(enc_lut, gs, threadIdx.x, blockDim.x);
   __syncthreads();
   const int ksteps = cols / 64;
@@ -37,9 +38,9 @@ __global__ void __launch_bounds__(256) nvfp4_quantize_kernel(const __nv_bfloat16
 #pragma unroll
     for (int b = 0; b < 4; ++b) {
       const float amax = fmaxf(fp4::amax8(v[2 * b]), fp4::amax8(v[2 * b + 1]));
-      const fp4::BlockScale bs = fp4::block_scale(amax, gs, enc_lut);
-      q[2 * b] = fp4::encode8(v[2 * b], bs.enc);
-      q[2 * b + 1] = fp4::encode8(v[2 * b + 1], bs.enc);
+      const fp4::BlockScale bs = fp4::block_scale(amax, quant, enc_lut);
+      q[2 * b] = fp4::encode8(v[2 * b], bs, gs);
+      q[2 * b + 1] = fp4::encode8(v[2 * b + 1], bs, gs);
       word |= bs.code << (8 * b);
     }
     uint4* dst = reinterpret_cast<uint4*>(codes + row * (cols / 2) + ks * 32);

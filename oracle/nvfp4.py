@@ -11,13 +11,22 @@ global scale; the accumulator is rescaled by alpha = 1 / (act_global_scale *
 qkv_weight_global_scale); then the bf16 stage's Q/K norm (with eps), RoPE
 (rope_cos_sin is per token, [M, 96]) and outputs.
 
-Readings where the page defers to other pages (the FP8 stage, fp4_quantize),
-which are not among the pages:
-* block scale s = ue4m3(RN32(RN32(amax / 6) * gs)), amax the largest |a| of
-  the 16 bf16 values; ue4m3 rounds to nearest even and saturates at 448;
-* element code q = e2m1(RN32(a * enc)), enc = RN32(gs / s) (0 when s = 0);
-  e2m1 rounds to nearest even over {0, .5, 1, 1.5, 2, 3, 4, 6}, saturates at
-  6 and keeps the sign (a negative value that rounds to 0 gives -0);
+The block quantisation is the FlashInfer block-16 convention that
+flashinfer.diffusion_ops.minimax_h3_nvfp4_out_proj prints in its summary:
+  sf   = UE4M3(block_amax * act_global_scale / 6)
+  code = RN(x * act_global_scale / sf)
+each a single rounding of the exact quotient.  Readings:
+* UE4M3 and E2M1 rounding is to nearest, ties to even; UE4M3 saturates at
+  448, E2M1 at 6; E2M1 keeps the sign (a negative value that rounds to 0
+  gives -0); where sf = 0 (the whole block rounds to a zero scale) the codes
+  are the signed zeros of x * 0;
+* the exact quotients are formed in float64: block_amax * gs and x * gs are
+  exact there (8 + 24 significant bits), and the one float64 rounding of the
+  division cannot move a value across, or onto, a UE4M3 or E2M1 rounding
+  boundary: those boundaries (times 6, or times sf) have at most 7
+  significant bits, so a numerator of at most 32 significant bits that is
+  not equal to one differs from it by at least 2^-32 of its size, far more
+  than a float64 rounding step (2^-53);
 * packing: byte j holds elements 2j (low nibble) and 2j + 1 (high nibble);
 * the GEMM sums the products (qa sa)(qw sw) exactly and rounds once to FP32
   (the FP32 accumulation of the bf16 stage's reading), then
@@ -65,9 +74,21 @@ def e2m1_values(codes: torch.Tensor) -> torch.Tensor:
     return torch.where((c & 8) != 0, -v, v)
 
 
+def ue4m3_round(v: torch.Tensor) -> torch.Tensor:
+    """Nearest UE4M3 value of non-negative float64 values, ties to even,
+    saturating at 448: three fraction bits at exponents >= -6, steps of 2^-9
+    below (subnormals).  Returns float64 values."""
+    v = v.to(F64)
+    _, e = torch.frexp(v)                         # v = f * 2^e, f in [0.5, 1)
+    lead = torch.clamp(e - 1, min=-6)             # exponent of the leading bit
+    step = torch.pow(2.0, (lead - 3).to(F64))     # spacing of UE4M3 values there
+    q = torch.round(v / step) * step              # exact scaling; round() ties to even
+    return torch.clamp(torch.where(v == 0, torch.zeros_like(v), q), max=UE4M3_MAX)
+
+
 def ue4m3_codes(x: torch.Tensor) -> torch.Tensor:
-    """UE4M3 codes of non-negative FP32 values: nearest even, saturated at 448."""
-    return torch.clamp(x.to(F32), 0.0, UE4M3_MAX).to(torch.float8_e4m3fn).view(torch.uint8)
+    """UE4M3 codes of non-negative values (rounded by ue4m3_round)."""
+    return ue4m3_round(x.to(F64)).to(F32).to(torch.float8_e4m3fn).view(torch.uint8)
 
 
 def ue4m3_values(codes: torch.Tensor) -> torch.Tensor:
@@ -76,16 +97,19 @@ def ue4m3_values(codes: torch.Tensor) -> torch.Tensor:
 
 def fp4_quantize(a: torch.Tensor, global_scale: float):
     """Per-row NVFP4 quantisation of bf16 a [T, K] (K a multiple of 16).
-    Returns (codes uint8 [T, K/2] packed, scales uint8 [T, K/16] row-major)."""
+    Returns (codes uint8 [T, K/2] packed, scales uint8 [T, K/16] row-major).
+
+    sf = UE4M3(amax * gs / 6) and code = E2M1(x * gs / sf), each one rounding
+    of the exact quotient (see the module docstring)."""
     T, K = a.shape
-    gs = torch.tensor(float(global_scale), dtype=F32)
-    blocks = a.to(F32).reshape(T, K // BLOCK, BLOCK)
+    gs = float(torch.tensor(float(global_scale), dtype=F32))  # the FP32 value
+    blocks = a.to(F64).reshape(T, K // BLOCK, BLOCK)
     amax = blocks.abs().amax(dim=-1)
-    t = torch.mul(torch.div(amax, torch.tensor(6.0, dtype=F32)), gs)
-    s_code = ue4m3_codes(t)
-    s = ue4m3_values(s_code)
-    enc = torch.where(s == 0, torch.zeros_like(s), torch.div(gs, torch.where(s == 0, 1.0, s)))
-    q = e2m1_codes(torch.mul(blocks, enc.unsqueeze(-1)).to(F32)).reshape(T, K)
+    s = ue4m3_round((amax * gs) / 6.0)            # amax * gs exact; one rounding
+    s_code = s.to(F32).to(torch.float8_e4m3fn).view(torch.uint8)
+    sv = s.unsqueeze(-1)
+    v = torch.where(sv == 0, blocks * 0.0, (blocks * gs) / torch.where(sv == 0, 1.0, sv))
+    q = e2m1_codes(v).reshape(T, K)
     packed = (q[:, 0::2] | (q[:, 1::2] << 4)).to(torch.uint8)
     return packed, s_code
 

@@ -91,6 +91,28 @@ def test_quantiser_e2m1_rounding_all_ties(cuda_lib):
     assert torch.equal(codes, ref_q)
 
 
+def test_quantiser_single_rounding_at_boundaries(cuda_lib):
+    """Blocks whose exact amax * gs / 6, or x * gs / sf, lies within one FP32
+    step of a UE4M3 or E2M1 rounding boundary (where rounding twice gives
+    another code): the kernel's codes are the exact quotients' codes."""
+    from test_oracle_nvfp4 import _element_cases, _scale_cases
+    for amax, gs, exact, _ in _scale_cases():
+        x = torch.zeros(1, 64)
+        x[0, 0] = amax
+        x[0, 16] = -amax
+        _, scales = gpu_quantize(x.to(BF16).cuda(), gs, False)
+        assert scales[0, :2].tolist() == [exact, exact], (amax, gs)
+    for xv, amax, gs, sf_code, exact, _ in _element_cases():
+        x = torch.zeros(1, 64)
+        x[0, :3] = torch.tensor([xv, -xv, amax])
+        x[0, 16 + 5] = xv                  # the same element at an odd position
+        x[0, 16 + 9] = amax
+        codes, scales = gpu_quantize(x.to(BF16).cuda(), gs, True)
+        q = f.unpack_codes(codes)[0].tolist()
+        assert scales[0, :2].tolist() == [sf_code, sf_code]
+        assert (q[0], q[1], q[16 + 5]) == (exact, exact | 8, exact), (xv, gs)
+
+
 # ------------------------------------------------------------- kernel 1 form
 def _dev(w):
     b = w.base

@@ -38,7 +38,7 @@ def _unpacked(out, tokens):
 # ----------------------------------------------------------- every token
 @pytest.mark.parametrize("key,M", [("c0", None), ("c1", None), ("c2", None),
                                    ("c2", 300), ("c2", 129), ("c3", 127), ("c0", 1),
-                                   ("c3", 40), ("c2", 17)])
+                                   ("c3", 40), ("c2", 17), ("c2", 48), ("c3", 49)])
 def test_full_parity(handle, key, M):
     wl = make_workload(key, M=M)
     d = to_device(wl)
@@ -240,3 +240,32 @@ def test_integer_gemm_is_exact_at_production_shape(handle):
     tok = oracle.ulysses_unpack_rows(out, list(range(M))).cpu()
     y = oracle.qkv_projection(a, W).reshape(M, 3, 56, 128)
     assert torch.equal(tok[:, :, 2].view(torch.int16), y[:, 2].view(torch.int16))
+
+
+def test_small_m_layouts_ignore_stale_shared_memory(handle):
+    # The 16- and 48-row layouts of the single-CTA GEMM let the MMA read 128
+    # A rows; the rows past the loaded box hold whatever other stages (or an
+    # earlier kernel) left in shared memory and feed only accumulator rows
+    # >= M, which are never stored.  Leave NaN and Inf patterns in shared
+    # memory first (a full 128-row GEMM on a workspace of NaN and Inf), then
+    # the small-M outputs must equal a run that followed clean inputs.
+    g = torch.Generator().manual_seed(23)
+    W = (torch.randn(21504, 5376, generator=g) / 73.3).to(torch.bfloat16).cuda()
+    qw = (1 + 0.1 * torch.randn(128, generator=g)).to(torch.bfloat16).cuda()
+    ang = torch.rand(64, 48, generator=g, dtype=torch.float64) * 6
+    cs = torch.cat([torch.cos(ang), torch.sin(ang)], 1).float().to(torch.bfloat16).cuda()
+    poison = torch.full((128, 5376), float("nan"), dtype=torch.bfloat16)
+    poison[::3] = float("inf")
+    poison[1::3] = -float("inf")
+    poison = poison.cuda()
+    finite = torch.randn(128, 5376, generator=g).to(torch.bfloat16).cuda()
+    for M in (16, 40, 48):
+        a = torch.randn(M, 5376, generator=g).to(torch.bfloat16).cuda()
+        pos = torch.arange(M, dtype=torch.int64).cuda()
+        _stage2(handle, finite, W, qw, qw, cs, torch.arange(128).cuda() % 64, 1)
+        clean = _stage2(handle, a, W, qw, qw, cs, pos, 1)
+        _stage2(handle, poison, W, qw, qw, cs, torch.arange(128).cuda() % 64, 1)
+        after = _stage2(handle, a, W, qw, qw, cs, pos, 1)
+        assert bool(torch.isfinite(clean).all())
+        assert torch.equal(clean.view(torch.int16), after.view(torch.int16)), M
+    _status_ok(handle)

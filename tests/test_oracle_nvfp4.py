@@ -185,3 +185,106 @@ def test_stage_matches_bf16_oracle_when_nvfp4_is_exact():
         t = oracle.rope_split_half(oracle.head_rmsnorm(y4[:, kind], wn, 1e-30), cs, torch.arange(M))
         assert torch.equal(got.qkv[:, :, kind].view(torch.int16), t.view(torch.int16))
     assert torch.equal(got.qkv[:, :, 2].view(torch.int16), y4[:, 2].view(torch.int16))
+
+
+# ------------------------------------------------ single rounding at midpoints
+# flashinfer.diffusion_ops.minimax_h3_nvfp4_out_proj, summary: the block-16
+# convention sf = UE4M3(block_amax * act_global_scale / 6) and
+# code = RN(x * act_global_scale / sf), one rounding of each exact quotient.
+# The cases below are built so that the exact quotient lies within one FP32
+# step of a rounding boundary: there the old two-rounding order
+# (RN32(RN32(amax / 6) * gs), RN32(x * RN32(gs / sf))) gives another code,
+# and exact rational arithmetic decides which one the formula means.
+
+import numpy as np  # noqa: E402
+
+UE4M3_ALL = [(c, (Fraction(c & 7, 8) * Fraction(1, 64)) if (c >> 3) == 0 else
+              (1 + Fraction(c & 7, 8)) * Fraction(2) ** ((c >> 3) - 7)) for c in range(127)]
+E2M1_ALL = [(c, Fraction(v).limit_denominator()) for c, v in enumerate(f.E2M1_VALUES)]
+
+
+def _nearest(q: Fraction, table, top):
+    """Code of the nearest table value to q >= 0, ties to the even code,
+    values above the largest saturating to it."""
+    if q >= top:
+        return table[-1][0]
+    best = min(abs(q - v) for _, v in table)
+    near = [c for c, v in table if abs(q - v) == best]
+    return near[0] if len(near) == 1 else [c for c in near if c % 2 == 0][0]
+
+
+def _f32(v) -> float:
+    return float(np.float32(v))
+
+
+def _f32_steps(v: float, k: int) -> float:
+    return float(np.array([v], dtype=np.float32).view(np.int32).__add__(k).view(np.float32)[0])
+
+
+def _scale_cases():
+    cases = []
+    mids = [(UE4M3_ALL[c][1] + UE4M3_ALL[c + 1][1]) / 2 for c in (8, 9, 13, 44, 57, 70, 100)]
+    for m in mids:
+        for amax in (1.5, 3.0, 5.25, 7.0, 9.5, 11.0, 13.0, 19.0, 23.0, 29.0, 37.0, 53.0):
+            g0 = _f32(float(6 * m) / amax)
+            for k in range(-3, 4):
+                gs = _f32_steps(g0, k)
+                exact = _nearest(Fraction(amax) * Fraction(gs) / 6, UE4M3_ALL, Fraction(448))
+                t2 = _f32(np.float32(_f32(np.float32(amax) / np.float32(6.0))) * np.float32(gs))
+                two = _nearest(Fraction(t2), UE4M3_ALL, Fraction(448))
+                if exact != two:
+                    cases.append((amax, gs, exact, two))
+    return cases
+
+
+def test_scale_is_one_rounding_of_the_exact_quotient():
+    cases = _scale_cases()
+    assert len(cases) >= 5, len(cases)
+    for amax, gs, exact, two in cases:
+        a = torch.tensor([[amax] + [0.0] * 15], dtype=BF16)
+        _, s = f.fp4_quantize(a, gs)
+        assert s.item() == exact != two, (amax, gs, s.item(), exact, two)
+
+
+def test_scale_exact_ties_go_to_even():
+    # amax * 1 / 6 = 1.0625, halfway between 1.0 (0x38) and 1.125 (0x39): even -> 1.0
+    # 7.125 / 6 = 1.1875, halfway between 1.125 (0x39) and 1.25 (0x3A): even -> 1.25
+    a = torch.tensor([[6.375] + [0.0] * 15 + [7.125] + [0.0] * 15], dtype=BF16)
+    _, s = f.fp4_quantize(a, 1.0)
+    assert s.tolist() == [[0x38, 0x3A]]
+
+
+def _element_cases():
+    cases = []
+    for sf_code in (0x39, 0x3B, 0x3D, 0x3F, 0x4B, 0x2D):
+        sf = UE4M3_ALL[sf_code][1]
+        for lo, hi in zip(E2M1_ALL[:-1], E2M1_ALL[1:]):
+            me = (lo[1] + hi[1]) / 2
+            for x in (0.3125, 0.5625, 0.8125, 1.0625, 1.4375, 1.8125, 2.6875, 3.0625):
+                g0 = _f32(float(me * sf) / x)
+                for k in range(-3, 4):
+                    gs = _f32_steps(g0, k)
+                    exact = _nearest(Fraction(x) * Fraction(gs) / sf, E2M1_ALL, Fraction(6))
+                    enc = np.float32(np.float32(gs) / np.float32(float(sf)))
+                    two = _nearest(Fraction(_f32(np.float32(x) * enc)), E2M1_ALL, Fraction(6))
+                    if exact == two:
+                        continue
+                    # a block whose amax gives exactly this sf at this gs
+                    amax = float(torch.tensor(float(6 * sf) / gs).to(BF16))
+                    if amax < x or _nearest(Fraction(amax) * Fraction(gs) / 6, UE4M3_ALL,
+                                            Fraction(448)) != sf_code:
+                        continue
+                    cases.append((x, amax, gs, sf_code, exact, two))
+    return cases
+
+
+def test_element_code_is_one_rounding_of_the_exact_quotient():
+    cases = _element_cases()
+    assert len(cases) >= 5, len(cases)
+    for x, amax, gs, sf_code, exact, two in cases:
+        a = torch.tensor([[x, -x, amax] + [0.0] * 13], dtype=BF16)
+        q, s = f.fp4_quantize(a, gs)
+        codes = f.unpack_codes(q)[0].tolist()
+        assert s.item() == sf_code
+        assert codes[0] == exact != two, (x, gs, codes[0], exact, two)
+        assert codes[1] == exact | 8  # the same magnitude, sign kept

@@ -38,8 +38,10 @@ def test_noalloc_matches_run_on_two_calls_in_a_row(cuda_lib):
     torch.cuda.set_device(0)
     h = binding.Handle(0)
     # call 1: the largest size the static workspace holds; call 2: a ragged
-    # smaller case with strided tables, explicit positions and P = 2.
-    cases = [to_device(make_workload("c1")), to_device(make_workload("c2", M=300))]
+    # smaller case with strided tables, explicit positions and P = 2; calls 3
+    # and 4: the sizes that take the GEMM's 16-row and 48-row layouts.
+    cases = [to_device(make_workload("c1")), to_device(make_workload("c2", M=300)),
+             to_device(make_workload("c0")), to_device(make_workload("c2", M=40))]
     refs = []
     for d in cases:
         ref = new_out(d.M, d.P)
