@@ -794,7 +794,7 @@ def main():
     ap.add_argument("--steps", type=int, default=30)
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
-    ap.add_argument("--cpu-rows", type=int, default=2048,
+    ap.add_argument("--cpu-rows", type=int, default=8192,
                     help="tokens of the oracle CPU-baseline sample (0 disables)")
     ap.add_argument("--ref-rows", type=int, default=64,
                     help="tokens per step of the reference (oracle) arm")
