@@ -644,6 +644,7 @@ def run_ours(args, world, rank, local):
     small = None
     if not args.skip_also:
         flush = torch.empty(80 * 2**20, dtype=torch.float32, device=dev)
+        reread = torch.empty(80 * 2**20, dtype=torch.float32, device=dev).fill_(1.0)
         small = {}
         for key in ("c0", "c1"):
             ws_ = make_workload(key)
@@ -651,12 +652,14 @@ def run_ours(args, world, rank, local):
             for _ in range(3):
                 stage(ws_, ds_)
             per = {}
-            for mode in ("warm", "cold"):
+            for mode in ("warm", "cold", "cold_clean"):
                 evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
                        for _ in range(SMALL_CALLS)]
                 for i, (s0, s1) in enumerate(evs):
-                    if mode == "cold":
-                        flush.fill_(float(i))
+                    if mode != "warm":
+                        flush.fill_(float(i))  # 320 MB written: nothing of the inputs stays in L2
+                    if mode == "cold_clean":
+                        reread.sum()  # 320 MB read: L2 left holding clean lines, no write-back due
                     s0.record(stream)
                     stage(ws_, ds_)
                     s1.record(stream)
@@ -664,11 +667,17 @@ def run_ours(args, world, rank, local):
                 per[mode] = statistics.median(s0.elapsed_time(s1) for s0, s1 in evs) * 1e3
             roof = stage_roofline_us(ws_, peaks)
             small[key] = {"workload": ws_.spec.name, "stage_us_warm": per["warm"],
-                          "stage_us_cold": per["cold"], "stage_roofline_us": roof,
+                          "stage_us_cold": per["cold"], "stage_us_cold_clean": per["cold_clean"],
+                          "stage_roofline_us": roof,
+                          "roofline_frac_warm": roof / per["warm"],
                           "roofline_frac_cold": roof / per["cold"],
-                          "timed": f"median of {SMALL_CALLS} calls, CUDA events around each"}
+                          "roofline_frac_cold_clean": roof / per["cold_clean"],
+                          "timed": f"median of {SMALL_CALLS} calls, CUDA events around each; "
+                                   "cold: after writing 320 MB (the write-backs of that buffer's "
+                                   "dirty lines then fall in the timed call); cold_clean: after "
+                                   "writing 320 MB and then reading another 320 MB"}
             del ds_
-        del flush
+        del flush, reread
     clk = clocks.stop()
     assert h.device_status(stream) == 0, "a kernel recorded a timeout"
 

@@ -30,7 +30,6 @@ enum : int {
   kStatusDrain = 0x105,
   kStatusRowFull = 0x106,
   kStatusEpiResidual = 0x107,
-  kStatusSkPartial = 0x108,  // a stream-K owner waited in vain for a partial tile
 };
 
 struct NormAdalnParams {
@@ -74,11 +73,6 @@ struct QkvParams {
   const float* act_gs = nullptr;  // device [1]
   float w_gs = 0.0f;
   int test_stall = 0;  // test hook: the producer issues no loads (bounded waits run out)
-  // Stream-K schedule of the single-CTA form (both null: one whole tile per
-  // CTA at a time).  sk_partial: [grid][4 warps][256 columns][32 lanes] FP32
-  // partial accumulators; sk_flags: [grid][4], zero between launches.
-  float* sk_partial = nullptr;
-  int* sk_flags = nullptr;
 };
 
 // num_sms: SM count of the device (the kernel is persistent over rows).
@@ -127,11 +121,6 @@ struct GatedResidualParams {
   int num_tiles;    // num_m_tiles * 21
   int* status;
   int test_stall = 0;  // test hook: the producer issues no loads (bounded waits run out)
-  // Stream-K schedule of the single-CTA form (both null: one whole tile per
-  // CTA at a time).  sk_partial: [grid][4 warps][256 columns][32 lanes] FP32
-  // partial accumulators; sk_flags: [grid][4], zero between launches.
-  float* sk_partial = nullptr;
-  int* sk_flags = nullptr;
 };
 using OutProjParams = GatedResidualParams<int32_t>;
 
@@ -155,11 +144,6 @@ struct SwigluParams {
   int num_tiles;    // num_m_tiles * 112
   int* status;
   int test_stall = 0;  // test hook: the producer issues no loads (bounded waits run out)
-  // Stream-K schedule of the single-CTA form (both null: one whole tile per
-  // CTA at a time).  sk_partial: [grid][4 warps][256 columns][32 lanes] FP32
-  // partial accumulators; sk_flags: [grid][4], zero between launches.
-  float* sk_partial = nullptr;
-  int* sk_flags = nullptr;
 };
 
 // fc1 + SwiGLU: y = bf16(bf16(silu(h_gate)) * h_up), h = bf16(a @ fc1^T).
@@ -188,9 +172,6 @@ cudaError_t launch_e4m3_quantize(const __nv_bfloat16* in, const float* descale, 
 int qkv_smem_bytes();
 cudaError_t qkv_prepare_device();  // raise the dynamic shared-memory limit
 cudaError_t launch_qkv(const QkvMaps& maps, const QkvParams& p, int grid, cudaStream_t stream);
-// Scratch of the single-CTA form's stream-K schedule for a grid of `grid` CTAs.
-size_t qkv_sk_partial_bytes(int grid);
-size_t qkv_sk_flags_bytes(int grid);
 
 // CTA-pair form (256 x 256 tiles on two SMs), used for M > 128.
 int qkv_pair_smem_bytes();

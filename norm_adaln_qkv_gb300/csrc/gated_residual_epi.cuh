@@ -31,7 +31,6 @@ struct GatedResidualEpi {
   using Params = GatedResidualParams<IndexT>;
   static constexpr int kKBlocks = KB;
   static constexpr int kNTiles = kHidden / kTileN;  // 21
-  static constexpr bool kHalfTail = false;
   static_assert(kHidden % kTileN == 0, "output columns must tile");
   __device__ static int b_row(int n_blk, int rank) { return gp::contiguous_b_row(n_blk, rank); }
 

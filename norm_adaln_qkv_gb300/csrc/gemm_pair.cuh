@@ -9,9 +9,6 @@
 //     __device__ static int b_row(int n_blk, int rank);  // first B row CTA `rank` loads
 //     __device__ static void prologue(float* scratch, int tid, int nthreads, const Params&);
 //     __device__ static void tile(const EpiCtx&, const Params&, int64_t row0, int n_blk);
-//     static constexpr bool kHalfTail;       // tile_half() exists (see below)
-//     __device__ static void tile_half(const EpiCtx&, const Params&, int64_t row0, int n_blk,
-//                                      int half);
 //   };
 //
 // A cluster of two CTAs owns a 256-row x 256-column output tile of
@@ -31,11 +28,6 @@
 // kGroupPairs row blocks (row block fastest) so that the operands in flight
 // stay in L2.  Only the producer waits on the previous grid
 // (griddepcontrol.wait) before it reads A.
-//
-// Tail split (policies with kHalfTail): when the tiles of the last wave would
-// occupy at most half of the clusters, each of them is cut into two
-// 128-column halves (one head each), run as M=256 N=128 MMAs whose B operand
-// is 64 rows per CTA; the last wave then takes about half as long.
 //
 // Every mbarrier wait is bounded (2 s): a role that gives up records a code
 // in the device status word and raises the abort flag of both CTAs; aborting
@@ -63,7 +55,6 @@ constexpr int kBBytes = BNC * BK * 2;  // 16 KB
 constexpr int kStageBytes = kABytes + kBBytes;
 constexpr int kThreads = 64 + kEpiWarps * 32;  // 192
 constexpr uint32_t kIdesc = idesc_bf16_f32(kPairRows, kTileN);
-constexpr uint32_t kIdescHalf = idesc_bf16_f32(kPairRows, kTileN / 2);
 constexpr uint16_t kBothCtas = 0x3;
 constexpr uint64_t kGraceNs = 50000000ull;  // 50 ms
 
@@ -136,29 +127,6 @@ __device__ __noinline__ inline void grace_period() { grace_period_inl(); }
 // The usual B split: the tile's 256 B rows, 128 per CTA of the pair.
 __device__ __forceinline__ int contiguous_b_row(int n_blk, int rank) {
   return n_blk * kTileN + rank * BNC;
-}
-
-// Work items of a cluster: whole tiles, or (tail split) one-head halves of
-// the last wave's tiles.  Item v of `count` items.
-struct WorkItem {
-  int t;     // tile index
-  int half;  // -1: the whole tile; 0 or 1: its first or second 128 columns
-};
-template <bool kHalfTail>
-__device__ __forceinline__ int tail_tiles(int num_tiles, int ncl) {
-  if (!kHalfTail) return 0;
-  const int tail = num_tiles % ncl;
-  return (tail > 0 && 2 * tail <= ncl) ? tail : 0;
-}
-template <bool kHalfTail>
-__device__ __forceinline__ int work_count(int num_tiles, int ncl) {
-  return num_tiles + tail_tiles<kHalfTail>(num_tiles, ncl);
-}
-template <bool kHalfTail>
-__device__ __forceinline__ WorkItem work_item(int v, int num_tiles, int ncl) {
-  const int full = num_tiles - tail_tiles<kHalfTail>(num_tiles, ncl);
-  if (v < full) return WorkItem{v, -1};
-  return WorkItem{full + (v - full) / 2, (v - full) & 1};
 }
 
 // What an epilogue warp gets for one 128-row x 256-column accumulator block.
@@ -239,15 +207,11 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
       // out and the kernel reports a status code instead of hanging
       bool ok = p.test_stall == 0;
       bool issued_any = false;
-      const int n_items = work_count<Epi::kHalfTail>(p.num_tiles, ncl);
-      for (int v = cid; v < n_items && ok; v += ncl) {
-        const WorkItem w = work_item<Epi::kHalfTail>(v, p.num_tiles, ncl);
+      for (int t = cid; t < p.num_tiles && ok; t += ncl) {
         int pr, n_blk;
-        tile_coords<kGroupPairs, kN>(w.t, p.num_m_tiles, pr, n_blk);
+        tile_coords<kGroupPairs, kN>(t, p.num_m_tiles, pr, n_blk);
         const int a_row = pr * kPairRows + static_cast<int>(rank) * BM;
-        // a half: its 128 B rows, 64 per CTA (the box's other 64 rows are not read)
-        const int b_row = w.half < 0 ? Epi::b_row(n_blk, static_cast<int>(rank))
-                                     : n_blk * kTileN + w.half * BNC + static_cast<int>(rank) * (BNC / 2);
+        const int b_row = Epi::b_row(n_blk, static_cast<int>(rank));
         for (int kb = 0; kb < kKB; ++kb) {
           if (!pair_wait(ctx, sm.empty(stage), phase ^ 1u, kStatusProducerEmpty)) {
             ok = false;
@@ -274,10 +238,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
       uint32_t phase = 0;
       bool ok = true;
       int it = 0;
-      const int n_items = work_count<Epi::kHalfTail>(p.num_tiles, ncl);
-      for (int v = cid; v < n_items && ok; v += ncl, ++it) {
-        const WorkItem w = work_item<Epi::kHalfTail>(v, p.num_tiles, ncl);
-        const uint32_t idesc = w.half < 0 ? kIdesc : kIdescHalf;
+      for (int t = cid; t < p.num_tiles && ok; t += ncl, ++it) {
         const int buf = it & 1;
         const uint32_t use = static_cast<uint32_t>(it >> 1);
         if (!pair_wait(ctx, sm.tempty(buf), (use & 1u) ^ 1u, kStatusMmaTmemEmpty)) {
@@ -297,7 +258,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
 #pragma unroll
           for (int k = 0; k < BK / 16; ++k) {
             // advance 16 elements (32 B) along K inside the swizzle atom
-            umma_bf16_pair(d_tmem, a_desc + 2 * k, b_desc + 2 * k, idesc,
+            umma_bf16_pair(d_tmem, a_desc + 2 * k, b_desc + 2 * k, kIdesc,
                            (kb | k) != 0 ? 1u : 0u);
           }
           umma_commit_pair_multicast(sm.empty(stage), kBothCtas);
@@ -322,9 +283,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     EpiCtx ec{0u, warp & 3, lane, sm.stg(ew), sm.epi_bar(ew), &epi_phase, sm.scratch(),
               &tm_out, &tm_aux, &ctx};
     int it = 0;
-    const int n_items = work_count<Epi::kHalfTail>(p.num_tiles, ncl);
-    for (int v = cid; v < n_items; v += ncl, ++it) {
-      const WorkItem w = work_item<Epi::kHalfTail>(v, p.num_tiles, ncl);
+    for (int t = cid; t < p.num_tiles; t += ncl, ++it) {
       const int buf = it & 1;
       const uint32_t use = static_cast<uint32_t>(it >> 1);
       bool ok = pair_wait(ctx, sm.tfull(buf), use & 1u, kStatusEpiTmemFull);
@@ -332,17 +291,10 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
       if (!ok) break;
       tc_fence_after();
       int pr, n_blk;
-      tile_coords<kGroupPairs, kN>(w.t, p.num_m_tiles, pr, n_blk);
+      tile_coords<kGroupPairs, kN>(t, p.num_m_tiles, pr, n_blk);
       ec.tmem_acc = tmem_base + static_cast<uint32_t>(buf * kTileN);
-      const int64_t row0 = static_cast<int64_t>(pr) * kPairRows + static_cast<int64_t>(rank) * BM;
-      if constexpr (Epi::kHalfTail) {
-        if (w.half >= 0)
-          Epi::tile_half(ec, p, row0, n_blk, w.half);
-        else
-          Epi::tile(ec, p, row0, n_blk);
-      } else {
-        Epi::tile(ec, p, row0, n_blk);
-      }
+      Epi::tile(ec, p, static_cast<int64_t>(pr) * kPairRows + static_cast<int64_t>(rank) * BM,
+                n_blk);
       // all TMEM reads of this accumulator are complete (tcgen05.wait::ld)
       tc_fence_before();
       __syncwarp();

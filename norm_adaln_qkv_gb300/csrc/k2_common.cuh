@@ -416,20 +416,18 @@ __device__ __forceinline__ void epilogue_head_regs(const uint32_t (&y)[64], int 
 //   n_blk     256-column block of the 21504 projection columns
 // Returns after every TMEM read of the block has completed; the stores may
 // still be in flight (bulk groups of this warp's lane 0).
-//   heads     which heads of the tile the block holds: 2 (both, columns
-//             0..255) or just head `first` (0 or 1) in columns 0..127
 template <bool kE4m3 = false>
 __device__ __forceinline__ void epilogue_block(uint32_t tmem_acc, int quad, int lane, uint32_t stg,
                                                const float* nw_all, const QkvParams& p,
-                                               int64_t row0, int n_blk, const CUtensorMap* tm_out,
-                                               int first = 0, int heads = 2) {
+                                               int64_t row0, int n_blk, const CUtensorMap* tm_out) {
   const int kind = n_blk / kNTilesPerKind;
-  const int head0 = (n_blk % kNTilesPerKind) * 2 + first;
-  const int64_t m = row0 + quad * 32 + lane;
-  const uint4* cs_row = rope_row(p, m, kind);
+  const int head0 = (n_blk % kNTilesPerKind) * 2;
   const int64_t m0 = row0 + quad * 32;
+  if (m0 >= p.M) return;  // this warp's rows are all past M: nothing is stored
+  const int64_t m = m0 + lane;
+  const uint4* cs_row = rope_row(p, m, kind);
 #pragma unroll 1
-  for (int j = 0; j < heads; ++j) {
+  for (int j = 0; j < 2; ++j) {
     const uint32_t tcol = tmem_acc + (static_cast<uint32_t>(quad * 32) << 16) +
                           static_cast<uint32_t>(j * kHeadDim);
     epilogue_head<kE4m3>(tcol, lane, stg, nw_all, p, m0, kind, head0 + j, cs_row, tm_out);

@@ -10,34 +10,18 @@
 // column c = kind*7168 + head*128 + d.
 //
 // Structure (one CTA per SM, persistent over 128 x 256 output tiles):
-//   warp 0      TMA producer: per 64-wide k-block, the tile's workspace
-//               rows and 256 weight rows (bf16, 128-B swizzle) into a
-//               shared-memory ring.
+//   warp 0      TMA producer: A (workspace) 128x64 and B (weight) 256x64 bf16
+//               boxes with 128-B swizzle into a 4-stage shared-memory ring;
+//               the first tile's weight boxes start before kernel 1 ends.
 //   warp 1      TMEM allocator and UMMA issuer: tcgen05.mma kind::f16,
 //               M=128 N=256 K=16, four per 64-wide k-block, FP32 accumulator
 //               in TMEM, double-buffered (2 x 256 columns) so the epilogue
 //               of tile i overlaps the main loop of tile i+1.
 //   warps 2..5  epilogue (k2_common.cuh).
-//
-// Schedules.  At these sizes the 84 tiles are fewer than the 152 SMs, and
-// the work is streaming the 231 MB weight.  With the stream-K schedule (the
-// handle path) the 84 x 84 (tile, k-block) units are cut into one
-// contiguous range per CTA, so every SM streams an equal share.  A CTA whose
-// range starts inside a tile writes that partial accumulator (FP32, its
-// first range piece) to a global slot and raises a per-warp flag; the CTA
-// that holds the tile's k-block 0 (and finishes its range with it) adds the
-// following CTAs' partials into its TMEM accumulator, then runs the usual
-// epilogue.  An owner only ever waits for other CTAs' first pieces, which
-// they compute first, so no wait is circular; all CTAs are resident (one per
-// SM, grid = SM count).  The sum is still the FP32 accumulation of the
-// pages, in another order.  Without scratch (the allocation-free entry
-// point) each CTA takes whole tiles.  The weight loads of the first ring
-// stages go out before the wait on kernel 1 (they do not depend on it).
-//
-// Every wait is bounded: past a 2 s limit the waiting role records a code in
-// the device status word, raises a CTA-wide abort flag, and all roles drain
-// what they issued (TMA loads, UMMAs, TMA stores) before TMEM is freed and
-// the CTA exits.
+// Every mbarrier wait is bounded: past a 2 s limit the waiting role records a
+// code in the device status word, raises a CTA-wide abort flag, and all roles
+// drain what they issued (TMA loads, UMMAs, TMA stores) before TMEM is freed
+// and the CTA exits.
 #include "k2_common.cuh"
 
 namespace mh3 {
@@ -115,90 +99,7 @@ struct Smem {
   __device__ float* norm_w() const { return reinterpret_cast<float*>(ptr + L::kOffNormW); }
 };
 
-// Iterates this CTA's (tile, k-block) units in issue order: with stream-K a
-// contiguous range of the num_tiles * 84 units, otherwise the tiles
-// blockIdx.x, blockIdx.x + G, ... with all 84 k-blocks each.
-template <bool kSK>
-struct Units {
-  int64_t u, u_end;  // stream-K range
-  int t, kb;         // current tile and k-block
-  int num_tiles;
-  __device__ Units(const QkvParams& p) : num_tiles(p.num_tiles) {
-    if (kSK) {
-      const int64_t U = static_cast<int64_t>(p.num_tiles) * kKBlocks;
-      u = static_cast<int64_t>(blockIdx.x) * U / gridDim.x;
-      u_end = static_cast<int64_t>(blockIdx.x + 1) * U / gridDim.x;
-      t = static_cast<int>(u / kKBlocks);
-      kb = static_cast<int>(u % kKBlocks);
-    } else {
-      u = u_end = 0;
-      t = blockIdx.x;
-      kb = 0;
-    }
-  }
-  __device__ bool valid() const { return kSK ? u < u_end : t < num_tiles; }
-  __device__ bool last_of_piece() const { return kb == kKBlocks - 1 || (kSK && u + 1 == u_end); }
-  __device__ bool first_of_piece(bool first_unit) const { return kb == 0 || first_unit; }
-  __device__ void next() {
-    if (kSK) ++u;
-    if (++kb == kKBlocks) {
-      kb = 0;
-      t += kSK ? 1 : static_cast<int>(gridDim.x);
-    }
-  }
-};
-
-// Stream-K partial slots: [cta][warp][column][lane] FP32.
-__device__ __forceinline__ float* sk_slot(const QkvParams& p, int cta, int quad) {
-  return p.sk_partial + ((static_cast<int64_t>(cta) * 4 + quad) * BN) * 32;
-}
-
-// This warp's 32 accumulator rows x 256 columns -> its partial slot.
-__device__ __forceinline__ void sk_store_partial(uint32_t tacc, float* slot, int lane) {
-#pragma unroll 1
-  for (int c = 0; c < BN / 32; ++c) {
-    uint32_t v[32];
-    tmem_ld_x32(tacc + 32 * c, v);
-    tmem_wait_ld();
-#pragma unroll
-    for (int i = 0; i < 32; ++i) __stcg(slot + (32 * c + i) * 32 + lane, __uint_as_float(v[i]));
-  }
-}
-
-// accumulator += partial slot (FP32 additions), in TMEM.
-__device__ __forceinline__ void sk_add_partial(uint32_t tacc, const float* slot, int lane) {
-#pragma unroll 1
-  for (int c = 0; c < BN / 32; ++c) {
-    uint32_t v[32];
-    float q[32];
-    tmem_ld_x32(tacc + 32 * c, v);
-#pragma unroll
-    for (int i = 0; i < 32; ++i) q[i] = __ldcg(slot + (32 * c + i) * 32 + lane);
-    tmem_wait_ld();
-#pragma unroll
-    for (int i = 0; i < 32; ++i) v[i] = __float_as_uint(__fadd_rn(__uint_as_float(v[i]), q[i]));
-    tmem_st_x32(tacc + 32 * c, v);
-  }
-  tmem_wait_st();
-}
-
-// Bounded wait (lane 0) for a flag to become 1; false on abort or timeout.
-__device__ __noinline__ bool sk_wait_flag(const int* flag, volatile int* abort_flag, int* status) {
-  const uint64_t t0 = globaltimer_ns();
-  for (uint32_t n = 0;; ++n) {
-    if (ld_acquire_gpu(flag) != 0) return true;
-    if ((n & 63u) == 63u) {
-      if (*abort_flag) return false;
-      if (globaltimer_ns() - t0 > kWaitLimitNs) {
-        *abort_flag = 1;
-        atomicCAS(status, 0, kStatusSkPartial);
-        return false;
-      }
-    }
-  }
-}
-
-template <class L, bool kSK>
+template <class L>
 __global__ void __launch_bounds__(kThreads, 1)
     qkv_gemm_kernel(const __grid_constant__ CUtensorMap tm_a, const __grid_constant__ CUtensorMap tm_b,
                     const __grid_constant__ CUtensorMap tm_out, const QkvParams p) {
@@ -250,41 +151,44 @@ __global__ void __launch_bounds__(kThreads, 1)
       uint32_t phase = 0;
       bool ok = true;
       uint32_t issued_mask = 0, issued_parity = 0;
-      Units<kSK> it(p);
-      // The weight does not depend on kernel 1: the first ring stages' weight
-      // boxes go out at once, their workspace boxes after kernel 1 is done.
-      int pre_t[kStages], pre_kb[kStages];
+      // The weight does not depend on kernel 1, which may still be running
+      // (the workspace is its output): the first tile's weight boxes for the
+      // whole ring go out at once, and only then does this thread wait for
+      // kernel 1 and load the workspace boxes of those stages.
       int n_pre = 0;
-      for (; n_pre < kStages && it.valid(); ++n_pre, it.next()) {
+      if (static_cast<int>(blockIdx.x) < p.num_tiles) {
         int m_blk, n_blk;
-        tile_coords<kGroupM>(it.t, p.num_m_tiles, m_blk, n_blk);
-        pre_t[n_pre] = m_blk;
-        pre_kb[n_pre] = it.kb;
-        mbar_arrive_expect_tx(sm.full(n_pre), L::kStageBytes);
-        tma_load_2d(sm.b(n_pre), &tm_b, sm.full(n_pre), it.kb * BK, n_blk * BN);
-        issued_mask |= 1u << n_pre;
-      }
-      griddep_wait();  // kernel 1 writes the workspace
-      for (int i = 0; i < n_pre; ++i)
-        tma_load_2d(sm.a(i), &tm_a, sm.full(i), pre_kb[i] * BK, pre_t[i] * BM);
-      stage = n_pre % kStages;
-      phase = n_pre == kStages ? 1u : 0u;
-      for (; it.valid() && ok; it.next()) {
-        int m_blk, n_blk;
-        tile_coords<kGroupM>(it.t, p.num_m_tiles, m_blk, n_blk);
-        if (!wait_phase<false>(sm.empty(stage), phase ^ 1u, abort_flag, p.status,
-                               kStatusProducerEmpty)) {
-          ok = false;
-          break;
+        tile_coords<kGroupM>(blockIdx.x, p.num_m_tiles, m_blk, n_blk);
+        for (; n_pre < kStages; ++n_pre) {
+          mbar_arrive_expect_tx(sm.full(n_pre), L::kStageBytes);
+          tma_load_2d(sm.b(n_pre), &tm_b, sm.full(n_pre), n_pre * BK, n_blk * BN);
+          issued_mask |= 1u << n_pre;
         }
-        mbar_arrive_expect_tx(sm.full(stage), L::kStageBytes);
-        tma_load_2d(sm.a(stage), &tm_a, sm.full(stage), it.kb * BK, m_blk * BM);
-        tma_load_2d(sm.b(stage), &tm_b, sm.full(stage), it.kb * BK, n_blk * BN);
-        issued_mask |= 1u << stage;
-        issued_parity = (issued_parity & ~(1u << stage)) | (phase << stage);
-        if (++stage == kStages) {
-          stage = 0;
-          phase ^= 1u;
+        griddep_wait();
+        for (int s = 0; s < n_pre; ++s)
+          tma_load_2d(sm.a(s), &tm_a, sm.full(s), s * BK, m_blk * BM);
+        phase = 1u;  // the ring has been filled once
+      } else {
+        griddep_wait();
+      }
+      for (int t = blockIdx.x; t < p.num_tiles && ok; t += gridDim.x) {
+        int m_blk, n_blk;
+        tile_coords<kGroupM>(t, p.num_m_tiles, m_blk, n_blk);
+        for (int kb = t == static_cast<int>(blockIdx.x) ? n_pre : 0; kb < kKBlocks; ++kb) {
+          if (!wait_phase<false>(sm.empty(stage), phase ^ 1u, abort_flag, p.status,
+                                 kStatusProducerEmpty)) {
+            ok = false;
+            break;
+          }
+          mbar_arrive_expect_tx(sm.full(stage), L::kStageBytes);
+          tma_load_2d(sm.a(stage), &tm_a, sm.full(stage), kb * BK, m_blk * BM);
+          tma_load_2d(sm.b(stage), &tm_b, sm.full(stage), kb * BK, n_blk * BN);
+          issued_mask |= 1u << stage;
+          issued_parity = (issued_parity & ~(1u << stage)) | (phase << stage);
+          if (++stage == kStages) {
+            stage = 0;
+            phase ^= 1u;
+          }
         }
       }
       if (!ok) {
@@ -300,44 +204,38 @@ __global__ void __launch_bounds__(kThreads, 1)
       int stage = 0;
       uint32_t phase = 0;
       bool ok = true;
-      int piece = 0;  // accumulator pieces started (whole tiles or stream-K parts)
-      uint32_t d_tmem = tmem_base;
-      bool first_unit = true;
-      for (Units<kSK> it(p); it.valid(); it.next()) {
-        const bool start = it.first_of_piece(first_unit);
-        first_unit = false;
-        if (start) {
-          const int buf = piece & 1;
-          const uint32_t use = static_cast<uint32_t>(piece >> 1);
-          if (!wait_phase<false>(sm.tempty(buf), (use & 1u) ^ 1u, abort_flag, p.status,
-                                 kStatusMmaTmemEmpty)) {
-            ok = false;
-            break;
-          }
-          tc_fence_after();
-          d_tmem = tmem_base + static_cast<uint32_t>(buf * BN);
-        }
-        if (!wait_phase<false>(sm.full(stage), phase, abort_flag, p.status, kStatusMmaFull)) {
+      int it = 0;
+      for (int t = blockIdx.x; t < p.num_tiles && ok; t += gridDim.x, ++it) {
+        const int buf = it & 1;
+        const uint32_t use = static_cast<uint32_t>(it >> 1);
+        if (!wait_phase<false>(sm.tempty(buf), (use & 1u) ^ 1u, abort_flag, p.status,
+                               kStatusMmaTmemEmpty)) {
           ok = false;
           break;
         }
         tc_fence_after();
-        const uint64_t a_desc = sw128_kmajor_desc(sm.a(stage));
-        const uint64_t b_desc = sw128_kmajor_desc(sm.b(stage));
+        const uint32_t d_tmem = tmem_base + static_cast<uint32_t>(buf * BN);
+        for (int kb = 0; kb < kKBlocks; ++kb) {
+          if (!wait_phase<false>(sm.full(stage), phase, abort_flag, p.status, kStatusMmaFull)) {
+            ok = false;
+            break;
+          }
+          tc_fence_after();
+          const uint64_t a_desc = sw128_kmajor_desc(sm.a(stage));
+          const uint64_t b_desc = sw128_kmajor_desc(sm.b(stage));
 #pragma unroll
-        for (int k = 0; k < BK / 16; ++k) {
-          // advance 16 elements (32 B) along K inside the swizzle atom
-          umma_bf16(d_tmem, a_desc + 2 * k, b_desc + 2 * k, kIdesc, (!start || k != 0) ? 1u : 0u);
+          for (int k = 0; k < BK / 16; ++k) {
+            // advance 16 elements (32 B) along K inside the swizzle atom
+            umma_bf16(d_tmem, a_desc + 2 * k, b_desc + 2 * k, kIdesc, (kb | k) != 0 ? 1u : 0u);
+          }
+          umma_commit(sm.empty(stage));
+          if (++stage == kStages) {
+            stage = 0;
+            phase ^= 1u;
+          }
         }
-        umma_commit(sm.empty(stage));
-        if (++stage == kStages) {
-          stage = 0;
-          phase ^= 1u;
-        }
-        if (it.last_of_piece()) {
-          umma_commit(sm.tfull(piece & 1));
-          ++piece;
-        }
+        if (!ok) break;
+        umma_commit(sm.tfull(buf));
       }
       if (!ok) {
         umma_commit(sm.drain());
@@ -349,23 +247,10 @@ __global__ void __launch_bounds__(kThreads, 1)
     // ------------------------------------------------------------ epilogue
     const int quad = warp & 3;  // TMEM lane quadrant this warp may read
     const uint32_t stg = sm.stg(warp - 2);
-    Units<kSK> it(p);
-    int piece = 0;
-    while (it.valid()) {
-      // the accumulator piece [k0, k1) of tile it.t
-      const int t = it.t;
-      const int k0 = it.kb;
-      int k1;
-      if (kSK) {
-        const int64_t left = it.u_end - it.u;
-        k1 = left < kKBlocks - k0 ? k0 + static_cast<int>(left) : kKBlocks;
-      } else {
-        k1 = kKBlocks;
-      }
-      for (int k = k0; k < k1; ++k) it.next();
-      const int buf = piece & 1;
-      const uint32_t use = static_cast<uint32_t>(piece >> 1);
-      ++piece;
+    int it = 0;
+    for (int t = blockIdx.x; t < p.num_tiles; t += gridDim.x, ++it) {
+      const int buf = it & 1;
+      const uint32_t use = static_cast<uint32_t>(it >> 1);
       bool ok = wait_phase<false>(sm.tfull(buf), use & 1u, abort_flag, p.status,
                                   kStatusEpiTmemFull);
       ok = __all_sync(0xFFFFFFFFu, ok);
@@ -373,50 +258,8 @@ __global__ void __launch_bounds__(kThreads, 1)
       tc_fence_after();
       int m_blk, n_blk;
       tile_coords<kGroupM>(t, p.num_m_tiles, m_blk, n_blk);
-      const uint32_t tacc = tmem_base + static_cast<uint32_t>(buf * BN) +
-                            (static_cast<uint32_t>(quad * 32) << 16);
-      const bool rows_used = static_cast<int64_t>(m_blk) * BM + quad * 32 < p.M;
-      if (kSK && k0 > 0) {
-        // not this tile's owner: hand the partial to the CTA that holds k-block 0
-        if (rows_used) {
-          sk_store_partial(tacc, sk_slot(p, blockIdx.x, quad), lane);
-          __threadfence();
-          __syncwarp();
-          if (lane == 0) st_release_gpu(p.sk_flags + blockIdx.x * 4 + quad, 1);
-        }
-      } else {
-        if (kSK && k1 < kKBlocks && rows_used) {
-          // owner of a split tile: add the following CTAs' pieces of it
-          const int64_t U = static_cast<int64_t>(p.num_tiles) * kKBlocks;
-          const int64_t tile_end = static_cast<int64_t>(t + 1) * kKBlocks;
-          bool got = true;
-          for (int c = blockIdx.x + 1;
-               c < static_cast<int>(gridDim.x) && static_cast<int64_t>(c) * U / gridDim.x < tile_end;
-               ++c) {
-            int* flag = p.sk_flags + c * 4 + quad;
-            bool w = true;
-            if (lane == 0) w = sk_wait_flag(flag, abort_flag, p.status);
-            w = __shfl_sync(0xFFFFFFFFu, w ? 1 : 0, 0) != 0;
-            if (!w) {
-              got = false;
-              break;
-            }
-            (void)ld_acquire_gpu(flag);  // every lane's own acquire of the partial
-            __syncwarp();
-            sk_add_partial(tacc, sk_slot(p, c, quad), lane);
-            __syncwarp();
-            if (lane == 0) flag[0] = 0;  // consumed: zero again for the next launch
-          }
-          if (!got) {
-            tc_fence_before();
-            __syncwarp();
-            if (lane == 0) mbar_arrive(sm.tempty(buf));
-            break;
-          }
-        }
-        epilogue_block(tmem_base + static_cast<uint32_t>(buf * BN), quad, lane, stg, sm.norm_w(),
-                       p, static_cast<int64_t>(m_blk) * BM, n_blk, &tm_out);
-      }
+      epilogue_block(tmem_base + static_cast<uint32_t>(buf * BN), quad, lane, stg, sm.norm_w(), p,
+                     static_cast<int64_t>(m_blk) * BM, n_blk, &tm_out);
       // all TMEM reads of this accumulator are complete (tcgen05.wait::ld)
       tc_fence_before();
       __syncwarp();
@@ -446,44 +289,29 @@ int qkv_a_box_rows(int64_t M) {
   return M <= kTinyRows ? kTinyRows : (M <= kSmallRows ? kSmallRows : BM);
 }
 
-template <bool kSK>
-cudaError_t prepare_layouts() {
-  cudaError_t e = cudaFuncSetAttribute(qkv_gemm_kernel<FullLayout, kSK>,
+cudaError_t qkv_prepare_device() {
+  cudaError_t e = cudaFuncSetAttribute(qkv_gemm_kernel<FullLayout>,
                                        cudaFuncAttributeMaxDynamicSharedMemorySize,
                                        FullLayout::kSmemAlloc);
   if (e != cudaSuccess) return e;
-  e = cudaFuncSetAttribute(qkv_gemm_kernel<SmallLayout, kSK>,
+  e = cudaFuncSetAttribute(qkv_gemm_kernel<SmallLayout>,
                            cudaFuncAttributeMaxDynamicSharedMemorySize, SmallLayout::kSmemAlloc);
   if (e != cudaSuccess) return e;
-  return cudaFuncSetAttribute(qkv_gemm_kernel<TinyLayout, kSK>,
+  return cudaFuncSetAttribute(qkv_gemm_kernel<TinyLayout>,
                               cudaFuncAttributeMaxDynamicSharedMemorySize, TinyLayout::kSmemAlloc);
-}
-
-cudaError_t qkv_prepare_device() {
-  const cudaError_t e = prepare_layouts<false>();
-  return e != cudaSuccess ? e : prepare_layouts<true>();
-}
-
-size_t qkv_sk_partial_bytes(int grid) { return static_cast<size_t>(grid) * 4 * BN * 32 * 4; }
-size_t qkv_sk_flags_bytes(int grid) { return static_cast<size_t>(grid) * 4 * sizeof(int); }
-
-template <bool kSK>
-cudaError_t launch_layout(const QkvMaps& maps, const QkvParams& p, int grid, cudaStream_t stream) {
-  // the A map's box height must be qkv_a_box_rows(p.M)
-  if (p.M <= kTinyRows)
-    return launch_k2(qkv_gemm_kernel<TinyLayout, kSK>, grid, kThreads, TinyLayout::kSmemAlloc,
-                     stream, maps, p);
-  if (p.M <= kSmallRows)
-    return launch_k2(qkv_gemm_kernel<SmallLayout, kSK>, grid, kThreads, SmallLayout::kSmemAlloc,
-                     stream, maps, p);
-  return launch_k2(qkv_gemm_kernel<FullLayout, kSK>, grid, kThreads, FullLayout::kSmemAlloc,
-                   stream, maps, p);
 }
 
 cudaError_t launch_qkv(const QkvMaps& maps, const QkvParams& p, int grid, cudaStream_t stream) {
   if (p.M <= 0) return cudaSuccess;
-  if (p.sk_partial != nullptr) return launch_layout<true>(maps, p, grid, stream);
-  return launch_layout<false>(maps, p, grid, stream);
+  // the A map's box height must be qkv_a_box_rows(p.M)
+  if (p.M <= kTinyRows)
+    return launch_k2(qkv_gemm_kernel<TinyLayout>, grid, kThreads, TinyLayout::kSmemAlloc, stream,
+                     maps, p);
+  if (p.M <= kSmallRows)
+    return launch_k2(qkv_gemm_kernel<SmallLayout>, grid, kThreads, SmallLayout::kSmemAlloc, stream,
+                     maps, p);
+  return launch_k2(qkv_gemm_kernel<FullLayout>, grid, kThreads, FullLayout::kSmemAlloc, stream,
+                   maps, p);
 }
 
 }  // namespace mh3

@@ -34,14 +34,6 @@ struct QkvPairEpiT {
     k2::epilogue_block<kE4m3>(c.tmem_acc, c.quad, c.lane, c.stg, c.scratch, p, row0, n_blk,
                               c.tm_out);
   }
-
-  // tail split: one head per work item
-  static constexpr bool kHalfTail = true;
-  __device__ static void tile_half(const gp::EpiCtx& c, const Params& p, int64_t row0, int n_blk,
-                                   int half) {
-    k2::epilogue_block<kE4m3>(c.tmem_acc, c.quad, c.lane, c.stg, c.scratch, p, row0, n_blk,
-                              c.tm_out, half, 1);
-  }
 };
 using QkvPairEpi = QkvPairEpiT<false>;
 using QkvE4m3PairEpi = QkvPairEpiT<true>;

@@ -49,8 +49,6 @@ struct mh3_preattn_ctx {
   void* act_sf = nullptr;
   size_t act_sf_bytes = 0;
   int test_stall_next = 0;  // test hook for the next CTA-pair QKV GEMM launch (bf16 or NVFP4)
-  float* sk_partial = nullptr;  // stream-K scratch of the single-CTA QKV GEMM (M <= 128)
-  int* sk_flags = nullptr;      // its per-(CTA, warp) flags, zero between launches
 };
 
 namespace {
@@ -268,8 +266,7 @@ int launch_stage1(cudaStream_t s, int num_sms, int* status, int64_t M, const mh3
 int launch_stage2(cudaStream_t s, int num_sms, int max_clusters, int* status, int64_t M,
                   const mh3_bf16* ws, const mh3_bf16* W, const mh3_bf16* qw, const mh3_bf16* kw,
                   const mh3_bf16* cs, int64_t S, const int64_t* pos, int P, float qk_eps,
-                  mh3_bf16* out, int* test_stall = nullptr, float* sk_partial = nullptr,
-                  int* sk_flags = nullptr) {
+                  mh3_bf16* out, int* test_stall = nullptr) {
   const bool pair = M > 128 && max_clusters > 0;
   QkvMaps maps;
   int rc = encode_maps(maps, M, ws, W, P, out, pair ? 128u : 256u,
@@ -299,13 +296,7 @@ int launch_stage2(cudaStream_t s, int num_sms, int max_clusters, int* status, in
   } else {
     p.num_m_tiles = static_cast<int>((M + 127) / 128);
     p.num_tiles = p.num_m_tiles * (kQkvRows / 256);
-    int grid = p.num_tiles < num_sms ? p.num_tiles : num_sms;
-    if (sk_partial != nullptr && sk_flags != nullptr) {
-      // stream-K: one CTA per SM, each streaming an equal share of the weight
-      p.sk_partial = sk_partial;
-      p.sk_flags = sk_flags;
-      grid = num_sms;
-    }
+    const int grid = p.num_tiles < num_sms ? p.num_tiles : num_sms;
     e = launch_qkv(maps, p, grid, s);
   }
   if (e != cudaSuccess) return cuda_fail(e, "QKV GEMM launch");
@@ -370,15 +361,10 @@ int mh3_preattn_create(mh3_preattn_t* handle, int device) {
   h->out_proj_clusters = out_proj_clusters;
   e = cudaMalloc(&h->d_status, sizeof(int));
   if (e == cudaSuccess) e = cudaMemset(h->d_status, 0, sizeof(int));
-  if (e == cudaSuccess) e = cudaMalloc(&h->sk_partial, qkv_sk_partial_bytes(h->num_sms));
-  if (e == cudaSuccess) e = cudaMalloc(&h->sk_flags, qkv_sk_flags_bytes(h->num_sms));
-  if (e == cudaSuccess) e = cudaMemset(h->sk_flags, 0, qkv_sk_flags_bytes(h->num_sms));
   if (e != cudaSuccess) {
-    for (void* b : {static_cast<void*>(h->d_status), static_cast<void*>(h->sk_partial),
-                    static_cast<void*>(h->sk_flags)})
-      if (b) cudaFree(b);
+    if (h->d_status) cudaFree(h->d_status);
     delete h;
-    return cuda_fail(e, "allocating the status word and the stream-K scratch");
+    return cuda_fail(e, "allocating the status word");
   }
   *handle = h;
   return MH3_OK;
@@ -391,8 +377,7 @@ int mh3_preattn_destroy(mh3_preattn_t h) {
     cudaError_t e = cudaFree(h->ws);
     if (e != cudaSuccess) rc = cuda_fail(e, "freeing the handle workspace");
   }
-  for (void* buf : {h->ws_y, h->act_q, h->act_sf, static_cast<void*>(h->sk_partial),
-                    static_cast<void*>(h->sk_flags)}) {
+  for (void* buf : {h->ws_y, h->act_q, h->act_sf}) {
     if (buf == nullptr) continue;
     cudaError_t e = cudaFree(buf);
     if (e != cudaSuccess && rc == MH3_OK) rc = cuda_fail(e, "freeing the handle workspace");
@@ -465,7 +450,7 @@ int mh3_preattn_run(mh3_preattn_t h, void* stream, int64_t M, const mh3_bf16* x,
   if (rc) return rc;
   return launch_stage2(s, h->num_sms, h->max_clusters, h->d_status, M, workspace, qkv_weight,
                        q_norm_weight, k_norm_weight, rope_cos_sin, S, rope_positions, P, qk, out,
-                       &h->test_stall_next, h->sk_partial, h->sk_flags);
+                       &h->test_stall_next);
 }
 
 int mh3_preattn_norm_adaln(mh3_preattn_t h, void* stream, int64_t M, const mh3_bf16* x,
@@ -498,8 +483,7 @@ int mh3_preattn_qkv(mh3_preattn_t h, void* stream, int64_t M, const mh3_bf16* wo
   if ((rc = check_ptr(workspace, "workspace", 16))) return rc;
   return launch_stage2(static_cast<cudaStream_t>(stream), h->num_sms, h->max_clusters,
                        h->d_status, M, workspace, qkv_weight, q_norm_weight, k_norm_weight,
-                       rope_cos_sin, S, rope_positions, P, qk_eps, out, &h->test_stall_next,
-                       h->sk_partial, h->sk_flags);
+                       rope_cos_sin, S, rope_positions, P, qk_eps, out, &h->test_stall_next);
 }
 
 int mh3_preattn_set_test_stall(mh3_preattn_t h, int stall) {
@@ -521,9 +505,6 @@ int mh3_preattn_device_status(mh3_preattn_t h, void* stream, int* device_code) {
   if (v != 0) {
     e = cudaMemset(h->d_status, 0, sizeof(int));
     if (e != cudaSuccess) return cuda_fail(e, "clearing the status word");
-    // a launch that gave up may have left stream-K flags raised
-    e = cudaMemset(h->sk_flags, 0, qkv_sk_flags_bytes(h->num_sms));
-    if (e != cudaSuccess) return cuda_fail(e, "clearing the stream-K flags");
   }
   *device_code = v;
   return MH3_OK;

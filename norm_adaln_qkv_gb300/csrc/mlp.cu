@@ -36,7 +36,6 @@ struct SwigluEpi {
   using Params = SwigluParams;
   static constexpr int kKBlocks = kHidden / BK;          // 84
   static constexpr int kNTiles = kMlpInter / kHeadDim;    // 112
-  static constexpr bool kHalfTail = false;
   __device__ static int b_row(int n_blk, int rank) {
     return (rank == 0 ? 0 : kMlpInter) + n_blk * kHeadDim;
   }

@@ -104,8 +104,8 @@ __device__ __forceinline__ float exact_diff_sign(float a, float b, float c) {
 
 // The bracket [t_lo, t_hi] rounds to the adjacent codes lo < hi: decide at
 // their midpoint m with the exact sign of amax * gs - 6m.
-static __device__ __noinline__ uint32_t scale_code_at_boundary(float amax, float gs, uint32_t lo,
-                                                        uint32_t hi) {
+__device__ __forceinline__ uint32_t scale_code_at_boundary(float amax, float gs, uint32_t lo,
+                                                           uint32_t hi) {
   const float six_m = __fmul_rn(__fadd_rn(ue4m3_value(lo), ue4m3_value(hi)), 3.0f);  // exact
   const float d = exact_diff_sign(amax, gs, six_m);
   if (d > 0.0f) return hi;
@@ -154,24 +154,29 @@ __device__ __forceinline__ uint32_t codes8(const uint4& w, float enc) {
   return e2m1x8(v);
 }
 
-// The elements whose two bracketing codes differ: decide each at the
-// midpoint m of its two codes with the exact sign of |v| * gs - m * sf.
-static __device__ __noinline__ uint32_t codes8_at_boundary(uint4 w, uint32_t c_lo, uint32_t c_hi, float gs,
-                                                    float sf) {
-  const uint32_t ws[4] = {w.x, w.y, w.z, w.w};
-  uint32_t out = c_lo;
-#pragma unroll 1
-  for (int j = 0; j < 8; ++j) {
-    const uint32_t a = (c_lo >> (4 * j)) & 0xFu, b = (c_hi >> (4 * j)) & 0xFu;
-    if (a == b) continue;
-    const uint32_t ma = a & 7u, mb = b & 7u;  // adjacent magnitudes, same sign
-    const uint32_t lo = ma < mb ? ma : mb, hi = ma < mb ? mb : ma;
-    const uint32_t h = ws[j >> 1] >> (16 * (j & 1));
+// The elements whose two bracketing codes differ (a nibble of lo ^ hi):
+// decide each at the midpoint m between its two adjacent magnitudes with the
+// exact sign of |v| * gs - m * sf.  4m for the midpoints above magnitude
+// codes 0..6 (0.25, 0.75, 1.25, 1.75, 2.5, 3.5, 5), five bits each.
+constexpr uint64_t kE2m1Mid4 = 1ull | 3ull << 5 | 5ull << 10 | 7ull << 15 | 10ull << 20 |
+                               14ull << 25 | 20ull << 30;
+__device__ __forceinline__ uint32_t codes8_at_boundary(const uint4& w, uint32_t lo, uint32_t hi,
+                                                       float gs, float sf) {
+  uint32_t out = lo;
+  uint32_t diff = lo ^ hi;
+  while (diff != 0u) {
+    const int j = (__ffs(static_cast<int>(diff)) - 1) >> 2;  // element with a differing code
+    diff &= ~(0xFu << (4 * j));
+    const uint32_t a = (lo >> (4 * j)) & 7u, b = (hi >> (4 * j)) & 7u;
+    const uint32_t ma = a < b ? a : b;  // adjacent magnitudes ma, ma + 1
+    const int word = j >> 1;
+    uint32_t h = word == 0 ? w.x : (word == 1 ? w.y : (word == 2 ? w.z : w.w));
+    h = (j & 1) ? (h >> 16) : h;
     const float mag = __uint_as_float((h & 0x7FFFu) << 16);  // |v|
-    const float m_sf = __fmul_rn(__fmul_rn(__fadd_rn(e2m1_value(lo), e2m1_value(hi)), 0.5f), sf);
-    const float d = exact_diff_sign(mag, gs, m_sf);
-    const uint32_t pick = d > 0.0f ? hi : (d < 0.0f ? lo : ((lo & 1u) ? hi : lo));
-    out = (out & ~(0xFu << (4 * j))) | ((pick | (a & 8u)) << (4 * j));
+    const float m = 0.25f * static_cast<float>((kE2m1Mid4 >> (5 * ma)) & 31u);
+    const float d = exact_diff_sign(mag, gs, __fmul_rn(m, sf));  // m * sf exact
+    const uint32_t pick = d > 0.0f ? ma + 1 : (d < 0.0f ? ma : ((ma & 1u) ? ma + 1 : ma));
+    out = (out & ~(7u << (4 * j))) | (pick << (4 * j));  // the sign bit stays
   }
   return out;
 }

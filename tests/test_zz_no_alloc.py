@@ -9,8 +9,8 @@ other test by the time it gets here.
 
 Calls in a row of the new entry point (different sizes, so each call starts
 from the previous call's leftover workspace) must give the same outputs as
-mh3_preattn_run, within the stage's output tolerance (and bit for bit where
-both run the same kernels, M > 128).
+mh3_preattn_run, within the stage's output tolerance (and, as both run the
+same kernels, bit for bit).
 """
 import pytest
 import torch
@@ -61,13 +61,8 @@ def test_noalloc_matches_run_on_two_calls_in_a_row(cuda_lib):
 
     for d, o, r in zip(cases, outs, refs):
         st = check_outputs(_tokens(o), _tokens(r), f"noalloc M={d.M}")
-        if d.M > 128:
-            # the same kernels on the same inputs: bit-identical as well
-            assert st["exact"] == 1.0, st
-        else:
-            # mh3_preattn_run splits these small GEMMs over all SMs (another
-            # FP32 summation order); the allocation-free call does not
-            assert st["exact"] > 0.97, st
+        # the same kernels on the same inputs: bit-identical as well
+        assert st["exact"] == 1.0, st
     h.close()
 
 
