@@ -337,6 +337,66 @@ int mh3_mlp_validate(int64_t M, const mh3_bf16* x, const mh3_bf16* x_norm_weight
 /* Bytes of the MLP intermediate y, [M, 14336] bf16: M * 14336 * 2 (0 for M <= 0). */
 size_t mh3_mlp_workspace_y_bytes(int64_t M);
 
+/* ------------------------------------------------------- FP8 (W8A8) MLP block
+ * The MLP block with E4M3 weights and per-token E4M3 activations, as the
+ * formula block of the page "flashinfer.diffusion_ops.minimax_h3_mlp_fp8_sm120"
+ * defines it:
+ *
+ *   n   = bf16(rmsnorm(x, eps) * x_norm_weight)
+ *   a   = bf16(adaln_shift[i] + n * bf16(1 + adaln_scale[i])),  0 for a bad i
+ *   a_q = e4m3(a / s_a),  s_a = RN(amax_row(|a|) / 448)            per token
+ *   h   = bf16(a_q @ fc1_weight_q^T * s_a * fc1_weight_scale)      FP32 accumulation
+ *   y   = bf16(bf16(silu(h_gate)) * h_up)                          [M, 14336]
+ *   y_q = e4m3(y / s_y),  s_y = RN(amax_row(|y|) / 448)            per token
+ *   o   = bf16(y_q @ fc2_weight_q^T * s_y * fc2_weight_scale)      FP32 accumulation
+ *   out = bf16(residual + bf16(gate[i] * o)),  gate 0 for a bad i
+ *
+ * e4m3(v / s) rounds the exact quotient once (nearest even, saturating at
+ * +-448, sign kept); a row whose amax is 0 gets s = 0 and codes +0.  The
+ * scale products are two FP32 roundings in the printed order.  Four kernels
+ * and one memset run on `stream`: the norm/AdaLN/quantisation kernel, the
+ * fc1 GEMM (tcgen05 kind::f8f6f4, SwiGLU epilogue, which also folds each
+ * row's largest |y| into workspace_y_scale), the y quantiser (which then
+ * replaces that amax by s_y), and the fc2 GEMM (gated-residual epilogue).
+ *
+ *   fc1_weight_q      E4M3 codes [28672, 5376] (rows [0, 14336) gate, the
+ *                     rest up), 16-B aligned; fc1_weight_scale FP32 [28672]
+ *   fc2_weight_q      E4M3 codes [5376, 14336]; fc2_weight_scale FP32 [5376]
+ *   workspace_a_q     E4M3 [M, 5376] or NULL; workspace_a_scale FP32 [M] or NULL
+ *   workspace_y       bf16 [M, 14336] or NULL
+ *   workspace_y_q     E4M3 [M, 14336] or NULL; workspace_y_scale FP32 [M] or NULL
+ *                     (NULL: handle-owned, grown on `stream`; runs of one
+ *                     handle on different streams then race)
+ *   other arguments as in mh3_mlp_run (int64 adaln_index, shared row count,
+ *   out may be residual or x).  Returns MH3_OK or an error code; nothing is
+ *   launched on an argument error. */
+int mh3_mlp_fp8_run(mh3_preattn_t handle, void* stream, int64_t M, const mh3_bf16* x,
+                    const mh3_bf16* x_norm_weight, const mh3_bf16* adaln_scale,
+                    int64_t scale_row_stride, const mh3_bf16* adaln_shift,
+                    int64_t shift_row_stride, const mh3_bf16* gate, int64_t gate_row_stride,
+                    int64_t rows, const int64_t* adaln_index, const mh3_bf16* residual,
+                    const uint8_t* fc1_weight_q, const float* fc1_weight_scale,
+                    const uint8_t* fc2_weight_q, const float* fc2_weight_scale, float eps,
+                    uint8_t* workspace_a_q, float* workspace_a_scale, mh3_bf16* workspace_y,
+                    uint8_t* workspace_y_q, float* workspace_y_scale, mh3_bf16* out);
+
+/* Host-only validation of an mh3_mlp_fp8_run argument set; same rules and codes. */
+int mh3_mlp_fp8_validate(int64_t M, const mh3_bf16* x, const mh3_bf16* x_norm_weight,
+                         const mh3_bf16* adaln_scale, int64_t scale_row_stride,
+                         const mh3_bf16* adaln_shift, int64_t shift_row_stride,
+                         const mh3_bf16* gate, int64_t gate_row_stride, int64_t rows,
+                         const int64_t* adaln_index, const mh3_bf16* residual,
+                         const uint8_t* fc1_weight_q, const float* fc1_weight_scale,
+                         const uint8_t* fc2_weight_q, const float* fc2_weight_scale, float eps,
+                         const uint8_t* workspace_a_q, const float* workspace_a_scale,
+                         const mh3_bf16* workspace_y, const uint8_t* workspace_y_q,
+                         const float* workspace_y_scale, const mh3_bf16* out);
+
+/* Bytes of one FP8 MLP workspace for M tokens: which = 0 a_q (M * 5376),
+ * 1 a scale (M * 4), 2 y (M * 14336 * 2), 3 y_q (M * 14336), 4 y scale
+ * (M * 4); 0 for M <= 0 or another `which`. */
+size_t mh3_mlp_fp8_workspace_bytes(int64_t M, int which);
+
 /* ------------------------------------------------------------ NVFP4 stage
  * The pre-attention stage with NVFP4 operands (page
  * "flashinfer.diffusion_ops.minimax_h3_nvfp4_pre_attention", summary and

@@ -37,7 +37,8 @@ EXPORTS = ("mh3_preattn_create", "mh3_preattn_destroy", "mh3_preattn_workspace_b
            "mh3_mlp_workspace_y_bytes", "mh3_preattn_run_e4m3", "mh3_preattn_out_e4m3_bytes",
            "mh3_e4m3_quantize", "mh3_nvfp4_codes_bytes", "mh3_nvfp4_scales_bytes",
            "mh3_nvfp4_quantize", "mh3_nvfp4_norm_quant", "mh3_nvfp4_preattn_run", "mh3_nvfp4_qkv",
-           "mh3_preattn_set_test_stall")
+           "mh3_preattn_set_test_stall", "mh3_mlp_fp8_run", "mh3_mlp_fp8_validate",
+           "mh3_mlp_fp8_workspace_bytes")
 
 _vp = ctypes.c_void_p
 _i64 = ctypes.c_int64
@@ -82,6 +83,11 @@ _SIGS = {
                                      _vp, _vp, _vp]),
     "mh3_preattn_run_noalloc": (_i32, [_vp, _i64, _vp, _vp, _vp, _i64, _vp, _i64, _i64, _vp, _vp,
                                        _vp, _vp, _vp, _i64, _vp, _i32, _f32, _f32, _vp, _vp]),
+    "mh3_mlp_fp8_run": (_i32, [_vp, _vp, _i64, _vp, _vp, _vp, _i64, _vp, _i64, _vp, _i64, _i64,
+                               _vp, _vp, _vp, _vp, _vp, _vp, _f32, _vp, _vp, _vp, _vp, _vp, _vp]),
+    "mh3_mlp_fp8_validate": (_i32, [_i64, _vp, _vp, _vp, _i64, _vp, _i64, _vp, _i64, _i64, _vp,
+                                    _vp, _vp, _vp, _vp, _vp, _f32, _vp, _vp, _vp, _vp, _vp, _vp]),
+    "mh3_mlp_fp8_workspace_bytes": (ctypes.c_size_t, [_i64, _i32]),
 }
 
 _lib = None
@@ -170,7 +176,8 @@ class Handle:
         """Test hook: the next CTA-pair QKV GEMM launch issues no loads, so its
         bounded waits run out and it reports a status code."""
         _check(load().mh3_preattn_set_test_stall(self._h, 1 if stall else 0),
-               "mh3_preattn_set_test_stall")
+               "mh3_preattn_set_test_stall", "mh3_mlp_fp8_run", "mh3_mlp_fp8_validate",
+           "mh3_mlp_fp8_workspace_bytes")
 
 
 _handles = {}
@@ -289,6 +296,56 @@ def mh3_mlp_run(handle: Handle, stream, M, x, x_norm_weight, adaln_scale, scale_
         scale_row_stride, _ptr(adaln_shift), shift_row_stride, _ptr(gate), gate_row_stride, rows,
         _ptr(adaln_index), _ptr(residual), _ptr(fc1_weight), _ptr(fc2_weight), float(eps),
         _ptr(workspace_a), _ptr(workspace_y), _ptr(out)), "mh3_mlp_run")
+
+
+def mh3_mlp_fp8_validate(M, x, x_norm_weight, adaln_scale, scale_row_stride, adaln_shift,
+                         shift_row_stride, gate, gate_row_stride, rows, adaln_index, residual,
+                         fc1_weight_q, fc1_weight_scale, fc2_weight_q, fc2_weight_scale, eps,
+                         workspace_a_q, workspace_a_scale, workspace_y, workspace_y_q,
+                         workspace_y_scale, out) -> int:
+    """Host-only validation of an FP8 MLP call; returns the status code."""
+    return load().mh3_mlp_fp8_validate(
+        M, _ptr(x), _ptr(x_norm_weight), _ptr(adaln_scale), scale_row_stride, _ptr(adaln_shift),
+        shift_row_stride, _ptr(gate), gate_row_stride, rows, _ptr(adaln_index), _ptr(residual),
+        _ptr(fc1_weight_q), _ptr(fc1_weight_scale), _ptr(fc2_weight_q), _ptr(fc2_weight_scale),
+        float(eps), _ptr(workspace_a_q), _ptr(workspace_a_scale), _ptr(workspace_y),
+        _ptr(workspace_y_q), _ptr(workspace_y_scale), _ptr(out))
+
+
+def mh3_mlp_fp8_run(handle: Handle, stream, M, x, x_norm_weight, adaln_scale, scale_row_stride,
+                    adaln_shift, shift_row_stride, gate, gate_row_stride, rows, adaln_index,
+                    residual, fc1_weight_q, fc1_weight_scale, fc2_weight_q, fc2_weight_scale,
+                    eps, workspace_a_q, workspace_a_scale, workspace_y, workspace_y_q,
+                    workspace_y_scale, out) -> None:
+    _check(load().mh3_mlp_fp8_run(
+        handle.ptr, _stream_ptr(stream), M, _ptr(x), _ptr(x_norm_weight), _ptr(adaln_scale),
+        scale_row_stride, _ptr(adaln_shift), shift_row_stride, _ptr(gate), gate_row_stride, rows,
+        _ptr(adaln_index), _ptr(residual), _ptr(fc1_weight_q), _ptr(fc1_weight_scale),
+        _ptr(fc2_weight_q), _ptr(fc2_weight_scale), float(eps), _ptr(workspace_a_q),
+        _ptr(workspace_a_scale), _ptr(workspace_y), _ptr(workspace_y_q), _ptr(workspace_y_scale),
+        _ptr(out)), "mh3_mlp_fp8_run")
+
+
+def minimax_h3_mlp_fp8(x, x_norm_weight, adaln_scale, adaln_shift, adaln_index, gate, residual,
+                       fc1_weight_q, fc1_weight_scale, fc2_weight_q, fc2_weight_scale, *,
+                       out: Optional[torch.Tensor] = None, workspace_a_q=None,
+                       workspace_a_scale=None, workspace_y=None, workspace_y_q=None,
+                       workspace_y_scale=None, eps: float = 1e-5, stream=None,
+                       handle: Optional[Handle] = None) -> torch.Tensor:
+    """Torch-tensor entry point of the FP8 MLP block (argument names of
+    flashinfer.diffusion_ops.minimax_h3_mlp_fp8_sm120); E4M3 weights are
+    uint8 (or float8_e4m3fn) tensors; returns ``out`` (allocated when None)."""
+    M = x.shape[0]
+    if out is None:
+        out = torch.empty_like(residual)
+    h = handle if handle is not None else default_handle(x.device.index or 0)
+    as_u8 = lambda t: None if t is None else t.view(torch.uint8)  # noqa: E731
+    mh3_mlp_fp8_run(h, stream, M, x, x_norm_weight, adaln_scale, adaln_scale.stride(0),
+                    adaln_shift, adaln_shift.stride(0), gate, gate.stride(0), adaln_scale.shape[0],
+                    adaln_index, residual, as_u8(fc1_weight_q), fc1_weight_scale,
+                    as_u8(fc2_weight_q), fc2_weight_scale, eps, as_u8(workspace_a_q),
+                    workspace_a_scale, workspace_y, as_u8(workspace_y_q), workspace_y_scale, out)
+    return out
 
 
 def minimax_h3_bf16_mlp(x, x_norm_weight, adaln_scale, adaln_shift, adaln_index, gate, residual,

@@ -52,6 +52,10 @@ struct NormAdalnParams {
   uint8_t* act_sf = nullptr;     // UE4M3 scales, tiled atoms or row-major [M, 336]
   const float* act_gs = nullptr; // device [1]: activation global scale
   int sf_tiled = 1;
+  // E4M3 form (a_q8 != nullptr, int64 indices): per token s = RN(amax|a| / 448)
+  // and codes e4m3(a / s) replace the bf16 workspace
+  uint8_t* a_q8 = nullptr;  // [M, 5376]
+  float* a_s8 = nullptr;    // [M]
 };
 
 struct QkvParams {
@@ -121,6 +125,9 @@ struct GatedResidualParams {
   int num_tiles;    // num_m_tiles * 21
   int* status;
   int test_stall = 0;  // test hook: the producer issues no loads (bounded waits run out)
+  // E4M3 operands (MLP fc2): o = bf16(RN(RN(acc * row_scale[m]) * col_scale[c]))
+  const float* row_scale = nullptr;  // [M]
+  const float* col_scale = nullptr;  // [5376]
 };
 using OutProjParams = GatedResidualParams<int32_t>;
 
@@ -144,6 +151,11 @@ struct SwigluParams {
   int num_tiles;    // num_m_tiles * 112
   int* status;
   int test_stall = 0;  // test hook: the producer issues no loads (bounded waits run out)
+  // E4M3 operands (FP8 block): h = bf16(RN(RN(acc * row_scale[m]) * col_scale[c])),
+  // and the largest |y| of every row is folded into y_amax[m] (FP32 bits)
+  const float* row_scale = nullptr;  // [M]
+  const float* col_scale = nullptr;  // [28672]
+  unsigned int* y_amax = nullptr;    // [M], zero before the launch
 };
 
 // fc1 + SwiGLU: y = bf16(bf16(silu(h_gate)) * h_up), h = bf16(a @ fc1^T).
@@ -153,6 +165,19 @@ cudaError_t launch_mlp_fc1(const CUtensorMap& a, const CUtensorMap& b, const CUt
                            const SwigluParams& p, int clusters, cudaStream_t stream);
 // fc2 + gated residual: out = bf16(residual + bf16(gate[i] * bf16(y @ fc2^T))).
 //   a: y [M, 14336]; b: fc2 [5376, 14336]; out, residual: [M, 5376].
+// The FP8 (W8A8) block: fc1 on E4M3 operands with the rescale, SwiGLU and
+// row amax of y; the y quantiser (s_y replaces the amax in place); fc2 on E4M3
+// operands with the rescale and the gated residual.  a / b maps are uint8
+// with 128-byte rows (box 128 x 128).
+cudaError_t mlp_fp8_fc1_prepare_device(int* max_clusters);
+cudaError_t launch_mlp_fp8_fc1(const CUtensorMap& a, const CUtensorMap& b, const CUtensorMap& y,
+                               const SwigluParams& p, int clusters, cudaStream_t stream);
+cudaError_t launch_mlp_quantize_y(const __nv_bfloat16* y, int64_t M, float* amax_then_scale,
+                                  uint8_t* y_q, int num_sms, cudaStream_t stream);
+cudaError_t mlp_fp8_fc2_prepare_device(int* max_clusters);
+cudaError_t launch_mlp_fp8_fc2(const CUtensorMap& a, const CUtensorMap& b, const CUtensorMap& out,
+                               const CUtensorMap& residual, const GatedResidualParams<int64_t>& p,
+                               int clusters, cudaStream_t stream);
 cudaError_t mlp_fc2_prepare_device(int* max_clusters);
 cudaError_t launch_mlp_fc2(const CUtensorMap& a, const CUtensorMap& b, const CUtensorMap& out,
                            const CUtensorMap& residual, const GatedResidualParams<int64_t>& p,

@@ -5,6 +5,10 @@
 //   out = bf16(residual + bf16(g * o)),  g = gate[index[m]], or 0 when the
 //         index lies outside [0, gate_rows) (out = residual)
 //
+// With E4M3 operands (kFp8) the accumulator is rescaled first, the two
+// factors in the order the MLP page prints them:
+//   o   = bf16(RN(RN(acc * row_scale[m]) * col_scale[c]))
+//
 // (flashinfer.diffusion_ops.minimax_h3_nvfp4_out_proj, summary formula; the
 // same last line as the formula block of
 // flashinfer.diffusion_ops.minimax_h3_mlp_fp8_sm120.)  N = 5376 = 21 tiles;
@@ -26,9 +30,10 @@ namespace gr {
 
 using namespace k2;
 
-template <int KB, typename IndexT>
+template <int KB, typename IndexT, bool kFp8T = false>
 struct GatedResidualEpi {
   using Params = GatedResidualParams<IndexT>;
+  static constexpr bool kFp8 = kFp8T;
   static constexpr int kKBlocks = KB;
   static constexpr int kNTiles = kHidden / kTileN;  // 21
   static_assert(kHidden % kTileN == 0, "output columns must tile");
@@ -42,6 +47,7 @@ struct GatedResidualEpi {
     const int64_t m = m0 + lane;
     const bool block_live = m0 < p.M;  // warp-uniform
     const uint4* grow = nullptr;
+    const float rs = kFp8T && m < p.M ? __ldg(p.row_scale + m) : 0.0f;
     if (m < p.M) {
       const int64_t gi = static_cast<int64_t>(__ldg(p.gate_index + m));
       if (gi >= 0 && gi < p.gate_rows)
@@ -81,13 +87,23 @@ struct GatedResidualEpi {
           const uint4 gw = grow ? __ldg(grow + (col0 >> 3) + chunk) : make_uint4(0u, 0u, 0u, 0u);
           const uint32_t rw[4] = {res.x, res.y, res.z, res.w};
           const uint32_t gg[4] = {gw.x, gw.y, gw.z, gw.w};
+          float cs[8];
+          if (kFp8T) {
+            const float4 c0 = __ldg(reinterpret_cast<const float4*>(p.col_scale + col0 + 8 * chunk));
+            const float4 c1 =
+                __ldg(reinterpret_cast<const float4*>(p.col_scale + col0 + 8 * chunk + 4));
+            cs[0] = c0.x; cs[1] = c0.y; cs[2] = c0.z; cs[3] = c0.w;
+            cs[4] = c1.x; cs[5] = c1.y; cs[6] = c1.z; cs[7] = c1.w;
+          }
           uint32_t ow[4];
 #pragma unroll
           for (int e = 0; e < 4; ++e) {
             float r2[2];
 #pragma unroll
             for (int h = 0; h < 2; ++h) {
-              const float o = round_bf16(__uint_as_float(v[8 * g + 2 * e + h]));
+              float acc = __uint_as_float(v[8 * g + 2 * e + h]);
+              if (kFp8T) acc = __fmul_rn(__fmul_rn(acc, rs), cs[2 * e + h]);
+              const float o = round_bf16(acc);
               const float gv = h ? bf16_hi(gg[e]) : bf16_lo(gg[e]);
               const float rv = h ? bf16_hi(rw[e]) : bf16_lo(rw[e]);
               r2[h] = __fadd_rn(rv, round_bf16(__fmul_rn(gv, o)));

@@ -4,7 +4,8 @@
 //
 //   struct Epi {
 //     using Params = ...;                    // has M, num_m_tiles, num_tiles, status
-//     static constexpr int kKBlocks;         // K / 64
+//     static constexpr bool kFp8;            // E4M3 operands (else bf16)
+//     static constexpr int kKBlocks;         // K / 64 (bf16) or K / 128 (E4M3): 128-B rows
 //     static constexpr int kNTiles;          // number of 256-column accumulator tiles
 //     __device__ static int b_row(int n_blk, int rank);  // first B row CTA `rank` loads
 //     __device__ static void prologue(float* scratch, int tid, int nthreads, const Params&);
@@ -55,6 +56,7 @@ constexpr int kBBytes = BNC * BK * 2;  // 16 KB
 constexpr int kStageBytes = kABytes + kBBytes;
 constexpr int kThreads = 64 + kEpiWarps * 32;  // 192
 constexpr uint32_t kIdesc = idesc_bf16_f32(kPairRows, kTileN);
+constexpr uint32_t kIdescFp8 = idesc_e4m3_f32(kPairRows, kTileN);
 constexpr uint16_t kBothCtas = 0x3;
 constexpr uint64_t kGraceNs = 50000000ull;  // 50 ms
 
@@ -153,6 +155,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
                      const typename Epi::Params p) {
   constexpr int kKB = Epi::kKBlocks;
   constexpr int kN = Epi::kNTiles;
+  constexpr int kBKElems = Epi::kFp8 ? 128 : BK;  // elements in one 128-byte k-block row
   extern __shared__ uint8_t smem_raw[];
   Smem sm;
   {
@@ -219,8 +222,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
           }
           const uint32_t leader_full = mapa_shared(sm.full(stage), 0);
           if (rank == 0) mbar_arrive_expect_tx(sm.full(stage), 2 * kStageBytes);
-          tma_load_2d_pair(sm.a(stage), &tm_a, leader_full, kb * BK, a_row);
-          tma_load_2d_pair(sm.b(stage), &tm_b, leader_full, kb * BK, b_row);
+          tma_load_2d_pair(sm.a(stage), &tm_a, leader_full, kb * kBKElems, a_row);
+          tma_load_2d_pair(sm.b(stage), &tm_b, leader_full, kb * kBKElems, b_row);
           issued_any = true;
           if (++stage == kStages) {
             stage = 0;
@@ -256,10 +259,14 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
           const uint64_t a_desc = sw128_kmajor_desc(sm.a(stage));
           const uint64_t b_desc = sw128_kmajor_desc(sm.b(stage));
 #pragma unroll
-          for (int k = 0; k < BK / 16; ++k) {
-            // advance 16 elements (32 B) along K inside the swizzle atom
-            umma_bf16_pair(d_tmem, a_desc + 2 * k, b_desc + 2 * k, kIdesc,
+          for (int k = 0; k < 4; ++k) {
+            // advance 32 B along K inside the swizzle atom (16 bf16 or 32 E4M3)
+            if constexpr (Epi::kFp8)
+              umma_f8_pair(d_tmem, a_desc + 2 * k, b_desc + 2 * k, kIdescFp8,
                            (kb | k) != 0 ? 1u : 0u);
+            else
+              umma_bf16_pair(d_tmem, a_desc + 2 * k, b_desc + 2 * k, kIdesc,
+                             (kb | k) != 0 ? 1u : 0u);
           }
           umma_commit_pair_multicast(sm.empty(stage), kBothCtas);
           if (++stage == kStages) {

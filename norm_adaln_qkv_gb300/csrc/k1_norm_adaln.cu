@@ -33,7 +33,14 @@
 // UE4M3 scales.  A block is two neighbouring lanes' chunks (one shuffle for
 // the amax), whose even lane stores the scale byte.  A guarded row gets zero
 // codes and scales.
+//
+// E4M3 form (flashinfer.diffusion_ops.minimax_h3_mlp_fp8_sm120, formula block:
+// a_q = e4m3(a / s_a), s_a = RN(amax_row(|a|) / 448)): int64 indices; the row
+// amax is one more fixed-order CTA reduction, then each thread quantises its
+// 24 values of a (e4m3_rows.cuh) and thread 0 stores s_a.  A guarded row gets
+// zero codes and s_a = 0.
 #include "common.cuh"
+#include "e4m3_rows.cuh"
 #include "nvfp4.cuh"
 #include "ptx.cuh"
 
@@ -101,11 +108,18 @@ __device__ __forceinline__ void fp4_chunk(const uint4& o, int lane, int c, int64
         static_cast<uint8_t>(bs.code);
 }
 
-template <bool kFp4>
+constexpr int kModeBf16 = 0;  // bf16 workspace
+constexpr int kModeFp4 = 1;   // NVFP4 codes and block scales
+constexpr int kModeFp8 = 2;   // E4M3 codes and a per-token scale
+
+template <int kMode>
 __global__ void __launch_bounds__(kThreads, kCtasPerSm) norm_adaln_kernel(const NormAdalnParams p) {
+  constexpr bool kFp4 = kMode == kModeFp4;
+  constexpr bool kFp8 = kMode == kModeFp8;
   __shared__ __align__(128) uint8_t rows_buf[kStages][kRowBytes];
   __shared__ __align__(8) uint64_t full[kStages];
   __shared__ float warp_ss[kWarps];
+  __shared__ float warp_amax[kFp8 ? kWarps : 1];
   __shared__ int go;
   __shared__ float2 enc_lut[kFp4 ? fp4::kEncLut : 1];
 
@@ -187,9 +201,12 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm) norm_adaln_kernel(const 
       for (int j = 0; j < kVecPerThread; ++j) {
         if (kFp4)
           fp4_chunk(z, lane, tid + kThreads * j, m, quant, enc_lut, p);  // codes 0, scale 0
+        else if (kFp8)
+          reinterpret_cast<uint2*>(p.a_q8 + m * kHidden)[tid + kThreads * j] = make_uint2(0u, 0u);
         else
           wr[tid + kThreads * j] = z;
       }
+      if (kFp8 && tid == 0) p.a_s8[m] = 0.0f;
       continue;
     }
     const float r =
@@ -198,6 +215,8 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm) norm_adaln_kernel(const 
     const uint4* wv = reinterpret_cast<const uint4*>(p.x_norm_weight);
     const uint4* scr = reinterpret_cast<const uint4*>(p.scale + idx * p.scale_stride);
     const uint4* shr = reinterpret_cast<const uint4*>(p.shift + idx * p.shift_stride);
+    uint4 a8[kFp8 ? kVecPerThread : 1];
+    float amax = 0.0f;
 #pragma unroll
     for (int j = 0; j < kVecPerThread; ++j) {
       const int c = tid + kThreads * j;
@@ -209,10 +228,30 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm) norm_adaln_kernel(const 
       o.y = adaln_pair(f2_from_bf16x2(v[j].y), w.y, sc.y, sh.y, r2);
       o.z = adaln_pair(f2_from_bf16x2(v[j].z), w.z, sc.z, sh.z, r2);
       o.w = adaln_pair(f2_from_bf16x2(v[j].w), w.w, sc.w, sh.w, r2);
-      if (kFp4)
+      if (kFp4) {
         fp4_chunk(o, lane, c, m, quant, enc_lut, p);
-      else
+      } else if (kFp8) {
+        a8[kFp8 ? j : 0] = o;
+        amax = fmaxf(amax, e4m3r::amax8(o));
+      } else {
         wr[c] = o;
+      }
+    }
+    if (kFp8) {
+      // row amax: warp butterflies, then the seven warp maxima (any order)
+#pragma unroll
+      for (int o = 16; o > 0; o >>= 1) amax = fmaxf(amax, __shfl_xor_sync(0xFFFFFFFFu, amax, o));
+      if (lane == 0) warp_amax[tid >> 5] = amax;
+      __syncthreads();
+      amax = warp_amax[0];
+#pragma unroll
+      for (int w = 1; w < kWarps; ++w) amax = fmaxf(amax, warp_amax[w]);
+      const e4m3r::RowScale rs = e4m3r::make_row_scale(amax);
+      uint2* q = reinterpret_cast<uint2*>(p.a_q8 + m * kHidden);
+#pragma unroll
+      for (int j = 0; j < kVecPerThread; ++j)
+        q[tid + kThreads * j] = e4m3r::quantize8(a8[kFp8 ? j : 0], rs);
+      if (tid == 0) p.a_s8[m] = rs.s;
     }
   }
 
@@ -232,9 +271,11 @@ cudaError_t launch_norm_adaln(const NormAdalnParams& p, int num_sms, cudaStream_
   const int64_t want = static_cast<int64_t>(num_sms) * kCtasPerSm;
   const int64_t grid = p.M < want ? p.M : want;
   if (p.act_q != nullptr)
-    norm_adaln_kernel<true><<<static_cast<unsigned>(grid), kThreads, 0, stream>>>(p);
+    norm_adaln_kernel<kModeFp4><<<static_cast<unsigned>(grid), kThreads, 0, stream>>>(p);
+  else if (p.a_q8 != nullptr)
+    norm_adaln_kernel<kModeFp8><<<static_cast<unsigned>(grid), kThreads, 0, stream>>>(p);
   else
-    norm_adaln_kernel<false><<<static_cast<unsigned>(grid), kThreads, 0, stream>>>(p);
+    norm_adaln_kernel<kModeBf16><<<static_cast<unsigned>(grid), kThreads, 0, stream>>>(p);
   return cudaGetLastError();
 }
 

@@ -49,6 +49,16 @@ struct mh3_preattn_ctx {
   void* act_sf = nullptr;
   size_t act_sf_bytes = 0;
   int test_stall_next = 0;  // test hook for the next CTA-pair QKV GEMM launch (bf16 or NVFP4)
+  int fc1_fp8_clusters = 0;     // resident clusters of the FP8 MLP GEMMs
+  int fc2_fp8_clusters = 0;
+  void* fp8_aq = nullptr;       // handle-owned FP8 MLP workspaces
+  size_t fp8_aq_bytes = 0;
+  void* fp8_as = nullptr;
+  size_t fp8_as_bytes = 0;
+  void* fp8_yq = nullptr;
+  size_t fp8_yq_bytes = 0;
+  void* fp8_ys = nullptr;
+  size_t fp8_ys_bytes = 0;
 };
 
 namespace {
@@ -224,6 +234,22 @@ int grow_buffer(void** buf, size_t* cap, size_t need, cudaStream_t s) {
   return MH3_OK;
 }
 
+// 2-D row-major uint8 tensor [rows, cols] (cols contiguous bytes), 128-B swizzle.
+int encode_u8_2d(CUtensorMap* map, const void* base, uint64_t cols, uint64_t rows,
+                 uint32_t box_cols, uint32_t box_rows, const char* what) {
+  PFN_cuTensorMapEncodeTiled_v12000 enc = encode_fn();
+  if (enc == nullptr) return fail(MH3_ERR_CUDA, "cuTensorMapEncodeTiled entry point not found");
+  const cuuint64_t dims[2] = {cols, rows};
+  const cuuint64_t strides[1] = {cols};
+  const cuuint32_t box[2] = {box_cols, box_rows};
+  const cuuint32_t unit[2] = {1, 1};
+  CUresult r = enc(map, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<void*>(base), dims, strides,
+                   box, unit, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                   CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  if (r != CUDA_SUCCESS) return fail(MH3_ERR_CUDA, "tensor map (%s) failed: %d", what, (int)r);
+  return MH3_OK;
+}
+
 // 2-D row-major bf16 tensor [rows, cols] (cols contiguous), 128-B swizzle.
 int encode_2d(CUtensorMap* map, const void* base, uint64_t cols, uint64_t rows, uint32_t box_cols,
               uint32_t box_rows, const char* what) {
@@ -349,6 +375,10 @@ int mh3_preattn_create(mh3_preattn_t* handle, int device) {
   int nvfp4_clusters = 0, nvfp4_e4m3_clusters = 0;
   e = nvfp4_qkv_prepare_device(&nvfp4_clusters, &nvfp4_e4m3_clusters);
   if (e != cudaSuccess) return cuda_fail(e, "preparing the NVFP4 GEMM");
+  int fc1_fp8_clusters = 0, fc2_fp8_clusters = 0;
+  e = mlp_fp8_fc1_prepare_device(&fc1_fp8_clusters);
+  if (e == cudaSuccess) e = mlp_fp8_fc2_prepare_device(&fc2_fp8_clusters);
+  if (e != cudaSuccess) return cuda_fail(e, "preparing the FP8 MLP GEMMs");
   mh3_preattn_ctx* h = new mh3_preattn_ctx();
   h->device = device;
   h->nvfp4_clusters = nvfp4_clusters;
@@ -356,6 +386,8 @@ int mh3_preattn_create(mh3_preattn_t* handle, int device) {
   h->fc1_clusters = fc1_clusters;
   h->e4m3_clusters = e4m3_clusters;
   h->fc2_clusters = fc2_clusters;
+  h->fc1_fp8_clusters = fc1_fp8_clusters;
+  h->fc2_fp8_clusters = fc2_fp8_clusters;
   h->num_sms = prop.multiProcessorCount;
   h->max_clusters = max_clusters;
   h->out_proj_clusters = out_proj_clusters;
@@ -377,7 +409,7 @@ int mh3_preattn_destroy(mh3_preattn_t h) {
     cudaError_t e = cudaFree(h->ws);
     if (e != cudaSuccess) rc = cuda_fail(e, "freeing the handle workspace");
   }
-  for (void* buf : {h->ws_y, h->act_q, h->act_sf}) {
+  for (void* buf : {h->ws_y, h->act_q, h->act_sf, h->fp8_aq, h->fp8_as, h->fp8_yq, h->fp8_ys}) {
     if (buf == nullptr) continue;
     cudaError_t e = cudaFree(buf);
     if (e != cudaSuccess && rc == MH3_OK) rc = cuda_fail(e, "freeing the handle workspace");
@@ -1049,6 +1081,147 @@ extern "C" int mh3_mlp_run(mh3_preattn_t h, void* stream, int64_t M, const mh3_b
   e = launch_mlp_fc2(ya, wb, mo, mr, p2, p2.num_tiles < h->fc2_clusters ? p2.num_tiles
                                                                          : h->fc2_clusters, s);
   if (e != cudaSuccess) return cuda_fail(e, "MLP fc2 launch");
+  return MH3_OK;
+}
+
+// ----------------------------------------------------------- FP8 MLP block
+extern "C" size_t mh3_mlp_fp8_workspace_bytes(int64_t M, int which) {
+  if (M <= 0) return 0;
+  switch (which) {
+    case 0: return static_cast<size_t>(M) * kHidden;        // a_q, E4M3 [M, 5376]
+    case 1: return static_cast<size_t>(M) * 4;              // a scale, FP32 [M]
+    case 2: return static_cast<size_t>(M) * kMlpInter * 2;  // y, bf16 [M, 14336]
+    case 3: return static_cast<size_t>(M) * kMlpInter;      // y_q, E4M3 [M, 14336]
+    case 4: return static_cast<size_t>(M) * 4;              // y scale, FP32 [M]
+    default: return 0;
+  }
+}
+
+extern "C" int mh3_mlp_fp8_validate(
+    int64_t M, const mh3_bf16* x, const mh3_bf16* x_norm_weight, const mh3_bf16* adaln_scale,
+    int64_t scale_row_stride, const mh3_bf16* adaln_shift, int64_t shift_row_stride,
+    const mh3_bf16* gate, int64_t gate_row_stride, int64_t rows, const int64_t* adaln_index,
+    const mh3_bf16* residual, const uint8_t* fc1_weight_q, const float* fc1_weight_scale,
+    const uint8_t* fc2_weight_q, const float* fc2_weight_scale, float eps,
+    const uint8_t* workspace_a_q, const float* workspace_a_scale, const mh3_bf16* workspace_y,
+    const uint8_t* workspace_y_q, const float* workspace_y_scale, const mh3_bf16* out) {
+  int rc = mh3_mlp_validate(M, x, x_norm_weight, adaln_scale, scale_row_stride, adaln_shift,
+                            shift_row_stride, gate, gate_row_stride, rows, adaln_index, residual,
+                            reinterpret_cast<const mh3_bf16*>(fc1_weight_q),
+                            reinterpret_cast<const mh3_bf16*>(fc2_weight_q), eps, nullptr,
+                            workspace_y, out);
+  if (rc) return rc;
+  if ((rc = check_ptr(fc1_weight_scale, "fc1_weight_scale", 16))) return rc;
+  if ((rc = check_ptr(fc2_weight_scale, "fc2_weight_scale", 16))) return rc;
+  if (M == 0) return MH3_OK;
+  const void* ws[4] = {workspace_a_q, workspace_a_scale, workspace_y_q, workspace_y_scale};
+  const char* names[4] = {"workspace_a_q", "workspace_a_scale", "workspace_y_q",
+                          "workspace_y_scale"};
+  for (int i = 0; i < 4; ++i)
+    if (ws[i] != nullptr && (rc = check_ptr(ws[i], names[i], 16))) return rc;
+  return MH3_OK;
+}
+
+extern "C" int mh3_mlp_fp8_run(
+    mh3_preattn_t h, void* stream, int64_t M, const mh3_bf16* x, const mh3_bf16* x_norm_weight,
+    const mh3_bf16* adaln_scale, int64_t scale_row_stride, const mh3_bf16* adaln_shift,
+    int64_t shift_row_stride, const mh3_bf16* gate, int64_t gate_row_stride, int64_t rows,
+    const int64_t* adaln_index, const mh3_bf16* residual, const uint8_t* fc1_weight_q,
+    const float* fc1_weight_scale, const uint8_t* fc2_weight_q, const float* fc2_weight_scale,
+    float eps, uint8_t* workspace_a_q, float* workspace_a_scale, mh3_bf16* workspace_y,
+    uint8_t* workspace_y_q, float* workspace_y_scale, mh3_bf16* out) {
+  int rc = check_handle(h);
+  if (rc) return rc;
+  rc = mh3_mlp_fp8_validate(M, x, x_norm_weight, adaln_scale, scale_row_stride, adaln_shift,
+                            shift_row_stride, gate, gate_row_stride, rows, adaln_index, residual,
+                            fc1_weight_q, fc1_weight_scale, fc2_weight_q, fc2_weight_scale, eps,
+                            workspace_a_q, workspace_a_scale, workspace_y, workspace_y_q,
+                            workspace_y_scale, out);
+  if (rc) return rc;
+  if (M == 0) return MH3_OK;
+  if (h->fc1_fp8_clusters <= 0 || h->fc2_fp8_clusters <= 0)
+    return fail(MH3_ERR_UNSUPPORTED, "no 2-CTA cluster of the FP8 MLP GEMMs fits this device");
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  struct Own {
+    void** ptr;
+    void** buf;
+    size_t* cap;
+    int which;
+  } own[5] = {{reinterpret_cast<void**>(&workspace_a_q), &h->fp8_aq, &h->fp8_aq_bytes, 0},
+              {reinterpret_cast<void**>(&workspace_a_scale), &h->fp8_as, &h->fp8_as_bytes, 1},
+              {reinterpret_cast<void**>(&workspace_y), &h->ws_y, &h->ws_y_bytes, 2},
+              {reinterpret_cast<void**>(&workspace_y_q), &h->fp8_yq, &h->fp8_yq_bytes, 3},
+              {reinterpret_cast<void**>(&workspace_y_scale), &h->fp8_ys, &h->fp8_ys_bytes, 4}};
+  for (const Own& o : own) {
+    if (*o.ptr != nullptr) continue;
+    if ((rc = grow_buffer(o.buf, o.cap, mh3_mlp_fp8_workspace_bytes(M, o.which), s))) return rc;
+    *o.ptr = *o.buf;
+  }
+  // the y scale buffer first collects each row's amax (FP32 bits, from 0);
+  // zeroed before kernel 1 so that kernel 1 and fc1 stay adjacent launches
+  cudaError_t e = cudaMemsetAsync(workspace_y_scale, 0, mh3_mlp_fp8_workspace_bytes(M, 4), s);
+  if (e != cudaSuccess) return cuda_fail(e, "cudaMemsetAsync (y amax)");
+  // kernel 1, E4M3 form: a_q and s_a
+  NormAdalnParams p1;
+  p1.x = reinterpret_cast<const __nv_bfloat16*>(x);
+  p1.x_norm_weight = reinterpret_cast<const __nv_bfloat16*>(x_norm_weight);
+  p1.scale = reinterpret_cast<const __nv_bfloat16*>(adaln_scale);
+  p1.shift = reinterpret_cast<const __nv_bfloat16*>(adaln_shift);
+  p1.scale_stride = scale_row_stride;
+  p1.shift_stride = shift_row_stride;
+  p1.rows = rows;
+  p1.index = adaln_index;
+  p1.workspace = nullptr;
+  p1.M = M;
+  p1.eps = eps;
+  p1.status = h->d_status;
+  p1.a_q8 = workspace_a_q;
+  p1.a_s8 = workspace_a_scale;
+  e = launch_norm_adaln(p1, h->num_sms, s);
+  if (e != cudaSuccess) return cuda_fail(e, "norm/AdaLN (E4M3) launch");
+  const int pairs = static_cast<int>((M + 255) / 256);
+  CUtensorMap ma, mb, my;
+  if ((rc = encode_u8_2d(&ma, workspace_a_q, kHidden, M, 128, 128, "workspace_a_q"))) return rc;
+  if ((rc = encode_u8_2d(&mb, fc1_weight_q, kHidden, 2 * kMlpInter, 128, 128, "fc1_weight_q")))
+    return rc;
+  if ((rc = encode_2d(&my, workspace_y, kMlpInter, M, 64, 32, "workspace_y (store)"))) return rc;
+  SwigluParams q1;
+  q1.M = M;
+  q1.num_m_tiles = pairs;
+  q1.num_tiles = pairs * (kMlpInter / 128);
+  q1.status = h->d_status;
+  q1.row_scale = workspace_a_scale;
+  q1.col_scale = fc1_weight_scale;
+  q1.y_amax = reinterpret_cast<unsigned int*>(workspace_y_scale);
+  e = launch_mlp_fp8_fc1(ma, mb, my, q1, q1.num_tiles < h->fc1_fp8_clusters ? q1.num_tiles
+                                                                            : h->fc1_fp8_clusters,
+                         s);
+  if (e != cudaSuccess) return cuda_fail(e, "FP8 MLP fc1 launch");
+  e = launch_mlp_quantize_y(reinterpret_cast<const __nv_bfloat16*>(workspace_y), M,
+                            workspace_y_scale, workspace_y_q, h->num_sms, s);
+  if (e != cudaSuccess) return cuda_fail(e, "y quantiser launch");
+  CUtensorMap ya, wb, mo, mr;
+  if ((rc = encode_u8_2d(&ya, workspace_y_q, kMlpInter, M, 128, 128, "workspace_y_q"))) return rc;
+  if ((rc = encode_u8_2d(&wb, fc2_weight_q, kMlpInter, kHidden, 128, 128, "fc2_weight_q")))
+    return rc;
+  if ((rc = encode_2d(&mo, out, kHidden, M, 64, 32, "out"))) return rc;
+  if ((rc = encode_2d(&mr, residual, kHidden, M, 64, 32, "residual"))) return rc;
+  GatedResidualParams<int64_t> q2;
+  q2.gate = reinterpret_cast<const __nv_bfloat16*>(gate);
+  q2.gate_stride = gate_row_stride;
+  q2.gate_rows = rows;
+  q2.gate_index = adaln_index;
+  q2.M = M;
+  q2.num_m_tiles = pairs;
+  q2.num_tiles = pairs * (kHidden / 256);
+  q2.status = h->d_status;
+  q2.row_scale = workspace_y_scale;
+  q2.col_scale = fc2_weight_scale;
+  e = launch_mlp_fp8_fc2(ya, wb, mo, mr, q2, q2.num_tiles < h->fc2_fp8_clusters
+                                                  ? q2.num_tiles
+                                                  : h->fc2_fp8_clusters,
+                         s);
+  if (e != cudaSuccess) return cuda_fail(e, "FP8 MLP fc2 launch");
   return MH3_OK;
 }
 

@@ -402,6 +402,17 @@ __device__ __forceinline__ void umma_bf16_pair(uint32_t d_tmem, uint64_t a_desc,
       "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(accumulate)
       : "memory");
 }
+// The same with E4M3 operands (kind::f8f6f4, K = 32 per instruction: one
+// 32-byte step of a 128-byte k-block row, as for kind::f16).
+__device__ __forceinline__ void umma_f8_pair(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc,
+                                             uint32_t idesc, uint32_t accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "setp.ne.b32 p, %4, 0;\n\t"
+      "tcgen05.mma.cta_group::2.kind::f8f6f4 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
+      "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(accumulate)
+      : "memory");
+}
 // Block-scaled pair MMA, kind::mxf4nvf4 with scale_vec::4X (E2M1 A and B in
 // shared memory, one UE4M3 scale per 16 elements, FP32 accumulator): each
 // CTA reads the A scales of its own rows and the B scales of all N rows from
@@ -508,6 +519,13 @@ __device__ __forceinline__ uint64_t sw128_kmajor_desc(uint32_t smem_addr) {
 __host__ __device__ constexpr uint32_t idesc_bf16_f32(int m, int n) {
   return (1u << 4) | (1u << 7) | (1u << 10) | (static_cast<uint32_t>(n >> 3) << 17) |
          (static_cast<uint32_t>(m >> 4) << 24);
+}
+
+// Instruction descriptor of kind::f8f6f4 with E4M3 A and B (format code 0 in
+// bits 7-9 and 10-12), FP32 accumulation (bits 4-5 = 1), K-major, N >> 3 in
+// bits 17-22, M >> 4 in bits 24-28.
+__host__ __device__ constexpr uint32_t idesc_e4m3_f32(int m, int n) {
+  return (1u << 4) | (static_cast<uint32_t>(n >> 3) << 17) | (static_cast<uint32_t>(m >> 4) << 24);
 }
 
 // Instruction descriptor of kind::mxf4nvf4: A and B E2M1 (bits 7-9 = 1,

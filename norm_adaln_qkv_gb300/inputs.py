@@ -381,6 +381,72 @@ def make_mlp_workload(M: int, seed: int = SEED_BASE + 200, rows: int = 9,
                        fc1_weight=fc1, fc2_weight=fc2)
 
 
+# ------------------------------------------------------- the FP8 MLP block
+@dataclass
+class MlpFp8Workload:
+    """Host tensors of one FP8 MLP-block case (shapes of
+    flashinfer.diffusion_ops.minimax_h3_mlp_fp8_sm120, Parameters): the
+    bf16 activations and tables of the BF16 block, and E4M3 weights with one
+    FP32 scale per output row (fc1 [28672, 5376] / [28672], rows [gate | up];
+    fc2 [5376, 14336] / [5376]).  The weight codes are drawn directly as E4M3
+    numbers (N(0, 1) * 32, rounded by torch's float8 conversion) and the
+    scales as 1 / (32 sqrt(K)) * (1 + 0.1 N(0, 1)), so code * scale has the
+    spread of the BF16 block's N(0, 1/K) weights."""
+
+    M: int
+    x: torch.Tensor
+    x_norm_weight: torch.Tensor
+    adaln_mod: torch.Tensor  # [rows, 6*HIDDEN]
+    adaln_index: torch.Tensor
+    residual: torch.Tensor
+    fc1_q: torch.Tensor      # uint8 [28672, 5376]
+    fc1_scale: torch.Tensor  # float32 [28672]
+    fc2_q: torch.Tensor      # uint8 [5376, 14336]
+    fc2_scale: torch.Tensor  # float32 [5376]
+    eps: float = 1e-5
+
+    def tables(self, mod: Optional[torch.Tensor] = None):
+        """(scale, shift, gate) views of the modulation tensor."""
+        mod = self.adaln_mod if mod is None else mod
+        sh, sc, gt = (mod[:, c * HIDDEN:(c + 1) * HIDDEN] for c in MLP_CHUNKS)
+        return sc, sh, gt
+
+
+def _e4m3_codes(gen: torch.Generator, rows: int, cols: int, chunk_rows: int = 4096) -> torch.Tensor:
+    out = torch.empty((rows, cols), dtype=torch.uint8)
+    for r0 in range(0, rows, chunk_rows):
+        r1 = min(rows, r0 + chunk_rows)
+        v = (_normal(gen, (r1 - r0, cols)) * 32.0).clamp(-448.0, 448.0)
+        out[r0:r1] = v.to(torch.float8_e4m3fn).view(torch.uint8)
+    return out
+
+
+def make_mlp_fp8_workload(M: int, seed: int = SEED_BASE + 300, rows: int = 9,
+                          bad_rate: float = 0.01) -> MlpFp8Workload:
+    """x, residual ~ N(0,1); x_norm_weight 1 + 0.1*N(0,1); modulation
+    0.1*N(0,1); index uniform in [0, rows) with bad_rate of the tokens set
+    cyclically to -1, 9, 2^40; E4M3 weights and FP32 row scales as described
+    on MlpFp8Workload."""
+    gen = torch.Generator().manual_seed(seed)
+    x = _x_bf16(gen, M, 1.0)
+    xw = (1.0 + 0.1 * _normal(gen, (HIDDEN,))).to(torch.bfloat16)
+    mod = (0.1 * _normal(gen, (rows, 6 * HIDDEN))).to(torch.bfloat16)
+    idx = torch.randint(0, rows, (M,), generator=gen, dtype=torch.int64)
+    n_bad = int(round(bad_rate * M))
+    if n_bad:
+        toks = torch.randperm(M, generator=gen)[:n_bad]
+        for j, t in enumerate(toks.tolist()):
+            idx[t] = BAD_INDEX_CYCLE[j % len(BAD_INDEX_CYCLE)]
+    res = _x_bf16(gen, M, 1.0)
+    fc1_q = _e4m3_codes(gen, 2 * MLP_INTER, HIDDEN)
+    fc1_s = (1.0 + 0.1 * _normal(gen, (2 * MLP_INTER,))) / (32.0 * math.sqrt(HIDDEN))
+    fc2_q = _e4m3_codes(gen, HIDDEN, MLP_INTER)
+    fc2_s = (1.0 + 0.1 * _normal(gen, (HIDDEN,))) / (32.0 * math.sqrt(MLP_INTER))
+    return MlpFp8Workload(M=M, x=x, x_norm_weight=xw, adaln_mod=mod, adaln_index=idx,
+                          residual=res, fc1_q=fc1_q, fc1_scale=fc1_s.to(torch.float32),
+                          fc2_q=fc2_q, fc2_scale=fc2_s.to(torch.float32))
+
+
 # ---------------------------------------------------------------- NVFP4 stage
 # The NVFP4 op takes int32 AdaLN indices and one cos/sin row per token
 # (flashinfer.diffusion_ops.minimax_h3_nvfp4_pre_attention, Parameters).

@@ -36,5 +36,6 @@ from .stage import (  # noqa: F401
 from . import preattn  # noqa: F401  (PyTorch restatement of the same steps)
 from . import out_proj  # noqa: F401  (attention output projection + gated residual)
 from . import mlp  # noqa: F401  (MLP block)
+from . import mlp_fp8  # noqa: F401  (FP8 MLP block)
 from . import e4m3  # noqa: F401  (e4m3 output mode)
 from . import nvfp4  # noqa: F401  (NVFP4 pre-attention)
