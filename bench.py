@@ -259,7 +259,10 @@ def run_ours(args, world, rank, local):
     torch.cuda.set_device(local)
     if world > 1:
         torch.distributed.init_process_group("nccl", device_id=torch.device("cuda", local))
-    build.build()
+    if args.lib:
+        binding.load(os.path.abspath(args.lib))  # another build of the library
+    else:
+        build.build()
     h = binding.Handle(local)
     dev = torch.device("cuda", local)
     stream = torch.cuda.current_stream(dev)
@@ -639,6 +642,44 @@ def run_ours(args, world, rank, local):
                     "us": mlp_ms * 1e3, "tflops": mlp_tf,
                     "frac_of_measured_bf16": mlp_tf / peaks["bf16"], "launches_per_call": 3}
         del xm, f1, f2, wam, wym, outm, rm
+    # ---- the FP8 (W8A8) MLP block (E4M3 weights and per-token activations)
+    mlp_fp8_line = None
+    if not args.skip_also:
+        from norm_adaln_qkv_gb300.inputs import make_mlp_fp8_workload
+        w8 = make_mlp_fp8_workload(wl.M)
+        mod8 = w8.adaln_mod.to(dev)
+        sc8, sh8, gt8 = w8.tables(mod8)
+        x8, xw8, i8, r8 = (w8.x.to(dev), w8.x_norm_weight.to(dev), w8.adaln_index.to(dev),
+                           w8.residual.to(dev))
+        f1q, f1s, f2q, f2s = (w8.fc1_q.to(dev), w8.fc1_scale.to(dev), w8.fc2_q.to(dev),
+                              w8.fc2_scale.to(dev))
+        lib8 = binding.load()
+        wsb = [torch.empty(lib8.mh3_mlp_fp8_workspace_bytes(wl.M, k), dtype=torch.uint8,
+                           device=dev) for k in range(5)]
+        out8 = torch.empty_like(r8)
+
+        def mlp8_call():
+            binding.mh3_mlp_fp8_run(h, stream, w8.M, x8, xw8, sc8, sc8.stride(0), sh8,
+                                    sh8.stride(0), gt8, gt8.stride(0), sc8.shape[0], i8, r8, f1q,
+                                    f1s, f2q, f2s, w8.eps, wsb[0], wsb[1], wsb[2], wsb[3], wsb[4],
+                                    out8)
+        for _ in range(3):
+            mlp8_call()
+        torch.cuda.synchronize()
+        m0, m1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        m0.record(stream)
+        for _ in range(args.steps):
+            mlp8_call()
+        m1.record(stream)
+        torch.cuda.synchronize()
+        mlp8_ms = m0.elapsed_time(m1) / args.steps
+        mlp8_tf = MLP_FLOP_PER_TOKEN * w8.M / (mlp8_ms * 1e-3) / 1e12
+        mlp_fp8_line = {"workload": f"MLP block (E4M3 W8A8), M={w8.M}, 5376 -> 2x14336 -> 5376",
+                        "us": mlp8_ms * 1e3, "tflops": mlp8_tf,
+                        "frac_of_fp8_peak": mlp8_tf / (2 * peaks["bf16"]),
+                        "fp8_peak_note": "FP8 peak = measured bf16 burst x 2 (nominal 4.5/2.25)",
+                        "launches_per_call": 4}
+        del x8, r8, f1q, f2q, wsb, out8, mod8
     # ---- the small configurations (M = 16, 1024): per-call medians of the
     # whole stage, back to back (warm) and after writing 320 MB (> 2x L2)
     small = None
@@ -754,6 +795,7 @@ def run_ours(args, world, rank, local):
         "nvfp4": nvfp4_line,
         "out_proj": out_proj,
         "mlp": mlp_line,
+        "mlp_fp8": mlp_fp8_line,
         "small": small,
     }
     print(json.dumps(line), flush=True)
@@ -816,6 +858,9 @@ def main():
                     help="out_proj: time the output projection alone (no JSON bench line)")
     ap.add_argument("--op-tokens", type=int, default=4096,
                     help="tokens of the --only out_proj case")
+    ap.add_argument("--lib", default=None,
+                    help="time this build of the library instead of the package's own "
+                         "(a variant from `python -m norm_adaln_qkv_gb300.build --out`)")
     args = ap.parse_args()
     world, rank, local = _dist()
     if args.impl == "reference":

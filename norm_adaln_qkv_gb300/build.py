@@ -1,8 +1,8 @@
 """Build the C-ABI library ``libmh3_preattn.so`` in-tree with nvcc for sm_103a.
 
-Six translation units (the C ABI host code, kernel 1, the two forms of
-kernel 2, the output projection, the MLP GEMMs) are
-compiled in parallel and linked with the CUDA runtime linked statically, so
+The translation units (the C ABI host code, kernel 1, the two forms of
+kernel 2, the output projection, the MLP GEMMs, the e4m3 and NVFP4 kernels)
+are compiled in parallel and linked with the CUDA runtime linked statically, so
 the library loads on a machine without a GPU driver (the driver is resolved
 on the first CUDA call).  Output: ``norm_adaln_qkv_gb300/libmh3_preattn.so``.
 """
@@ -34,19 +34,6 @@ def _flags(extra=()):
                    "-I", os.path.join(ROOT, "include"), "-I", CSRC, *extra]
 
 
-def _compile(src: str, extra=(), verbose=False) -> str:
-    obj = os.path.join(BUILD, os.path.splitext(src)[0] + ".o")
-    cmd = [nvcc(), "-c", os.path.join(CSRC, src), "-o", obj, *_flags(extra)]
-    if verbose:
-        cmd.append("-Xptxas=-v")
-    r = subprocess.run(cmd, capture_output=True, text=True)
-    if r.returncode != 0:
-        raise RuntimeError(f"nvcc failed for {src}:\n{r.stdout}\n{r.stderr}")
-    if verbose and r.stderr:
-        print(r.stderr)
-    return obj
-
-
 def _stale() -> bool:
     if not os.path.exists(LIB):
         return True
@@ -58,22 +45,46 @@ def _stale() -> bool:
     return os.path.getmtime(__file__) > t
 
 
-def build(force: bool = False, verbose: bool = False) -> str:
-    """Compile and link the library if any source is newer; returns its path."""
-    if not force and not _stale():
+def build(force: bool = False, verbose: bool = False, defines=(), out: str = LIB) -> str:
+    """Compile and link the library if any source is newer; returns its path.
+
+    ``defines`` (e.g. ``("MH3_GROUP_PAIRS=16",)``) are extra -D flags of a
+    variant build, which goes to ``out`` (its objects beside it) instead of
+    the package's own library."""
+    if out == LIB and not defines and not force and not _stale():
         return LIB
-    os.makedirs(BUILD, exist_ok=True)
+    build_dir = BUILD if out == LIB else os.path.splitext(out)[0] + "_build"
+    os.makedirs(build_dir, exist_ok=True)
+    extra = [f"-D{d}" for d in defines]
+
+    def compile_one(src):
+        obj = os.path.join(build_dir, os.path.splitext(src)[0] + ".o")
+        cmd = [nvcc(), "-c", os.path.join(CSRC, src), "-o", obj, *_flags(extra)]
+        if verbose:
+            cmd.append("-Xptxas=-v")
+        r = subprocess.run(cmd, capture_output=True, text=True)
+        if r.returncode != 0:
+            raise RuntimeError(f"nvcc failed for {src}:\n{r.stdout}\n{r.stderr}")
+        if verbose and r.stderr:
+            print(r.stderr)
+        return obj
+
     with ThreadPoolExecutor(len(SOURCES)) as ex:
-        objs = list(ex.map(lambda s: _compile(s, verbose=verbose), SOURCES))
-    tmp = LIB + ".tmp"
+        objs = list(ex.map(compile_one, SOURCES))
+    tmp = out + ".tmp"
     cmd = [nvcc(), *ARCH, "-shared", "-cudart", "static", "-o", tmp, *objs]
     r = subprocess.run(cmd, capture_output=True, text=True)
     if r.returncode != 0:
         raise RuntimeError(f"link failed:\n{r.stdout}\n{r.stderr}")
-    os.replace(tmp, LIB)
-    return LIB
+    os.replace(tmp, out)
+    return out
 
 
 if __name__ == "__main__":
-    import sys
-    print(build(force=True, verbose="-v" in sys.argv))
+    import argparse
+    ap = argparse.ArgumentParser(description="build the CUDA library (or a variant of it)")
+    ap.add_argument("-v", "--verbose", action="store_true", help="print ptxas resource usage")
+    ap.add_argument("--define", action="append", default=[], help="extra -D flag (repeatable)")
+    ap.add_argument("--out", default=LIB, help="library path of a variant build")
+    a = ap.parse_args()
+    print(build(force=True, verbose=a.verbose, defines=a.define, out=os.path.abspath(a.out)))

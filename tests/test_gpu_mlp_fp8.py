@@ -158,3 +158,28 @@ def test_fp8_mlp_invalid_arguments_and_empty(handle, weights):
     binding.mh3_mlp_fp8_run(handle, None, 0, *args)  # M = 0: nothing to do
     torch.cuda.synchronize()
     assert bool((out == 3.0).all())
+
+
+def test_fp8_mlp_production_size_sampled(handle, weights):
+    """M = 32760 in the bench's launch configuration; the oracle on a sample
+    of tokens (every 512th, the last, and the guarded ones)."""
+    base = weights["host"]
+    wl = make_mlp_fp8_workload(32760)
+    wl.fc1_q, wl.fc1_scale, wl.fc2_q, wl.fc2_scale = base.fc1_q, base.fc1_scale, base.fc2_q, \
+        base.fc2_scale
+    ws, a, out = _run(handle, wl, weights)
+    sc, sh, gt = wl.tables()
+    bad = (wl.adaln_index < 0) | (wl.adaln_index >= gt.shape[0])
+    tokens = sorted(set(range(0, wl.M, 512)) | {wl.M - 1} |
+                    set(torch.nonzero(bad).flatten().tolist()[:24]))
+    t = torch.tensor(tokens)
+    aq, s_a = f8.quantize_rows(a[t])
+    assert torch.equal(ws["aq"][t], aq) and torch.equal(ws["as_"][t], s_a)
+    yq, s_y = f8.quantize_rows(ws["y"][t])
+    assert torch.equal(ws["yq"][t], yq) and torch.equal(ws["ys"][t], s_y)
+    full = f8.mlp_block_fp8(wl.x, wl.x_norm_weight, sc, sh, gt, wl.adaln_index, wl.residual,
+                            wl.fc1_q, wl.fc1_scale, wl.fc2_q, wl.fc2_scale, eps=wl.eps,
+                            tokens=tokens)
+    _bar(out[t], full["out"], "out (oracle block) M=32760 sampled")
+    assert torch.equal(out[bad].view(torch.int16), wl.residual[bad].view(torch.int16))
+    assert bool(torch.isfinite(out.double()).all())
