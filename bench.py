@@ -583,6 +583,7 @@ def run_ours(args, world, rank, local):
     # ---- the attention output projection with the gated residual (the
     # step after attention, same GEMM machinery), at the bench's M
     out_proj = None
+    out_proj_nvfp4 = None
     if not args.skip_also:
         from norm_adaln_qkv_gb300.inputs import make_out_proj_workload
         wo = make_out_proj_workload(wl.M)
@@ -608,7 +609,54 @@ def run_ours(args, world, rank, local):
         op_tf = OUT_PROJ_FLOP_PER_TOKEN * wo.M / (op_ms * 1e-3) / 1e12
         out_proj = {"workload": f"out-projection + gated residual, M={wo.M}, K=7168, N=5376",
                     "us": op_ms * 1e3, "tflops": op_tf, "frac_of_measured_bf16": op_tf / peaks["bf16"]}
-        del ao, Wo, gio, reso, outo, mod_o
+        # the W4A4 (NVFP4) form: activation quantiser + block-scaled GEMM
+        from norm_adaln_qkv_gb300.inputs import out_proj_nvfp4_global_scales
+        ags, wgs = out_proj_nvfp4_global_scales()
+        lib4 = binding.load()
+        wq4 = torch.empty((5376, 3584), dtype=torch.uint8, device=dev)
+        wsf4 = torch.empty(lib4.mh3_nvfp4_scales_bytes(5376, 7168, 1), dtype=torch.uint8,
+                           device=dev)
+        binding.mh3_nvfp4_quantize(stream, Wo, torch.tensor([wgs], device=dev), wq4, wsf4, True)
+        ags_d = torch.tensor([ags], dtype=torch.float32, device=dev)
+        aq4 = torch.empty((wo.M, 3584), dtype=torch.uint8, device=dev)
+        asf4 = torch.empty(lib4.mh3_nvfp4_scales_bytes(wo.M, 7168, 1), dtype=torch.uint8,
+                           device=dev)
+
+        def op4_call():
+            binding.mh3_nvfp4_out_proj_run(h, stream, wo.M, ao, wq4, wsf4, wgs, ags_d, gate_o,
+                                           gate_o.stride(0), gate_o.shape[0], gio, reso, aq4,
+                                           asf4, outo)
+
+        def q4_call():
+            binding.mh3_nvfp4_quantize(stream, ao, ags_d, aq4, asf4, True)
+        res4 = {}
+        for name, fn in (("call", op4_call), ("quantiser", q4_call)):
+            for _ in range(3):
+                fn()
+            torch.cuda.synchronize()
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            e0.record(stream)
+            for _ in range(args.steps):
+                fn()
+            e1.record(stream)
+            torch.cuda.synchronize()
+            res4[name] = e0.elapsed_time(e1) / args.steps
+        op4_tf = OUT_PROJ_FLOP_PER_TOKEN * wo.M / (res4["call"] * 1e-3) / 1e12
+        q4_bytes = wo.M * (7168 * 2 + 3584 + 448)  # bf16 in; codes and scales out
+        gemm4_ms = res4["call"] - res4["quantiser"]
+        out_proj_nvfp4 = {
+            "workload": f"W4A4 (NVFP4) out-projection + gated residual, M={wo.M}, K=7168, N=5376",
+            "us": res4["call"] * 1e3, "tflops": op4_tf,
+            "frac_of_fp4_peak_bf16x4": op4_tf / (4 * peaks["bf16"]),
+            "quantiser_us": res4["quantiser"] * 1e3,
+            "quantiser_frac_of_measured_hbm":
+                q4_bytes / (res4["quantiser"] * 1e-3) / 1e9 / peaks["hbm"],
+            "gemm_us_by_difference": gemm4_ms * 1e3,
+            "gemm_tflops_by_difference": OUT_PROJ_FLOP_PER_TOKEN * wo.M / (gemm4_ms * 1e-3) / 1e12,
+            "fp4_peak_note": "FP4 peak = measured bf16 burst x 4 (the per-clock FP4/bf16 ratio "
+                             "measured for this MMA shape)",
+            "launches_per_call": 2}
+        del ao, Wo, gio, reso, outo, mod_o, wq4, wsf4, aq4, asf4
     # ---- the MLP block (norm/AdaLN, fc1 + SwiGLU, fc2 + gated residual)
     mlp_line = None
     if not args.skip_also:
@@ -794,6 +842,7 @@ def run_ours(args, world, rank, local):
         "e4m3": e4m3_line,
         "nvfp4": nvfp4_line,
         "out_proj": out_proj,
+        "out_proj_nvfp4": out_proj_nvfp4,
         "mlp": mlp_line,
         "mlp_fp8": mlp_fp8_line,
         "small": small,

@@ -402,10 +402,13 @@ size_t mh3_mlp_fp8_workspace_bytes(int64_t M, int which);
  * "flashinfer.diffusion_ops.minimax_h3_nvfp4_pre_attention", summary and
  * Parameters).  NVFP4 here: E2M1 element codes packed two per byte (element
  * 2j in the low nibble of byte j), one UE4M3 scale per block of 16
- * consecutive elements of a row, and an FP32 global scale gs:
- *   s    = ue4m3(RN(RN(amax / 6) * gs))    amax = max |v| of the block
- *   code = e2m1(RN(v * RN(gs / s)))         (0 when s = 0); v ~ code * s / gs
- * both roundings to nearest even and saturating (448, 6).
+ * consecutive elements of a row, and an FP32 global scale gs, in the
+ * FlashInfer block-16 convention the page
+ * "flashinfer.diffusion_ops.minimax_h3_nvfp4_out_proj" prints in its summary:
+ *   s    = ue4m3(amax * gs / 6)            amax = max |v| of the block
+ *   code = e2m1(v * gs / s)                 (signed zero when s = 0)
+ * each ONE rounding of the exact quotient, to nearest even, saturating at
+ * 448 and 6; v ~ code * s / gs.
  * Scale layouts: row-major [rows, cols/16] (tiled = 0), or tiled (tiled = 1):
  * 512-byte atoms of 128 rows x 4 scales (one 64-element step), row r of an
  * atom at byte (r % 32) * 16 + (r / 32) * 4, atoms ordered [rows/128][cols/64]
@@ -500,6 +503,63 @@ int mh3_nvfp4_qkv(mh3_preattn_t handle, void* stream, int64_t M, const uint8_t* 
                   const mh3_bf16* q_norm_weight, const mh3_bf16* k_norm_weight,
                   const mh3_bf16* rope_cos_sin, int P, float eps, const float* qkv_descale,
                   void* out);
+
+/* ---------------------------------------------------------------------------
+ * The W4A4 attention output projection with the fused gated residual (page
+ * "flashinfer.diffusion_ops.minimax_h3_nvfp4_out_proj", summary and
+ * Parameters): attn_out is quantised to NVFP4 per token with the activation
+ * global scale (the block-16 convention above), multiplied on the
+ * block-scaled FP4 tensor cores (tcgen05 kind::mxf4nvf4, CTA pairs) by the
+ * quantised o_weight, and the accumulator takes the gated residual:
+ *
+ *   acc   = sum_k (qa sa)(qw sw)                        FP32
+ *   alpha = RN(1 / RN(act_gs * o_weight_global_scale))  (on the device)
+ *   o     = bf16(RN(alpha * acc))
+ *   out   = bf16(residual + bf16(g * o)),  g = gate[gate_index[m]], or 0 when
+ *           gate_index[m] lies outside [0, gate_rows)    (out = residual)
+ *
+ * Two launches on `stream` (the activation quantiser, then the GEMM, which
+ * starts its weight-independent set-up while the quantiser drains); no host
+ * synchronisation.
+ *   M                      tokens, >= 0 (M == 0 launches nothing)
+ *   attn_out               DEVICE bf16 [M, 7168] row-major, 16-byte aligned
+ *   o_weight_q             DEVICE [5376, 3584] E2M1 codes of o_weight (two
+ *                          per byte), 16-byte aligned (mh3_nvfp4_quantize)
+ *   o_weight_sf            DEVICE tiled scales of o_weight,
+ *                          mh3_nvfp4_scales_bytes(5376, 7168, 1) bytes,
+ *                          16-byte aligned
+ *   o_weight_global_scale  host float, finite and > 0
+ *   act_global_scale       DEVICE pointer to one float (read on the device)
+ *   gate, gate_row_stride, gate_rows, gate_index, residual, out
+ *                          as in mh3_out_proj_run (out may be residual)
+ *   act_q, act_sf          workspaces: [M, 3584] code bytes and the tiled
+ *                          scales of [M, 7168] (mh3_nvfp4_scales_bytes(M,
+ *                          7168, 1) bytes: M * 448 when M is a multiple of
+ *                          128), each 16-byte aligned, or NULL for
+ *                          handle-owned buffers (grown with cudaMallocAsync
+ *                          on `stream`); they hold the quantised activation
+ *                          after the call
+ * Returns MH3_ERR_INVALID_ARG / MH3_ERR_ALIGNMENT for bad arguments,
+ * MH3_ERR_UNSUPPORTED when no CTA pair of the GEMM fits the device,
+ * MH3_ERR_CUDA for a failed launch.  Bounded waits report to the handle's
+ * status word (mh3_preattn_device_status). */
+int mh3_nvfp4_out_proj_run(mh3_preattn_t handle, void* stream, int64_t M,
+                           const mh3_bf16* attn_out, const uint8_t* o_weight_q,
+                           const uint8_t* o_weight_sf, float o_weight_global_scale,
+                           const float* act_global_scale, const mh3_bf16* gate,
+                           int64_t gate_row_stride, int64_t gate_rows,
+                           const int32_t* gate_index, const mh3_bf16* residual, uint8_t* act_q,
+                           uint8_t* act_sf, mh3_bf16* out);
+
+/* Host-only validation of an mh3_nvfp4_out_proj_run argument set (the
+ * arguments other than the handle, the stream and the workspaces; no device
+ * access); same rules and status codes. */
+int mh3_nvfp4_out_proj_validate(int64_t M, const mh3_bf16* attn_out, const uint8_t* o_weight_q,
+                                const uint8_t* o_weight_sf, float o_weight_global_scale,
+                                const float* act_global_scale, const mh3_bf16* gate,
+                                int64_t gate_row_stride, int64_t gate_rows,
+                                const int32_t* gate_index, const mh3_bf16* residual,
+                                const mh3_bf16* out);
 
 /* Message of the calling thread's last failed call ("" if none). */
 const char* mh3_preattn_last_error(void);

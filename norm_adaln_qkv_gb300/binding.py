@@ -38,7 +38,8 @@ EXPORTS = ("mh3_preattn_create", "mh3_preattn_destroy", "mh3_preattn_workspace_b
            "mh3_e4m3_quantize", "mh3_nvfp4_codes_bytes", "mh3_nvfp4_scales_bytes",
            "mh3_nvfp4_quantize", "mh3_nvfp4_norm_quant", "mh3_nvfp4_preattn_run", "mh3_nvfp4_qkv",
            "mh3_preattn_set_test_stall", "mh3_mlp_fp8_run", "mh3_mlp_fp8_validate",
-           "mh3_mlp_fp8_workspace_bytes")
+           "mh3_mlp_fp8_workspace_bytes", "mh3_nvfp4_out_proj_run",
+           "mh3_nvfp4_out_proj_validate")
 
 _vp = ctypes.c_void_p
 _i64 = ctypes.c_int64
@@ -88,6 +89,10 @@ _SIGS = {
     "mh3_mlp_fp8_validate": (_i32, [_i64, _vp, _vp, _vp, _i64, _vp, _i64, _vp, _i64, _i64, _vp,
                                     _vp, _vp, _vp, _vp, _vp, _f32, _vp, _vp, _vp, _vp, _vp, _vp]),
     "mh3_mlp_fp8_workspace_bytes": (ctypes.c_size_t, [_i64, _i32]),
+    "mh3_nvfp4_out_proj_run": (_i32, [_vp, _vp, _i64, _vp, _vp, _vp, _f32, _vp, _vp, _i64, _i64,
+                                      _vp, _vp, _vp, _vp, _vp]),
+    "mh3_nvfp4_out_proj_validate": (_i32, [_i64, _vp, _vp, _vp, _f32, _vp, _vp, _i64, _i64, _vp,
+                                           _vp, _vp]),
 }
 
 _lib = None
@@ -177,7 +182,8 @@ class Handle:
         bounded waits run out and it reports a status code."""
         _check(load().mh3_preattn_set_test_stall(self._h, 1 if stall else 0),
                "mh3_preattn_set_test_stall", "mh3_mlp_fp8_run", "mh3_mlp_fp8_validate",
-           "mh3_mlp_fp8_workspace_bytes")
+           "mh3_mlp_fp8_workspace_bytes", "mh3_nvfp4_out_proj_run",
+           "mh3_nvfp4_out_proj_validate")
 
 
 _handles = {}
@@ -448,6 +454,70 @@ def mh3_nvfp4_qkv(handle: Handle, stream, M, act_q, act_sf, weight_q, weight_sf,
         _ptr(weight_sf), float(weight_global_scale), _ptr(act_global_scale),
         float("nan") if alpha is None else float(alpha), _ptr(q_norm_weight), _ptr(k_norm_weight),
         _ptr(rope_cos_sin), P, float(eps), _ptr(qkv_descale), _ptr(out)), "mh3_nvfp4_qkv")
+
+
+def mh3_nvfp4_out_proj_validate(M, attn_out, o_weight_q, o_weight_sf, o_weight_global_scale,
+                                act_global_scale, gate, gate_row_stride, gate_rows, gate_index,
+                                residual, out) -> int:
+    """Host-only validation of a W4A4 output-projection call; returns the status."""
+    return load().mh3_nvfp4_out_proj_validate(
+        M, _ptr(attn_out), _ptr(o_weight_q), _ptr(o_weight_sf), float(o_weight_global_scale),
+        _ptr(act_global_scale), _ptr(gate), gate_row_stride, gate_rows, _ptr(gate_index),
+        _ptr(residual), _ptr(out))
+
+
+def mh3_nvfp4_out_proj_run(handle: Handle, stream, M, attn_out, o_weight_q, o_weight_sf,
+                           o_weight_global_scale, act_global_scale, gate, gate_row_stride,
+                           gate_rows, gate_index, residual, act_q, act_sf, out) -> None:
+    _check(load().mh3_nvfp4_out_proj_run(
+        handle.ptr, _stream_ptr(stream), M, _ptr(attn_out), _ptr(o_weight_q), _ptr(o_weight_sf),
+        float(o_weight_global_scale), _ptr(act_global_scale), _ptr(gate), gate_row_stride,
+        gate_rows, _ptr(gate_index), _ptr(residual), _ptr(act_q), _ptr(act_sf), _ptr(out)),
+        "mh3_nvfp4_out_proj_run")
+
+
+def minimax_h3_nvfp4_out_proj(attn_out, o_weight_q, o_weight_sf, o_weight_global_scale,
+                              act_global_scale, gate, gate_index, residual, *,
+                              out: Optional[torch.Tensor] = None,
+                              act_q: Optional[torch.Tensor] = None,
+                              act_sf: Optional[torch.Tensor] = None, stream=None,
+                              handle: Optional[Handle] = None) -> torch.Tensor:
+    """Torch-tensor entry point with the argument list of the page
+    flashinfer.diffusion_ops.minimax_h3_nvfp4_out_proj; returns ``out``
+    (allocated when None; may be ``residual``).  o_weight_sf is in this
+    library's tiled layout (mh3_nvfp4_quantize with tiled=True); act_sf, when
+    given, holds mh3_nvfp4_scales_bytes(M, 7168, 1) bytes."""
+    M = attn_out.shape[0]
+    bf = torch.bfloat16
+    u8 = torch.uint8
+    width = NUM_HEADS * HEAD_DIM
+    _check_tensor(attn_out, "attn_out", bf, (M, width))
+    _check_tensor(o_weight_q, "o_weight_q", u8, (HIDDEN, width // 2))
+    _check_tensor(o_weight_sf, "o_weight_sf", u8)
+    if o_weight_sf.numel() != int(load().mh3_nvfp4_scales_bytes(HIDDEN, width, 1)):
+        raise ValueError("o_weight_sf must hold the tiled scales of [5376, 7168]")
+    if isinstance(o_weight_global_scale, torch.Tensor):
+        o_weight_global_scale = float(o_weight_global_scale.reshape(-1)[0])
+    _check_tensor(act_global_scale, "act_global_scale", torch.float32, (1,))
+    _check_tensor(gate, "gate", bf, contiguous=False)
+    if gate.dim() != 2 or gate.shape[1] != HIDDEN or gate.stride(1) != 1:
+        raise ValueError(f"gate must be [rows, {HIDDEN}] with stride(1) == 1")
+    _check_tensor(gate_index, "gate_index", torch.int32, (M,))
+    _check_tensor(residual, "residual", bf, (M, HIDDEN))
+    if out is None:
+        out = torch.empty_like(residual)
+    _check_tensor(out, "out", bf, (M, HIDDEN))
+    if act_q is not None:
+        _check_tensor(act_q, "act_q", u8, (M, width // 2))
+    if act_sf is not None:
+        _check_tensor(act_sf, "act_sf", u8)
+        if act_sf.numel() < int(load().mh3_nvfp4_scales_bytes(M, width, 1)):
+            raise ValueError("act_sf is smaller than the tiled scales of [M, 7168]")
+    h = handle if handle is not None else default_handle(attn_out.device.index)
+    mh3_nvfp4_out_proj_run(h, stream, M, attn_out, o_weight_q, o_weight_sf,
+                           o_weight_global_scale, act_global_scale, gate, gate.stride(0),
+                           gate.shape[0], gate_index, residual, act_q, act_sf, out)
+    return out
 
 
 def mh3_preattn_norm_adaln(handle: Handle, stream, M, x, x_norm_weight, adaln_scale,

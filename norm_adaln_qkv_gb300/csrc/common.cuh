@@ -96,11 +96,33 @@ struct Nvfp4Maps {
   CUtensorMap b;    // weight codes [21504, 2688] bytes, box 128 B x 128 rows, 128-B swizzle
   CUtensorMap sfa;  // act scales, tiled atoms as u32 (128, 84, ceil(M/128)), box 128 x 4 x 1
   CUtensorMap sfb;  // weight scales, tiled atoms as u32 (128, 84, 168), box 128 x 4 x 2
-  CUtensorMap out;  // as QkvMaps::out (bf16) or the e4m3 byte map
+  CUtensorMap out;  // as QkvMaps::out (bf16) or the e4m3 byte map; out-projection: [M, 5376]
+  CUtensorMap aux;  // out-projection: residual [M, 5376], box 64 x 32
 };
 cudaError_t nvfp4_qkv_prepare_device(int* max_clusters, int* max_clusters_e4m3);
 cudaError_t launch_nvfp4_qkv(const Nvfp4Maps& maps, const QkvParams& p, int clusters, bool e4m3,
                              cudaStream_t stream);
+
+// W4A4 output projection with the gated residual (the same block-scaled GEMM):
+//   o = bf16(RN(alpha * acc)), out = bf16(residual + bf16(g * o)).
+//   a: attn codes [M, 3584] bytes; b: o_weight codes [5376, 3584]; scales tiled.
+struct Nvfp4OutProjParams {
+  int64_t M;
+  int num_m_tiles;  // 256-row blocks
+  int num_tiles;    // num_m_tiles * 21
+  int* status;
+  int test_stall = 0;
+  float alpha = 1.0f;              // given (finite, > 0) or derived as in QkvParams
+  const float* act_gs = nullptr;
+  float w_gs = 0.0f;
+  const __nv_bfloat16* gate;       // [gate_rows, 5376] view
+  int64_t gate_stride;
+  int64_t gate_rows;
+  const int32_t* gate_index;       // [M]
+};
+cudaError_t nvfp4_out_proj_prepare_device(int* max_clusters);
+cudaError_t launch_nvfp4_out_proj(const Nvfp4Maps& maps, const Nvfp4OutProjParams& p,
+                                  int clusters, cudaStream_t stream);
 
 // Standalone NVFP4 quantiser: rows x cols bf16 (cols a multiple of 64) ->
 // packed codes [rows, cols/2] and scales (tiled atoms or row-major).

@@ -1,7 +1,9 @@
-// k2_nvfp4_pair.cu -- kernel 2 of the NVFP4 pre-attention stage: the QKV
-// projection with block-scaled FP4 operands on the CTA-pair tcgen05 MMA,
-// with the Q/K RMSNorm, RoPE and destination-major pack epilogue applied to
-// y = bf16(RN(alpha * acc))
+// k2_nvfp4_pair.cu -- the block-scaled FP4 (NVFP4) CTA-pair GEMM: kernel 2
+// of the NVFP4 pre-attention stage (the QKV projection, with the Q/K
+// RMSNorm, RoPE and destination-major pack epilogue applied to
+// y = bf16(RN(alpha * acc))), and, with another epilogue policy, the W4A4
+// attention output projection with the gated residual
+// (flashinfer.diffusion_ops.minimax_h3_nvfp4_out_proj, summary)
 // (flashinfer.diffusion_ops.minimax_h3_nvfp4_pre_attention, summary:
 // NVFP4 operands, accumulator rescaled by alpha; Parameters: qkv_weight_q,
 // qkv_weight_sf, qkv_weight_global_scale, act_global_scale, alpha).
@@ -54,8 +56,6 @@ constexpr int FBM = 128;                       // A rows per CTA
 constexpr int kFTileN = 256;                   // two heads
 constexpr int kFBRows = kFTileN / 2;           // B rows per CTA
 constexpr int kFBytesPerRow = 128;             // one k-block of one row
-constexpr int kFKBlocks = kHidden / 256;       // 21
-constexpr int kFNTiles = kQkvRows / kFTileN;   // 84
 constexpr int kFNTilesPerKind = kKindCols / kFTileN;  // 28
 constexpr int kFStages = 5;
 constexpr int kFABytes = FBM * kFBytesPerRow;       // 16 KB
@@ -96,8 +96,9 @@ constexpr int kFOffSfb = kFOffSfa + kFStages * kFSfaBytes;
 constexpr int kFOffStg = kFOffSfb + kFStages * kFSfbBytes;
 constexpr int kFOffBar = kFOffStg + kEpiWarps * kStgWarpBytes;
 // per stage: operands full, empty, scales full, ready (scales in TMEM and
-// operands landed); tmem full, tmem empty, drain, copy drain
-constexpr int kFNumBars = 4 * kFStages + 4;
+// operands landed); tmem full, tmem empty, drain, copy drain; one per
+// epilogue warp (loads into its staging buffer)
+constexpr int kFNumBars = 4 * kFStages + 4 + kEpiWarps;
 constexpr int kFOffTmemPtr = kFOffBar + kFNumBars * 8;
 constexpr int kFOffAbort = kFOffTmemPtr + 4;
 constexpr int kFOffScratch = kFOffBar + 256;
@@ -124,6 +125,7 @@ struct FSmem {
   __device__ uint32_t tempty() const { return base + kFOffBar + (4 * kFStages + 1) * 8; }
   __device__ uint32_t drain() const { return base + kFOffBar + (4 * kFStages + 2) * 8; }
   __device__ uint32_t cpdrain() const { return base + kFOffBar + (4 * kFStages + 3) * 8; }
+  __device__ uint32_t epi_bar(int ew) const { return base + kFOffBar + (4 * kFStages + 4 + ew) * 8; }
   __device__ uint32_t stg(int ew) const { return base + kFOffStg + ew * kStgWarpBytes; }
   __device__ uint32_t tmem_ptr_addr() const { return base + kFOffTmemPtr; }
   __device__ uint32_t* tmem_ptr() const { return reinterpret_cast<uint32_t*>(ptr + kFOffTmemPtr); }
@@ -163,13 +165,135 @@ __device__ __forceinline__ void finish_role(bool tmem_owner, uint32_t tmem_base)
   }
 }
 
+// What an epilogue warp gets for one tile whose accumulator it has drained
+// into registers (y[i] = bf16 columns 2i, 2i + 1 of the 256, RN(alpha acc)).
+struct FEpiCtx {
+  int lane;
+  int quad;          // TMEM lane quadrant (warp % 4)
+  uint32_t rank;     // CTA of the pair
+  uint32_t stg;      // this warp's staging buffer (8 KB)
+  uint32_t epi_bar;  // this warp's own mbarrier
+  uint32_t* epi_phase;
+  const float* scratch;
+  const CUtensorMap* tm_out;
+  const CUtensorMap* tm_aux;
+  const gp::PairCtx* pair;
+};
+
+// Epilogue policies (all members inline: warps with different register
+// budgets may share no out-of-line code):
+//   Params (with M, num_m_tiles, num_tiles, status, test_stall, alpha, act_gs,
+//   w_gs), kKBlocks (K / 256), kNTiles (N / 256), prologue(), tile().
+
+// The pre-attention QKV projection: Q/K RMSNorm, RoPE and pack per head.
 template <bool kE4m3>
+struct QkvFp4Epi {
+  using Params = QkvParams;
+  static constexpr int kKBlocks = kHidden / 256;      // 21
+  static constexpr int kNTiles = kQkvRows / kFTileN;  // 84
+  // q then k norm weights as FP32
+  __device__ static __forceinline__ void prologue(float* scratch, int tid, const Params& p) {
+    for (int i = tid; i < 2 * kHeadDim; i += kFThreads) {
+      const __nv_bfloat16 w = i < kHeadDim ? p.q_norm_weight[i] : p.k_norm_weight[i - kHeadDim];
+      scratch[i] = __bfloat162float(w);
+    }
+  }
+  __device__ static __forceinline__ void tile(const uint32_t (&y)[128], const FEpiCtx& c,
+                                              const Params& p, int pr, int n_blk) {
+    const int kind = n_blk / kFNTilesPerKind;
+    const int head0 = (n_blk % kFNTilesPerKind) * 2;
+    const int64_t m0 = static_cast<int64_t>(pr) * (2 * FBM) + static_cast<int64_t>(c.rank) * FBM +
+                       c.quad * 32;
+    const uint4* cs_row = rope_row(p, m0 + c.lane, kind);
+#pragma unroll
+    for (int j = 0; j < 2; ++j) {
+      uint32_t yh[64];
+#pragma unroll
+      for (int i = 0; i < 64; ++i) yh[i] = y[64 * j + i];
+      epilogue_head_regs<kE4m3>(yh, c.lane, c.stg, c.scratch, p, m0, kind, head0 + j, cs_row,
+                                c.tm_out);
+    }
+  }
+};
+
+// The attention output projection with the gated residual (W4A4):
+//   o = bf16(RN(alpha acc)),  out = bf16(residual + bf16(g * o)),
+//   g = gate[gate_index[m]], or 0 for an index outside [0, gate_rows).
+// Per warp and 128-column half: the residual block is TMA-loaded into the
+// staging buffer, combined in place and TMA-stored to out (so out may alias
+// residual: a block is read before the same warp writes it).
+struct OutProjFp4Epi {
+  using Params = Nvfp4OutProjParams;
+  static constexpr int kKBlocks = kAttnWidth / 256;  // 28
+  static constexpr int kNTiles = kHidden / kFTileN;  // 21
+  __device__ static __forceinline__ void prologue(float*, int, const Params&) {}
+  __device__ static __forceinline__ void tile(const uint32_t (&y)[128], const FEpiCtx& c,
+                                              const Params& p, int pr, int n_blk) {
+    const int64_t m0 = static_cast<int64_t>(pr) * (2 * FBM) + static_cast<int64_t>(c.rank) * FBM +
+                       c.quad * 32;
+    if (m0 >= p.M) return;  // no row of this warp is stored
+    const int64_t m = m0 + c.lane;
+    const uint4* grow = nullptr;
+    if (m < p.M) {
+      const int64_t gi = static_cast<int64_t>(__ldg(p.gate_index + m));
+      if (gi >= 0 && gi < p.gate_rows)
+        grow = reinterpret_cast<const uint4*>(p.gate + gi * p.gate_stride);
+    }
+    const uint64_t pol = policy_evict_first();
+#pragma unroll
+    for (int j = 0; j < 2; ++j) {  // unrolled: y stays in registers
+      const int col0 = n_blk * kFTileN + j * kHeadDim;
+      if (c.lane == 0) bulk_wait_group_read0();  // the previous store has read the staging
+      __syncwarp();
+      if (c.lane == 0) {
+        mbar_arrive_expect_tx(c.epi_bar, 2 * kStgHalfBytes);
+        tma_load_2d(c.stg, c.tm_aux, c.epi_bar, col0, static_cast<int32_t>(m0));
+        tma_load_2d(c.stg + kStgHalfBytes, c.tm_aux, c.epi_bar, col0 + 64,
+                    static_cast<int32_t>(m0));
+      }
+      wait_phase_inl<false>(c.epi_bar, *c.epi_phase, c.pair->abort_flag, c.pair->status,
+                            kStatusEpiResidual);
+      __syncwarp();
+      *c.epi_phase ^= 1u;
+#pragma unroll
+      for (int chunk = 0; chunk < 16; ++chunk) {
+        const uint32_t addr = stg_addr(c.stg, c.lane, chunk);
+        const uint4 res = ld_shared_v4(addr);
+        const uint4 gw = grow ? __ldg(grow + (col0 >> 3) + chunk) : make_uint4(0u, 0u, 0u, 0u);
+        const uint32_t rw[4] = {res.x, res.y, res.z, res.w};
+        const uint32_t gg[4] = {gw.x, gw.y, gw.z, gw.w};
+        uint32_t ow[4];
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+          const uint32_t yw = y[64 * j + 4 * chunk + e];
+          const float r0 = __fadd_rn(bf16_lo(rw[e]), round_bf16(__fmul_rn(bf16_lo(gg[e]), bf16_lo(yw))));
+          const float r1 = __fadd_rn(bf16_hi(rw[e]), round_bf16(__fmul_rn(bf16_hi(gg[e]), bf16_hi(yw))));
+          ow[e] = pack_bf16x2(r0, r1);
+        }
+        st_shared_v4(addr, make_uint4(ow[0], ow[1], ow[2], ow[3]));
+      }
+      fence_proxy_async_smem();
+      __syncwarp();
+      if (c.lane == 0) {
+        tma_store_2d_hint(c.tm_out, c.stg, col0, static_cast<int32_t>(m0), pol);
+        tma_store_2d_hint(c.tm_out, c.stg + kStgHalfBytes, col0 + 64, static_cast<int32_t>(m0),
+                          pol);
+        bulk_commit_group();
+      }
+    }
+  }
+};
+
+template <class Epi>
 __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kFThreads, 1)
-    nvfp4_qkv_kernel(const __grid_constant__ CUtensorMap tm_a,
-                     const __grid_constant__ CUtensorMap tm_b,
-                     const __grid_constant__ CUtensorMap tm_sfa,
-                     const __grid_constant__ CUtensorMap tm_sfb,
-                     const __grid_constant__ CUtensorMap tm_out, const QkvParams p) {
+    nvfp4_pair_kernel(const __grid_constant__ CUtensorMap tm_a,
+                      const __grid_constant__ CUtensorMap tm_b,
+                      const __grid_constant__ CUtensorMap tm_sfa,
+                      const __grid_constant__ CUtensorMap tm_sfb,
+                      const __grid_constant__ CUtensorMap tm_out,
+                      const __grid_constant__ CUtensorMap tm_aux, const typename Epi::Params p) {
+  constexpr int kFKBlocks = Epi::kKBlocks;
+  constexpr int kFNTiles = Epi::kNTiles;
   extern __shared__ uint8_t smem_raw[];
   FSmem sm;
   {
@@ -194,6 +318,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kFThreads, 1)
     mbar_init(sm.tempty(), 2 * kEpiWarps);
     mbar_init(sm.drain(), 1);
     mbar_init(sm.cpdrain(), kCpWarps);
+    for (int w = 0; w < kEpiWarps; ++w) mbar_init(sm.epi_bar(w), 1);
     *sm.abort_flag() = 0;
     fence_mbar_init();
     prefetch_tmap(&tm_a);
@@ -201,12 +326,9 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kFThreads, 1)
     prefetch_tmap(&tm_sfa);
     prefetch_tmap(&tm_sfb);
     prefetch_tmap(&tm_out);
+    prefetch_tmap(&tm_aux);
   }
-  // q then k norm weights as FP32
-  for (int i = threadIdx.x; i < 2 * kHeadDim; i += kFThreads) {
-    const __nv_bfloat16 w = i < kHeadDim ? p.q_norm_weight[i] : p.k_norm_weight[i - kHeadDim];
-    sm.scratch()[i] = __bfloat162float(w);
-  }
+  Epi::prologue(sm.scratch(), threadIdx.x, p);
   if (warp == 1) {
     tmem_alloc_pair(sm.tmem_ptr_addr(), kTmemCols);
     tmem_relinquish_pair();
@@ -225,7 +347,9 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kFThreads, 1)
     // ------------------------------------------------- epilogue (both CTAs)
     const int ew = warp - kFEpiWarp0;
     const int quad = warp & 3;
-    const uint32_t stg = sm.stg(ew);
+    uint32_t epi_phase = 0;
+    const FEpiCtx ec{lane, quad, rank, sm.stg(ew), sm.epi_bar(ew), &epi_phase, sm.scratch(),
+                     &tm_out, &tm_aux, &ctx};
     const float alpha = isfinite(p.alpha) && p.alpha > 0.0f
                             ? p.alpha
                             : __frcp_rn(__fmul_rn(__ldg(p.act_gs), p.w_gs));
@@ -243,19 +367,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kFThreads, 1)
       if (lane == 0) mbar_arrive_cluster(mapa_shared(sm.tempty(), 0));
       int pr, n_blk;
       tile_coords<gp::kGroupPairs, kFNTiles>(t, p.num_m_tiles, pr, n_blk);
-      const int kind = n_blk / kFNTilesPerKind;
-      const int head0 = (n_blk % kFNTilesPerKind) * 2;
-      const int64_t m0 = static_cast<int64_t>(pr) * (2 * FBM) + static_cast<int64_t>(rank) * FBM +
-                         quad * 32;
-      const uint4* cs_row = rope_row(p, m0 + lane, kind);
-#pragma unroll
-      for (int j = 0; j < 2; ++j) {
-        uint32_t yh[64];
-#pragma unroll
-        for (int i = 0; i < 64; ++i) yh[i] = y[64 * j + i];
-        epilogue_head_regs<kE4m3>(yh, lane, stg, sm.scratch(), p, m0, kind, head0 + j, cs_row,
-                                  &tm_out);
-      }
+      Epi::tile(y, ec, p, pr, n_blk);
     }
     if (lane == 0) bulk_wait_group0();
     __syncwarp();
@@ -408,29 +520,30 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kFThreads, 1)
   }
 }
 
-template <bool kE4m3>
+template <class Epi>
 cudaError_t prepare_one(int* max_clusters) {
   *max_clusters = 0;
   // The register split (setmaxnreg) is sized for a launch at exactly
   // kRegsLaunch registers per thread; with any other entry allocation an
   // `inc` could wait forever, so such a build is refused here.
   cudaFuncAttributes fa;
-  cudaError_t e = cudaFuncGetAttributes(&fa, nvfp4_qkv_kernel<kE4m3>);
+  cudaError_t e = cudaFuncGetAttributes(&fa, nvfp4_pair_kernel<Epi>);
   if (e != cudaSuccess) return e;
   if (fa.numRegs != kRegsLaunch || fa.maxThreadsPerBlock < kFThreads)
     return cudaErrorInvalidConfiguration;
-  e = cudaFuncSetAttribute(nvfp4_qkv_kernel<kE4m3>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+  e = cudaFuncSetAttribute(nvfp4_pair_kernel<Epi>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                            kFSmemAlloc);
   if (e != cudaSuccess) return e;
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(2, 1, 1);
   cfg.blockDim = dim3(kFThreads, 1, 1);
   cfg.dynamicSmemBytes = kFSmemAlloc;
-  return cudaOccupancyMaxActiveClusters(max_clusters, nvfp4_qkv_kernel<kE4m3>, &cfg);
+  return cudaOccupancyMaxActiveClusters(max_clusters, nvfp4_pair_kernel<Epi>, &cfg);
 }
 
-template <bool kE4m3>
-cudaError_t launch_one(const Nvfp4Maps& m, const QkvParams& p, int clusters, cudaStream_t stream) {
+template <class Epi>
+cudaError_t launch_one(const Nvfp4Maps& m, const typename Epi::Params& p, int clusters,
+                       cudaStream_t stream) {
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(static_cast<unsigned>(2 * clusters), 1, 1);
   cfg.blockDim = dim3(kFThreads, 1, 1);
@@ -441,22 +554,35 @@ cudaError_t launch_one(const Nvfp4Maps& m, const QkvParams& p, int clusters, cud
   attr[0].val.programmaticStreamSerializationAllowed = MH3_PDL ? 1 : 0;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  return cudaLaunchKernelEx(&cfg, nvfp4_qkv_kernel<kE4m3>, m.a, m.b, m.sfa, m.sfb, m.out, p);
+  // the QKV form has no auxiliary input: its output map stands in
+  return cudaLaunchKernelEx(&cfg, nvfp4_pair_kernel<Epi>, m.a, m.b, m.sfa, m.sfb, m.out, m.aux, p);
 }
 
 }  // namespace
 
 cudaError_t nvfp4_qkv_prepare_device(int* max_clusters, int* max_clusters_e4m3) {
-  cudaError_t e = prepare_one<false>(max_clusters);
+  cudaError_t e = prepare_one<QkvFp4Epi<false>>(max_clusters);
   if (e != cudaSuccess) return e;
-  return prepare_one<true>(max_clusters_e4m3);
+  return prepare_one<QkvFp4Epi<true>>(max_clusters_e4m3);
 }
 
 cudaError_t launch_nvfp4_qkv(const Nvfp4Maps& maps, const QkvParams& p, int clusters, bool e4m3,
                              cudaStream_t stream) {
   if (p.M <= 0) return cudaSuccess;
-  return e4m3 ? launch_one<true>(maps, p, clusters, stream)
-              : launch_one<false>(maps, p, clusters, stream);
+  Nvfp4Maps m = maps;
+  m.aux = maps.out;
+  return e4m3 ? launch_one<QkvFp4Epi<true>>(m, p, clusters, stream)
+              : launch_one<QkvFp4Epi<false>>(m, p, clusters, stream);
+}
+
+cudaError_t nvfp4_out_proj_prepare_device(int* max_clusters) {
+  return prepare_one<OutProjFp4Epi>(max_clusters);
+}
+
+cudaError_t launch_nvfp4_out_proj(const Nvfp4Maps& maps, const Nvfp4OutProjParams& p,
+                                  int clusters, cudaStream_t stream) {
+  if (p.M <= 0) return cudaSuccess;
+  return launch_one<OutProjFp4Epi>(maps, p, clusters, stream);
 }
 
 }  // namespace mh3

@@ -44,6 +44,7 @@ struct mh3_preattn_ctx {
   size_t ws_bytes = 0;
   int nvfp4_clusters = 0;       // resident clusters of the NVFP4 GEMM (bf16 out)
   int nvfp4_e4m3_clusters = 0;  // ... and its e4m3-output form
+  int nvfp4_out_clusters = 0;   // ... and the W4A4 output projection
   void* act_q = nullptr;        // handle-owned NVFP4 stage-1 workspaces
   size_t act_q_bytes = 0;
   void* act_sf = nullptr;
@@ -375,6 +376,9 @@ int mh3_preattn_create(mh3_preattn_t* handle, int device) {
   int nvfp4_clusters = 0, nvfp4_e4m3_clusters = 0;
   e = nvfp4_qkv_prepare_device(&nvfp4_clusters, &nvfp4_e4m3_clusters);
   if (e != cudaSuccess) return cuda_fail(e, "preparing the NVFP4 GEMM");
+  int nvfp4_out_clusters = 0;
+  e = nvfp4_out_proj_prepare_device(&nvfp4_out_clusters);
+  if (e != cudaSuccess) return cuda_fail(e, "preparing the NVFP4 output projection");
   int fc1_fp8_clusters = 0, fc2_fp8_clusters = 0;
   e = mlp_fp8_fc1_prepare_device(&fc1_fp8_clusters);
   if (e == cudaSuccess) e = mlp_fp8_fc2_prepare_device(&fc2_fp8_clusters);
@@ -383,6 +387,7 @@ int mh3_preattn_create(mh3_preattn_t* handle, int device) {
   h->device = device;
   h->nvfp4_clusters = nvfp4_clusters;
   h->nvfp4_e4m3_clusters = nvfp4_e4m3_clusters;
+  h->nvfp4_out_clusters = nvfp4_out_clusters;
   h->fc1_clusters = fc1_clusters;
   h->e4m3_clusters = e4m3_clusters;
   h->fc2_clusters = fc2_clusters;
@@ -545,10 +550,12 @@ int mh3_preattn_device_status(mh3_preattn_t h, void* stream, int* device_code) {
 }  // extern "C"
 
 // --------------------------------------------- attention output projection
-extern "C" int mh3_out_proj_validate(int64_t M, const mh3_bf16* attn_out, const mh3_bf16* o_weight,
-                                     const mh3_bf16* gate, int64_t gate_row_stride,
-                                     int64_t gate_rows, const int32_t* gate_index,
-                                     const mh3_bf16* residual, const mh3_bf16* out) {
+namespace {
+
+// The output projection's arguments other than the weight (BF16 and NVFP4).
+int check_out_proj_args(int64_t M, const mh3_bf16* attn_out, const mh3_bf16* gate,
+                        int64_t gate_row_stride, int64_t gate_rows, const int32_t* gate_index,
+                        const mh3_bf16* residual, const mh3_bf16* out) {
   int rc;
   if ((rc = check_M(M))) return rc;
   if (gate_rows < 1)
@@ -559,7 +566,6 @@ extern "C" int mh3_out_proj_validate(int64_t M, const mh3_bf16* attn_out, const 
   if (gate_row_stride % 8 != 0)
     return fail(MH3_ERR_ALIGNMENT, "gate_row_stride must be a multiple of 8 elements (got %lld)",
                 (long long)gate_row_stride);
-  if ((rc = check_ptr(o_weight, "o_weight", 16))) return rc;
   if ((rc = check_ptr(gate, "gate", 16))) return rc;
   if (M == 0) return MH3_OK;
   if ((rc = check_ptr(attn_out, "attn_out", 16))) return rc;
@@ -571,6 +577,18 @@ extern "C" int mh3_out_proj_validate(int64_t M, const mh3_bf16* attn_out, const 
   if (ro != oo && ro < oo + bytes && oo < ro + bytes)
     return fail(MH3_ERR_INVALID_ARG, "out may equal residual but must not partially overlap it");
   return MH3_OK;
+}
+
+}  // namespace
+
+extern "C" int mh3_out_proj_validate(int64_t M, const mh3_bf16* attn_out, const mh3_bf16* o_weight,
+                                     const mh3_bf16* gate, int64_t gate_row_stride,
+                                     int64_t gate_rows, const int32_t* gate_index,
+                                     const mh3_bf16* residual, const mh3_bf16* out) {
+  int rc;
+  if ((rc = check_ptr(o_weight, "o_weight", 16))) return rc;
+  return check_out_proj_args(M, attn_out, gate, gate_row_stride, gate_rows, gate_index, residual,
+                             out);
 }
 
 extern "C" int mh3_out_proj_run(mh3_preattn_t h, void* stream, int64_t M, const mh3_bf16* attn_out,
@@ -909,6 +927,130 @@ extern "C" int mh3_nvfp4_qkv(mh3_preattn_t h, void* stream, int64_t M, const uin
   return launch_fp4_gemm(h, static_cast<cudaStream_t>(stream), M, act_q, act_sf, weight_q,
                          weight_sf, weight_global_scale, act_global_scale, alpha, alpha_given,
                          q_norm_weight, k_norm_weight, rope_cos_sin, P, eps, qkv_descale, out);
+}
+
+// ---------------------------------------- NVFP4 (W4A4) output projection
+namespace {
+
+constexpr int kOutKSteps = kAttnWidth / 64;  // 112 scale words per token
+
+int check_fp4_out_proj(int64_t M, const mh3_bf16* attn_out, const uint8_t* w_q,
+                       const uint8_t* w_sf, float w_gs, const float* act_gs,
+                       const mh3_bf16* gate, int64_t gate_row_stride, int64_t gate_rows,
+                       const int32_t* gate_index, const mh3_bf16* residual, const mh3_bf16* out) {
+  int rc;
+  if (!(std::isfinite(w_gs) && w_gs > 0.0f))
+    return fail(MH3_ERR_INVALID_ARG, "o_weight_global_scale must be finite and > 0");
+  if ((rc = check_ptr(w_q, "o_weight_q", 16))) return rc;
+  if ((rc = check_ptr(w_sf, "o_weight_sf", 16))) return rc;
+  if ((rc = check_out_proj_args(M, attn_out, gate, gate_row_stride, gate_rows, gate_index,
+                                residual, out)))
+    return rc;
+  if (M > 0 && (rc = check_ptr(act_gs, "act_global_scale", 4))) return rc;
+  return MH3_OK;
+}
+
+}  // namespace
+
+extern "C" int mh3_nvfp4_out_proj_validate(int64_t M, const mh3_bf16* attn_out,
+                                           const uint8_t* o_weight_q, const uint8_t* o_weight_sf,
+                                           float o_weight_global_scale,
+                                           const float* act_global_scale, const mh3_bf16* gate,
+                                           int64_t gate_row_stride, int64_t gate_rows,
+                                           const int32_t* gate_index, const mh3_bf16* residual,
+                                           const mh3_bf16* out) {
+  return check_fp4_out_proj(M, attn_out, o_weight_q, o_weight_sf, o_weight_global_scale,
+                            act_global_scale, gate, gate_row_stride, gate_rows, gate_index,
+                            residual, out);
+}
+
+extern "C" int mh3_nvfp4_out_proj_run(mh3_preattn_t h, void* stream, int64_t M,
+                                      const mh3_bf16* attn_out, const uint8_t* o_weight_q,
+                                      const uint8_t* o_weight_sf, float o_weight_global_scale,
+                                      const float* act_global_scale, const mh3_bf16* gate,
+                                      int64_t gate_row_stride, int64_t gate_rows,
+                                      const int32_t* gate_index, const mh3_bf16* residual,
+                                      uint8_t* act_q, uint8_t* act_sf, mh3_bf16* out) {
+  int rc = check_handle(h);
+  if (rc) return rc;
+  if ((rc = check_fp4_out_proj(M, attn_out, o_weight_q, o_weight_sf, o_weight_global_scale,
+                               act_global_scale, gate, gate_row_stride, gate_rows, gate_index,
+                               residual, out)))
+    return rc;
+  if (M == 0) return MH3_OK;
+  if (act_q != nullptr && (rc = check_ptr(act_q, "act_q", 16))) return rc;
+  if (act_sf != nullptr && (rc = check_ptr(act_sf, "act_sf", 16))) return rc;
+  if (h->nvfp4_out_clusters <= 0)
+    return fail(MH3_ERR_UNSUPPORTED, "no 2-CTA cluster of the NVFP4 output projection fits");
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  if (act_q == nullptr) {
+    if ((rc = grow_buffer(&h->act_q, &h->act_q_bytes, mh3_nvfp4_codes_bytes(M, kAttnWidth), s)))
+      return rc;
+    act_q = static_cast<uint8_t*>(h->act_q);
+  }
+  if (act_sf == nullptr) {
+    if ((rc = grow_buffer(&h->act_sf, &h->act_sf_bytes,
+                          mh3_nvfp4_scales_bytes(M, kAttnWidth, 1), s)))
+      return rc;
+    act_sf = static_cast<uint8_t*>(h->act_sf);
+  }
+  Nvfp4Maps maps;
+  {
+    const cuuint64_t dims[2] = {kAttnWidth / 2, static_cast<cuuint64_t>(M)};
+    const cuuint64_t strides[1] = {kAttnWidth / 2};
+    const cuuint32_t box[2] = {128, 128};
+    if ((rc = encode_tiled(&maps.a, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, act_q, dims, strides, box,
+                           CU_TENSOR_MAP_SWIZZLE_128B, "act_q")))
+      return rc;
+  }
+  {
+    const cuuint64_t dims[2] = {kAttnWidth / 2, kHidden};
+    const cuuint64_t strides[1] = {kAttnWidth / 2};
+    const cuuint32_t box[2] = {128, 128};
+    if ((rc = encode_tiled(&maps.b, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, o_weight_q, dims, strides,
+                           box, CU_TENSOR_MAP_SWIZZLE_128B, "o_weight_q")))
+      return rc;
+  }
+  {
+    const cuuint64_t groups_a = static_cast<cuuint64_t>((M + 127) / 128);
+    const cuuint64_t dims_a[3] = {128, kOutKSteps, groups_a};
+    const cuuint64_t dims_b[3] = {128, kOutKSteps, kHidden / 128};
+    const cuuint64_t strides[2] = {512, 512 * kOutKSteps};
+    const cuuint32_t box_a[3] = {128, 4, 1};
+    const cuuint32_t box_b[3] = {128, 4, 2};
+    if ((rc = encode_tiled(&maps.sfa, CU_TENSOR_MAP_DATA_TYPE_UINT32, 3, act_sf, dims_a, strides,
+                           box_a, CU_TENSOR_MAP_SWIZZLE_NONE, "act_sf")))
+      return rc;
+    if ((rc = encode_tiled(&maps.sfb, CU_TENSOR_MAP_DATA_TYPE_UINT32, 3, o_weight_sf, dims_b,
+                           strides, box_b, CU_TENSOR_MAP_SWIZZLE_NONE, "o_weight_sf")))
+      return rc;
+  }
+  if ((rc = encode_2d(&maps.out, out, kHidden, M, 64, 32, "out"))) return rc;
+  if ((rc = encode_2d(&maps.aux, residual, kHidden, M, 64, 32, "residual"))) return rc;
+  // 1. the activation's block-16 quantisation with act_global_scale (tiled scales)
+  cudaError_t e = launch_nvfp4_quantize(reinterpret_cast<const __nv_bfloat16*>(attn_out), M,
+                                        kAttnWidth, act_global_scale, act_q, act_sf, true,
+                                        h->num_sms, s);
+  if (e != cudaSuccess) return cuda_fail(e, "NVFP4 activation quantiser launch");
+  // 2. the block-scaled GEMM with the gated residual
+  Nvfp4OutProjParams p;
+  p.M = M;
+  p.num_m_tiles = static_cast<int>((M + 255) / 256);
+  p.num_tiles = p.num_m_tiles * (kHidden / 256);
+  p.status = h->d_status;
+  p.alpha = -1.0f;  // derived on the device: RN(1 / RN(act_gs * w_gs))
+  p.act_gs = act_global_scale;
+  p.w_gs = o_weight_global_scale;
+  p.gate = reinterpret_cast<const __nv_bfloat16*>(gate);
+  p.gate_stride = gate_row_stride;
+  p.gate_rows = gate_rows;
+  p.gate_index = gate_index;
+  p.test_stall = 0;
+  const int clusters =
+      p.num_tiles < h->nvfp4_out_clusters ? p.num_tiles : h->nvfp4_out_clusters;
+  e = launch_nvfp4_out_proj(maps, p, clusters, s);
+  if (e != cudaSuccess) return cuda_fail(e, "NVFP4 output projection launch");
+  return MH3_OK;
 }
 
 extern "C" int mh3_e4m3_quantize(void* stream, int64_t n, const mh3_bf16* values,

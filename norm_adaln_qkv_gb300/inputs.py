@@ -20,7 +20,7 @@ from __future__ import annotations
 
 import math
 from dataclasses import dataclass, field
-from typing import Optional
+from typing import Optional, Tuple
 
 import torch
 
@@ -328,6 +328,17 @@ def make_out_proj_workload(M: int, seed: int = SEED_BASE + 100, rows: int = 9,
         res[r0:r1] = _normal(gen, (r1 - r0, HIDDEN)).to(torch.bfloat16)
     return OutProjWorkload(M=M, attn_out=attn, o_weight=w, adaln_mod=mod, gate_index=gi,
                            residual=res)
+
+
+# Global scales of the W4A4 output projection (448 * 6 / amax, Parameters of
+# flashinfer.diffusion_ops.minimax_h3_nvfp4_out_proj): the calibration amax 8
+# for attn_out ~ N(0, 1), and 6 sigma of the weight distribution N(0, 1/7168).
+OUT_ACT_AMAX = 8.0
+
+
+def out_proj_nvfp4_global_scales() -> Tuple[float, float]:
+    """(act_global_scale, o_weight_global_scale)."""
+    return 448.0 * 6.0 / OUT_ACT_AMAX, 448.0 * 6.0 / (6.0 / math.sqrt(ATTN_WIDTH))
 
 
 # ------------------------------------------------------------- the MLP block

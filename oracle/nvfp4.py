@@ -174,3 +174,30 @@ def pre_attention_nvfp4_tokens(x, x_norm_weight, adaln_scale, adaln_shift, adaln
     out = PreAttnTokens(tokens=tok, n=n, a=a, y=y, qkv=qkv)
     out.act_q, out.act_sf, out.alpha = act_q, act_sf, al
     return out
+
+
+def out_proj_nvfp4(attn_out, o_weight_q, o_weight_sf, o_weight_global_scale: float,
+                   act_global_scale: float, gate, gate_index, residual, *,
+                   tokens: Optional[Sequence[int]] = None) -> dict:
+    """The W4A4 attention output projection with the gated residual
+    (flashinfer.diffusion_ops.minimax_h3_nvfp4_out_proj, summary and
+    Parameters): attn_out bf16 [M, 7168] is quantised per token with
+    act_global_scale (the block-16 convention above); o_weight_q [5376, 3584]
+    and o_weight_sf [5376, 448] (row-major) are the quantised weight;
+      o   = bf16(RN32(alpha * RN32(sum_k (qa sa)(qw sw)))),
+      alpha = RN32(1 / RN32(act_gs * w_gs))   (the dequantisation the
+              pre-attention page names alpha; this page derives it from the
+              two global scales)
+      out = bf16(residual + bf16(g * o)),  g = gate[gate_index[m]], 0 outside
+            [0, rows).
+    Returns the activation codes and scales, alpha, o and out for the given
+    tokens (default all)."""
+    from .out_proj import gated_residual
+    if tokens is not None:
+        t = torch.as_tensor(list(tokens), dtype=torch.int64)
+        attn_out, gate_index, residual = attn_out[t], gate_index[t], residual[t]
+    act_q, act_sf = fp4_quantize(attn_out, act_global_scale)
+    al = alpha_from_scales(act_global_scale, o_weight_global_scale)
+    o = nvfp4_projection(act_q, act_sf, o_weight_q, o_weight_sf, al)
+    out = gated_residual(o, gate, gate_index, residual)
+    return dict(act_q=act_q, act_sf=act_sf, alpha=al, o=o, out=out)

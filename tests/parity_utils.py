@@ -95,6 +95,18 @@ def oracle_tokens(wl: Workload, tokens: Optional[Sequence[int]] = None) -> oracl
         rope_positions=wl.rope_positions, tokens=tokens)
 
 
+def untile(tiled: torch.Tensor, rows: int, cols: int) -> torch.Tensor:
+    """Tiled NVFP4 scale atoms -> row-major [rows, cols/16] (the layout the
+    C header states: row r of an atom at byte (r % 32) * 16 + (r / 32) * 4,
+    atoms ordered [rows/128][cols/64])."""
+    ks = cols // 64
+    r = torch.arange(rows).view(-1, 1, 1)
+    k = torch.arange(ks).view(1, -1, 1)
+    j = torch.arange(4).view(1, 1, -1)
+    off = ((r // 128) * ks + k) * 512 + (r % 32) * 16 + ((r // 32) % 4) * 4 + j
+    return tiled.view(-1)[off.reshape(-1)].view(rows, ks * 4)
+
+
 def ulp_bf16(v: torch.Tensor) -> torch.Tensor:
     av = v.abs().to(torch.float64).clamp_min(2.0 ** -126)
     return torch.pow(2.0, torch.floor(torch.log2(av)) - 7)

@@ -12,21 +12,10 @@ import oracle
 from norm_adaln_qkv_gb300 import binding
 from norm_adaln_qkv_gb300.inputs import make_nvfp4_workload
 
-from parity_utils import check_outputs
+from parity_utils import check_outputs, untile
 
 pytestmark = pytest.mark.gpu
 BF16 = torch.bfloat16
-
-
-def untile(tiled: torch.Tensor, rows: int, cols: int) -> torch.Tensor:
-    """Tiled scale atoms -> row-major [rows, cols/16] (the layout stated in
-    the header: row r of an atom at byte (r % 32) * 16 + (r / 32) * 4)."""
-    ks = cols // 64
-    r = torch.arange(rows).view(-1, 1, 1)
-    k = torch.arange(ks).view(1, -1, 1)
-    j = torch.arange(4).view(1, 1, -1)
-    off = ((r // 128) * ks + k) * 512 + (r % 32) * 16 + ((r // 32) % 4) * 4 + j
-    return tiled.view(-1)[off.reshape(-1)].view(rows, ks * 4)
 
 
 @pytest.fixture(scope="module")

@@ -288,3 +288,57 @@ def test_element_code_is_one_rounding_of_the_exact_quotient():
         assert s.item() == sf_code
         assert codes[0] == exact != two, (x, gs, codes[0], exact, two)
         assert codes[1] == exact | 8  # the same magnitude, sign kept
+
+
+# ---------------------------------------------- W4A4 output projection
+def _exact_out_proj_inputs(M, K, N, gs_a, gs_w, seed):
+    """attn_out and o_weight whose every 16-block is e2m1 values times a
+    power of two p (one 6 per block) divided by the global scale: the block
+    scale is then p exactly and every code is the e2m1 value, so NVFP4 is
+    lossless."""
+    g = torch.Generator().manual_seed(seed)
+    def grid(rows, gs):
+        c = torch.randint(0, 16, (rows, K), generator=g, dtype=torch.uint8)
+        c[:, ::16] = 7                                           # amax 6
+        p = torch.exp2(torch.randint(-2, 3, (rows, K // 16), generator=g).double())
+        v = f.e2m1_values(c) * p.repeat_interleave(16, dim=1) / gs
+        return v.to(BF16)
+    return grid(M, gs_a), grid(N, gs_w)
+
+
+def test_out_proj_nvfp4_equals_bf16_out_proj_when_exact():
+    """With lossless operands and power-of-two global scales (alpha exact),
+    the W4A4 projection with the gated residual is the BF16 output
+    projection's oracle bit for bit, bad gate indices included."""
+    from oracle import out_proj as op
+    M, K, N = 7, 128, 40
+    gs_a, gs_w = 4.0, 0.5
+    a, w = _exact_out_proj_inputs(M, K, N, gs_a, gs_w, seed=21)
+    wq, wsf = f.fp4_quantize(w, gs_w)
+    assert torch.equal(f.dequantize(wq, wsf, gs_w), w.double())
+    g = torch.Generator().manual_seed(22)
+    gate = torch.randn(3, N, generator=g).to(BF16)
+    gi = torch.tensor([0, 2, -1, 1, 3, 2, 2 ** 30], dtype=torch.int32)
+    res = torch.randn(M, N, generator=g).to(BF16)
+    got = f.out_proj_nvfp4(a, wq, wsf, gs_w, gs_a, gate, gi, res)
+    assert got["alpha"] == 0.5
+    assert torch.equal(f.dequantize(got["act_q"], got["act_sf"], gs_a), a.double())
+    ref = op.out_proj_gated_residual(a, w, gate, gi, res)
+    assert torch.equal(got["out"].view(torch.int16), ref.view(torch.int16))
+    for m in (2, 6):  # bad index: out is the residual
+        assert torch.equal(got["out"][m].view(torch.int16), res[m].view(torch.int16))
+
+
+def test_out_proj_nvfp4_token_subset_is_row_subset():
+    g = torch.Generator().manual_seed(23)
+    M, K, N = 9, 64, 24
+    a = torch.randn(M, K, generator=g).to(BF16)
+    w = (torch.randn(N, K, generator=g) / 8).to(BF16)
+    wq, wsf = f.fp4_quantize(w, 448.0 * 6 / 0.75)
+    gate = torch.randn(2, N, generator=g).to(BF16)
+    gi = torch.tensor([0, 1, 1, 0, -1, 1, 0, 1, 2], dtype=torch.int32)
+    res = torch.randn(M, N, generator=g).to(BF16)
+    full = f.out_proj_nvfp4(a, wq, wsf, 448.0 * 6 / 0.75, 336.0, gate, gi, res)
+    sub = f.out_proj_nvfp4(a, wq, wsf, 448.0 * 6 / 0.75, 336.0, gate, gi, res, tokens=[8, 3, 4])
+    assert torch.equal(sub["out"].view(torch.int16), full["out"][[8, 3, 4]].view(torch.int16))
+    assert torch.equal(sub["act_q"], full["act_q"][[8, 3, 4]])
