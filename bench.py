@@ -563,14 +563,27 @@ def run_ours(args, world, rank, local):
             torch.cuda.synchronize()
             return t0.elapsed_time(t1) / n
 
+        ocodes = torch.empty(lib.mh3_preattn_out_nvfp4_bytes(Mf, 0), dtype=torch.uint8, device=dev)
+        osf = torch.empty(lib.mh3_preattn_out_nvfp4_bytes(Mf, 1), dtype=torch.uint8, device=dev)
+        ogs = torch.tensor([336.0, 448.0, 268.8], dtype=torch.float32, device=dev)
+
+        def f_stage_fp4out():
+            binding.mh3_nvfp4_preattn_run_nvfp4_out(
+                h, stream, Mf, d["x"], d["xw"], d["sc"], d["sc"].stride(0), d["sh"],
+                d["sh"].stride(0), wl.spec.rows, idx32, wq, wsf, wf.weight_global_scale, gsa, None,
+                d["qw"], d["kw"], csf, Pf, wl.spec.eps, ogs, aq, asf, ocodes, osf)
+
         st_ms = timed(f_stage, args.steps)
         k1f_ms = timed(f_k1, args.steps)
         k2f_ms = timed(f_k2, args.steps)
+        st4_ms = timed(f_stage_fp4out, args.steps)
+        del ocodes, osf
         tf4 = FLOP_PER_TOKEN * Mf / (k2f_ms * 1e-3) / 1e12
         k1f_bytes = Mf * 10752 + Mf * 4 + Mf * 2688 + Mf * 336
         nvfp4_line = {
             "workload": f"{wl.spec.name}, NVFP4 operands (W4A4, block 16, UE4M3 scales)",
             "stage_us": st_ms * 1e3, "k1_us": k1f_ms * 1e3, "k2_us": k2f_ms * 1e3,
+            "stage_us_out_mode_nvfp4": st4_ms * 1e3,
             "k2_tflops": tf4,
             "k2_frac_of_bf16x4": tf4 / (4 * peaks["bf16"]),
             "k2_frac_of_bf16x6": tf4 / (6 * peaks["bf16"]),

@@ -504,6 +504,37 @@ int mh3_nvfp4_qkv(mh3_preattn_t handle, void* stream, int64_t M, const uint8_t* 
                   const mh3_bf16* rope_cos_sin, int P, float eps, const float* qkv_descale,
                   void* out);
 
+/* The NVFP4 stage with NVFP4 outputs (out_mode "nvfp4" of the page
+ * "flashinfer.diffusion_ops.minimax_h3_nvfp4_pre_attention", Parameters:
+ * out_mode, q_sf/k_sf/v_sf, q/k/v_global_scale).  The shapes are defined on
+ * the FP8 stage's page, which is not available; this library's reading:
+ * each output row of 128 values (one token, head and kind, after the Q/K
+ * norm and RoPE, rounded to bf16 as in the bf16 output) is quantised in the
+ * block-16 convention above with the global scale of its kind, and written
+ * in the bf16 output's destination-major order:
+ *   out_codes  DEVICE [P, M, 56/P, 3, 64] bytes (E2M1 codes, element 2j in
+ *              the low nibble of byte j), 16-byte aligned,
+ *              mh3_preattn_out_nvfp4_bytes(M, 0) bytes
+ *   out_sf     DEVICE [P, M, 56/P, 3, 8] UE4M3 scales (block b covers
+ *              elements 16b..16b+15), 8-byte aligned,
+ *              mh3_preattn_out_nvfp4_bytes(M, 1) bytes
+ *   qkv_global_scale  DEVICE float [3]: the q, k and v global scales
+ * Other arguments and rules as in mh3_nvfp4_preattn_run (no qkv_descale,
+ * no bf16 out). */
+int mh3_nvfp4_preattn_run_nvfp4_out(
+    mh3_preattn_t handle, void* stream, int64_t M, const mh3_bf16* x,
+    const mh3_bf16* x_norm_weight, const mh3_bf16* adaln_scale, int64_t scale_row_stride,
+    const mh3_bf16* adaln_shift, int64_t shift_row_stride, int64_t rows,
+    const int32_t* adaln_index, const uint8_t* weight_q, const uint8_t* weight_sf,
+    float weight_global_scale, const float* act_global_scale, float alpha,
+    const mh3_bf16* q_norm_weight, const mh3_bf16* k_norm_weight, const mh3_bf16* rope_cos_sin,
+    int P, float eps, const float* qkv_global_scale, uint8_t* act_q, uint8_t* act_sf,
+    uint8_t* out_codes, uint8_t* out_sf);
+
+/* Bytes of the NVFP4 outputs for M tokens: which = 0 the codes
+ * (M * 10752), 1 the scales (M * 1344); 0 for M <= 0 or another `which`. */
+size_t mh3_preattn_out_nvfp4_bytes(int64_t M, int which);
+
 /* ---------------------------------------------------------------------------
  * The W4A4 attention output projection with the fused gated residual (page
  * "flashinfer.diffusion_ops.minimax_h3_nvfp4_out_proj", summary and

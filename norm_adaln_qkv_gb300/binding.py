@@ -39,7 +39,8 @@ EXPORTS = ("mh3_preattn_create", "mh3_preattn_destroy", "mh3_preattn_workspace_b
            "mh3_nvfp4_quantize", "mh3_nvfp4_norm_quant", "mh3_nvfp4_preattn_run", "mh3_nvfp4_qkv",
            "mh3_preattn_set_test_stall", "mh3_mlp_fp8_run", "mh3_mlp_fp8_validate",
            "mh3_mlp_fp8_workspace_bytes", "mh3_nvfp4_out_proj_run",
-           "mh3_nvfp4_out_proj_validate")
+           "mh3_nvfp4_out_proj_validate", "mh3_nvfp4_preattn_run_nvfp4_out",
+           "mh3_preattn_out_nvfp4_bytes")
 
 _vp = ctypes.c_void_p
 _i64 = ctypes.c_int64
@@ -91,6 +92,10 @@ _SIGS = {
     "mh3_mlp_fp8_workspace_bytes": (ctypes.c_size_t, [_i64, _i32]),
     "mh3_nvfp4_out_proj_run": (_i32, [_vp, _vp, _i64, _vp, _vp, _vp, _f32, _vp, _vp, _i64, _i64,
                                       _vp, _vp, _vp, _vp, _vp]),
+    "mh3_nvfp4_preattn_run_nvfp4_out": (_i32, [_vp, _vp, _i64, _vp, _vp, _vp, _i64, _vp, _i64,
+                                               _i64, _vp, _vp, _vp, _f32, _vp, _f32, _vp, _vp,
+                                               _vp, _i32, _f32, _vp, _vp, _vp, _vp, _vp]),
+    "mh3_preattn_out_nvfp4_bytes": (ctypes.c_size_t, [_i64, _i32]),
     "mh3_nvfp4_out_proj_validate": (_i32, [_i64, _vp, _vp, _vp, _f32, _vp, _vp, _i64, _i64, _vp,
                                            _vp, _vp]),
 }
@@ -183,7 +188,8 @@ class Handle:
         _check(load().mh3_preattn_set_test_stall(self._h, 1 if stall else 0),
                "mh3_preattn_set_test_stall", "mh3_mlp_fp8_run", "mh3_mlp_fp8_validate",
            "mh3_mlp_fp8_workspace_bytes", "mh3_nvfp4_out_proj_run",
-           "mh3_nvfp4_out_proj_validate")
+           "mh3_nvfp4_out_proj_validate", "mh3_nvfp4_preattn_run_nvfp4_out",
+           "mh3_preattn_out_nvfp4_bytes")
 
 
 _handles = {}
@@ -444,6 +450,21 @@ def mh3_nvfp4_preattn_run(handle: Handle, stream, M, x, x_norm_weight, adaln_sca
         float("nan") if alpha is None else float(alpha), _ptr(q_norm_weight),
         _ptr(k_norm_weight), _ptr(rope_cos_sin), P, float(eps), _ptr(qkv_descale), _ptr(act_q),
         _ptr(act_sf), _ptr(out)), "mh3_nvfp4_preattn_run")
+
+
+def mh3_nvfp4_preattn_run_nvfp4_out(handle: Handle, stream, M, x, x_norm_weight, adaln_scale,
+                                    scale_row_stride, adaln_shift, shift_row_stride, rows,
+                                    adaln_index, weight_q, weight_sf, weight_global_scale,
+                                    act_global_scale, alpha, q_norm_weight, k_norm_weight,
+                                    rope_cos_sin, P, eps, qkv_global_scale, act_q, act_sf,
+                                    out_codes, out_sf) -> None:
+    _check(load().mh3_nvfp4_preattn_run_nvfp4_out(
+        handle.ptr, _stream_ptr(stream), M, _ptr(x), _ptr(x_norm_weight), _ptr(adaln_scale),
+        scale_row_stride, _ptr(adaln_shift), shift_row_stride, rows, _ptr(adaln_index),
+        _ptr(weight_q), _ptr(weight_sf), float(weight_global_scale), _ptr(act_global_scale),
+        float("nan") if alpha is None else float(alpha), _ptr(q_norm_weight), _ptr(k_norm_weight),
+        _ptr(rope_cos_sin), P, float(eps), _ptr(qkv_global_scale), _ptr(act_q), _ptr(act_sf),
+        _ptr(out_codes), _ptr(out_sf)), "mh3_nvfp4_preattn_run_nvfp4_out")
 
 
 def mh3_nvfp4_qkv(handle: Handle, stream, M, act_q, act_sf, weight_q, weight_sf,

@@ -77,6 +77,11 @@ struct QkvParams {
   const float* act_gs = nullptr;  // device [1]
   float w_gs = 0.0f;
   int test_stall = 0;  // test hook: the producer issues no loads (bounded waits run out)
+  // NVFP4 output mode of the NVFP4 stage: q, k, v global scales (device [3]),
+  // codes [P, M, 56/P, 3, 64] and block scales [P, M, 56/P, 3, 8]
+  const float* out_gs = nullptr;
+  uint8_t* out_codes = nullptr;
+  uint8_t* out_sf = nullptr;
 };
 
 // num_sms: SM count of the device (the kernel is persistent over rows).
@@ -99,8 +104,13 @@ struct Nvfp4Maps {
   CUtensorMap out;  // as QkvMaps::out (bf16) or the e4m3 byte map; out-projection: [M, 5376]
   CUtensorMap aux;  // out-projection: residual [M, 5376], box 64 x 32
 };
-cudaError_t nvfp4_qkv_prepare_device(int* max_clusters, int* max_clusters_e4m3);
-cudaError_t launch_nvfp4_qkv(const Nvfp4Maps& maps, const QkvParams& p, int clusters, bool e4m3,
+// Output forms of the NVFP4 stage's GEMM.
+constexpr int kOutBf16 = 0;
+constexpr int kOutE4m3 = 1;
+constexpr int kOutNvfp4 = 2;
+cudaError_t nvfp4_qkv_prepare_device(int* max_clusters, int* max_clusters_e4m3,
+                                     int* max_clusters_nvfp4);
+cudaError_t launch_nvfp4_qkv(const Nvfp4Maps& maps, const QkvParams& p, int clusters, int out_mode,
                              cudaStream_t stream);
 
 // W4A4 output projection with the gated residual (the same block-scaled GEMM):

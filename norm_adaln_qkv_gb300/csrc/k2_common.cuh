@@ -22,6 +22,7 @@
 
 #include "common.cuh"
 #include "e4m3.cuh"
+#include "nvfp4.cuh"
 #include "ptx.cuh"
 
 namespace mh3 {
@@ -318,15 +319,46 @@ __device__ __forceinline__ void epilogue_head(uint32_t tcol, int lane, uint32_t 
   }
 }
 
+// NVFP4 output mode: this thread's staged bf16 row (128 values of one head,
+// token m) as 8 blocks of 16 -> 64 bytes of E2M1 codes and 8 UE4M3 scales
+// (nvfp4.cuh, one rounding of each exact quotient), stored straight to
+// global memory (row m < M only).
+__device__ __forceinline__ void stage_row_to_nvfp4(uint32_t stg, int lane, const fp4::Table16& q,
+                                                   uint8_t* codes, uint8_t* sf, bool store) {
+  uint32_t cw[16];
+  uint32_t sw[2] = {0u, 0u};
+#pragma unroll
+  for (int b = 0; b < 8; ++b) {
+    const uint4 w0 = ld_shared_v4(stg_addr(stg, lane, 2 * b));
+    const uint4 w1 = ld_shared_v4(stg_addr(stg, lane, 2 * b + 1));
+    const float amax = fmaxf(fp4::amax8(w0), fp4::amax8(w1));
+    const fp4::BlockScale bs = fp4::block_scale_t16(amax, q);
+    cw[2 * b] = fp4::encode8(w0, bs, q.gs);
+    cw[2 * b + 1] = fp4::encode8(w1, bs, q.gs);
+    sw[b >> 2] |= bs.code << (8 * (b & 3));
+  }
+  if (store) {
+    uint4* c4 = reinterpret_cast<uint4*>(codes);
+#pragma unroll
+    for (int i = 0; i < 4; ++i)
+      __stcs(c4 + i, make_uint4(cw[4 * i], cw[4 * i + 1], cw[4 * i + 2], cw[4 * i + 3]));
+    __stcs(reinterpret_cast<uint2*>(sf), make_uint2(sw[0], sw[1]));
+  }
+}
+
 // The epilogue of one head whose bf16 projection y is already in registers
 // (y[i] holds columns 2i (low half) and 2i + 1): the same operations, in the
-// same order, as epilogue_head on an accumulator in TMEM.
-template <bool kE4m3>
+// same order, as epilogue_head on an accumulator in TMEM.  kOut: kOutBf16,
+// kOutE4m3 (codes through the staging buffer and TMA) or kOutNvfp4 (codes
+// and scales stored from registers; fq: the q, k, v quantiser tables).
+template <int kOut>
 __device__ __forceinline__ void epilogue_head_regs(const uint32_t (&y)[64], int lane, uint32_t stg,
                                                    const float* nw_all, const QkvParams& p,
                                                    int64_t m0, int kind, int head,
                                                    const uint4* cs_row,
-                                                   const CUtensorMap* tm_out) {
+                                                   const CUtensorMap* tm_out,
+                                                   const fp4::Table16* fq = nullptr) {
+  constexpr bool kE4m3 = kOut == kOutE4m3;
   if (lane == 0) bulk_wait_group_read0();
   __syncwarp();
   if (kind == 2) {
@@ -391,6 +423,16 @@ __device__ __forceinline__ void epilogue_head_regs(const uint32_t (&y)[64], int 
       }
       st_shared_v4(stg_addr(stg, lane, c), make_uint4(o[0], o[1], o[2], o[3]));
     }
+  }
+  if (kOut == kOutNvfp4) {
+    // each thread reads back only its own staged row
+    const int64_t m = m0 + lane;
+    const int dst = head / p.heads_per_dst;
+    const int slot = (head % p.heads_per_dst) * 3 + kind;
+    const int64_t r = (static_cast<int64_t>(dst) * p.M + m) * (3 * p.heads_per_dst) + slot;
+    stage_row_to_nvfp4(stg, lane, fq[kind], p.out_codes + r * 64, p.out_sf + r * 8, m < p.M);
+    __syncwarp();  // the staging buffer is free again for the next head
+    return;
   }
   if (kE4m3) stage_to_e4m3(stg, lane, __ldg(p.descales + kind));
   fence_proxy_async_smem();

@@ -101,8 +101,11 @@ constexpr int kFOffBar = kFOffStg + kEpiWarps * kStgWarpBytes;
 constexpr int kFNumBars = 4 * kFStages + 4 + kEpiWarps;
 constexpr int kFOffTmemPtr = kFOffBar + kFNumBars * 8;
 constexpr int kFOffAbort = kFOffTmemPtr + 4;
-constexpr int kFOffScratch = kFOffBar + 256;
-constexpr int kFSmemUsed = kFOffScratch + 1024;
+constexpr int kFOffScratch = kFOffBar + 256;  // norm weights (1 KB), NVFP4 output tables
+constexpr int kFScratchTables = 256;           // float offset of the q, k, v Table16s
+constexpr int kFSmemUsed = kFOffScratch + 1536;
+static_assert(kFScratchTables * 4 + 3 * static_cast<int>(sizeof(fp4::Table16)) <= 1536,
+              "scratch overflow");
 constexpr int kFSmemAlloc = kFSmemUsed + 1024;
 static_assert(kFOffAbort + 4 <= kFOffScratch, "barrier block overflow");
 static_assert(kFSmemAlloc <= 232448, "exceeds the 227 KB per-CTA limit");
@@ -185,8 +188,9 @@ struct FEpiCtx {
 //   Params (with M, num_m_tiles, num_tiles, status, test_stall, alpha, act_gs,
 //   w_gs), kKBlocks (K / 256), kNTiles (N / 256), prologue(), tile().
 
-// The pre-attention QKV projection: Q/K RMSNorm, RoPE and pack per head.
-template <bool kE4m3>
+// The pre-attention QKV projection: Q/K RMSNorm, RoPE and pack per head,
+// written as bf16, e4m3 or NVFP4 (kOut).
+template <int kOut>
 struct QkvFp4Epi {
   using Params = QkvParams;
   static constexpr int kKBlocks = kHidden / 256;      // 21
@@ -196,6 +200,10 @@ struct QkvFp4Epi {
     for (int i = tid; i < 2 * kHeadDim; i += kFThreads) {
       const __nv_bfloat16 w = i < kHeadDim ? p.q_norm_weight[i] : p.k_norm_weight[i - kHeadDim];
       scratch[i] = __bfloat162float(w);
+    }
+    if (kOut == kOutNvfp4 && tid < 96) {  // warp k fills the table of q, k or v
+      fp4::Table16* t = reinterpret_cast<fp4::Table16*>(scratch + kFScratchTables);
+      fp4::init_table16(t + (tid >> 5), __ldg(p.out_gs + (tid >> 5)), tid & 31);
     }
   }
   __device__ static __forceinline__ void tile(const uint32_t (&y)[128], const FEpiCtx& c,
@@ -210,8 +218,9 @@ struct QkvFp4Epi {
       uint32_t yh[64];
 #pragma unroll
       for (int i = 0; i < 64; ++i) yh[i] = y[64 * j + i];
-      epilogue_head_regs<kE4m3>(yh, c.lane, c.stg, c.scratch, p, m0, kind, head0 + j, cs_row,
-                                c.tm_out);
+      epilogue_head_regs<kOut>(yh, c.lane, c.stg, c.scratch, p, m0, kind, head0 + j, cs_row,
+                               c.tm_out,
+                               reinterpret_cast<const fp4::Table16*>(c.scratch + kFScratchTables));
     }
   }
 };
@@ -560,19 +569,24 @@ cudaError_t launch_one(const Nvfp4Maps& m, const typename Epi::Params& p, int cl
 
 }  // namespace
 
-cudaError_t nvfp4_qkv_prepare_device(int* max_clusters, int* max_clusters_e4m3) {
-  cudaError_t e = prepare_one<QkvFp4Epi<false>>(max_clusters);
-  if (e != cudaSuccess) return e;
-  return prepare_one<QkvFp4Epi<true>>(max_clusters_e4m3);
+cudaError_t nvfp4_qkv_prepare_device(int* max_clusters, int* max_clusters_e4m3,
+                                     int* max_clusters_nvfp4) {
+  cudaError_t e = prepare_one<QkvFp4Epi<kOutBf16>>(max_clusters);
+  if (e == cudaSuccess) e = prepare_one<QkvFp4Epi<kOutE4m3>>(max_clusters_e4m3);
+  if (e == cudaSuccess) e = prepare_one<QkvFp4Epi<kOutNvfp4>>(max_clusters_nvfp4);
+  return e;
 }
 
-cudaError_t launch_nvfp4_qkv(const Nvfp4Maps& maps, const QkvParams& p, int clusters, bool e4m3,
+cudaError_t launch_nvfp4_qkv(const Nvfp4Maps& maps, const QkvParams& p, int clusters, int out_mode,
                              cudaStream_t stream) {
   if (p.M <= 0) return cudaSuccess;
   Nvfp4Maps m = maps;
   m.aux = maps.out;
-  return e4m3 ? launch_one<QkvFp4Epi<true>>(m, p, clusters, stream)
-              : launch_one<QkvFp4Epi<false>>(m, p, clusters, stream);
+  switch (out_mode) {
+    case kOutE4m3: return launch_one<QkvFp4Epi<kOutE4m3>>(m, p, clusters, stream);
+    case kOutNvfp4: return launch_one<QkvFp4Epi<kOutNvfp4>>(m, p, clusters, stream);
+    default: return launch_one<QkvFp4Epi<kOutBf16>>(m, p, clusters, stream);
+  }
 }
 
 cudaError_t nvfp4_out_proj_prepare_device(int* max_clusters) {

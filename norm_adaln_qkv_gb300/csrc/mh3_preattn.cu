@@ -44,6 +44,7 @@ struct mh3_preattn_ctx {
   size_t ws_bytes = 0;
   int nvfp4_clusters = 0;       // resident clusters of the NVFP4 GEMM (bf16 out)
   int nvfp4_e4m3_clusters = 0;  // ... and its e4m3-output form
+  int nvfp4_fp4out_clusters = 0;  // ... and its NVFP4-output form
   int nvfp4_out_clusters = 0;   // ... and the W4A4 output projection
   void* act_q = nullptr;        // handle-owned NVFP4 stage-1 workspaces
   size_t act_q_bytes = 0;
@@ -373,8 +374,8 @@ int mh3_preattn_create(mh3_preattn_t* handle, int device) {
   e = mlp_fc1_prepare_device(&fc1_clusters);
   if (e == cudaSuccess) e = mlp_fc2_prepare_device(&fc2_clusters);
   if (e != cudaSuccess) return cuda_fail(e, "preparing the MLP GEMMs");
-  int nvfp4_clusters = 0, nvfp4_e4m3_clusters = 0;
-  e = nvfp4_qkv_prepare_device(&nvfp4_clusters, &nvfp4_e4m3_clusters);
+  int nvfp4_clusters = 0, nvfp4_e4m3_clusters = 0, nvfp4_fp4out_clusters = 0;
+  e = nvfp4_qkv_prepare_device(&nvfp4_clusters, &nvfp4_e4m3_clusters, &nvfp4_fp4out_clusters);
   if (e != cudaSuccess) return cuda_fail(e, "preparing the NVFP4 GEMM");
   int nvfp4_out_clusters = 0;
   e = nvfp4_out_proj_prepare_device(&nvfp4_out_clusters);
@@ -388,6 +389,7 @@ int mh3_preattn_create(mh3_preattn_t* handle, int device) {
   h->nvfp4_clusters = nvfp4_clusters;
   h->nvfp4_e4m3_clusters = nvfp4_e4m3_clusters;
   h->nvfp4_out_clusters = nvfp4_out_clusters;
+  h->nvfp4_fp4out_clusters = nvfp4_fp4out_clusters;
   h->fc1_clusters = fc1_clusters;
   h->e4m3_clusters = e4m3_clusters;
   h->fc2_clusters = fc2_clusters;
@@ -741,9 +743,14 @@ int launch_fp4_gemm(mh3_preattn_ctx* h, cudaStream_t s, int64_t M, const uint8_t
                     float weight_global_scale, const float* act_global_scale, float alpha,
                     bool alpha_given, const mh3_bf16* q_norm_weight, const mh3_bf16* k_norm_weight,
                     const mh3_bf16* rope_cos_sin, int P, float eps, const float* qkv_descale,
-                    void* out) {
-  const bool e4m3 = qkv_descale != nullptr;
-  const int max_clusters = e4m3 ? h->nvfp4_e4m3_clusters : h->nvfp4_clusters;
+                    void* out, const float* out_gs = nullptr, uint8_t* out_sf = nullptr) {
+  // NVFP4 outputs when out_gs is given (out: the codes), else e4m3 when
+  // qkv_descale is, else bf16
+  const int mode = out_gs != nullptr ? kOutNvfp4 : (qkv_descale != nullptr ? kOutE4m3 : kOutBf16);
+  const bool e4m3 = mode == kOutE4m3;
+  const int max_clusters = mode == kOutNvfp4 ? h->nvfp4_fp4out_clusters
+                           : e4m3            ? h->nvfp4_e4m3_clusters
+                                             : h->nvfp4_clusters;
   if (max_clusters <= 0)
     return fail(MH3_ERR_UNSUPPORTED, "no 2-CTA cluster of the NVFP4 GEMM fits this device");
   int rc;
@@ -779,8 +786,25 @@ int launch_fp4_gemm(mh3_preattn_ctx* h, cudaStream_t s, int64_t M, const uint8_t
                            strides, box_b, CU_TENSOR_MAP_SWIZZLE_NONE, "qkv_weight_sf")))
       return rc;
   }
-  if ((rc = encode_out_map(&maps.out, out, M, P, e4m3))) return rc;
+  if (mode == kOutNvfp4) {
+    // the codes as a 4-D byte map (d 64, slot, m, dst); the NVFP4 form
+    // stores from registers and never issues a TMA store through it
+    const int64_t slots = 3 * (kHeads / P);
+    const cuuint64_t dims[4] = {64, static_cast<cuuint64_t>(slots), static_cast<cuuint64_t>(M),
+                                static_cast<cuuint64_t>(P)};
+    const cuuint64_t strides[3] = {64, static_cast<cuuint64_t>(slots) * 64,
+                                   static_cast<cuuint64_t>(M) * slots * 64};
+    const cuuint32_t box[4] = {64, 1, 32, 1};
+    if ((rc = encode_tiled(&maps.out, CU_TENSOR_MAP_DATA_TYPE_UINT8, 4, out, dims, strides, box,
+                           CU_TENSOR_MAP_SWIZZLE_NONE, "out_codes")))
+      return rc;
+  } else if ((rc = encode_out_map(&maps.out, out, M, P, e4m3))) {
+    return rc;
+  }
   QkvParams p;
+  p.out_gs = out_gs;
+  p.out_codes = mode == kOutNvfp4 ? static_cast<uint8_t*>(out) : nullptr;
+  p.out_sf = out_sf;
   p.positions = nullptr;  // one cos/sin row per token
   p.cos_sin = reinterpret_cast<const __nv_bfloat16*>(rope_cos_sin);
   p.q_norm_weight = reinterpret_cast<const __nv_bfloat16*>(q_norm_weight);
@@ -799,7 +823,7 @@ int launch_fp4_gemm(mh3_preattn_ctx* h, cudaStream_t s, int64_t M, const uint8_t
   p.test_stall = h->test_stall_next;  // test hook: consumed by this launch
   h->test_stall_next = 0;
   const int clusters = p.num_tiles < max_clusters ? p.num_tiles : max_clusters;
-  cudaError_t e = launch_nvfp4_qkv(maps, p, clusters, e4m3, s);
+  cudaError_t e = launch_nvfp4_qkv(maps, p, clusters, mode, s);
   if (e != cudaSuccess) return cuda_fail(e, "NVFP4 GEMM launch");
   return MH3_OK;
 }
@@ -902,6 +926,57 @@ extern "C" int mh3_nvfp4_preattn_run(
   return launch_fp4_gemm(h, s, M, act_q, act_sf, weight_q, weight_sf, weight_global_scale,
                          act_global_scale, alpha, alpha_given, q_norm_weight, k_norm_weight,
                          rope_cos_sin, P, eps, qkv_descale, out);
+}
+
+extern "C" size_t mh3_preattn_out_nvfp4_bytes(int64_t M, int which) {
+  if (M <= 0) return 0;
+  const size_t rows = static_cast<size_t>(M) * kHeads * 3;  // (token, head, kind) rows of 128
+  if (which == 0) return rows * (kHeadDim / 2);
+  if (which == 1) return rows * (kHeadDim / 16);
+  return 0;
+}
+
+extern "C" int mh3_nvfp4_preattn_run_nvfp4_out(
+    mh3_preattn_t h, void* stream, int64_t M, const mh3_bf16* x, const mh3_bf16* x_norm_weight,
+    const mh3_bf16* adaln_scale, int64_t scale_row_stride, const mh3_bf16* adaln_shift,
+    int64_t shift_row_stride, int64_t rows, const int32_t* adaln_index, const uint8_t* weight_q,
+    const uint8_t* weight_sf, float weight_global_scale, const float* act_global_scale,
+    float alpha, const mh3_bf16* q_norm_weight, const mh3_bf16* k_norm_weight,
+    const mh3_bf16* rope_cos_sin, int P, float eps, const float* qkv_global_scale,
+    uint8_t* act_q, uint8_t* act_sf, uint8_t* out_codes, uint8_t* out_sf) {
+  int rc = check_handle(h);
+  if (rc) return rc;
+  rc = check_fp4_stage1(M, x, x_norm_weight, adaln_scale, scale_row_stride, adaln_shift,
+                        shift_row_stride, rows, adaln_index, eps, act_global_scale);
+  if (rc) return rc;
+  bool alpha_given = false;
+  if ((rc = check_fp4_gemm_fixed(P, alpha, weight_global_scale, weight_q, weight_sf, q_norm_weight,
+                                 k_norm_weight, &alpha_given)))
+    return rc;
+  if (M == 0) return MH3_OK;
+  if ((rc = check_fp4_gemm_rows(rope_cos_sin, out_codes, nullptr))) return rc;
+  if ((rc = check_ptr(qkv_global_scale, "qkv_global_scale", 4))) return rc;
+  if ((rc = check_ptr(out_sf, "out_sf", 8))) return rc;
+  if (act_q != nullptr && (rc = check_ptr(act_q, "act_q", 16))) return rc;
+  if (act_sf != nullptr && (rc = check_ptr(act_sf, "act_sf", 16))) return rc;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  if (act_q == nullptr) {
+    if ((rc = grow_buffer(&h->act_q, &h->act_q_bytes, mh3_nvfp4_codes_bytes(M, kHidden), s)))
+      return rc;
+    act_q = static_cast<uint8_t*>(h->act_q);
+  }
+  if (act_sf == nullptr) {
+    if ((rc = grow_buffer(&h->act_sf, &h->act_sf_bytes, mh3_nvfp4_scales_bytes(M, kHidden, 1), s)))
+      return rc;
+    act_sf = static_cast<uint8_t*>(h->act_sf);
+  }
+  rc = launch_fp4_stage1(s, h->num_sms, h->d_status, M, x, x_norm_weight, adaln_scale,
+                         scale_row_stride, adaln_shift, shift_row_stride, rows, adaln_index, eps,
+                         act_global_scale, act_q, act_sf, true);
+  if (rc) return rc;
+  return launch_fp4_gemm(h, s, M, act_q, act_sf, weight_q, weight_sf, weight_global_scale,
+                         act_global_scale, alpha, alpha_given, q_norm_weight, k_norm_weight,
+                         rope_cos_sin, P, eps, nullptr, out_codes, qkv_global_scale, out_sf);
 }
 
 extern "C" int mh3_nvfp4_qkv(mh3_preattn_t h, void* stream, int64_t M, const uint8_t* act_q,

@@ -129,6 +129,54 @@ __device__ __forceinline__ BlockScale block_scale(float amax, const Quantiser& q
   return b;
 }
 
+// The same multipliers from a 16-entry table per global scale, for kernels
+// without room for kEncLut entries: a UE4M3 code with exponent field e and
+// mantissa j has the value n 2^(E - 10), n = 8 + j and E = e for e >= 1, and
+// n = j, E = 1 for e = 0.  So gs / sf = (gs / n) 2^(10 - E): the table holds
+// (RD(RD(gs / n)(1 - 2^-23)), RU(RU(gs / n)(1 + 2^-23))) for n = 1..15, and
+// the power of two is applied with a product rounded the same way, which
+// keeps each multiplier on its side of (gs / sf)(1 -+ 2^-23).
+struct Table16 {
+  float gs, c_lo, c_hi, pad;
+  float2 t[16];
+};
+// Fill with threads tid = 0..16 of the block (others return), then synchronise.
+__device__ __forceinline__ void init_table16(Table16* q, float gs, int tid) {
+  if (tid == 16) {
+    q->gs = gs;
+    q->c_lo = __fdiv_rd(gs, 6.0f);
+    q->c_hi = __fdiv_ru(gs, 6.0f);
+    q->pad = 0.0f;
+  } else if (tid < 16) {
+    float2 e = make_float2(0.0f, 0.0f);
+    if (tid > 0) {
+      const float n = static_cast<float>(tid);
+      e.x = __fmul_rd(__fdiv_rd(gs, n), 0x1.fffffep-1f);
+      e.y = __fmul_ru(__fdiv_ru(gs, n), 0x1.000002p+0f);
+    }
+    q->t[tid] = e;
+  }
+}
+
+__device__ __forceinline__ BlockScale block_scale_t16(float amax, const Table16& q) {
+  const float t_lo = __fmul_rd(amax, q.c_lo);
+  const float t_hi = __fmul_ru(amax, q.c_hi);
+  const uint32_t both = e4m3x2_satfinite(t_lo, t_hi);
+  uint32_t code = both & 0xFFu;
+  if (code != (both >> 8)) code = scale_code_at_boundary(amax, q.gs, code, both >> 8);
+  BlockScale b;
+  b.code = code;
+  b.sf = ue4m3_value(code);
+  const uint32_t e = code >> 3, j = code & 7u;
+  const uint32_t n = e ? 8u + j : j;
+  const uint32_t E = e ? e : 1u;
+  const float pw = __uint_as_float((137u - E) << 23);  // 2^(10 - E), exact
+  const float2 t = q.t[n];
+  b.enc_lo = __fmul_rd(t.x, pw);
+  b.enc_hi = __fmul_ru(t.y, pw);
+  return b;
+}
+
 // Eight FP32 values -> eight E2M1 codes in one word (element 0 in bits 0-3).
 __device__ __forceinline__ uint32_t e2m1x8(const float (&v)[8]) {
   uint32_t r;

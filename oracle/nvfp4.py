@@ -201,3 +201,19 @@ def out_proj_nvfp4(attn_out, o_weight_q, o_weight_sf, o_weight_global_scale: flo
     o = nvfp4_projection(act_q, act_sf, o_weight_q, o_weight_sf, al)
     out = gated_residual(o, gate, gate_index, residual)
     return dict(act_q=act_q, act_sf=act_sf, alpha=al, o=o, out=out)
+
+
+def quantize_outputs(qkv: torch.Tensor, global_scales: Sequence[float]):
+    """NVFP4 outputs of the stage (minimax_h3_nvfp4_pre_attention,
+    Parameters: out_mode "nvfp4", q/k/v_global_scale): every row of 128
+    values (token t, head h, kind k) of the bf16 output qkv [T, H, 3, 128] is
+    quantised with fp4_quantize and the global scale of its kind.  Returns
+    codes uint8 [T, H, 3, 64] and scales uint8 [T, H, 3, 8]."""
+    T, H, K3, D = qkv.shape
+    codes = torch.empty((T, H, K3, D // 2), dtype=torch.uint8)
+    scales = torch.empty((T, H, K3, D // BLOCK), dtype=torch.uint8)
+    for kind in range(K3):
+        c, s = fp4_quantize(qkv[:, :, kind, :].reshape(T * H, D), global_scales[kind])
+        codes[:, :, kind] = c.view(T, H, D // 2)
+        scales[:, :, kind] = s.view(T, H, D // BLOCK)
+    return codes, scales

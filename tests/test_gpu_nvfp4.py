@@ -239,6 +239,45 @@ def test_e4m3_output_and_alpha(handle, weight):
     assert torch.equal(codes.cpu(), e4m3.quantize_packed(out.cpu(), ds))
 
 
+# out_mode "nvfp4": q, k, v with their own global scales (calibration amax
+# 8, 6 and 10: 448 * 6 / amax)
+OUT_GS = (448.0 * 6 / 8, 448.0 * 6 / 6, 448.0 * 6 / 10)
+
+
+def run_stage_nvfp4_out(h, w, d, weight, codes, sf, gs_dev, P):
+    binding.mh3_nvfp4_preattn_run_nvfp4_out(
+        h, None, w.M, d["x"], d["xw"], d["sc"], d["sc"].stride(0), d["sh"], d["sh"].stride(0),
+        d["sc"].shape[0], d["idx32"], weight["q_dev"], weight["sf_dev"], weight["gs"], d["gs"],
+        None, d["qw"], d["kw"], d["cs"], P, w.eps, gs_dev, None, None, codes, sf)
+
+
+@pytest.mark.parametrize("key,M,P", [("c2", 300, 2), ("c2", 257, 8), ("c0", None, 1)])
+def test_nvfp4_outputs_quantise_the_bf16_outputs(handle, weight, key, M, P):
+    """Every code and scale of the NVFP4 output form equals the oracle's
+    quantisation of the same call's bf16 outputs (guarded tokens included:
+    their rows are zero, so are their codes and scales)."""
+    w = make_nvfp4_workload(key, M)
+    d = _dev(w)
+    M = w.M
+    out = torch.empty((P, M, 56 // P, 3, 128), dtype=BF16, device="cuda")
+    run_stage(handle, w, d, weight, out, P=P)
+    lib = binding.load()
+    codes = torch.full((lib.mh3_preattn_out_nvfp4_bytes(M, 0),), 0xEE, dtype=torch.uint8,
+                       device="cuda")
+    sf = torch.full((lib.mh3_preattn_out_nvfp4_bytes(M, 1),), 0xEE, dtype=torch.uint8,
+                    device="cuda")
+    run_stage_nvfp4_out(handle, w, d, weight, codes, sf,
+                        torch.tensor(OUT_GS, dtype=torch.float32, device="cuda"), P)
+    torch.cuda.synchronize()
+    assert handle.device_status() == 0
+    toks = range(M)
+    got_c = oracle.ulysses_unpack_rows(codes.cpu().view(P, M, 56 // P, 3, 64), toks)
+    got_s = oracle.ulysses_unpack_rows(sf.cpu().view(P, M, 56 // P, 3, 8), toks)
+    ref_c, ref_s = f.quantize_outputs(oracle.ulysses_unpack_rows(out.cpu(), toks), OUT_GS)
+    assert torch.equal(got_s, ref_s), int((got_s != ref_s).sum())
+    assert torch.equal(got_c, ref_c), int((got_c != ref_c).sum())
+
+
 def test_invalid_arguments(handle, weight):
     w = make_nvfp4_workload("c2", 8)
     d = _dev(w)

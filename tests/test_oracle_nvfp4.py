@@ -342,3 +342,26 @@ def test_out_proj_nvfp4_token_subset_is_row_subset():
     sub = f.out_proj_nvfp4(a, wq, wsf, 448.0 * 6 / 0.75, 336.0, gate, gi, res, tokens=[8, 3, 4])
     assert torch.equal(sub["out"].view(torch.int16), full["out"][[8, 3, 4]].view(torch.int16))
     assert torch.equal(sub["act_q"], full["act_q"][[8, 3, 4]])
+
+
+def test_output_quantisation_is_lossless_per_kind():
+    """Rows built to be exact in NVFP4 under their own kind's global scale
+    (three different scales) dequantise back bit for bit; a kind read with
+    another kind's scale, or a row landing in another (token, head, kind)
+    slot, would not."""
+    g = torch.Generator().manual_seed(31)
+    T, H = 3, 5
+    gss = (4.0, 0.25, 64.0)
+    qkv = torch.empty(T, H, 3, 128, dtype=BF16)
+    for kind, gs in enumerate(gss):
+        c = torch.randint(0, 16, (T * H, 128), generator=g, dtype=torch.uint8)
+        c[:, ::16] = 7
+        p = torch.exp2(torch.randint(-3, 3, (T * H, 8), generator=g).double()).repeat_interleave(16, 1)
+        qkv[:, :, kind] = (f.e2m1_values(c) * p / gs).to(BF16).view(T, H, 128)
+    codes, sf = f.quantize_outputs(qkv, gss)
+    assert codes.shape == (T, H, 3, 64) and sf.shape == (T, H, 3, 8)
+    for kind, gs in enumerate(gss):
+        deq = f.dequantize(codes[:, :, kind].reshape(T * H, 64), sf[:, :, kind].reshape(T * H, 8), gs)
+        assert torch.equal(deq, qkv[:, :, kind].reshape(T * H, 128).double()), kind
+    # the three kinds' scales differ by the ratio of their global scales
+    assert not torch.equal(sf[:, :, 0], sf[:, :, 1])
