@@ -186,10 +186,7 @@ class Handle:
         """Test hook: the next CTA-pair QKV GEMM launch issues no loads, so its
         bounded waits run out and it reports a status code."""
         _check(load().mh3_preattn_set_test_stall(self._h, 1 if stall else 0),
-               "mh3_preattn_set_test_stall", "mh3_mlp_fp8_run", "mh3_mlp_fp8_validate",
-           "mh3_mlp_fp8_workspace_bytes", "mh3_nvfp4_out_proj_run",
-           "mh3_nvfp4_out_proj_validate", "mh3_nvfp4_preattn_run_nvfp4_out",
-           "mh3_preattn_out_nvfp4_bytes")
+               "mh3_preattn_set_test_stall")
 
 
 _handles = {}

@@ -93,19 +93,16 @@ __device__ __forceinline__ uint32_t adaln_pair(uint64_t x2, uint32_t w, uint32_t
   return pack_bf16x2(fma_bf16_lo(n, g, bf16_lo(sh)), fma_bf16_hi(n, g, bf16_hi(sh)));
 }
 
-// NVFP4 outputs of one 8-element chunk c of row m (a in `o`): the block of
-// 16 is this thread's chunk and its neighbour's (lanes 2b, 2b+1); the even
-// lane stores the block's scale byte.
-__device__ __forceinline__ void fp4_chunk(const uint4& o, int lane, int c, int64_t m,
-                                          const fp4::Quantiser& q, const float2* enc_lut,
-                                          const NormAdalnParams& p) {
+// NVFP4 outputs of one 8-element chunk (a in `o`): the block of 16 is this
+// thread's chunk and its neighbour's (lanes 2b, 2b+1); the even lane stores
+// the block's scale byte.  q: the chunk's code word; sf: its scale byte.
+__device__ __forceinline__ void fp4_chunk(const uint4& o, int lane, uint32_t* q, uint8_t* sf,
+                                          const fp4::Quantiser& qt, const float2* enc_lut) {
   float amax = fp4::amax8(o);
   amax = fmaxf(amax, __shfl_xor_sync(0xFFFFFFFFu, amax, 1));
-  const fp4::BlockScale bs = fp4::block_scale(amax, q, enc_lut);
-  *reinterpret_cast<uint32_t*>(p.act_q + m * (kHidden / 2) + 4 * c) = fp4::encode8(o, bs, q.gs);
-  if ((lane & 1) == 0)
-    p.act_sf[fp4::scale_offset(m, c >> 3, kHidden / 64, p.sf_tiled != 0) + ((lane & 7) >> 1)] =
-        static_cast<uint8_t>(bs.code);
+  const fp4::BlockScale bs = fp4::block_scale(amax, qt, enc_lut);
+  *q = fp4::encode8(o, bs, qt.gs);
+  if ((lane & 1) == 0) *sf = static_cast<uint8_t>(bs.code);
 }
 
 constexpr int kModeBf16 = 0;  // bf16 workspace
@@ -137,6 +134,14 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm) norm_adaln_kernel(const 
   const float gs = kFp4 ? __ldg(p.act_gs) : 0.0f;
   const fp4::Quantiser quant = fp4::make_quantiser(gs);
   if (kFp4) fp4::init_enc_lut(enc_lut, gs, tid, kThreads);  // visible after the first barrier
+  // scale byte of chunk j within its row's scales (row part added per row)
+  int sf_off[kVecPerThread];
+#pragma unroll
+  for (int j = 0; j < kVecPerThread; ++j) {
+    const int c = tid + kThreads * j;
+    sf_off[j] = p.sf_tiled ? (c >> 3) * fp4::kAtomBytes + ((lane & 7) >> 1)
+                           : (c >> 3) * 4 + ((lane & 7) >> 1);
+  }
 
   uint64_t policy = 0;
   if (tid == 0) {
@@ -195,13 +200,19 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm) norm_adaln_kernel(const 
                    __fadd_rn(__fadd_rn(warp_ss[4], warp_ss[5]), warp_ss[6]));
 
     uint4* wr = reinterpret_cast<uint4*>(p.workspace + m * kHidden);
+    uint32_t* qrow = kFp4 ? reinterpret_cast<uint32_t*>(p.act_q + m * (kHidden / 2)) : nullptr;
+    uint8_t* sfrow = !kFp4 ? nullptr
+                     : p.act_sf + (p.sf_tiled ? (m >> 7) * (kHidden / 64) * fp4::kAtomBytes +
+                                                    (m & 31) * 16 + ((m >> 5) & 3) * 4
+                                              : m * (kHidden / 16));
     if (idx < 0 || idx >= p.rows) {
       const uint4 z = make_uint4(0u, 0u, 0u, 0u);
 #pragma unroll
       for (int j = 0; j < kVecPerThread; ++j) {
-        if (kFp4)
-          fp4_chunk(z, lane, tid + kThreads * j, m, quant, enc_lut, p);  // codes 0, scale 0
-        else if (kFp8)
+        if (kFp4) {
+          qrow[tid + kThreads * j] = 0u;  // codes 0, scale 0
+          if ((lane & 1) == 0) sfrow[sf_off[j]] = 0;
+        } else if (kFp8)
           reinterpret_cast<uint2*>(p.a_q8 + m * kHidden)[tid + kThreads * j] = make_uint2(0u, 0u);
         else
           wr[tid + kThreads * j] = z;
@@ -229,7 +240,7 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm) norm_adaln_kernel(const 
       o.z = adaln_pair(f2_from_bf16x2(v[j].z), w.z, sc.z, sh.z, r2);
       o.w = adaln_pair(f2_from_bf16x2(v[j].w), w.w, sc.w, sh.w, r2);
       if (kFp4) {
-        fp4_chunk(o, lane, c, m, quant, enc_lut, p);
+        fp4_chunk(o, lane, qrow + c, sfrow + sf_off[j], quant, enc_lut);
       } else if (kFp8) {
         a8[kFp8 ? j : 0] = o;
         amax = fmaxf(amax, e4m3r::amax8(o));

@@ -4,7 +4,7 @@
 // quantize_minimax_h3_qkv_weight_nvfp4) and a direct check of the
 // quantisation the stage's first kernel applies to the activation.
 // One thread per (row, 64-element step): 128 B of input, 32 B of codes and
-// one 4-byte scale word out.  HBM-bound.
+// one 4-byte scale word out.
 #include "nvfp4.cuh"
 
 namespace mh3 {
@@ -23,12 +23,19 @@ __global__ void __launch_bounds__(256) nvfp4_quantize_kernel(const __nv_bfloat16
   fp4::init_enc_lut(enc_lut, gs, threadIdx.x, blockDim.x);
   __syncthreads();
   const int ksteps = cols / 64;
-  const int64_t total = rows * ksteps;
+  // grid-stride over (row, step) items, the index pair advanced without a
+  // division per item
   const int64_t stride = static_cast<int64_t>(gridDim.x) * blockDim.x;
-  for (int64_t t = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x; t < total;
-       t += stride) {
-    const int64_t row = t / ksteps;
-    const int ks = static_cast<int>(t - row * ksteps);
+  const int64_t stride_rows = stride / ksteps;
+  const int stride_ks = static_cast<int>(stride - stride_rows * ksteps);
+  const int64_t t0 = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x;
+  int64_t row = t0 / ksteps;
+  int ks = static_cast<int>(t0 - row * ksteps);
+  for (; row < rows; row += stride_rows, ks += stride_ks) {
+    if (ks >= ksteps) {
+      ks -= ksteps;
+      if (++row >= rows) break;
+    }
     const uint4* src = reinterpret_cast<const uint4*>(in + row * cols + ks * 64);
     uint4 v[8];
 #pragma unroll

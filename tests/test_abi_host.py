@@ -169,3 +169,30 @@ def test_mlp_validate(lib):
                        (dict(workspace_y=BASE + 0x40000004), 2), (dict(eps=0.0), 1),
                        (dict(out=BASE + 10752 * 2), 1), (dict(residual=None), 1)]:
         assert v(**over) == code, over
+
+
+def test_binding_wrappers_marshal_without_a_gpu(monkeypatch):
+    """Every wrapper of the binding hands its C call to the status check
+    (_check(rc, name)); the Handle methods run against a stub library that
+    records the call, so a marshalling slip fails here rather than on a GPU."""
+    import ast
+    tree = ast.parse(open(binding.__file__).read())
+    for node in ast.walk(tree):
+        if isinstance(node, ast.Call) and getattr(node.func, "id", "") == "_check":
+            assert len(node.args) == 2, f"_check with {len(node.args)} arguments at line {node.lineno}"
+
+    calls = []
+
+    class Stub:
+        def __getattr__(self, name):
+            def f(*args):
+                calls.append(name)
+                return 0
+            return f
+
+    monkeypatch.setattr(binding, "load", lambda *a, **k: Stub())
+    h = object.__new__(binding.Handle)
+    h._h = binding._vp(1)
+    h.set_test_stall(True)
+    assert h.device_status(stream=0) == 0  # 0: the default stream, no torch stream needed
+    assert calls == ["mh3_preattn_set_test_stall", "mh3_preattn_device_status"]
