@@ -38,9 +38,13 @@ using namespace k2;
 static_assert(kMlpInter % kHeadDim == 0, "y column blocks of 128");
 static_assert(kMlpInter % BK == 0, "fc2 K must tile");
 
-// silu(v) = v / (1 + exp(-v)) in FP32 (expf, IEEE add and division).
+// silu(v) = v * (1 / (1 + exp(-v))) in FP32 from the fast exponential and
+// reciprocal (__expf, __fdividef): branch-free, so the 32 outputs of a TMEM
+// load interleave, and within a few FP32 ulps; the value is rounded to bf16
+// at once, where those ulps move about one value in 10^4 by one bf16 step.
+// For v < -87, 1 + exp(-v) exceeds 2^126 and the reciprocal is 0: silu = -0.
 __device__ __forceinline__ float silu_f32(float v) {
-  return __fdiv_rn(v, __fadd_rn(1.0f, expf(-v)));
+  return __fmul_rn(v, __fdividef(1.0f, __fadd_rn(1.0f, __expf(-v))));
 }
 
 struct SwigluEpi {
