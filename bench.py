@@ -43,7 +43,8 @@ FLOP_PER_TOKEN = 2 * 5376 * 21504
 K2_SOURCES = ("norm_adaln_qkv_gb300/csrc/k2_qkv_gemm_pair.cu",
               "norm_adaln_qkv_gb300/csrc/gemm_pair.cuh",
               "norm_adaln_qkv_gb300/csrc/k2_common.cuh", "norm_adaln_qkv_gb300/csrc/ptx.cuh",
-              "norm_adaln_qkv_gb300/csrc/common.cuh", "norm_adaln_qkv_gb300/csrc/e4m3.cuh")
+              "norm_adaln_qkv_gb300/csrc/common.cuh", "norm_adaln_qkv_gb300/csrc/e4m3.cuh",
+              "norm_adaln_qkv_gb300/csrc/nvfp4.cuh")
 OUT_PROJ_FLOP_PER_TOKEN = 2 * 7168 * 5376
 MLP_FLOP_PER_TOKEN = 2 * 5376 * 28672 + 2 * 14336 * 5376
 TRAFFIC_FILE = os.path.join(ROOT, "profiles", "k2_traffic.json")
