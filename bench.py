@@ -137,8 +137,11 @@ class ClockSampler:
         names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
         reasons = sorted({names[i] for r in rows for i in range(4) if r[5 + i].lower() == "active"})
         busy = [s for s in sm if smax and s > 0.5 * max(smax)] or sm
+        pw = [num(r[3]) for r in rows if num(r[3]) is not None and num(r[1]) is not None
+              and smax and num(r[1]) > 0.5 * max(smax)]
         return {"sm_mhz": statistics.median(busy) if busy else None,
                 "sm_max_mhz": max(smax) if smax else None,
+                "power_w": statistics.median(pw) if pw else None,
                 "reasons": reasons, "samples": len(rows)}
 
 
