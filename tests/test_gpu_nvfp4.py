@@ -340,6 +340,43 @@ def test_production_size_sampled_parity(handle, weight, key):
     print(key, len(tokens), st, st2, code_eq, sf_eq)
 
 
+def test_nvfp4_outputs_production_size_sampled(handle, weight):
+    """out_mode "nvfp4" at the production size (M = 32760, P = 8) in the
+    bench's launch configuration: the codes and scales of sampled tokens
+    (every 64th, the last, guarded ones) against the oracle's quantisation of
+    the same call's bf16 outputs, and every guarded token's codes and scales
+    zero (by value)."""
+    w = make_nvfp4_workload("c3")
+    d = _dev(w)
+    M, P = w.M, w.base.spec.P
+    out = torch.empty((P, M, 56 // P, 3, 128), dtype=BF16, device="cuda")
+    run_stage(handle, w, d, weight, out)
+    lib = binding.load()
+    codes = torch.full((lib.mh3_preattn_out_nvfp4_bytes(M, 0),), 0xEE, dtype=torch.uint8,
+                       device="cuda")
+    sf = torch.full((lib.mh3_preattn_out_nvfp4_bytes(M, 1),), 0xEE, dtype=torch.uint8,
+                    device="cuda")
+    run_stage_nvfp4_out(handle, w, d, weight, codes, sf,
+                        torch.tensor(OUT_GS, dtype=torch.float32, device="cuda"), P)
+    torch.cuda.synchronize()
+    assert handle.device_status() == 0
+    bad = (w.adaln_index < 0) | (w.adaln_index >= w.base.spec.rows)
+    tokens = sorted(set(range(0, M, 64)) | {M - 1} | set(torch.nonzero(bad).flatten().tolist()[:48]))
+    c5 = codes.view(P, M, 56 // P, 3, 64)
+    s5 = sf.view(P, M, 56 // P, 3, 8)
+    got_c = oracle.ulysses_unpack_rows(c5, tokens).cpu()
+    got_s = oracle.ulysses_unpack_rows(s5, tokens).cpu()
+    ref_c, ref_s = f.quantize_outputs(oracle.ulysses_unpack_rows(out, tokens).cpu(), OUT_GS)
+    assert torch.equal(got_s, ref_s), int((got_s != ref_s).sum())
+    assert torch.equal(got_c, ref_c), int((got_c != ref_c).sum())
+    bad_d = bad.cuda()
+    assert int(bad.sum()) > 0
+    # zero by value: the bf16 outputs of a guarded token are +0 or -0, and a
+    # -0 keeps its sign bit in the E2M1 code
+    assert bool(((c5.permute(1, 0, 2, 3, 4)[bad_d] & 0x77) == 0).all())
+    assert bool((s5.permute(1, 0, 2, 3, 4)[bad_d] == 0).all())
+
+
 def test_repacking_is_bit_identical_across_P(handle, weight):
     """The pack is a pure relabelling: every P gives the same per-token values."""
     w = make_nvfp4_workload("c2", 300)
