@@ -25,7 +25,9 @@
 // the codes of the exact quotients; where a pair of codes differs, the sign
 // of |v| * gs - m * sf at the midpoint m between them decides (m * sf has at
 // most 7 significant bits).  Ties (the exact quotient on the midpoint) go to
-// the even code.
+// the even code.  Where gs / sf itself is an FP32 number of at most 16
+// significant bits, both multipliers are that value: the products are exact
+// and the conversion rounds them once, ties included, with no exact step.
 //
 // Codes are packed two per byte, element 2j in the low nibble.  Scales are
 // stored either row-major ([rows, cols/16]) or in the tiled form the
@@ -68,21 +70,28 @@ __device__ __forceinline__ Quantiser make_quantiser(float gs) {
   return q;
 }
 
-// enc[c] = (multiplier just below gs / s_c, multiplier just above) for every
-// UE4M3 code c ((0, 0) for c = 0).  With e_lo <= (gs / s)(1 - 2^-23) and
-// e_hi >= (gs / s)(1 + 2^-23), one round-to-nearest product |v| * e_lo stays
-// strictly below |v| * gs / s and |v| * e_hi strictly above (for v != 0).
-// Fill with all threads of the block, then synchronise.
+// Multipliers of gs / q for a nonzero divisor q: where gs / q is an FP32
+// number with at most 16 significant bits, both are that exact value, so
+// |v| * (gs / q) is exact for any bf16 v (at most 8 + 16 bits) and the E2M1
+// conversion's own nearest-even rounding is the single rounding, ties
+// included; the two code words then always agree.  Otherwise a multiplier
+// e_lo <= (gs / q)(1 - 2^-23) and one e_hi >= (gs / q)(1 + 2^-23): one
+// round-to-nearest product |v| * e_lo stays strictly below |v| * gs / q and
+// |v| * e_hi strictly above (for v != 0).
+__device__ __forceinline__ float2 enc_pair(float gs, float q) {
+  const float lo = __fdiv_rd(gs, q), hi = __fdiv_ru(gs, q);
+  if (lo == hi && (__float_as_uint(lo) & 0xFFu) == 0u) return make_float2(lo, lo);
+  return make_float2(__fmul_rd(lo, 0x1.fffffep-1f),   // 1 - 2^-23
+                     __fmul_ru(hi, 0x1.000002p+0f));  // 1 + 2^-23
+}
+
+// enc[c] = the multipliers of gs / s_c for every UE4M3 code c ((0, 0) for
+// c = 0).  Fill with all threads of the block, then synchronise.
 constexpr int kEncLut = 128;
 __device__ __forceinline__ void init_enc_lut(float2* lut, float gs, int tid, int nthreads) {
   for (int c = tid; c < kEncLut; c += nthreads) {
     const float s = c < 127 ? ue4m3_value(static_cast<uint32_t>(c)) : 0.0f;
-    float2 e = make_float2(0.0f, 0.0f);
-    if (s != 0.0f) {
-      e.x = __fmul_rd(__fdiv_rd(gs, s), 0x1.fffffep-1f);  // 1 - 2^-23
-      e.y = __fmul_ru(__fdiv_ru(gs, s), 0x1.000002p+0f);  // 1 + 2^-23
-    }
-    lut[c] = e;
+    lut[c] = s != 0.0f ? enc_pair(gs, s) : make_float2(0.0f, 0.0f);
   }
 }
 
@@ -133,9 +142,9 @@ __device__ __forceinline__ BlockScale block_scale(float amax, const Quantiser& q
 // without room for kEncLut entries: a UE4M3 code with exponent field e and
 // mantissa j has the value n 2^(E - 10), n = 8 + j and E = e for e >= 1, and
 // n = j, E = 1 for e = 0.  So gs / sf = (gs / n) 2^(10 - E): the table holds
-// (RD(RD(gs / n)(1 - 2^-23)), RU(RU(gs / n)(1 + 2^-23))) for n = 1..15, and
-// the power of two is applied with a product rounded the same way, which
-// keeps each multiplier on its side of (gs / sf)(1 -+ 2^-23).
+// enc_pair(gs, n) for n = 1..15, and the power of two is applied with a
+// product rounded the same way, which keeps each bracketing multiplier on
+// its side of (gs / sf)(1 -+ 2^-23) and an exact one exact.
 struct Table16 {
   float gs, c_lo, c_hi, pad;
   float2 t[16];
@@ -148,13 +157,7 @@ __device__ __forceinline__ void init_table16(Table16* q, float gs, int tid) {
     q->c_hi = __fdiv_ru(gs, 6.0f);
     q->pad = 0.0f;
   } else if (tid < 16) {
-    float2 e = make_float2(0.0f, 0.0f);
-    if (tid > 0) {
-      const float n = static_cast<float>(tid);
-      e.x = __fmul_rd(__fdiv_rd(gs, n), 0x1.fffffep-1f);
-      e.y = __fmul_ru(__fdiv_ru(gs, n), 0x1.000002p+0f);
-    }
-    q->t[tid] = e;
+    q->t[tid] = tid > 0 ? enc_pair(gs, static_cast<float>(tid)) : make_float2(0.0f, 0.0f);
   }
 }
 
