@@ -100,6 +100,20 @@ int mh3_preattn_validate(int64_t M, const mh3_bf16* x, const mh3_bf16* x_norm_we
  * two launches on `stream` (page summary: "two kernel launches on the current
  * stream").
  *
+ * Split tail: when M > 128 and the GEMM's last wave of 256 x 256 tiles holds
+ * at most half as many tiles as there are resident CTA pairs, each of those
+ * tiles is computed by two pairs, one per half of K; the first adds its FP32
+ * partial to the second's accumulator (one FP32 addition per element, fixed
+ * order, deterministic) before the epilogue.  Those tiles' accumulators are
+ * summed in another order than a whole tile's, so their outputs may differ
+ * from mh3_preattn_run_noalloc's (which never splits) within the stage's
+ * tolerance.  The partials live in a scratch of the handle, grown with
+ * stream-ordered cudaMallocAsync the first time a split size needs more
+ * (even with a caller workspace): capture a split size into a graph after
+ * one direct call at that size.  Its flags are cleared with a memset before
+ * each such call (a graph replays that memset), and runs of one handle on
+ * different streams race on the scratch.
+ *
  *   M                 tokens, >= 0 (M == 0 launches nothing and returns MH3_OK)
  *   x                 [M, 5376] row-major, 16-byte aligned
  *   x_norm_weight     [5376], 16-byte aligned
@@ -195,7 +209,7 @@ int mh3_preattn_norm_adaln(mh3_preattn_t handle, void* stream, int64_t M, const 
 /* Kernel 2 alone: out = pack(rope(norm(bf16(workspace @ qkv_weight^T)))),
  * reading an already-filled workspace [M, 5376].  Arguments as in
  * mh3_preattn_run (qk_eps here must be finite and > 0: there is no eps to
- * fall back to). */
+ * fall back to); the same split tail, with the same handle scratch. */
 int mh3_preattn_qkv(mh3_preattn_t handle, void* stream, int64_t M, const mh3_bf16* workspace,
                     const mh3_bf16* qkv_weight, const mh3_bf16* q_norm_weight,
                     const mh3_bf16* k_norm_weight, const mh3_bf16* rope_cos_sin, int64_t S,

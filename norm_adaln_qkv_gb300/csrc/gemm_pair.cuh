@@ -36,6 +36,8 @@
 // signal the other CTA) before the final cluster barrier and TMEM release.
 #pragma once
 
+#include <type_traits>
+
 #include "k2_common.cuh"
 
 namespace mh3 {
@@ -146,6 +148,118 @@ struct EpiCtx {
 };
 
 
+// Whether an epilogue policy takes part in the split tail (Params with the
+// sk_* fields of QkvParams): policies opt in with kSplitTail = true.
+template <class E, class = void>
+struct split_tail : std::false_type {};
+template <class E>
+struct split_tail<E, std::void_t<decltype(E::kSplitTail)>> : std::bool_constant<E::kSplitTail> {};
+
+// One piece of a cluster's work: k-blocks [kb0, kb1) of tile t; role 0 is a
+// whole tile, 1 the first half of a split tile (its partial is handed to the
+// owner), 2 the second half (the owner: adds the partial, runs the epilogue).
+struct Piece {
+  int t, kb0, kb1, role;
+};
+
+// The pieces of cluster cid in order: whole tiles cid, cid + ncl, ... below
+// `whole_end`, then its half of split tile whole_end + cid / 2 if cid < 2 *
+// sk_tail.  The producer, the MMA issuer and the epilogue each walk their own
+// copy.
+template <class Epi>
+struct Schedule {
+  int t, ncl, whole_end, kkb;
+  int tail_tile, tail_half;
+  __device__ Schedule(const typename Epi::Params& p, int cid, int ncl_)
+      : t(cid), ncl(ncl_), kkb(Epi::kKBlocks), tail_tile(-1), tail_half(0) {
+    whole_end = p.num_tiles;
+    if constexpr (split_tail<Epi>::value) {
+      if (p.sk_tail > 0) {
+        whole_end = p.sk_dp;
+        if (cid < 2 * p.sk_tail) {
+          tail_tile = p.sk_dp + cid / 2;
+          tail_half = cid & 1;
+        }
+      }
+    }
+  }
+  __device__ bool next(Piece& w) {
+    if (t < whole_end) {
+      w = Piece{t, 0, kkb, 0};
+      t += ncl;
+      return true;
+    }
+    if (tail_tile >= 0) {
+      const int h = kkb / 2;
+      w = Piece{tail_tile, tail_half * h, tail_half ? kkb : h, 1 + tail_half};
+      tail_tile = -1;
+      return true;
+    }
+    return false;
+  }
+};
+
+// Split tail, first half: this warp's 32 accumulator rows x 256 columns to
+// its partial slot ([column][lane], coalesced), then the flag (every lane's
+// stores fenced, the warp synchronised, lane 0 releases the sequence value).
+__device__ __forceinline__ void split_store(uint32_t tacc, float* slot, int* flag, int seq,
+                                            int lane) {
+#pragma unroll 1
+  for (int c = 0; c < kTileN / 32; ++c) {
+    uint32_t v[32];
+    tmem_ld_x32(tacc + 32 * c, v);
+    tmem_wait_ld();
+#pragma unroll
+    for (int i = 0; i < 32; ++i) __stcg(slot + (32 * c + i) * 32 + lane, __uint_as_float(v[i]));
+  }
+  __threadfence();
+  __syncwarp();
+  if (lane == 0) st_release_gpu(flag, seq);
+}
+
+// Split tail, second half: bounded wait for the partner's flag, then the
+// accumulator becomes acc + partial (one FP32 addition per element) in TMEM.
+// False when the wait gave up (status recorded, both CTAs' abort raised).
+__device__ __forceinline__ bool split_add(uint32_t tacc, const float* slot, const int* flag,
+                                          int seq, int lane, const PairCtx& ctx) {
+  bool ok = true;
+  if (lane == 0) {
+    const uint64_t t0 = globaltimer_ns();
+    for (uint32_t n = 0; ld_acquire_gpu(flag) != seq; ++n) {
+      if ((n & 63u) == 63u) {
+        if (*ctx.abort_flag) {
+          ok = false;
+          break;
+        }
+        if (globaltimer_ns() - t0 > kWaitLimitNs) {
+          *ctx.abort_flag = 1;
+          st_shared_cluster_u32(ctx.peer_abort, 1u);
+          atomicCAS(ctx.status, 0, kStatusSplitPartial);
+          ok = false;
+          break;
+        }
+      }
+    }
+  }
+  ok = __shfl_sync(0xFFFFFFFFu, ok ? 1 : 0, 0) != 0;
+  if (!ok) return false;
+  (void)ld_acquire_gpu(flag);  // every lane's own acquire before it reads the partial
+#pragma unroll 1
+  for (int c = 0; c < kTileN / 32; ++c) {
+    uint32_t v[32];
+    float q[32];
+    tmem_ld_x32(tacc + 32 * c, v);
+#pragma unroll
+    for (int i = 0; i < 32; ++i) q[i] = __ldcg(slot + (32 * c + i) * 32 + lane);
+    tmem_wait_ld();
+#pragma unroll
+    for (int i = 0; i < 32; ++i) v[i] = __float_as_uint(__fadd_rn(__uint_as_float(v[i]), q[i]));
+    tmem_st_x32(tacc + 32 * c, v);
+  }
+  tmem_wait_st();
+  return true;
+}
+
 template <class Epi>
 __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     gemm_pair_kernel(const __grid_constant__ CUtensorMap tm_a,
@@ -210,12 +324,14 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
       // out and the kernel reports a status code instead of hanging
       bool ok = p.test_stall == 0;
       bool issued_any = false;
-      for (int t = cid; t < p.num_tiles && ok; t += ncl) {
+      Schedule<Epi> sched(p, cid, ncl);
+      Piece w;
+      while (ok && sched.next(w)) {
         int pr, n_blk;
-        tile_coords<kGroupPairs, kN>(t, p.num_m_tiles, pr, n_blk);
+        tile_coords<kGroupPairs, kN>(w.t, p.num_m_tiles, pr, n_blk);
         const int a_row = pr * kPairRows + static_cast<int>(rank) * BM;
         const int b_row = Epi::b_row(n_blk, static_cast<int>(rank));
-        for (int kb = 0; kb < kKB; ++kb) {
+        for (int kb = w.kb0; kb < w.kb1; ++kb) {
           if (!pair_wait(ctx, sm.empty(stage), phase ^ 1u, kStatusProducerEmpty)) {
             ok = false;
             break;
@@ -241,7 +357,9 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
       uint32_t phase = 0;
       bool ok = true;
       int it = 0;
-      for (int t = cid; t < p.num_tiles && ok; t += ncl, ++it) {
+      Schedule<Epi> sched(p, cid, ncl);
+      Piece w;
+      for (; ok && sched.next(w); ++it) {
         const int buf = it & 1;
         const uint32_t use = static_cast<uint32_t>(it >> 1);
         if (!pair_wait(ctx, sm.tempty(buf), (use & 1u) ^ 1u, kStatusMmaTmemEmpty)) {
@@ -250,7 +368,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
         }
         tc_fence_after();
         const uint32_t d_tmem = tmem_base + static_cast<uint32_t>(buf * kTileN);
-        for (int kb = 0; kb < kKB; ++kb) {
+        for (int kb = w.kb0; kb < w.kb1; ++kb) {
           if (!pair_wait(ctx, sm.full(stage), phase, kStatusMmaFull)) {
             ok = false;
             break;
@@ -261,12 +379,12 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
 #pragma unroll
           for (int k = 0; k < 4; ++k) {
             // advance 32 B along K inside the swizzle atom (16 bf16 or 32 E4M3)
+            // the piece's first MMA starts the accumulator
+            const uint32_t acc = (kb != w.kb0 || k != 0) ? 1u : 0u;
             if constexpr (Epi::kFp8)
-              umma_f8_pair(d_tmem, a_desc + 2 * k, b_desc + 2 * k, kIdescFp8,
-                           (kb | k) != 0 ? 1u : 0u);
+              umma_f8_pair(d_tmem, a_desc + 2 * k, b_desc + 2 * k, kIdescFp8, acc);
             else
-              umma_bf16_pair(d_tmem, a_desc + 2 * k, b_desc + 2 * k, kIdesc,
-                             (kb | k) != 0 ? 1u : 0u);
+              umma_bf16_pair(d_tmem, a_desc + 2 * k, b_desc + 2 * k, kIdesc, acc);
           }
           umma_commit_pair_multicast(sm.empty(stage), kBothCtas);
           if (++stage == kStages) {
@@ -290,7 +408,9 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     EpiCtx ec{0u, warp & 3, lane, sm.stg(ew), sm.epi_bar(ew), &epi_phase, sm.scratch(),
               &tm_out, &tm_aux, &ctx};
     int it = 0;
-    for (int t = cid; t < p.num_tiles; t += ncl, ++it) {
+    Schedule<Epi> sched(p, cid, ncl);
+    Piece w;
+    for (; sched.next(w); ++it) {
       const int buf = it & 1;
       const uint32_t use = static_cast<uint32_t>(it >> 1);
       bool ok = pair_wait(ctx, sm.tfull(buf), use & 1u, kStatusEpiTmemFull);
@@ -298,10 +418,28 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
       if (!ok) break;
       tc_fence_after();
       int pr, n_blk;
-      tile_coords<kGroupPairs, kN>(t, p.num_m_tiles, pr, n_blk);
+      tile_coords<kGroupPairs, kN>(w.t, p.num_m_tiles, pr, n_blk);
       ec.tmem_acc = tmem_base + static_cast<uint32_t>(buf * kTileN);
-      Epi::tile(ec, p, static_cast<int64_t>(pr) * kPairRows + static_cast<int64_t>(rank) * BM,
-                n_blk);
+      bool run = true;
+      if constexpr (split_tail<Epi>::value) {
+        if (w.role != 0) {
+          // this warp's slot and flag: [split tile][CTA][TMEM lane quadrant]
+          const int64_t slot_id =
+              (static_cast<int64_t>(w.t - p.sk_dp) * 2 + static_cast<int64_t>(rank)) * 4 + ec.quad;
+          float* slot = p.sk_partial + slot_id * (kTileN * 32);
+          int* flag = p.sk_flags + slot_id;
+          const uint32_t tq = ec.tmem_acc + (static_cast<uint32_t>(ec.quad * 32) << 16);
+          if (w.role == 1) {
+            split_store(tq, slot, flag, p.sk_seq, lane);
+            run = false;  // the owner runs the epilogue of this tile
+          } else {
+            run = split_add(tq, slot, flag, p.sk_seq, lane, ctx);
+          }
+        }
+      }
+      if (run)
+        Epi::tile(ec, p, static_cast<int64_t>(pr) * kPairRows + static_cast<int64_t>(rank) * BM,
+                  n_blk);
       // all TMEM reads of this accumulator are complete (tcgen05.wait::ld)
       tc_fence_before();
       __syncwarp();

@@ -19,6 +19,7 @@ template <bool kE4m3>
 struct QkvPairEpiT {
   using Params = QkvParams;
   static constexpr bool kFp8 = false;
+  static constexpr bool kSplitTail = true;  // takes part in the split tail (p.sk_*)
   static constexpr int kKBlocks = k2::kKBlocks;  // 84
   static constexpr int kNTiles = k2::kNTiles;    // 84
   __device__ static int b_row(int n_blk, int rank) { return gp::contiguous_b_row(n_blk, rank); }

@@ -51,6 +51,8 @@ struct mh3_preattn_ctx {
   void* act_sf = nullptr;
   size_t act_sf_bytes = 0;
   int test_stall_next = 0;  // test hook for the next CTA-pair QKV GEMM launch (bf16 or NVFP4)
+  void* sk_buf = nullptr;   // split-tail scratch of the pair form (flags, partials)
+  size_t sk_bytes = 0;
   int fc1_fp8_clusters = 0;     // resident clusters of the FP8 MLP GEMMs
   int fc2_fp8_clusters = 0;
   void* fp8_aq = nullptr;       // handle-owned FP8 MLP workspaces
@@ -289,12 +291,60 @@ int launch_stage1(cudaStream_t s, int num_sms, int* status, int64_t M, const mh3
   return MH3_OK;
 }
 
+// Scratch of the pair form's split tail, owned by a handle: one flag per
+// (split tile, CTA, epilogue warp), then the FP32 partials.  The flags are
+// cleared on the stream before every split launch (also inside a captured
+// graph, where the memset node replays with the kernels); a partial's writer
+// sets its flag to 1.
+constexpr int kSplitMaxTiles = 128;  // more than half of any resident cluster count
+constexpr size_t kSplitFlagBytes = kSplitMaxTiles * 8 * sizeof(int);
+constexpr size_t kSplitSlotBytes = 8 * 256 * 32 * sizeof(float);  // 2 CTAs x 4 warps x 256 x 32
+struct SplitScratch {
+  void** buf;
+  size_t* bytes;
+};
+
+// Tiles of the pair form's last wave that are split (0: no split): the last
+// wave must hold at most half as many tiles as there are clusters.
+int split_tiles(int64_t M, int max_clusters) {
+  if (M <= 128 || max_clusters <= 0) return 0;
+  const int tiles = static_cast<int>((M + 255) / 256) * (kQkvRows / 256);
+  const int clusters = tiles < max_clusters ? tiles : max_clusters;
+  const int rem = tiles % clusters;
+  return tiles > clusters && rem > 0 && 2 * rem <= clusters && rem <= kSplitMaxTiles ? rem : 0;
+}
+
+// Grows the scratch to `tiles` split tiles and clears the flags on `s`.
+int prepare_split(const SplitScratch& sk, int tiles, cudaStream_t s) {
+  const size_t need = kSplitFlagBytes + static_cast<size_t>(tiles) * kSplitSlotBytes;
+  if (*sk.bytes < need) {
+    if (*sk.buf) {
+      cudaError_t e = cudaFreeAsync(*sk.buf, s);
+      *sk.buf = nullptr;
+      *sk.bytes = 0;
+      if (e != cudaSuccess) return cuda_fail(e, "cudaFreeAsync (split scratch)");
+    }
+    cudaError_t e = cudaMallocAsync(sk.buf, need, s);
+    if (e != cudaSuccess) {
+      *sk.buf = nullptr;
+      return fail(MH3_ERR_OOM, "cudaMallocAsync of %zu B split scratch failed: %s", need,
+                  cudaGetErrorString(e));
+    }
+    *sk.bytes = need;
+  }
+  cudaError_t e = cudaMemsetAsync(*sk.buf, 0, kSplitFlagBytes, s);
+  if (e != cudaSuccess) return cuda_fail(e, "clearing the split flags");
+  return MH3_OK;
+}
+
 // Kernel 2: the CTA-pair form for M > 128 (when pairs can be resident), the
-// single-CTA form otherwise.
+// single-CTA form otherwise.  With `sk`, a pair-form launch whose last wave
+// holds at most half as many tiles as there are clusters splits those tiles
+// along K over two clusters each (the last wave then takes half a tile).
 int launch_stage2(cudaStream_t s, int num_sms, int max_clusters, int* status, int64_t M,
                   const mh3_bf16* ws, const mh3_bf16* W, const mh3_bf16* qw, const mh3_bf16* kw,
                   const mh3_bf16* cs, int64_t S, const int64_t* pos, int P, float qk_eps,
-                  mh3_bf16* out, int* test_stall = nullptr) {
+                  mh3_bf16* out, int* test_stall = nullptr, const SplitScratch* sk = nullptr) {
   const bool pair = M > 128 && max_clusters > 0;
   QkvMaps maps;
   int rc = encode_maps(maps, M, ws, W, P, out, pair ? 128u : 256u,
@@ -316,6 +366,15 @@ int launch_stage2(cudaStream_t s, int num_sms, int max_clusters, int* status, in
     p.num_m_tiles = static_cast<int>((M + 255) / 256);
     p.num_tiles = p.num_m_tiles * (kQkvRows / 256);
     const int clusters = p.num_tiles < max_clusters ? p.num_tiles : max_clusters;
+    // the caller has prepared the scratch for this M (prepare_split)
+    const int rem = sk != nullptr ? split_tiles(M, max_clusters) : 0;
+    if (rem > 0) {
+      p.sk_dp = p.num_tiles - rem;
+      p.sk_tail = rem;
+      p.sk_flags = static_cast<int*>(*sk->buf);
+      p.sk_partial = reinterpret_cast<float*>(static_cast<uint8_t*>(*sk->buf) + kSplitFlagBytes);
+      p.sk_seq = 1;
+    }
     if (test_stall != nullptr) {
       p.test_stall = *test_stall;
       *test_stall = 0;
@@ -416,7 +475,8 @@ int mh3_preattn_destroy(mh3_preattn_t h) {
     cudaError_t e = cudaFree(h->ws);
     if (e != cudaSuccess) rc = cuda_fail(e, "freeing the handle workspace");
   }
-  for (void* buf : {h->ws_y, h->act_q, h->act_sf, h->fp8_aq, h->fp8_as, h->fp8_yq, h->fp8_ys}) {
+  for (void* buf : {h->ws_y, h->act_q, h->act_sf, h->fp8_aq, h->fp8_as, h->fp8_yq, h->fp8_ys,
+                    h->sk_buf}) {
     if (buf == nullptr) continue;
     cudaError_t e = cudaFree(buf);
     if (e != cudaSuccess && rc == MH3_OK) rc = cuda_fail(e, "freeing the handle workspace");
@@ -483,13 +543,18 @@ int mh3_preattn_run(mh3_preattn_t h, void* stream, int64_t M, const mh3_bf16* x,
     }
     workspace = static_cast<mh3_bf16*>(h->ws);
   }
+  // the split tail's flags are cleared before kernel 1, so that kernel 2
+  // still follows kernel 1 directly (programmatic dependent launch)
+  const SplitScratch sk{&h->sk_buf, &h->sk_bytes};
+  const int split = split_tiles(M, h->max_clusters);
+  if (split > 0 && (rc = prepare_split(sk, split, s))) return rc;
   rc = launch_stage1(s, h->num_sms, h->d_status, M, x, x_norm_weight, adaln_scale,
                      scale_row_stride, adaln_shift, shift_row_stride, rows, adaln_index, eps,
                      workspace);
   if (rc) return rc;
   return launch_stage2(s, h->num_sms, h->max_clusters, h->d_status, M, workspace, qkv_weight,
                        q_norm_weight, k_norm_weight, rope_cos_sin, S, rope_positions, P, qk, out,
-                       &h->test_stall_next);
+                       &h->test_stall_next, &sk);
 }
 
 int mh3_preattn_norm_adaln(mh3_preattn_t h, void* stream, int64_t M, const mh3_bf16* x,
@@ -520,9 +585,12 @@ int mh3_preattn_qkv(mh3_preattn_t h, void* stream, int64_t M, const mh3_bf16* wo
   if (rc) return rc;
   if (M == 0) return MH3_OK;
   if ((rc = check_ptr(workspace, "workspace", 16))) return rc;
+  const SplitScratch sk{&h->sk_buf, &h->sk_bytes};
+  const int split = split_tiles(M, h->max_clusters);
+  if (split > 0 && (rc = prepare_split(sk, split, static_cast<cudaStream_t>(stream)))) return rc;
   return launch_stage2(static_cast<cudaStream_t>(stream), h->num_sms, h->max_clusters,
                        h->d_status, M, workspace, qkv_weight, q_norm_weight, k_norm_weight,
-                       rope_cos_sin, S, rope_positions, P, qk_eps, out, &h->test_stall_next);
+                       rope_cos_sin, S, rope_positions, P, qk_eps, out, &h->test_stall_next, &sk);
 }
 
 int mh3_preattn_set_test_stall(mh3_preattn_t h, int stall) {

@@ -9,8 +9,13 @@ other test by the time it gets here.
 
 Calls in a row of the new entry point (different sizes, so each call starts
 from the previous call's leftover workspace) must give the same outputs as
-mh3_preattn_run, within the stage's output tolerance (and, as both run the
-same kernels, bit for bit).
+mh3_preattn_run, within the stage's output tolerance.  At the single-CTA
+sizes (M <= 128) both run the same kernels and agree bit for bit.  At the
+CTA-pair sizes mh3_preattn_run may split the tiles of its last wave along K
+over two clusters (an FP32 partial added to the other half), which has no
+scratch in the allocation-free call: those tiles' accumulators are summed in
+another FP32 order, so there the outputs agree within the tolerance and
+almost all bit for bit.
 """
 import pytest
 import torch
@@ -61,8 +66,11 @@ def test_noalloc_matches_run_on_two_calls_in_a_row(cuda_lib):
 
     for d, o, r in zip(cases, outs, refs):
         st = check_outputs(_tokens(o), _tokens(r), f"noalloc M={d.M}")
-        # the same kernels on the same inputs: bit-identical as well
-        assert st["exact"] == 1.0, st
+        if d.M <= 128:
+            # the same kernels on the same inputs: bit-identical as well
+            assert st["exact"] == 1.0, st
+        else:
+            assert st["exact"] > 0.98, st
     h.close()
 
 
