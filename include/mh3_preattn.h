@@ -167,7 +167,8 @@ int mh3_preattn_run(mh3_preattn_t handle, void* stream, int64_t M, const mh3_bf1
  *   out           [P, M, 56/P, 3, 128] bytes (e4m3 codes), the bf16 mode's
  *                 pack, 16-byte aligned; M * 21504 bytes
  * Other arguments and rules as in mh3_preattn_run.  Kernel 2 always runs in
- * its CTA-pair form here. */
+ * its CTA-pair form here, with mh3_preattn_run's split tail for M > 128 (the
+ * same accumulators, so the codes are those of mh3_preattn_run's outputs). */
 int mh3_preattn_run_e4m3(mh3_preattn_t handle, void* stream, int64_t M, const mh3_bf16* x,
                          const mh3_bf16* x_norm_weight, const mh3_bf16* adaln_scale,
                          int64_t scale_row_stride, const mh3_bf16* adaln_shift,

@@ -57,6 +57,10 @@ struct NormAdalnParams {
   // and codes e4m3(a / s) replace the bf16 workspace
   uint8_t* a_q8 = nullptr;  // [M, 5376]
   float* a_s8 = nullptr;    // [M]
+  // ints cleared by CTA 0 for the kernel that follows (the split-tail flags
+  // of the QKV GEMM, which reads them only after this grid has completed)
+  int* clear = nullptr;
+  int clear_count = 0;
 };
 
 struct QkvParams {

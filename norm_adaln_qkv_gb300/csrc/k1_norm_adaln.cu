@@ -131,6 +131,8 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm) norm_adaln_kernel(const 
   // kernel 2 may start its prologue (barriers, TMEM, tensor maps) now; it
   // waits for this grid's completion before it reads the workspace
   griddep_launch_dependents();
+  if (blockIdx.x == 0)
+    for (int i = threadIdx.x; i < p.clear_count; i += kThreads) p.clear[i] = 0;
   const float gs = kFp4 ? __ldg(p.act_gs) : 0.0f;
   const fp4::Quantiser quant = fp4::make_quantiser(gs);
   if (kFp4) fp4::init_enc_lut(enc_lut, gs, tid, kThreads);  // visible after the first barrier

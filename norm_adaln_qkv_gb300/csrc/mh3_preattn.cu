@@ -272,8 +272,11 @@ int encode_2d(CUtensorMap* map, const void* base, uint64_t cols, uint64_t rows, 
 
 int launch_stage1(cudaStream_t s, int num_sms, int* status, int64_t M, const mh3_bf16* x,
                   const mh3_bf16* xw, const mh3_bf16* sc, int64_t sc_stride, const mh3_bf16* sh,
-                  int64_t sh_stride, int64_t rows, const int64_t* idx, float eps, mh3_bf16* ws) {
+                  int64_t sh_stride, int64_t rows, const int64_t* idx, float eps, mh3_bf16* ws,
+                  int* clear = nullptr, int clear_count = 0) {
   NormAdalnParams p;
+  p.clear = clear;
+  p.clear_count = clear_count;
   p.x = reinterpret_cast<const __nv_bfloat16*>(x);
   p.x_norm_weight = reinterpret_cast<const __nv_bfloat16*>(xw);
   p.scale = reinterpret_cast<const __nv_bfloat16*>(sc);
@@ -293,9 +296,9 @@ int launch_stage1(cudaStream_t s, int num_sms, int* status, int64_t M, const mh3
 
 // Scratch of the pair form's split tail, owned by a handle: one flag per
 // (split tile, CTA, epilogue warp), then the FP32 partials.  The flags are
-// cleared on the stream before every split launch (also inside a captured
-// graph, where the memset node replays with the kernels); a partial's writer
-// sets its flag to 1.
+// cleared before every split launch, on the stream (inside a captured graph
+// too): by kernel 1 of the same call, or by a memset when kernel 2 runs
+// alone.  A partial's writer sets its flag to 1.
 constexpr int kSplitMaxTiles = 128;  // more than half of any resident cluster count
 constexpr size_t kSplitFlagBytes = kSplitMaxTiles * 8 * sizeof(int);
 constexpr size_t kSplitSlotBytes = 8 * 256 * 32 * sizeof(float);  // 2 CTAs x 4 warps x 256 x 32
@@ -314,8 +317,9 @@ int split_tiles(int64_t M, int max_clusters) {
   return tiles > clusters && rem > 0 && 2 * rem <= clusters && rem <= kSplitMaxTiles ? rem : 0;
 }
 
-// Grows the scratch to `tiles` split tiles and clears the flags on `s`.
-int prepare_split(const SplitScratch& sk, int tiles, cudaStream_t s) {
+// Grows the scratch to `tiles` split tiles; clears the flags on `s` when
+// `clear` (otherwise kernel 1 of the call clears them).
+int prepare_split(const SplitScratch& sk, int tiles, cudaStream_t s, bool clear) {
   const size_t need = kSplitFlagBytes + static_cast<size_t>(tiles) * kSplitSlotBytes;
   if (*sk.bytes < need) {
     if (*sk.buf) {
@@ -332,6 +336,7 @@ int prepare_split(const SplitScratch& sk, int tiles, cudaStream_t s) {
     }
     *sk.bytes = need;
   }
+  if (!clear) return MH3_OK;
   cudaError_t e = cudaMemsetAsync(*sk.buf, 0, kSplitFlagBytes, s);
   if (e != cudaSuccess) return cuda_fail(e, "clearing the split flags");
   return MH3_OK;
@@ -543,14 +548,15 @@ int mh3_preattn_run(mh3_preattn_t h, void* stream, int64_t M, const mh3_bf16* x,
     }
     workspace = static_cast<mh3_bf16*>(h->ws);
   }
-  // the split tail's flags are cleared before kernel 1, so that kernel 2
-  // still follows kernel 1 directly (programmatic dependent launch)
+  // kernel 1 clears the split tail's flags (kernel 2 reads them only after
+  // kernel 1 has completed)
   const SplitScratch sk{&h->sk_buf, &h->sk_bytes};
   const int split = split_tiles(M, h->max_clusters);
-  if (split > 0 && (rc = prepare_split(sk, split, s))) return rc;
+  if (split > 0 && (rc = prepare_split(sk, split, s, false))) return rc;
   rc = launch_stage1(s, h->num_sms, h->d_status, M, x, x_norm_weight, adaln_scale,
                      scale_row_stride, adaln_shift, shift_row_stride, rows, adaln_index, eps,
-                     workspace);
+                     workspace, split > 0 ? static_cast<int*>(h->sk_buf) : nullptr,
+                     split > 0 ? static_cast<int>(kSplitFlagBytes / sizeof(int)) : 0);
   if (rc) return rc;
   return launch_stage2(s, h->num_sms, h->max_clusters, h->d_status, M, workspace, qkv_weight,
                        q_norm_weight, k_norm_weight, rope_cos_sin, S, rope_positions, P, qk, out,
@@ -587,7 +593,8 @@ int mh3_preattn_qkv(mh3_preattn_t h, void* stream, int64_t M, const mh3_bf16* wo
   if ((rc = check_ptr(workspace, "workspace", 16))) return rc;
   const SplitScratch sk{&h->sk_buf, &h->sk_bytes};
   const int split = split_tiles(M, h->max_clusters);
-  if (split > 0 && (rc = prepare_split(sk, split, static_cast<cudaStream_t>(stream)))) return rc;
+  if (split > 0 && (rc = prepare_split(sk, split, static_cast<cudaStream_t>(stream), true)))
+    return rc;
   return launch_stage2(static_cast<cudaStream_t>(stream), h->num_sms, h->max_clusters,
                        h->d_status, M, workspace, qkv_weight, q_norm_weight, k_norm_weight,
                        rope_cos_sin, S, rope_positions, P, qk_eps, out, &h->test_stall_next, &sk);
@@ -1241,9 +1248,15 @@ extern "C" int mh3_preattn_run_e4m3(
     if ((rc = grow_buffer(&h->ws, &h->ws_bytes, mh3_preattn_workspace_bytes(M), s))) return rc;
     workspace = static_cast<mh3_bf16*>(h->ws);
   }
+  // the same split tail as the bf16 stage (the same accumulators, so the
+  // codes are those of the bf16 outputs); kernel 1 clears its flags
+  const SplitScratch sk{&h->sk_buf, &h->sk_bytes};
+  const int split = split_tiles(M, h->e4m3_clusters);
+  if (split > 0 && (rc = prepare_split(sk, split, s, false))) return rc;
   rc = launch_stage1(s, h->num_sms, h->d_status, M, x, x_norm_weight, adaln_scale,
                      scale_row_stride, adaln_shift, shift_row_stride, rows, adaln_index, eps,
-                     workspace);
+                     workspace, split > 0 ? static_cast<int*>(h->sk_buf) : nullptr,
+                     split > 0 ? static_cast<int>(kSplitFlagBytes / sizeof(int)) : 0);
   if (rc) return rc;
   QkvMaps maps;
   if ((rc = encode_2d(&maps.a, workspace, kHidden, M, 64, 128, "workspace"))) return rc;
@@ -1263,6 +1276,13 @@ extern "C" int mh3_preattn_run_e4m3(
   p.num_m_tiles = static_cast<int>((M + 255) / 256);
   p.num_tiles = p.num_m_tiles * (kQkvRows / 256);
   const int clusters = p.num_tiles < h->e4m3_clusters ? p.num_tiles : h->e4m3_clusters;
+  if (split > 0) {
+    p.sk_dp = p.num_tiles - split;
+    p.sk_tail = split;
+    p.sk_flags = static_cast<int*>(h->sk_buf);
+    p.sk_partial = reinterpret_cast<float*>(static_cast<uint8_t*>(h->sk_buf) + kSplitFlagBytes);
+    p.sk_seq = 1;
+  }
   cudaError_t e = launch_qkv_e4m3(maps, p, clusters, s);
   if (e != cudaSuccess) return cuda_fail(e, "e4m3 QKV GEMM launch");
   return MH3_OK;
