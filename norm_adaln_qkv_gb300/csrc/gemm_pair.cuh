@@ -52,6 +52,9 @@ constexpr int kStages = 6;
 #ifndef MH3_GROUP_PAIRS
 #define MH3_GROUP_PAIRS 8
 #endif
+#ifndef MH3_PAIR_L2_HINTS
+#define MH3_PAIR_L2_HINTS 0
+#endif
 constexpr int kGroupPairs = MH3_GROUP_PAIRS;
 constexpr int kABytes = BM * BK * 2;   // 16 KB
 constexpr int kBBytes = BNC * BK * 2;  // 16 KB
@@ -324,6 +327,11 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
       // out and the kernel reports a status code instead of hanging
       bool ok = p.test_stall == 0;
       bool issued_any = false;
+#if MH3_PAIR_L2_HINTS
+      // A blocks are read by every column tile of their group, B boxes by the
+      // group's row blocks only: keep A, let B go first
+      const uint64_t pol_a = policy_evict_last(), pol_b = policy_evict_first();
+#endif
       Schedule<Epi> sched(p, cid, ncl);
       Piece w;
       while (ok && sched.next(w)) {
@@ -338,8 +346,13 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
           }
           const uint32_t leader_full = mapa_shared(sm.full(stage), 0);
           if (rank == 0) mbar_arrive_expect_tx(sm.full(stage), 2 * kStageBytes);
+#if MH3_PAIR_L2_HINTS
+          tma_load_2d_pair_hint(sm.a(stage), &tm_a, leader_full, kb * kBKElems, a_row, pol_a);
+          tma_load_2d_pair_hint(sm.b(stage), &tm_b, leader_full, kb * kBKElems, b_row, pol_b);
+#else
           tma_load_2d_pair(sm.a(stage), &tm_a, leader_full, kb * kBKElems, a_row);
           tma_load_2d_pair(sm.b(stage), &tm_b, leader_full, kb * kBKElems, b_row);
+#endif
           issued_any = true;
           if (++stage == kStages) {
             stage = 0;
