@@ -84,13 +84,18 @@ struct QkvParams {
   int test_stall = 0;  // test hook: the producer issues no loads (bounded waits run out)
   // Split tail of the CTA-pair form: tiles [0, sk_dp) whole, then tiles
   // sk_dp + j (j < sk_tail) split along K over clusters 2j (first half: its
-  // FP32 partial goes to sk_partial, flagged with sk_seq) and 2j + 1 (second
-  // half: adds the partial, then the epilogue).  sk_tail = 0: no split.
+  // FP32 partial goes to sk_partial, then its flag is set to sk_seq; the
+  // flags are cleared before every launch) and 2j + 1 (second half: adds the
+  // partial, then the epilogue).  sk_tail = 0: no split.
   int sk_dp = 0;
   int sk_tail = 0;
   float* sk_partial = nullptr;  // [sk_tail][2 CTAs][4 warps][256 columns][32 lanes]
   int* sk_flags = nullptr;      // [sk_tail][2][4]
   int sk_seq = 0;
+  // The grid before this one is the stage's kernel 1, which writes A alone:
+  // the pair form may load the weight boxes of its first stages before it
+  // waits for that grid (0: wait first, as for a caller's kernel).
+  int b_early = 0;
   // NVFP4 output mode of the NVFP4 stage: q, k, v global scales (device [3]),
   // codes [P, M, 56/P, 3, 64] and block scales [P, M, 56/P, 3, 8]
   const float* out_gs = nullptr;

@@ -158,6 +158,14 @@ struct split_tail : std::false_type {};
 template <class E>
 struct split_tail<E, std::void_t<decltype(E::kSplitTail)>> : std::bool_constant<E::kSplitTail> {};
 
+// Policies whose Params say that the previous grid writes A alone (b_early)
+// may have the weight boxes of the first stages loaded before the wait.
+template <class E, class = void>
+struct has_b_early : std::false_type {};
+template <class E>
+struct has_b_early<E, std::void_t<decltype(std::declval<typename E::Params>().b_early)>>
+    : std::true_type {};
+
 // One piece of a cluster's work: k-blocks [kb0, kb1) of tile t; role 0 is a
 // whole tile, 1 the first half of a split tile (its partial is handed to the
 // owner), 2 the second half (the owner: adds the partial, runs the epilogue).
@@ -318,9 +326,6 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
   if (warp == 0) {
     // ------------------------------------------------- producer (both CTAs)
     if (lane == 0) {
-      // A may be written by the kernel before this one, which may still be
-      // finishing (programmatic dependent launch)
-      griddep_wait();
       int stage = 0;
       uint32_t phase = 0;
       // test hook: issue nothing, so that the consumers' bounded waits run
@@ -334,12 +339,43 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
 #endif
       Schedule<Epi> sched(p, cid, ncl);
       Piece w;
-      while (ok && sched.next(w)) {
+      bool have = ok && sched.next(w);
+      // Stages of the first piece whose weight boxes go out before the wait
+      // (the ring is fresh: no empty wait); their A boxes follow it.
+      int pre = 0;
+      if constexpr (has_b_early<Epi>::value) {
+        if (have && p.b_early != 0) {
+          int pr, n_blk;
+          tile_coords<kGroupPairs, kN>(w.t, p.num_m_tiles, pr, n_blk);
+          const int b_row = Epi::b_row(n_blk, static_cast<int>(rank));
+          pre = w.kb1 - w.kb0 < kStages ? w.kb1 - w.kb0 : kStages;
+          for (int s = 0; s < pre; ++s) {
+            if (rank == 0) mbar_arrive_expect_tx(sm.full(s), 2 * kStageBytes);
+            tma_load_2d_pair(sm.b(s), &tm_b, mapa_shared(sm.full(s), 0), (w.kb0 + s) * kBKElems,
+                             b_row);
+          }
+        }
+      }
+      // A may be written by the kernel before this one, which may still be
+      // finishing (programmatic dependent launch)
+      griddep_wait();
+      if (pre > 0) {
+        int pr, n_blk;
+        tile_coords<kGroupPairs, kN>(w.t, p.num_m_tiles, pr, n_blk);
+        const int a_row = pr * kPairRows + static_cast<int>(rank) * BM;
+        for (int s = 0; s < pre; ++s)
+          tma_load_2d_pair(sm.a(s), &tm_a, mapa_shared(sm.full(s), 0), (w.kb0 + s) * kBKElems,
+                           a_row);
+        issued_any = true;
+        stage = pre == kStages ? 0 : pre;
+        phase = pre == kStages ? 1u : 0u;
+      }
+      for (; have; pre = 0, have = ok && sched.next(w)) {
         int pr, n_blk;
         tile_coords<kGroupPairs, kN>(w.t, p.num_m_tiles, pr, n_blk);
         const int a_row = pr * kPairRows + static_cast<int>(rank) * BM;
         const int b_row = Epi::b_row(n_blk, static_cast<int>(rank));
-        for (int kb = w.kb0; kb < w.kb1; ++kb) {
+        for (int kb = w.kb0 + pre; kb < w.kb1; ++kb) {
           if (!pair_wait(ctx, sm.empty(stage), phase ^ 1u, kStatusProducerEmpty)) {
             ok = false;
             break;

@@ -346,10 +346,13 @@ int prepare_split(const SplitScratch& sk, int tiles, cudaStream_t s, bool clear)
 // single-CTA form otherwise.  With `sk`, a pair-form launch whose last wave
 // holds at most half as many tiles as there are clusters splits those tiles
 // along K over two clusters each (the last wave then takes half a tile).
+// after_k1: the launch follows this stage's kernel 1 on the stream, so the
+// pair form may fetch its first weight boxes before waiting for that grid.
 int launch_stage2(cudaStream_t s, int num_sms, int max_clusters, int* status, int64_t M,
                   const mh3_bf16* ws, const mh3_bf16* W, const mh3_bf16* qw, const mh3_bf16* kw,
                   const mh3_bf16* cs, int64_t S, const int64_t* pos, int P, float qk_eps,
-                  mh3_bf16* out, int* test_stall = nullptr, const SplitScratch* sk = nullptr) {
+                  mh3_bf16* out, int* test_stall = nullptr, const SplitScratch* sk = nullptr,
+                  bool after_k1 = false) {
   const bool pair = M > 128 && max_clusters > 0;
   QkvMaps maps;
   int rc = encode_maps(maps, M, ws, W, P, out, pair ? 128u : 256u,
@@ -384,6 +387,7 @@ int launch_stage2(cudaStream_t s, int num_sms, int max_clusters, int* status, in
       p.test_stall = *test_stall;
       *test_stall = 0;
     }
+    p.b_early = after_k1 ? 1 : 0;
     e = launch_qkv_pair(maps, p, clusters, s);
   } else {
     p.num_m_tiles = static_cast<int>((M + 127) / 128);
@@ -560,7 +564,7 @@ int mh3_preattn_run(mh3_preattn_t h, void* stream, int64_t M, const mh3_bf16* x,
   if (rc) return rc;
   return launch_stage2(s, h->num_sms, h->max_clusters, h->d_status, M, workspace, qkv_weight,
                        q_norm_weight, k_norm_weight, rope_cos_sin, S, rope_positions, P, qk, out,
-                       &h->test_stall_next, &sk);
+                       &h->test_stall_next, &sk, true);
 }
 
 int mh3_preattn_norm_adaln(mh3_preattn_t h, void* stream, int64_t M, const mh3_bf16* x,
@@ -1283,6 +1287,7 @@ extern "C" int mh3_preattn_run_e4m3(
     p.sk_partial = reinterpret_cast<float*>(static_cast<uint8_t*>(h->sk_buf) + kSplitFlagBytes);
     p.sk_seq = 1;
   }
+  p.b_early = 1;  // kernel 1 just launched on this stream writes A alone
   cudaError_t e = launch_qkv_e4m3(maps, p, clusters, s);
   if (e != cudaSuccess) return cuda_fail(e, "e4m3 QKV GEMM launch");
   return MH3_OK;
@@ -1622,5 +1627,5 @@ extern "C" int mh3_preattn_run_noalloc(
   if (rc) return rc;
   return launch_stage2(s, d.num_sms, d.max_clusters, device_status, M, d.workspace, qkv_weight,
                        q_norm_weight, k_norm_weight, rope_cos_sin, S, rope_positions, P,
-                       qk_eps_means_default(qk_eps) ? eps : qk_eps, out);
+                       qk_eps_means_default(qk_eps) ? eps : qk_eps, out, nullptr, nullptr, true);
 }
