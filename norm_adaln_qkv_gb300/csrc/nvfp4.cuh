@@ -96,8 +96,8 @@ __device__ __forceinline__ void init_enc_lut(float2* lut, float gs, int tid, int
 }
 
 struct BlockScale {
-  uint32_t code;  // UE4M3 scale code
-  float sf;       // its value
+  uint32_t code;  // UE4M3 scale code (its value sf is decoded only where an
+                  // element needs the exact step)
   float enc_lo;   // multipliers bracketing gs / sf
   float enc_hi;
 };
@@ -131,7 +131,6 @@ __device__ __forceinline__ BlockScale block_scale(float amax, const Quantiser& q
   if (code != (both >> 8)) code = scale_code_at_boundary(amax, q.gs, code, both >> 8);
   BlockScale b;
   b.code = code;
-  b.sf = ue4m3_value(code);
   const float2 e = enc_lut[code];
   b.enc_lo = e.x;
   b.enc_hi = e.y;
@@ -169,7 +168,6 @@ __device__ __forceinline__ BlockScale block_scale_t16(float amax, const Table16&
   if (code != (both >> 8)) code = scale_code_at_boundary(amax, q.gs, code, both >> 8);
   BlockScale b;
   b.code = code;
-  b.sf = ue4m3_value(code);
   const uint32_t e = code >> 3, j = code & 7u;
   const uint32_t n = e ? 8u + j : j;
   const uint32_t E = e ? e : 1u;
@@ -236,7 +234,7 @@ __device__ __forceinline__ uint32_t codes8_at_boundary(const uint4& w, uint32_t 
 __device__ __forceinline__ uint32_t encode8(const uint4& w, const BlockScale& b, float gs) {
   const uint32_t lo = codes8(w, b.enc_lo);
   const uint32_t hi = codes8(w, b.enc_hi);
-  return lo == hi ? lo : codes8_at_boundary(w, lo, hi, gs, b.sf);
+  return lo == hi ? lo : codes8_at_boundary(w, lo, hi, gs, ue4m3_value(b.code));
 }
 
 // max |v| of eight bf16 values (exact): packed magnitude maxima
