@@ -14,7 +14,7 @@ def pytest_configure(config):
 
 @pytest.fixture(scope="session")
 def cuda_lib():
-    """The built C-ABI library on a GPU machine; GPU tests fail loudly without it."""
+    """The built C-ABI library on a machine with a GB300; GPU tests fail loudly without it."""
     import torch
     if not torch.cuda.is_available():
         pytest.fail("GPU test collected on a machine without CUDA")
