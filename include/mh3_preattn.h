@@ -69,7 +69,11 @@ typedef struct mh3_preattn_ctx* mh3_preattn_t;
 
 /* Create a handle bound to CUDA device `device` (made current for the call).
  * Caches the SM count, raises the GEMM's shared-memory limit and allocates a
- * 4-byte device status word.  No per-M state.  *handle is set only on MH3_OK. */
+ * 4-byte device status word.  No per-M state.  *handle is set only on MH3_OK.
+ * The handle's own device buffers (the status word, the workspace it grows
+ * when a call passes none, and the split-tail scratch) serve every call made
+ * through it: calls through one handle on streams that may overlap on the GPU
+ * race on them, so give each concurrent stream its own handle. */
 int mh3_preattn_create(mh3_preattn_t* handle, int device);
 
 /* Destroy a handle: frees its status word and its own workspace (if any).
