@@ -96,9 +96,12 @@ class ClockSampler:
         self.gpu = gpu_index
         self.proc = None
         self.path = None
+        self.rows = []
+        self.started = False
 
     def start(self):
         import tempfile
+        self.started = True
         fd, self.path = tempfile.mkstemp(prefix="clocks_", suffix=".csv")
         os.close(fd)
         try:
@@ -109,21 +112,32 @@ class ClockSampler:
         except Exception:
             self.proc = None
 
-    def stop(self):
+    def pause(self):
+        """Stop polling and keep the samples so far.  The polling slows the
+        host<->device copies of the end-to-end passes (their times alternate
+        by up to 40 % while it runs), so it is paused around them."""
         if self.proc is None:
-            return None
+            return
         self.proc.terminate()
         try:
             self.proc.wait(timeout=5)
         except Exception:
             self.proc.kill()
-        rows = []
+        self.proc = None
         with open(self.path) as f:
             for line in f:
                 parts = [p.strip() for p in line.split(",")]
                 if len(parts) >= 9:
-                    rows.append(parts)
+                    self.rows.append(parts)
         os.unlink(self.path)
+
+    def resume(self):
+        if self.started and self.proc is None:
+            self.start()
+
+    def stop(self):
+        self.pause()
+        rows = self.rows
         if not rows:
             return None
 
@@ -377,6 +391,7 @@ def run_ours(args, world, rank, local):
     torch.cuda.synchronize()
     k1_alone_ms = a0.elapsed_time(a1) / args.steps
 
+    clocks.pause()  # the polling would slow the copies of the passes below
     # ---- end to end through the public API: every step copies its inputs
     # (x, index, positions, AdaLN tensor) from pinned host memory and its
     # result (out) back.  Two buffer sets and three streams pipeline the
@@ -473,6 +488,7 @@ def run_ours(args, world, rank, local):
     # the result of the last step really came back
     assert torch.equal(houts[(n_e2e - 1) % 2].view(torch.int16)[0, :4],
                        sets[(n_e2e - 1) % 2]["out"].view(torch.int16)[0, :4].cpu())
+    clocks.resume()
 
     # ---- the 4096-token block named by the metric (same stage, P = 2)
     also = None
@@ -852,7 +868,8 @@ def run_ours(args, world, rank, local):
                 "passes_us": [v * 1e3 / world for v in e2e_passes],
                 "how": "pinned host inputs in and out back every step; copies of neighbouring "
                        "steps overlap the kernels (2 buffer sets; input, compute and "
-                       f"{n_out} read-back streams)"},
+                       f"{n_out} read-back streams); the clock sampling is paused during "
+                       "these passes (its polling slows the host<->device copies)"},
         "gpu_launches": gpu_launches,
         "clocks": clk,
         "also": also,
