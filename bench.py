@@ -111,6 +111,14 @@ class ClockSampler:
                 stdout=open(self.path, "w"), stderr=subprocess.DEVNULL)
         except Exception:
             self.proc = None
+            return
+        # polling is live before the caller's timed work starts (short runs
+        # would otherwise end before the first sample): wait up to 3 s for it
+        t0 = time.time()
+        while time.time() - t0 < 3.0 and self.proc.poll() is None:
+            if os.path.getsize(self.path) > 0:
+                break
+            time.sleep(0.02)
 
     def pause(self):
         """Stop polling and keep the samples so far.  The polling slows the
