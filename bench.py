@@ -111,6 +111,7 @@ class ClockSampler:
                 stdout=open(self.path, "w"), stderr=subprocess.DEVNULL)
         except Exception:
             self.proc = None
+            os.unlink(self.path)
             return
         # polling is live before the caller's timed work starts (short runs
         # would otherwise end before the first sample): wait up to 3 s for it
