@@ -114,9 +114,9 @@ int mh3_preattn_validate(int64_t M, const mh3_bf16* x, const mh3_bf16* x_norm_we
  * tolerance.  The partials live in a scratch of the handle, grown with
  * stream-ordered cudaMallocAsync the first time a split size needs more
  * (even with a caller workspace): capture a split size into a graph after
- * one direct call at that size.  Its flags are cleared with a memset before
- * each such call (a graph replays that memset), and runs of one handle on
- * different streams race on the scratch.
+ * one direct call at that size.  Its flags are cleared on the stream before
+ * each such call, by kernel 1 of the same call (so a graph replay clears them
+ * too), and runs of one handle on different streams race on the scratch.
  *
  *   M                 tokens, >= 0 (M == 0 launches nothing and returns MH3_OK)
  *   x                 [M, 5376] row-major, 16-byte aligned
@@ -214,7 +214,8 @@ int mh3_preattn_norm_adaln(mh3_preattn_t handle, void* stream, int64_t M, const 
 /* Kernel 2 alone: out = pack(rope(norm(bf16(workspace @ qkv_weight^T)))),
  * reading an already-filled workspace [M, 5376].  Arguments as in
  * mh3_preattn_run (qk_eps here must be finite and > 0: there is no eps to
- * fall back to); the same split tail, with the same handle scratch. */
+ * fall back to); the same split tail, with the same handle scratch, whose
+ * flags this call clears with a memset on the stream before kernel 2. */
 int mh3_preattn_qkv(mh3_preattn_t handle, void* stream, int64_t M, const mh3_bf16* workspace,
                     const mh3_bf16* qkv_weight, const mh3_bf16* q_norm_weight,
                     const mh3_bf16* k_norm_weight, const mh3_bf16* rope_cos_sin, int64_t S,
